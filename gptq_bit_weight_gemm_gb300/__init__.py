@@ -1,0 +1,190 @@
+"""GB300 (sm_103a) GPTQ mixed-precision GEMM -- Python binding of the C ABI (include/gptq.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA library
+``_lib/libgptq_gb300.so`` (built in-tree by ``build.py``).  PyTorch supplies device memory
+and streams.  There is no fallback: if the library is missing or the device is not a GB300
+(sm_103), calls raise ``GPTQError``.
+
+Operations (page "增强 vLLM 对 GPTQv2 格式的支持：分析与实现", sections "LLM 的权重量化",
+"从 GPTQv1 到 GPTQv2", "调整细节：根据格式选择处理方式"):
+
+  gemm(A, qweight, qzeros, scales, g_idx, bits, group, fmt)  -> C = A @ dequant(W)
+  dequant(qweight, qzeros, scales, g_idx, K, bits, group, fmt, dtype) -> W [K, N]
+  quantize_rtn(W, bits, group, g_idx, sym, fmt)              -> (qweight, qzeros, scales)
+  repack_zeros_v1_to_v2(qzeros_v1, N, bits)                  (host memory)
+  device_status(stream)                                      -> GPTQ_DEV_* bits
+"""
+import ctypes
+import os
+import re
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "_lib", "libgptq_gb300.so")
+HEADER = os.path.join(os.path.dirname(HERE), "include", "gptq.h")
+
+F16, BF16 = 0, 1
+V1, V2 = 1, 2
+DEV_TIMEOUT, DEV_GIDX_RANGE, DEV_SCALE_OVERFLOW = 0x1, 0x2, 0x4
+DECODE_MAX_M = 16
+
+_STATUS = {0: "GPTQ_OK", -1: "GPTQ_ERR_ARG", -2: "GPTQ_ERR_SHAPE", -3: "GPTQ_ERR_ALIGN",
+           -4: "GPTQ_ERR_WORKSPACE", -5: "GPTQ_ERR_ZERO_OVERFLOW", -6: "GPTQ_ERR_CUDA",
+           -7: "GPTQ_ERR_UNSUPPORTED", -8: "GPTQ_ERR_DEVICE"}
+
+
+class GPTQError(RuntimeError):
+    def __init__(self, code, what=""):
+        self.code = code
+        msg = "%s (%d)" % (_STATUS.get(code, "unknown"), code)
+        try:
+            msg = lib().gptq_strerror(code).decode()
+        except Exception:
+            pass
+        super().__init__("%s%s" % (what + ": " if what else "", msg))
+
+
+_lib = None
+
+_P, _I, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+_SIGNATURES = {
+    "gptq_dequant": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
+    "gptq_gemm": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P]),
+    "gptq_gemm_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
+    "gptq_repack_zeros_v1_to_v2": (_I, [_P, _P, _I, _I, _I]),
+    "gptq_quantize_rtn": (_I, [_P, _I, _I, _I, _I, _P, _I, _I, _P, _P, _P, _P]),
+    "gptq_get_device_status": (_I, [_P, ctypes.POINTER(ctypes.c_uint)]),
+    "gptq_strerror": (ctypes.c_char_p, [_I]),
+}
+
+
+def lib():
+    """The loaded C library (ctypes).  Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("GPTQ CUDA library not built (%s): run "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`" % LIB_PATH)
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+def header_functions():
+    """Names of the functions include/gptq.h declares."""
+    with open(HEADER) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^\s*(?:int|size_t|const char\s*\*)\s+(gptq_\w+)\s*\(", text, re.M)))
+
+
+def _check(rc, what):
+    if rc != 0:
+        raise GPTQError(rc, what)
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t):
+    torch = _torch()
+    if t.dtype == torch.float16:
+        return F16
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise TypeError("activations must be float16 or bfloat16, got %s" % t.dtype)
+
+
+def _ptr(t, dtype=None, name="tensor"):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def gemm(A, qweight, qzeros, scales, g_idx=None, *, bits, group, fmt=V2, out=None, stream=None):
+    """C[M, N] = A[M, K] @ dequant(qweight, qzeros, scales, g_idx) on the current stream."""
+    torch = _torch()
+    M, K = A.shape
+    N = qweight.shape[1]
+    if out is None:
+        out = torch.empty((M, N), dtype=A.dtype, device=A.device)
+    rc = lib().gptq_gemm(_ptr(A, name="A"), M, K, _dtype_code(A),
+                         _ptr(qweight, torch.int32, "qweight"), _ptr(qzeros, torch.int32, "qzeros"),
+                         _ptr(scales, torch.float16, "scales"), _ptr(g_idx, torch.int32, "g_idx"),
+                         N, bits, group, fmt, _ptr(out, A.dtype, "out"), None, 0, _stream(stream))
+    _check(rc, "gptq_gemm")
+    return out
+
+
+def dequant(qweight, qzeros, scales, g_idx=None, *, K, bits, group, fmt=V2, dtype=None, out=None,
+            stream=None):
+    """W[K, N] = RN((q - zero) * scale) in `dtype` (float16 default)."""
+    torch = _torch()
+    dtype = torch.float16 if dtype is None else dtype
+    N = qweight.shape[1]
+    if out is None:
+        out = torch.empty((K, N), dtype=dtype, device=qweight.device)
+    code = F16 if dtype == torch.float16 else BF16
+    rc = lib().gptq_dequant(_ptr(qweight, torch.int32, "qweight"), _ptr(qzeros, torch.int32, "qzeros"),
+                            _ptr(scales, torch.float16, "scales"), _ptr(g_idx, torch.int32, "g_idx"),
+                            K, N, bits, group, fmt, code, _ptr(out, dtype, "out"), _stream(stream))
+    _check(rc, "gptq_dequant")
+    return out
+
+
+def quantize_rtn(W, *, bits, group, g_idx=None, sym=False, fmt=V2, stream=None):
+    """Round-to-nearest checkpoint of fp32 weights W [K, N]: (qweight, qzeros, scales)."""
+    torch = _torch()
+    K, N = W.shape
+    G = 1 if group == -1 else K // group
+    qweight = torch.empty((K * bits // 32, N), dtype=torch.int32, device=W.device)
+    qzeros = torch.empty((G, N * bits // 32), dtype=torch.int32, device=W.device)
+    scales = torch.empty((G, N), dtype=torch.float16, device=W.device)
+    rc = lib().gptq_quantize_rtn(_ptr(W, torch.float32, "W"), K, N, bits, group,
+                                 _ptr(g_idx, torch.int32, "g_idx"), int(bool(sym)), fmt,
+                                 _ptr(qweight), _ptr(qzeros), _ptr(scales), _stream(stream))
+    _check(rc, "gptq_quantize_rtn")
+    return qweight, qzeros, scales
+
+
+def repack_zeros_v1_to_v2(qzeros_v1, N, bits):
+    """Host repack of v1 qzeros (numpy int32 [G, N*bits/32]) into a new v2 array."""
+    src = np.ascontiguousarray(qzeros_v1, dtype=np.int32)
+    out = np.empty_like(src)
+    G = src.shape[0]
+    rc = lib().gptq_repack_zeros_v1_to_v2(src.ctypes.data_as(_P), out.ctypes.data_as(_P), G, N, bits)
+    _check(rc, "gptq_repack_zeros_v1_to_v2")
+    return out
+
+
+def workspace_size(M, K, N, bits, group):
+    return int(lib().gptq_gemm_workspace_size(M, K, N, bits, group))
+
+
+def device_status(stream=None):
+    """Synchronize `stream`, read and clear the device status word (GPTQ_DEV_* bits)."""
+    v = ctypes.c_uint(0)
+    _check(lib().gptq_get_device_status(_stream(stream), ctypes.byref(v)), "gptq_get_device_status")
+    return int(v.value)
+
+
+def strerror(code):
+    return lib().gptq_strerror(code).decode()

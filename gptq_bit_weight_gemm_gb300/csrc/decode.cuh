@@ -1,0 +1,373 @@
+// decode.cuh -- memory-bound GPTQ GEMM for few tokens (M <= 16): C = A @ dequant(W).
+//
+// This is the decode case of vLLM's gptq_gemm (page "增强 vLLM 对 GPTQv2 格式的支持：分析与实
+// 现", section "调整细节：根据格式选择处理方式": zeros[i] + zero_offset, zero_offset =
+// use_v2_format ? 0 : 1); the same page notes that the 2-bit GEMV case is slower than the
+// GEMM case and lists "improve gptq_gemm decode speed" as follow-up work.  Every weight is read
+// from HBM exactly once, so the kernel is built to stream qweight at full bandwidth:
+//
+//  * grid = (cluster of CS CTAs along K) x (slabs of 128 columns).  Each lane owns 4 adjacent
+//    columns, so one 16-byte load brings in one packed unit row for all of them; a warp reads
+//    512 contiguous bytes per row.  The CTAs of a cluster and the 8 warps of a CTA split the
+//    K units (split-K) into contiguous ranges; loads are double-buffered in registers.
+//  * q - zero is built exactly as a 16-bit float (magic-number unpack) and multiplied with the
+//    activation by a mixed-precision fma (f16/bf16 x f16/bf16 + f32 -> f32), so products are
+//    exact and sums are fp32.  Within a quantization group the scale is factored out:
+//    acc += scale * sum_k a_k (q_k - zero).  Act-order (g_idx) and the widths without a 16-bit
+//    unpack (3-bit, bf16 8-bit) take the general path: w = (q - zero) * scale in fp32 (exact)
+//    and fp32 fmas.
+//  * partial sums are reduced across warps in shared memory and across the cluster through
+//    distributed shared memory, in a fixed order (deterministic), then rounded once to the
+//    output dtype.  No global workspace and no atomics.
+#pragma once
+
+#include <cooperative_groups.h>
+
+#include "gptq_device.cuh"
+#include "gptq_internal.h"
+
+namespace gptq {
+namespace decode {
+
+namespace cg = cooperative_groups;
+
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+constexpr int kSlab = 128;    // columns per CTA (4 per lane)
+constexpr int kBatch = 4;     // units per load stage
+
+struct Args {
+  const void* A;
+  int M, K, N;
+  const int32_t* qweight;
+  const int32_t* qzeros;
+  const __half* scales;
+  const int32_t* g_idx;
+  int group, G, zero_offset, zwords, units;
+  void* C;
+  unsigned* status;
+};
+
+__device__ __forceinline__ void split(int total, int parts, int idx, int& b, int& e) {
+  b = static_cast<int>(static_cast<long long>(total) * idx / parts);
+  e = static_cast<int>(static_cast<long long>(total) * (idx + 1) / parts);
+}
+
+// Scales (as fp32) and runtime zeros of columns n0..n0+3 for group g.
+template <int BITS>
+__device__ __forceinline__ void load_sz(const Args& a, int g, int n0, float (&s)[4],
+                                        int (&z)[4]) {
+  const uint2 sv = __ldg(reinterpret_cast<const uint2*>(a.scales + static_cast<long long>(g) * a.N + n0));
+  s[0] = __half2float(__ushort_as_half(static_cast<uint16_t>(sv.x & 0xFFFFu)));
+  s[1] = __half2float(__ushort_as_half(static_cast<uint16_t>(sv.x >> 16)));
+  s[2] = __half2float(__ushort_as_half(static_cast<uint16_t>(sv.y & 0xFFFFu)));
+  s[3] = __half2float(__ushort_as_half(static_cast<uint16_t>(sv.y >> 16)));
+  const uint32_t zf = zeros4<BITS>(a.qzeros + static_cast<long long>(g) * a.zwords, n0);
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    z[c] = static_cast<int>((zf >> (BITS * c)) & Pack<BITS>::kMask) + a.zero_offset;
+}
+
+__device__ __forceinline__ int checked_group(const Args& a, int k) {
+  int g = __ldg(a.g_idx + k);
+  if (g < 0 || g >= a.G) {
+    atomicOr(a.status, kStatusGidxRange);
+    g = g < 0 ? 0 : a.G - 1;
+  }
+  return g;
+}
+
+// Code j of column c within a loaded unit (ROWS x uint4, one word per column per row).
+template <int BITS>
+__device__ __forceinline__ uint32_t unit_code(const uint4 (&u)[Pack<BITS>::kRowsPerUnit], int c,
+                                              int j) {
+  if constexpr (BITS == 3) {
+    const uint32_t w0 = (&u[0].x)[c], w1 = (&u[1].x)[c], w2 = (&u[2].x)[c];
+    return code3(w0, w1, w2, j);
+  } else {
+    return ((&u[0].x)[c] >> (BITS * j)) & Pack<BITS>::kMask;
+  }
+}
+
+template <int BITS, int MT, typename T, bool FACTORED, bool ACT>
+__global__ void __launch_bounds__(kThreads) k_decode(const Args a) {
+  using P = Pack<BITS>;
+  constexpr int PER = P::kPerUnit;
+  constexpr int ROWS = P::kRowsPerUnit;
+  using AT = typename std::conditional<FACTORED, T, float>::type;   // staged activation type
+  extern __shared__ __align__(16) unsigned char smem[];
+  AT* sA = reinterpret_cast<AT*>(smem);
+
+  cg::cluster_group cluster = cg::this_cluster();
+  const int cs = static_cast<int>(gridDim.x);   // grid x == cluster x
+  const int rank = static_cast<int>(blockIdx.x);
+  const int n_base = static_cast<int>(blockIdx.y) * kSlab;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n0 = n_base + lane * 4;
+  const bool col_ok = n0 < a.N;
+
+  int cu0, cu1;
+  split(a.units, cs, rank, cu0, cu1);
+  const int kbase = cu0 * PER;
+  const int kcount = (cu1 - cu0) * PER;
+
+  // Stage this CTA's activations as sA[k - kbase][m]; rows m >= M are zero.
+  const T* A = static_cast<const T*>(a.A);
+  for (int i = threadIdx.x; i < kcount * MT; i += kThreads) {
+    const int m = i / kcount, kk = i - m * kcount;
+    AT v;
+    if constexpr (FACTORED) {
+      v = m < a.M ? A[static_cast<long long>(m) * a.K + kbase + kk] : F16Traits<T>::from_f32(0.f);
+    } else {
+      v = m < a.M ? F16Traits<T>::to_f32(A[static_cast<long long>(m) * a.K + kbase + kk]) : 0.f;
+    }
+    sA[kk * MT + m] = v;
+  }
+  __syncthreads();
+
+  int wu0, wu1;
+  split(cu1 - cu0, kWarps, warp, wu0, wu1);
+  wu0 += cu0;
+  wu1 += cu0;
+
+  float acc[MT][4];
+#pragma unroll
+  for (int m = 0; m < MT; ++m)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc[m][c] = 0.f;
+
+  float accg[FACTORED ? MT : 1][4];
+  float s[4];
+  int z[4];
+  int cur_g = -1;
+  if constexpr (FACTORED) {
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) accg[m][c] = 0.f;
+  }
+
+  const int32_t* qw = a.qweight + n0;
+  const long long row_stride = a.N;
+  uint4 cur[kBatch][ROWS], nxt[kBatch][ROWS];
+
+  auto load = [&](uint4 (&dst)[kBatch][ROWS], int ufirst) {
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b)
+#pragma unroll
+      for (int r = 0; r < ROWS; ++r) {
+        const int u = ufirst + b;
+        if (col_ok && u < wu1)
+          dst[b][r] = ld_stream_v4(qw + (static_cast<long long>(u) * ROWS + r) * row_stride);
+        else
+          dst[b][r] = make_uint4(0u, 0u, 0u, 0u);
+      }
+  };
+
+  load(cur, wu0);
+  for (int ub = wu0; ub < wu1; ub += kBatch) {
+    if (ub + kBatch < wu1) load(nxt, ub + kBatch);
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int u = ub + b;
+      if (u >= wu1) break;
+      const int k0 = u * PER;
+      const int kk0 = k0 - kbase;
+      if constexpr (FACTORED) {
+        const int g = k0 / a.group;
+        if (g != cur_g) {
+          if (cur_g >= 0) {
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                acc[m][c] = fmaf(s[c], accg[m][c], acc[m][c]);
+                accg[m][c] = 0.f;
+              }
+          }
+          if (col_ok) load_sz<BITS>(a, g, n0, s, z);
+          cur_g = g;
+        }
+        // activations of this unit: PER x MT 16-bit values, contiguous in shared memory
+        constexpr int kWords = PER * MT / 2;
+        uint32_t av[kWords];
+        const uint32_t* src = reinterpret_cast<const uint32_t*>(sA + kk0 * MT);
+        if constexpr (kWords % 4 == 0) {
+#pragma unroll
+          for (int i = 0; i < kWords / 4; ++i) {
+            const uint4 v = reinterpret_cast<const uint4*>(src)[i];
+            av[4 * i] = v.x; av[4 * i + 1] = v.y; av[4 * i + 2] = v.z; av[4 * i + 3] = v.w;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < kWords / 2; ++i) {
+            const uint2 v = reinterpret_cast<const uint2*>(src)[i];
+            av[2 * i] = v.x; av[2 * i + 1] = v.y;
+          }
+        }
+        auto a16 = [&](int j, int m) -> uint16_t {
+          const int e = j * MT + m;
+          return (e & 1) ? hi16(av[e >> 1]) : lo16(av[e >> 1]);
+        };
+        using DP = DiffPairs<T, BITS>;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t d[DP::kPairs];
+          DP::run((&cur[b][0].x)[c], z[c], d);
+#pragma unroll
+          for (int p = 0; p < DP::kPairs; ++p)
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+              accg[m][c] = fma_mix(a16(DP::lo_k(p), m), lo16(d[p]), accg[m][c], T());
+              accg[m][c] = fma_mix(a16(DP::hi_k(p), m), hi16(d[p]), accg[m][c], T());
+            }
+        }
+      } else {
+#pragma unroll 4
+        for (int j = 0; j < PER; ++j) {
+          const int k = k0 + j;
+          const int g = ACT ? checked_group(a, k) : k / a.group;
+          if (ACT || g != cur_g) {
+            if (col_ok) load_sz<BITS>(a, g, n0, s, z);
+            cur_g = g;
+          }
+          float w[4];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) w[c] = diff_f32(unit_code<BITS>(cur[b], c, j), z[c]) * s[c];
+          const float* ak = sA + (kk0 + j) * MT;
+#pragma unroll
+          for (int m = 0; m < MT; ++m) {
+            const float av = ak[m];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) acc[m][c] = fmaf(av, w[c], acc[m][c]);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b)
+#pragma unroll
+      for (int r = 0; r < ROWS; ++r) cur[b][r] = nxt[b][r];
+  }
+  if constexpr (FACTORED) {
+    if (cur_g >= 0) {
+#pragma unroll
+      for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[m][c] = fmaf(s[c], accg[m][c], acc[m][c]);
+    }
+  }
+
+  // ---- reduction: warps (shared memory), then the cluster (distributed shared memory)
+  __syncthreads();   // every warp is done reading sA
+  float* red = reinterpret_cast<float*>(smem);   // [kWarps][MT][kSlab]
+#pragma unroll
+  for (int m = 0; m < MT; ++m)
+    *reinterpret_cast<float4*>(red + (warp * MT + m) * kSlab + lane * 4) =
+        make_float4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]);
+  __syncthreads();
+  for (int i = threadIdx.x; i < MT * kSlab; i += kThreads) {
+    float v = red[i];
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w) v += red[w * MT * kSlab + i];
+    red[i] = v;
+  }
+  cluster.sync();
+  const int per_rank = kSlab / cs;
+  T* C = static_cast<T*>(a.C);
+  for (int i = threadIdx.x; i < MT * per_rank; i += kThreads) {
+    const int m = i / per_rank;
+    const int col = rank * per_rank + (i - m * per_rank);
+    const int n = n_base + col;
+    if (m < a.M && n < a.N) {
+      float v = 0.f;
+      for (int q = 0; q < cs; ++q) v += cluster.map_shared_rank(red, q)[m * kSlab + col];
+      C[static_cast<long long>(m) * a.N + n] = F16Traits<T>::from_f32(v);
+    }
+  }
+  cluster.sync();   // keep this CTA's shared memory alive until the cluster has read it
+}
+
+// Shared memory bytes for one CTA.
+template <int BITS, int MT, bool FACTORED>
+constexpr size_t smem_bytes(int units_per_cta) {
+  const size_t stage = static_cast<size_t>(units_per_cta) * Pack<BITS>::kPerUnit * MT *
+                       (FACTORED ? 2 : 4);
+  const size_t red = static_cast<size_t>(kWarps) * MT * kSlab * 4;
+  return stage > red ? stage : red;
+}
+
+template <int BITS, int MT, typename T, bool FACTORED, bool ACT>
+cudaError_t launch_one(const Problem& p, int cs, cudaStream_t stream) {
+  Args a;
+  a.A = p.A; a.M = p.M; a.K = p.K; a.N = p.N;
+  a.qweight = p.qweight; a.qzeros = p.qzeros;
+  a.scales = static_cast<const __half*>(p.scales);
+  a.g_idx = p.g_idx; a.group = p.group; a.G = p.G; a.zero_offset = p.zero_offset;
+  a.zwords = p.N * BITS / 32;
+  a.units = p.K / Pack<BITS>::kPerUnit;
+  a.C = p.out; a.status = p.status;
+  const int slabs = (p.N + kSlab - 1) / kSlab;
+  const int units_per_cta = (a.units + cs - 1) / cs;
+  const size_t smem = smem_bytes<BITS, MT, FACTORED>(units_per_cta);
+  auto kern = k_decode<BITS, MT, T, FACTORED, ACT>;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cs, slabs, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+// Cluster size: enough warps to fill the GPU (about 16 per SM), at least one unit per warp.
+inline int choose_cluster(const Problem& p, int per_unit) {
+  const int slabs = (p.N + kSlab - 1) / kSlab;
+  const int units = p.K / per_unit;
+  const int target = device_info().sm_count * 16;
+  int cs = 1;
+  while (cs < 8 && slabs * cs * kWarps < target && units >= 2 * cs * kWarps) cs *= 2;
+  return cs;
+}
+
+template <int BITS, int MT, typename T>
+cudaError_t launch_mt(const Problem& p, cudaStream_t stream) {
+  const int cs = choose_cluster(p, Pack<BITS>::kPerUnit);
+  constexpr bool kHas16 = (BITS == 2 || BITS == 4 || (BITS == 8 && std::is_same<T, __half>::value));
+  const bool factorable = p.g_idx == nullptr && (p.group % Pack<BITS>::kPerUnit) == 0;
+  if constexpr (kHas16 && MT <= 4) {
+    if (factorable) return launch_one<BITS, MT, T, true, false>(p, cs, stream);
+  }
+  if (p.g_idx) return launch_one<BITS, MT, T, false, true>(p, cs, stream);
+  return launch_one<BITS, MT, T, false, false>(p, cs, stream);
+}
+
+template <int BITS>
+cudaError_t launch_bits(const Problem& p, cudaStream_t stream) {
+  if (p.dtype == 0) {
+    if (p.M <= 1) return launch_mt<BITS, 1, __half>(p, stream);
+    if (p.M <= 2) return launch_mt<BITS, 2, __half>(p, stream);
+    if (p.M <= 4) return launch_mt<BITS, 4, __half>(p, stream);
+    if (p.M <= 8) return launch_mt<BITS, 8, __half>(p, stream);
+    return launch_mt<BITS, 16, __half>(p, stream);
+  }
+  if (p.M <= 1) return launch_mt<BITS, 1, __nv_bfloat16>(p, stream);
+  if (p.M <= 2) return launch_mt<BITS, 2, __nv_bfloat16>(p, stream);
+  if (p.M <= 4) return launch_mt<BITS, 4, __nv_bfloat16>(p, stream);
+  if (p.M <= 8) return launch_mt<BITS, 8, __nv_bfloat16>(p, stream);
+  return launch_mt<BITS, 16, __nv_bfloat16>(p, stream);
+}
+
+}  // namespace decode
+}  // namespace gptq

@@ -1,0 +1,9 @@
+// decode_b3.cu -- 3-bit instantiations of the decode kernel (kept in their own
+// translation unit so the widths compile in parallel).
+#include "decode.cuh"
+
+namespace gptq {
+cudaError_t launch_decode_b3(const Problem& p, cudaStream_t stream) {
+  return decode::launch_bits<3>(p, stream);
+}
+}  // namespace gptq

@@ -1,0 +1,246 @@
+// gptq_api.cu -- the C ABI (include/gptq.h): host-side validation, dispatch, the host v1 -> v2
+// zero repack and the device status word.
+#include <cuda_runtime.h>
+
+#include <mutex>
+#include <vector>
+
+#include "../../include/gptq.h"
+#include "gptq_internal.h"
+
+namespace gptq {
+
+cudaError_t launch_decode_b2(const Problem& p, cudaStream_t stream);
+cudaError_t launch_decode_b3(const Problem& p, cudaStream_t stream);
+cudaError_t launch_decode_b4(const Problem& p, cudaStream_t stream);
+cudaError_t launch_decode_b8(const Problem& p, cudaStream_t stream);
+
+cudaError_t launch_decode(const Problem& p, cudaStream_t stream) {
+  switch (p.bits) {
+    case 2: return launch_decode_b2(p, stream);
+    case 3: return launch_decode_b3(p, stream);
+    case 4: return launch_decode_b4(p, stream);
+    case 8: return launch_decode_b8(p, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+// One word per device; kernels OR error bits into it (GPTQ_DEV_*).
+__device__ unsigned g_device_status;
+
+struct DeviceState {
+  std::once_flag once;
+  DeviceInfo info;
+  unsigned* status = nullptr;
+  cudaError_t init_error = cudaSuccess;
+};
+
+DeviceState g_devices[kMaxDevices];
+
+DeviceState* current_state(cudaError_t* err) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    *err = e != cudaSuccess ? e : cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  DeviceState& st = g_devices[dev];
+  std::call_once(st.once, [&st, dev]() {
+    st.info.device = dev;
+    cudaError_t r = cudaDeviceGetAttribute(&st.info.sm_count, cudaDevAttrMultiProcessorCount, dev);
+    if (r == cudaSuccess)
+      r = cudaDeviceGetAttribute(&st.info.cc_major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (r == cudaSuccess)
+      r = cudaDeviceGetAttribute(&st.info.cc_minor, cudaDevAttrComputeCapabilityMinor, dev);
+    int smem = 0;
+    if (r == cudaSuccess)
+      r = cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    st.info.smem_optin = static_cast<size_t>(smem);
+    if (r == cudaSuccess) r = cudaGetSymbolAddress(reinterpret_cast<void**>(&st.status), g_device_status);
+    st.init_error = r;
+  });
+  *err = st.init_error;
+  return st.init_error == cudaSuccess ? &st : nullptr;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool bits_ok(int bits) { return bits == 2 || bits == 3 || bits == 4 || bits == 8; }
+
+// Shape/argument checks shared by every device entry point; fills p.G and p.group.
+int check_common(const int32_t* qweight, const int32_t* qzeros, const void* scales,
+                 const int32_t* g_idx, int K, int N, int bits, int group, Problem* p) {
+  if (!bits_ok(bits)) return GPTQ_ERR_ARG;
+  if (!qweight || !qzeros || !scales) return GPTQ_ERR_ARG;
+  if (K <= 0 || N <= 0 || K % 32 || N % 32) return GPTQ_ERR_SHAPE;
+  if (group == -1) {
+    if (g_idx) return GPTQ_ERR_SHAPE;
+    p->group = K;
+    p->G = 1;
+  } else {
+    if (group <= 0 || K % group) return GPTQ_ERR_SHAPE;
+    p->group = group;
+    p->G = K / group;
+  }
+  if (!aligned(qweight, 16) || !aligned(qzeros, 16) || !aligned(scales, 16)) return GPTQ_ERR_ALIGN;
+  if (g_idx && !aligned(g_idx, 4)) return GPTQ_ERR_ALIGN;
+  p->qweight = qweight;
+  p->qzeros = qzeros;
+  p->scales = scales;
+  p->g_idx = g_idx;
+  p->K = K;
+  p->N = N;
+  p->bits = bits;
+  return GPTQ_OK;
+}
+
+int device_ready(Problem* p) {
+  cudaError_t err;
+  DeviceState* st = current_state(&err);
+  if (!st) return GPTQ_ERR_CUDA;
+  if (st->info.cc_major != 10 || st->info.cc_minor != 3) return GPTQ_ERR_UNSUPPORTED;
+  p->status = st->status;
+  return GPTQ_OK;
+}
+
+int from_cuda(cudaError_t e) { return e == cudaSuccess ? GPTQ_OK : GPTQ_ERR_CUDA; }
+
+}  // namespace
+
+const DeviceInfo& device_info() {
+  cudaError_t err;
+  DeviceState* st = current_state(&err);
+  static DeviceInfo fallback{0, 1, 0, 0, 48 * 1024};
+  return st ? st->info : fallback;
+}
+
+}  // namespace gptq
+
+using gptq::Problem;
+
+extern "C" int gptq_dequant(const int32_t* qweight, const int32_t* qzeros, const void* scales,
+                            const int32_t* g_idx, int K, int N, int bits, int group, int fmt,
+                            int out_dtype, void* W_out, void* stream) {
+  Problem p = {};
+  int rc = gptq::check_common(qweight, qzeros, scales, g_idx, K, N, bits, group, &p);
+  if (rc) return rc;
+  if (fmt != GPTQ_FMT_V1 && fmt != GPTQ_FMT_V2) return GPTQ_ERR_ARG;
+  if (out_dtype != GPTQ_F16 && out_dtype != GPTQ_BF16) return GPTQ_ERR_ARG;
+  if (!W_out) return GPTQ_ERR_ARG;
+  if (!gptq::aligned(W_out, 16)) return GPTQ_ERR_ALIGN;
+  rc = gptq::device_ready(&p);
+  if (rc) return rc;
+  p.dtype = out_dtype;
+  p.zero_offset = fmt == GPTQ_FMT_V1 ? 1 : 0;
+  p.out = W_out;
+  return gptq::from_cuda(gptq::launch_dequant(p, static_cast<cudaStream_t>(stream)));
+}
+
+extern "C" size_t gptq_gemm_workspace_size(int M, int K, int N, int bits, int group) {
+  (void)M; (void)K; (void)N; (void)bits; (void)group;
+  return 0;
+}
+
+extern "C" int gptq_gemm(const void* A, int M, int K, int a_dtype, const int32_t* qweight,
+                         const int32_t* qzeros, const void* scales, const int32_t* g_idx, int N,
+                         int bits, int group, int fmt, void* C, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  Problem p = {};
+  int rc = gptq::check_common(qweight, qzeros, scales, g_idx, K, N, bits, group, &p);
+  if (rc) return rc;
+  if (fmt != GPTQ_FMT_V1 && fmt != GPTQ_FMT_V2) return GPTQ_ERR_ARG;
+  if (a_dtype != GPTQ_F16 && a_dtype != GPTQ_BF16) return GPTQ_ERR_ARG;
+  if (M < 0) return GPTQ_ERR_SHAPE;
+  if (workspace_bytes < gptq_gemm_workspace_size(M, K, N, bits, group)) return GPTQ_ERR_WORKSPACE;
+  (void)workspace;
+  if (M == 0) return GPTQ_OK;
+  if (!A || !C) return GPTQ_ERR_ARG;
+  if (!gptq::aligned(A, 16) || !gptq::aligned(C, 16)) return GPTQ_ERR_ALIGN;
+  rc = gptq::device_ready(&p);
+  if (rc) return rc;
+  p.A = A;
+  p.M = M;
+  p.dtype = a_dtype;
+  p.zero_offset = fmt == GPTQ_FMT_V1 ? 1 : 0;
+  p.out = C;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (M <= gptq::kDecodeMaxM) return gptq::from_cuda(gptq::launch_decode(p, s));
+  return gptq::from_cuda(gptq::launch_prefill(p, s));
+}
+
+extern "C" int gptq_quantize_rtn(const float* W, int K, int N, int bits, int group,
+                                 const int32_t* g_idx, int sym, int fmt, int32_t* qweight,
+                                 int32_t* qzeros, void* scales, void* stream) {
+  Problem p = {};
+  int rc = gptq::check_common(qweight, qzeros, scales, g_idx, K, N, bits, group, &p);
+  if (rc) return rc;
+  if (!W) return GPTQ_ERR_ARG;
+  if (fmt != GPTQ_FMT_V1 && fmt != GPTQ_FMT_V2) return GPTQ_ERR_ARG;
+  if (sym != 0 && sym != 1) return GPTQ_ERR_ARG;
+  if (!gptq::aligned(W, 16)) return GPTQ_ERR_ALIGN;
+  rc = gptq::device_ready(&p);
+  if (rc) return rc;
+  gptq::QuantProblem q;
+  q.W = W; q.K = K; q.N = N; q.bits = bits; q.group = p.group; q.G = p.G;
+  q.g_idx = g_idx; q.sym = sym; q.fmt = fmt;
+  q.qweight = qweight; q.qzeros = qzeros; q.scales = scales; q.status = p.status;
+  return gptq::from_cuda(gptq::launch_quantize(q, static_cast<cudaStream_t>(stream)));
+}
+
+// Host repack: reads every field of a row's LSB-first stream, adds one, writes it back.
+extern "C" int gptq_repack_zeros_v1_to_v2(const int32_t* qz_v1, int32_t* qz_v2, int G, int N,
+                                          int bits) {
+  if (!gptq::bits_ok(bits) || !qz_v1 || !qz_v2) return GPTQ_ERR_ARG;
+  if (G <= 0 || N <= 0 || N % 32) return GPTQ_ERR_SHAPE;
+  const int words = N * bits / 32;
+  const uint32_t mask = (1u << bits) - 1u;
+  std::vector<uint32_t> out(static_cast<size_t>(G) * words, 0u);
+  for (int g = 0; g < G; ++g) {
+    const uint32_t* in = reinterpret_cast<const uint32_t*>(qz_v1) + static_cast<size_t>(g) * words;
+    uint32_t* o = out.data() + static_cast<size_t>(g) * words;
+    for (int n = 0; n < N; ++n) {
+      const int bit = bits * n, w = bit >> 5, s = bit & 31;
+      uint64_t pair = in[w];
+      if (s + bits > 32) pair |= static_cast<uint64_t>(in[w + 1]) << 32;
+      const uint32_t f = static_cast<uint32_t>(pair >> s) & mask;
+      if (f == mask) return GPTQ_ERR_ZERO_OVERFLOW;
+      const uint64_t v = static_cast<uint64_t>(f + 1) << s;
+      o[w] |= static_cast<uint32_t>(v);
+      if (s + bits > 32) o[w + 1] |= static_cast<uint32_t>(v >> 32);
+    }
+  }
+  for (size_t i = 0; i < out.size(); ++i) qz_v2[i] = static_cast<int32_t>(out[i]);
+  return GPTQ_OK;
+}
+
+extern "C" int gptq_get_device_status(void* stream, unsigned int* out) {
+  if (!out) return GPTQ_ERR_ARG;
+  cudaError_t err;
+  gptq::DeviceState* st = gptq::current_state(&err);
+  if (!st) return GPTQ_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  err = cudaStreamSynchronize(s);
+  if (err == cudaSuccess) err = cudaMemcpy(out, st->status, sizeof(unsigned), cudaMemcpyDeviceToHost);
+  if (err == cudaSuccess) err = cudaMemset(st->status, 0, sizeof(unsigned));
+  if (err == cudaSuccess) err = cudaDeviceSynchronize();
+  return gptq::from_cuda(err);
+}
+
+extern "C" const char* gptq_strerror(int code) {
+  switch (code) {
+    case GPTQ_OK: return "GPTQ_OK";
+    case GPTQ_ERR_ARG: return "GPTQ_ERR_ARG: invalid argument (NULL pointer or bits/fmt/dtype/sym)";
+    case GPTQ_ERR_SHAPE: return "GPTQ_ERR_SHAPE: unsupported shape (K, N multiples of 32; group divides K)";
+    case GPTQ_ERR_ALIGN: return "GPTQ_ERR_ALIGN: pointer not 16-byte aligned";
+    case GPTQ_ERR_WORKSPACE: return "GPTQ_ERR_WORKSPACE: workspace too small";
+    case GPTQ_ERR_ZERO_OVERFLOW: return "GPTQ_ERR_ZERO_OVERFLOW: v1 zero of 2^bits-1 has no v2 encoding";
+    case GPTQ_ERR_CUDA: return "GPTQ_ERR_CUDA: CUDA call or launch failed";
+    case GPTQ_ERR_UNSUPPORTED: return "GPTQ_ERR_UNSUPPORTED: device is not sm_103 (GB300)";
+    case GPTQ_ERR_DEVICE: return "GPTQ_ERR_DEVICE: device status word reported an error";
+    default: return "unknown gptq status";
+  }
+}

@@ -1,0 +1,226 @@
+// gptq_device.cuh -- device-side building blocks shared by the GPTQ kernels (sm_103a).
+//
+// Packed layout (page "增强 vLLM 对 GPTQv2 格式的支持：分析与实现", section
+// "调整细节：根据格式选择处理方式", which unpacks 16 two-bit codes from one int32 word): each
+// qweight column is an LSB-first bit stream of its K codes, code k at stream bits
+// [b*k, b*k + b).  For b in {2, 4, 8} a "unit" is one word holding 32/b consecutive k; for
+// b = 3 a unit is three consecutive words holding 32 consecutive k (codes 10 and 21 of the
+// unit straddle words).  qzeros rows use the same stream rule along N.
+//
+// Dequantization is w = (q - zero) * scale with zero = stored + zero_offset (0 for GPTQv2, 1
+// for GPTQv1).  q - zero is an integer in [-256, 255] and is produced here exactly, either as a
+// 16-bit float (the "magic number" construction: OR the code into the mantissa of a float
+// whose unit in the last place is 1, then subtract the magic plus the zero) or as an fp32.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include <type_traits>
+
+namespace gptq {
+
+constexpr unsigned kStatusTimeout = 0x1u;
+constexpr unsigned kStatusGidxRange = 0x2u;
+
+template <int BITS>
+struct Pack {
+  static constexpr int kPerUnit = BITS == 3 ? 32 : 32 / BITS;   // k values per unit
+  static constexpr int kRowsPerUnit = BITS == 3 ? 3 : 1;        // qweight rows per unit
+  static constexpr uint32_t kMask = (1u << BITS) - 1u;
+};
+
+// ------------------------------------------------------------------------------------------
+// Loads
+// ------------------------------------------------------------------------------------------
+// Streaming 16-byte load through the non-coherent path, not kept in L1.
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t mask, uint32_t magic) {
+  uint32_t r;
+  // (a & mask) | magic
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(a), "r"(mask), "r"(magic));
+  return r;
+}
+
+// Code j (0..31) of a 3-bit unit whose words are w0, w1, w2 (LSB-first 96-bit stream).
+__device__ __forceinline__ uint32_t code3(uint32_t w0, uint32_t w1, uint32_t w2, int j) {
+  const int bit = 3 * j;
+  if (bit + 3 <= 32) return (w0 >> bit) & 7u;
+  if (bit < 32) return __funnelshift_r(w0, w1, bit) & 7u;
+  if (bit + 3 <= 64) return (w1 >> (bit - 32)) & 7u;
+  if (bit < 64) return __funnelshift_r(w1, w2, bit - 32) & 7u;
+  return (w2 >> (bit - 64)) & 7u;
+}
+
+// Stored zeros of 4 adjacent columns n0..n0+3 (n0 % 4 == 0) of qzeros row `row` (words),
+// returned as a 4 x BITS-bit field: column n0 + c at bits [BITS*c, BITS*c + BITS).
+template <int BITS>
+__device__ __forceinline__ uint32_t zeros4(const int32_t* __restrict__ row, int n0) {
+  if constexpr (BITS == 3) {
+    const int bit = 3 * n0;
+    const int w = bit >> 5, s = bit & 31;
+    uint32_t lo = static_cast<uint32_t>(__ldg(row + w));
+    uint32_t hi = (s + 12 > 32) ? static_cast<uint32_t>(__ldg(row + w + 1)) : 0u;
+    return __funnelshift_r(lo, hi, s) & 0xFFFu;
+  } else {
+    const int bit = BITS * n0;
+    uint32_t word = static_cast<uint32_t>(__ldg(row + (bit >> 5)));
+    return BITS == 8 ? word : (word >> (bit & 31)) & ((1u << (4 * BITS)) - 1u);
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// 16-bit float traits
+// ------------------------------------------------------------------------------------------
+template <typename T>
+struct F16Traits;
+
+template <>
+struct F16Traits<__half> {
+  using T2 = __half2;
+  static constexpr uint32_t kMagic2 = 0x64006400u;   // (1024, 1024): ulp 1 on [1024, 2048)
+  static constexpr float kMagic = 1024.0f;
+  __device__ static __forceinline__ float to_f32(__half x) { return __half2float(x); }
+  __device__ static __forceinline__ __half from_f32(float x) { return __float2half_rn(x); }
+  __device__ static __forceinline__ uint16_t bits(__half x) { return __half_as_ushort(x); }
+};
+
+template <>
+struct F16Traits<__nv_bfloat16> {
+  using T2 = __nv_bfloat162;
+  static constexpr uint32_t kMagic2 = 0x43004300u;   // (128, 128): ulp 1 on [128, 256)
+  static constexpr float kMagic = 128.0f;
+  __device__ static __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+  __device__ static __forceinline__ __nv_bfloat16 from_f32(float x) {
+    return __float2bfloat16_rn(x);
+  }
+  __device__ static __forceinline__ uint16_t bits(__nv_bfloat16 x) {
+    return __bfloat16_as_ushort(x);
+  }
+};
+
+// d = a * b + c with a, b 16-bit floats and c, d fp32: exact product, one rounding.
+__device__ __forceinline__ float fma_mix(uint16_t a, uint16_t b, float c, __half) {
+  float d;
+  asm("fma.rn.f32.f16 %0, %1, %2, %3;" : "=f"(d) : "h"(a), "h"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float fma_mix(uint16_t a, uint16_t b, float c, __nv_bfloat16) {
+  float d;
+  asm("fma.rn.f32.bf16 %0, %1, %2, %3;" : "=f"(d) : "h"(a), "h"(b), "f"(c));
+  return d;
+}
+
+__device__ __forceinline__ uint16_t lo16(uint32_t x) { return static_cast<uint16_t>(x & 0xFFFFu); }
+__device__ __forceinline__ uint16_t hi16(uint32_t x) { return static_cast<uint16_t>(x >> 16); }
+
+__device__ __forceinline__ uint32_t sub2(uint32_t a, uint32_t b, __half) {
+  __half2 r = __hsub2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+__device__ __forceinline__ uint32_t sub2(uint32_t a, uint32_t b, __nv_bfloat16) {
+  __nv_bfloat162 r =
+      __hsub2(*reinterpret_cast<__nv_bfloat162*>(&a), *reinterpret_cast<__nv_bfloat162*>(&b));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+__device__ __forceinline__ uint32_t fma2(uint32_t a, uint32_t b, uint32_t c, __half) {
+  __half2 r = __hfma2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b),
+                      *reinterpret_cast<__half2*>(&c));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
+// Pack two fp32 into a 16-bit pair (lo, hi), rounding to nearest-even.
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, __half) {
+  __half2 r = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, __nv_bfloat16) {
+  __nv_bfloat162 r = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
+// Replicate a 16-bit float value into both halves.
+template <typename T>
+__device__ __forceinline__ uint32_t splat2(float x) {
+  uint32_t h = F16Traits<T>::bits(F16Traits<T>::from_f32(x));
+  return h | (h << 16);
+}
+
+// ------------------------------------------------------------------------------------------
+// Exact (q - zero) pairs from one packed word, as 16-bit floats.
+//
+// DiffPairs<T, BITS>::run(word, z) fills d[kPairs] with two k values each; pair p holds k
+// indices lo_k(p) (low half) and hi_k(p) (high half) of the word's kPerUnit codes.  z is the
+// runtime zero (stored + offset, up to 256).  Valid for T = __half with every width and for
+// T = __nv_bfloat16 with BITS <= 4 (the code must fit in the 7-bit bf16 mantissa).
+// ------------------------------------------------------------------------------------------
+template <typename T, int BITS>
+struct DiffPairs;
+
+template <typename T>
+struct DiffPairs<T, 4> {
+  static constexpr int kPairs = 4;
+  __device__ static __forceinline__ int lo_k(int p) { return p; }
+  __device__ static __forceinline__ int hi_k(int p) { return p + 4; }
+  __device__ static __forceinline__ void run(uint32_t w, int z, uint32_t (&d)[4]) {
+    const uint32_t M2 = F16Traits<T>::kMagic2;
+    const uint32_t zz = splat2<T>(F16Traits<T>::kMagic + static_cast<float>(z));
+    if constexpr (std::is_same<T, __half>::value) {
+      // fp16: nibble pairs at bits (4p, 4p + 16).  A code at bits 4..7 of a half reads as
+      // 1024 + 16 q, so x * (1/16) - (64 + z) = q - z (exact: one fma, representable result).
+      const uint32_t w8 = w >> 8;
+      const uint32_t nz16 = splat2<T>(-(64.0f + static_cast<float>(z)));
+      const uint32_t inv16 = 0x2C002C00u;   // (1/16, 1/16)
+      d[0] = sub2(lop3_and_or(w, 0x000F000Fu, M2), zz, T());
+      d[1] = fma2(lop3_and_or(w, 0x00F000F0u, M2), inv16, nz16, T());
+      d[2] = sub2(lop3_and_or(w8, 0x000F000Fu, M2), zz, T());
+      d[3] = fma2(lop3_and_or(w8, 0x00F000F0u, M2), inv16, nz16, T());
+    } else {
+      d[0] = sub2(lop3_and_or(w, 0x000F000Fu, M2), zz, T());
+      d[1] = sub2(lop3_and_or(w >> 4, 0x000F000Fu, M2), zz, T());
+      d[2] = sub2(lop3_and_or(w >> 8, 0x000F000Fu, M2), zz, T());
+      d[3] = sub2(lop3_and_or(w >> 12, 0x000F000Fu, M2), zz, T());
+    }
+  }
+};
+
+template <typename T>
+struct DiffPairs<T, 2> {
+  static constexpr int kPairs = 8;
+  __device__ static __forceinline__ int lo_k(int p) { return p; }
+  __device__ static __forceinline__ int hi_k(int p) { return p + 8; }
+  __device__ static __forceinline__ void run(uint32_t w, int z, uint32_t (&d)[8]) {
+    const uint32_t M2 = F16Traits<T>::kMagic2;
+    const uint32_t zz = splat2<T>(F16Traits<T>::kMagic + static_cast<float>(z));
+#pragma unroll
+    for (int p = 0; p < 8; ++p) d[p] = sub2(lop3_and_or(w >> (2 * p), 0x00030003u, M2), zz, T());
+  }
+};
+
+template <>
+struct DiffPairs<__half, 8> {
+  static constexpr int kPairs = 2;
+  __device__ static __forceinline__ int lo_k(int p) { return p; }
+  __device__ static __forceinline__ int hi_k(int p) { return p + 2; }
+  __device__ static __forceinline__ void run(uint32_t w, int z, uint32_t (&d)[2]) {
+    const uint32_t zz = splat2<__half>(1024.0f + static_cast<float>(z));
+    // bytes (0, 2) and (1, 3) under the 0x64 exponent byte
+    d[0] = sub2(__byte_perm(w, 0x64646464u, 0x4240u), zz, __half());
+    d[1] = sub2(__byte_perm(w, 0x64646464u, 0x4341u), zz, __half());
+  }
+};
+
+// Exact q - z as an fp32 (any width): magic 2^23 has ulp 1.
+__device__ __forceinline__ float diff_f32(uint32_t code, int z) {
+  return __uint_as_float(0x4B000000u | code) - (8388608.0f + static_cast<float>(z));
+}
+
+}  // namespace gptq

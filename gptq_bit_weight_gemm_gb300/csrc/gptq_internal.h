@@ -1,0 +1,56 @@
+// gptq_internal.h -- host-side launch interface between the C ABI (gptq_api.cu) and the
+// kernels.  Not installed; the public interface is include/gptq.h.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace gptq {
+
+// A validated problem: every field checked by the C ABI before a launcher sees it.
+struct Problem {
+  const void* A;             // [M, K] fp16/bf16 (gemm) or nullptr
+  int M, K, N;
+  int dtype;                 // 0 fp16, 1 bf16 (activations / outputs)
+  const int32_t* qweight;    // [K*bits/32, N]
+  const int32_t* qzeros;     // [G, N*bits/32]
+  const void* scales;        // [G, N] fp16
+  const int32_t* g_idx;      // [K] or nullptr
+  int bits;
+  int group;                 // K when the caller passed -1
+  int G;
+  int zero_offset;           // 1 for GPTQv1, 0 for GPTQv2
+  void* out;                 // C [M, N] or W [K, N]
+  unsigned* status;          // device status word of the current device
+};
+
+struct DeviceInfo {
+  int device;
+  int sm_count;
+  int cc_major, cc_minor;
+  size_t smem_optin;         // max dynamic shared memory per block (opt-in)
+};
+
+const DeviceInfo& device_info();   // current device, cached
+
+cudaError_t launch_dequant(const Problem& p, cudaStream_t stream);
+cudaError_t launch_decode(const Problem& p, cudaStream_t stream);
+cudaError_t launch_prefill(const Problem& p, cudaStream_t stream);
+
+struct QuantProblem {
+  const float* W;
+  int K, N, bits, group, G;
+  const int32_t* g_idx;
+  int sym, fmt;
+  int32_t* qweight;
+  int32_t* qzeros;
+  void* scales;
+  unsigned* status;
+};
+cudaError_t launch_quantize(const QuantProblem& q, cudaStream_t stream);
+
+// Largest M handled by the decode (split-K GEMV) kernel.
+constexpr int kDecodeMaxM = 16;
+
+}  // namespace gptq

@@ -1,0 +1,149 @@
+/*
+ * gptq.h -- C ABI of the GB300 (sm_103a) GPTQ mixed-precision GEMM library.
+ *
+ * The library multiplies fp16/bf16 activations by 2/3/4/8-bit GPTQ weights packed in int32
+ * words, dequantizing group-wise with  w = (q - zero) * scale.  It follows the page
+ * "增强 vLLM 对 GPTQv2 格式的支持：分析与实现" (xxxxyu.github.io):
+ *   section "LLM 的权重量化"             quantizer, its inverse w_hat = (q - zero) * scale,
+ *                                        symmetric zero round((2^b - 1) / 2);
+ *   section "从 GPTQv1 到 GPTQv2"         v1 checkpoints store clamp(zero - 1) and add 1 at run
+ *                                        time, v2 checkpoints store zero; v1 -> v2 is lossless;
+ *   section "调整细节：根据格式选择处理方式" the gptq_gemm op takes a use_v2_format flag and
+ *                                        adds zero_offset = use_v2_format ? 0 : 1 to the
+ *                                        unpacked zeros.
+ *
+ * Layouts (all row-major, contiguous, no padding between rows):
+ *   A        [M, K]             fp16 or bf16 activations (a_dtype)
+ *   qweight  [K * bits / 32, N] int32; column n is an LSB-first bit stream of its K codes:
+ *                               code k occupies stream bits [bits*k, bits*k + bits), the
+ *                               stream's words being qweight[0][n], qweight[1][n], ...
+ *                               (2/4/8-bit: 16/8/4 codes per word; 3-bit: 32 codes in
+ *                               every 3 consecutive words, two codes straddling words)
+ *   qzeros   [G, N * bits / 32] int32; row g is an LSB-first stream of the N stored zeros
+ *   scales   [G, N]             fp16
+ *   g_idx    [K]                int32 group of each input row (act-order), or NULL
+ *   C        [M, N]             same dtype as A
+ *   W        [K, N]             dequantized weights (fp16 or bf16)
+ * where G = K / group, or G = 1 when group == -1 (one group spanning all rows).
+ * Words are bit patterns (read as uint32).  The runtime zero is stored + 1 for
+ * GPTQ_FMT_V1 and stored for GPTQ_FMT_V2, in plain integer arithmetic.
+ *
+ * Shapes the library accepts: K > 0 and N > 0, both multiples of 32; group == -1 or a
+ * positive divisor of K; g_idx only with group != -1, every entry in [0, G).  M >= 0;
+ * M == 0 is a no-op.
+ *
+ * Ownership: the caller allocates and frees every buffer.  Device entry points take device
+ * pointers, must be 16-byte aligned (g_idx: 4-byte), and run asynchronously on `stream`
+ * (a cudaStream_t; NULL = legacy default stream) on the current device.  The library keeps
+ * only a per-device status word and per-device launch attributes; it never allocates device
+ * memory in these calls.
+ *
+ * Errors: every entry point returns GPTQ_OK (0) or a negative gptq_status from host-side
+ * validation or a failed launch; nothing is launched when validation fails.  Kernels never
+ * trap: a bounded wait that runs out, or an act-order index outside [0, G), sets a bit in
+ * the device status word, read and cleared by gptq_get_device_status().
+ */
+#ifndef GPTQ_GB300_H
+#define GPTQ_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { GPTQ_FMT_V1 = 1, GPTQ_FMT_V2 = 2 } gptq_fmt;
+typedef enum { GPTQ_F16 = 0, GPTQ_BF16 = 1 } gptq_dtype;
+
+typedef enum {
+  GPTQ_OK = 0,
+  GPTQ_ERR_ARG = -1,            /* NULL required pointer, bits/fmt/dtype/sym out of range */
+  GPTQ_ERR_SHAPE = -2,          /* K/N not multiples of 32, group does not divide K, g_idx
+                                   with group == -1, negative M, too many groups           */
+  GPTQ_ERR_ALIGN = -3,          /* a pointer not 16-byte aligned (g_idx: 4-byte)            */
+  GPTQ_ERR_WORKSPACE = -4,      /* workspace smaller than gptq_gemm_workspace_size()        */
+  GPTQ_ERR_ZERO_OVERFLOW = -5,  /* v1 -> v2 repack of a stored zero equal to 2^bits - 1     */
+  GPTQ_ERR_CUDA = -6,           /* a CUDA runtime call or launch failed                     */
+  GPTQ_ERR_UNSUPPORTED = -7,    /* the current device is not a Blackwell sm_10x part        */
+  GPTQ_ERR_DEVICE = -8          /* the device status word reported an error                 */
+} gptq_status;
+
+/* Bits of the device status word (see gptq_get_device_status). */
+#define GPTQ_DEV_TIMEOUT 0x1u     /* a bounded wait inside a kernel ran out; output invalid */
+#define GPTQ_DEV_GIDX_RANGE 0x2u  /* an act-order g_idx entry was outside [0, G)            */
+#define GPTQ_DEV_SCALE_OVERFLOW 0x4u /* gptq_quantize_rtn: a group's scale overflowed fp16   */
+
+/*
+ * gptq_dequant -- write the dequantized weights W[k][n] = RN((q - zero) * scale).
+ * Page section "LLM 的权重量化" (w_hat = (q - zero) * scale) and the reconstruct kernel in
+ * "调整细节：根据格式选择处理方式" (zeros[i] + zero_offset).  The product is taken in fp32,
+ * where it is exact, and rounded once, to nearest-even, to out_dtype, so W is bit-exact.
+ * Device pointers: qweight, qzeros, scales, g_idx (nullable), W_out [K, N].
+ * Returns GPTQ_OK or a negative gptq_status.  An out-of-range g_idx entry is clamped to
+ * [0, G) and flagged with GPTQ_DEV_GIDX_RANGE.
+ */
+int gptq_dequant(const int32_t* qweight, const int32_t* qzeros, const void* scales,
+                 const int32_t* g_idx, int K, int N, int bits, int group, int fmt,
+                 int out_dtype, void* W_out, void* stream);
+
+/*
+ * gptq_gemm -- C[M, N] = A[M, K] @ W[K, N] with W dequantized on the fly, the operation
+ * vLLM's gptq_gemm(..., use_v2_format) performs (page section "调整细节：根据格式选择处理
+ * 方式"; fmt == GPTQ_FMT_V2 is use_v2_format = true).  Products are accumulated in fp32 and
+ * C is rounded once to A's dtype.  M <= 16 runs the memory-bound decode kernel (split-K
+ * over a thread-block cluster, reduced through distributed shared memory); larger M runs
+ * the tcgen05 tensor-core kernel.
+ * Device pointers: A, qweight, qzeros, scales, g_idx (nullable), C.  `workspace` may be NULL
+ * when gptq_gemm_workspace_size() returns 0 (every current path); otherwise it must be a
+ * device buffer of at least that many bytes, owned by the caller.
+ * Returns GPTQ_OK or a negative gptq_status.
+ */
+int gptq_gemm(const void* A, int M, int K, int a_dtype, const int32_t* qweight,
+              const int32_t* qzeros, const void* scales, const int32_t* g_idx, int N, int bits,
+              int group, int fmt, void* C, void* workspace, size_t workspace_bytes,
+              void* stream);
+
+/* Bytes of device workspace gptq_gemm needs for this problem (0 for every current path). */
+size_t gptq_gemm_workspace_size(int M, int K, int N, int bits, int group);
+
+/*
+ * gptq_repack_zeros_v1_to_v2 -- HOST function: rewrite a v1 qzeros array ([G, N*bits/32],
+ * host memory) as v2 by adding 1 to every stored field (page section "从 GPTQv1 到 GPTQv2":
+ * the conversion is lossless).  A v1 field of 2^bits - 1 has no v2 encoding: the call then
+ * returns GPTQ_ERR_ZERO_OVERFLOW and leaves qz_v2 unchanged.  qz_v1 and qz_v2 may alias.
+ */
+int gptq_repack_zeros_v1_to_v2(const int32_t* qz_v1, int32_t* qz_v2, int G, int N, int bits);
+
+/*
+ * gptq_quantize_rtn -- write a GPTQ checkpoint from fp32 weights on the device with the
+ * page's round-to-nearest quantizer (section "LLM 的权重量化"):
+ *   asymmetric: scale = (wmax - wmin) / (2^b - 1), zero = clamp(-round(wmin / scale)),
+ *   symmetric:  scale = 2 max|w| / (2^b - 1),      zero = round((2^b - 1) / 2),
+ *   q = clamp(round(w / scale) + zero, 0, 2^b - 1),
+ * over each group of rows (rows k with g_idx[k] == g when g_idx is given).  The scale is
+ * computed in fp32 and stored as fp16; zero and q use the stored scale; round is
+ * half-to-even; a scale that rounds to 0 is stored as 1.  fmt == GPTQ_FMT_V1 stores
+ * clamp(zero - 1) (section "从 GPTQv1 到 GPTQv2").
+ * Device pointers: W [K, N] fp32, g_idx (nullable), qweight, qzeros, scales (outputs).
+ * Returns GPTQ_OK or a negative gptq_status.
+ */
+int gptq_quantize_rtn(const float* W, int K, int N, int bits, int group, const int32_t* g_idx,
+                      int sym, int fmt, int32_t* qweight, int32_t* qzeros, void* scales,
+                      void* stream);
+
+/*
+ * gptq_get_device_status -- synchronize `stream`, then read and clear the current device's
+ * status word (GPTQ_DEV_* bits; 0 = no error since the last call).  Returns GPTQ_OK, or
+ * GPTQ_ERR_CUDA if the synchronize or the read failed.
+ */
+int gptq_get_device_status(void* stream, unsigned int* out);
+
+/* Human-readable name of a gptq_status code (static string). */
+const char* gptq_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GPTQ_GB300_H */

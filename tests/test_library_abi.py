@@ -1,0 +1,109 @@
+"""The C-ABI library: it loads, exports every function include/gptq.h declares, and its host-only
+paths (argument validation, the v1 -> v2 zero repack, error strings) behave as documented.
+No compute call is made here: these tests run without a GPU."""
+import ctypes
+
+import numpy as np
+import pytest
+
+import gptq_bit_weight_gemm_gb300 as g
+import oracle
+from gptq_bit_weight_gemm_gb300 import build as lib_build
+
+
+@pytest.fixture(scope="module")
+def lib():
+    lib_build.build()
+    return g.lib()
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = g.header_functions()
+    assert declared == sorted(["gptq_dequant", "gptq_gemm", "gptq_gemm_workspace_size",
+                               "gptq_repack_zeros_v1_to_v2", "gptq_quantize_rtn",
+                               "gptq_get_device_status", "gptq_strerror"])
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_strerror_and_workspace(lib):
+    for code in range(0, -9, -1):
+        assert g.strerror(code).startswith(g._STATUS[code])
+    assert g.workspace_size(1, 4096, 11008, 4, 128) == 0
+
+
+P = ctypes.c_void_p
+FAKE = P(0x10000)   # never dereferenced: validation fails before any device work
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(bits=5), -1), (dict(bits=1), -1), (dict(fmt=3), -1), (dict(dtype=2), -1),
+    (dict(K=48), -2), (dict(N=40), -2), (dict(group=96), -2), (dict(group=0), -2),
+    (dict(group=-1, g_idx=FAKE), -2), (dict(M=-1), -2),
+    (dict(qweight=P(0x10004)), -3), (dict(A=P(0x10008)), -3),
+    (dict(qweight=None), -1),
+])
+def test_gemm_validation_without_gpu(lib, kw, code):
+    a = dict(A=FAKE, M=1, K=256, dtype=0, qweight=FAKE, qzeros=FAKE, scales=FAKE, g_idx=None,
+             N=256, bits=4, group=128, fmt=2, C=FAKE)
+    a.update(kw)
+    rc = lib.gptq_gemm(a["A"], a["M"], a["K"], a["dtype"], a["qweight"], a["qzeros"], a["scales"],
+                       a["g_idx"], a["N"], a["bits"], a["group"], a["fmt"], a["C"], None, 0, None)
+    assert rc == code
+
+
+def test_gemm_m0_is_noop(lib):
+    rc = lib.gptq_gemm(None, 0, 256, 0, FAKE, FAKE, FAKE, None, 256, 4, 128, 2, None, None, 0, None)
+    assert rc == 0
+
+
+def test_dequant_and_quantize_validation_without_gpu(lib):
+    assert lib.gptq_dequant(FAKE, FAKE, FAKE, None, 256, 256, 4, 128, 2, 5, FAKE, None) == -1
+    assert lib.gptq_dequant(FAKE, FAKE, FAKE, None, 256, 256, 4, 100, 2, 0, FAKE, None) == -2
+    assert lib.gptq_dequant(FAKE, FAKE, FAKE, None, 256, 256, 4, 128, 2, 0, P(0x10002), None) == -3
+    assert lib.gptq_quantize_rtn(FAKE, 256, 256, 4, 128, None, 2, 2, FAKE, FAKE, FAKE, None) == -1
+    assert lib.gptq_quantize_rtn(None, 256, 256, 4, 128, None, 0, 2, FAKE, FAKE, FAKE, None) == -1
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4, 8])
+def test_host_repack_matches_oracle(lib, bits):
+    rng = np.random.default_rng(bits)
+    G, N = 7, 96
+    z = rng.integers(0, (1 << bits) - 1, (G, N)).astype(np.int32)   # never 2^b - 1
+    qz_v1 = oracle.pack_n(z, bits)
+    got = g.repack_zeros_v1_to_v2(qz_v1, N, bits)
+    assert np.array_equal(got, oracle.repack_v1_to_v2(qz_v1, G, N, bits))
+    assert np.array_equal(oracle.unpack_n(got, G, N, bits), z + 1)
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4, 8])
+def test_host_repack_overflow(lib, bits):
+    z = np.zeros((2, 64), np.int32)
+    z[1, 37] = (1 << bits) - 1
+    qz = oracle.pack_n(z, bits)
+    before = qz.copy()
+    rc = lib.gptq_repack_zeros_v1_to_v2(qz.ctypes.data_as(P), qz.ctypes.data_as(P), 2, 64, bits)
+    assert rc == -5
+    assert np.array_equal(qz, before)    # left unchanged (in place)
+    with pytest.raises(g.GPTQError):
+        g.repack_zeros_v1_to_v2(qz, 64, bits)
+
+
+def test_host_repack_in_place(lib):
+    z = np.arange(64, dtype=np.int32).reshape(1, 64) % 15
+    qz = oracle.pack_n(z, 4)
+    rc = lib.gptq_repack_zeros_v1_to_v2(qz.ctypes.data_as(P), qz.ctypes.data_as(P), 1, 64, 4)
+    assert rc == 0
+    assert np.array_equal(oracle.unpack_n(qz, 1, 64, 4), z + 1)
+
+
+def test_product_does_not_import_oracle():
+    import os
+    import re
+    pkg = os.path.dirname(g.__file__)
+    for root, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(root, f)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), f
+                assert "gptq_oracle" not in text, f
