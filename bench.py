@@ -186,14 +186,15 @@ def run_ours(args, rank, world, local_rank):
     main_graph = capture(R)
     rem_graphs = {}
 
+    for n in (args.warmup, args.steps):   # every graph is captured before anything is timed
+        if n % R and n % R not in rem_graphs:
+            rem_graphs[n % R] = capture(n % R)
+
     def run_steps(n):
         for _ in range(n // R):
             main_graph.replay()
-        r = n % R
-        if r:
-            if r not in rem_graphs:
-                rem_graphs[r] = capture(r)
-            rem_graphs[r].replay()
+        if n % R:
+            rem_graphs[n % R].replay()
 
     uuid = "GPU-" + str(props.uuid) if hasattr(props, "uuid") else str(local_rank)
     sampler = ClockSampler(uuid)

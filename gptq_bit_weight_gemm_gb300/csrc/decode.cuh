@@ -6,19 +6,24 @@
 // GEMM case and lists "improve gptq_gemm decode speed" as follow-up work.  Every weight is read
 // from HBM exactly once, so the kernel is built to stream qweight at full bandwidth:
 //
-//  * grid = (cluster of CS CTAs along K) x (slabs of 128 columns).  Each lane owns 4 adjacent
-//    columns, so one 16-byte load brings in one packed unit row for all of them; a warp reads
-//    512 contiguous bytes per row.  The CTAs of a cluster and the 8 warps of a CTA split the
-//    K units (split-K) into contiguous ranges; loads are double-buffered in registers.
-//  * q - zero is built exactly as a 16-bit float (magic-number unpack) and multiplied with the
-//    activation by a mixed-precision fma (f16/bf16 x f16/bf16 + f32 -> f32), so products are
-//    exact and sums are fp32.  Within a quantization group the scale is factored out:
-//    acc += scale * sum_k a_k (q_k - zero).  Act-order (g_idx) and the widths without a 16-bit
-//    unpack (3-bit, bf16 8-bit) take the general path: w = (q - zero) * scale in fp32 (exact)
+//  * grid = (cluster of CS CTAs along K) x (slabs of 128 columns), 4 warps per CTA.  Each lane
+//    owns 4 adjacent columns, so one 16-byte load brings in one packed unit row for all of them
+//    and a warp reads 512 contiguous bytes per row.  The CTAs of a cluster and the warps of a
+//    CTA split the K units (split-K) into contiguous ranges; loads are double-buffered in
+//    registers and the first ones are issued before the activations are staged.
+//  * 16-bit path (M <= 4, fp16 any of 2/4/8 bits, bf16 2/4 bits, no act-order): q - zero is
+//    built exactly as a pair of 16-bit floats (magic-number unpack, one sub/fma with a per-group
+//    constant), multiplied by the activation pair and summed with one fp16x2/bf16x2 fma per pair;
+//    the 16-bit partial sums are flushed into fp32 after every unit (bf16) or every 4 units
+//    (fp16), and the scale is applied once per group: acc += scale * sum_k a_k (q_k - zero).
+//  * fp32 path (act-order, 3-bit, bf16 8-bit, M > 4): w = (q - zero) * scale in fp32 (exact)
 //    and fp32 fmas.
 //  * partial sums are reduced across warps in shared memory and across the cluster through
 //    distributed shared memory, in a fixed order (deterministic), then rounded once to the
 //    output dtype.  No global workspace and no atomics.
+//  * programmatic dependent launch: each CTA lets the next kernel in the stream start launching
+//    at once, and waits (griddepcontrol.wait) for the previous kernel before touching global
+//    memory, so launch latency overlaps the previous kernel's tail.
 #pragma once
 
 #include <cooperative_groups.h>
@@ -31,7 +36,7 @@ namespace decode {
 
 namespace cg = cooperative_groups;
 
-constexpr int kWarps = 8;
+constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kSlab = 128;    // columns per CTA (4 per lane)
 constexpr int kBatch = 4;     // units per load stage
@@ -89,15 +94,19 @@ __device__ __forceinline__ uint32_t unit_code(const uint4 (&u)[Pack<BITS>::kRows
   }
 }
 
-template <int BITS, int MT, typename T, bool FACTORED, bool ACT>
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <int BITS, int MT, typename T, bool HALF, bool ACT>
 __global__ void __launch_bounds__(kThreads) k_decode(const Args a) {
   using P = Pack<BITS>;
   constexpr int PER = P::kPerUnit;
   constexpr int ROWS = P::kRowsPerUnit;
-  using AT = typename std::conditional<FACTORED, T, float>::type;   // staged activation type
   extern __shared__ __align__(16) unsigned char smem[];
-  AT* sA = reinterpret_cast<AT*>(smem);
 
+  pdl_launch_dependents();
   cg::cluster_group cluster = cg::this_cluster();
   const int cs = static_cast<int>(gridDim.x);   // grid x == cluster x
   const int rank = static_cast<int>(blockIdx.x);
@@ -108,49 +117,14 @@ __global__ void __launch_bounds__(kThreads) k_decode(const Args a) {
 
   int cu0, cu1;
   split(a.units, cs, rank, cu0, cu1);
-  const int kbase = cu0 * PER;
-  const int kcount = (cu1 - cu0) * PER;
-
-  // Stage this CTA's activations as sA[k - kbase][m]; rows m >= M are zero.
-  const T* A = static_cast<const T*>(a.A);
-  for (int i = threadIdx.x; i < kcount * MT; i += kThreads) {
-    const int m = i / kcount, kk = i - m * kcount;
-    AT v;
-    if constexpr (FACTORED) {
-      v = m < a.M ? A[static_cast<long long>(m) * a.K + kbase + kk] : F16Traits<T>::from_f32(0.f);
-    } else {
-      v = m < a.M ? F16Traits<T>::to_f32(A[static_cast<long long>(m) * a.K + kbase + kk]) : 0.f;
-    }
-    sA[kk * MT + m] = v;
-  }
-  __syncthreads();
-
   int wu0, wu1;
   split(cu1 - cu0, kWarps, warp, wu0, wu1);
   wu0 += cu0;
   wu1 += cu0;
 
-  float acc[MT][4];
-#pragma unroll
-  for (int m = 0; m < MT; ++m)
-#pragma unroll
-    for (int c = 0; c < 4; ++c) acc[m][c] = 0.f;
-
-  float accg[FACTORED ? MT : 1][4];
-  float s[4];
-  int z[4];
-  int cur_g = -1;
-  if constexpr (FACTORED) {
-#pragma unroll
-    for (int m = 0; m < MT; ++m)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) accg[m][c] = 0.f;
-  }
-
   const int32_t* qw = a.qweight + n0;
   const long long row_stride = a.N;
   uint4 cur[kBatch][ROWS], nxt[kBatch][ROWS];
-
   auto load = [&](uint4 (&dst)[kBatch][ROWS], int ufirst) {
 #pragma unroll
     for (int b = 0; b < kBatch; ++b)
@@ -164,65 +138,139 @@ __global__ void __launch_bounds__(kThreads) k_decode(const Args a) {
       }
   };
 
-  load(cur, wu0);
-  for (int ub = wu0; ub < wu1; ub += kBatch) {
-    if (ub + kBatch < wu1) load(nxt, ub + kBatch);
+  pdl_wait();            // the previous kernel's writes are visible from here on
+  load(cur, wu0);        // first weights in flight while the activations are staged
+
+  const T* A = static_cast<const T*>(a.A);
+  const int kbase = cu0 * PER;
+  const int ucount = cu1 - cu0;
+
+  float acc[MT][4];
 #pragma unroll
-    for (int b = 0; b < kBatch; ++b) {
-      const int u = ub + b;
-      if (u >= wu1) break;
-      const int k0 = u * PER;
-      const int kk0 = k0 - kbase;
-      if constexpr (FACTORED) {
-        const int g = k0 / a.group;
+  for (int m = 0; m < MT; ++m)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc[m][c] = 0.f;
+
+  if constexpr (HALF) {
+    // ---------------------------------------------------------------- 16-bit path
+    using DP = DiffPairs<T, BITS>;
+    constexpr int NP = DP::kPairs;
+    constexpr bool kFlushEveryUnit = std::is_same<T, __nv_bfloat16>::value;
+    // activation pairs: sAP[(unit * NP + p) * MT + m] = (a[m][k0 + lo_k(p)], a[m][k0 + hi_k(p)])
+    uint32_t* sAP = reinterpret_cast<uint32_t*>(smem);
+    const uint16_t* A16 = reinterpret_cast<const uint16_t*>(A);
+    for (int i = threadIdx.x; i < ucount * NP * MT; i += kThreads) {
+      const int m = i % MT, up = i / MT, p = up % NP, uu = up / NP;
+      uint32_t v = 0u;
+      if (m < a.M) {
+        const long long row = static_cast<long long>(m) * a.K + kbase + uu * PER;
+        v = static_cast<uint32_t>(A16[row + DP::lo_k(p)]) |
+            (static_cast<uint32_t>(A16[row + DP::hi_k(p)]) << 16);
+      }
+      sAP[i] = v;
+    }
+    __syncthreads();
+
+    float accg[MT][4];
+    uint32_t acch[MT][4];
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) { accg[m][c] = 0.f; acch[m][c] = 0u; }
+    float s[4];
+    uint32_t kz[4][DP::kConsts];
+    int cur_g = -1;
+
+    auto flush = [&]() {
+#pragma unroll
+      for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          accg[m][c] += sum2_f32(acch[m][c], T());
+          acch[m][c] = 0u;
+        }
+    };
+    auto fold = [&]() {
+#pragma unroll
+      for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          acc[m][c] = fmaf(s[c], accg[m][c], acc[m][c]);
+          accg[m][c] = 0.f;
+        }
+    };
+
+    for (int ub = wu0; ub < wu1; ub += kBatch) {
+      if (ub + kBatch < wu1) load(nxt, ub + kBatch);
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        const int u = ub + b;
+        if (u >= wu1) break;
+        const int g = (u * PER) / a.group;
         if (g != cur_g) {
-          if (cur_g >= 0) {
+          if (cur_g >= 0) { flush(); fold(); }
+          if (col_ok) {
+            int z[4];
+            load_sz<BITS>(a, g, n0, s, z);
 #pragma unroll
-            for (int m = 0; m < MT; ++m)
-#pragma unroll
-              for (int c = 0; c < 4; ++c) {
-                acc[m][c] = fmaf(s[c], accg[m][c], acc[m][c]);
-                accg[m][c] = 0.f;
-              }
+            for (int c = 0; c < 4; ++c) DP::consts(z[c], kz[c]);
           }
-          if (col_ok) load_sz<BITS>(a, g, n0, s, z);
           cur_g = g;
         }
-        // activations of this unit: PER x MT 16-bit values, contiguous in shared memory
-        constexpr int kWords = PER * MT / 2;
-        uint32_t av[kWords];
-        const uint32_t* src = reinterpret_cast<const uint32_t*>(sA + kk0 * MT);
-        if constexpr (kWords % 4 == 0) {
+        uint32_t ap[NP * MT];
+        const uint32_t* src = sAP + (u - cu0) * NP * MT;
+        if constexpr ((NP * MT) % 4 == 0) {
 #pragma unroll
-          for (int i = 0; i < kWords / 4; ++i) {
+          for (int i = 0; i < NP * MT / 4; ++i) {
             const uint4 v = reinterpret_cast<const uint4*>(src)[i];
-            av[4 * i] = v.x; av[4 * i + 1] = v.y; av[4 * i + 2] = v.z; av[4 * i + 3] = v.w;
+            ap[4 * i] = v.x; ap[4 * i + 1] = v.y; ap[4 * i + 2] = v.z; ap[4 * i + 3] = v.w;
           }
         } else {
 #pragma unroll
-          for (int i = 0; i < kWords / 2; ++i) {
+          for (int i = 0; i < NP * MT / 2; ++i) {
             const uint2 v = reinterpret_cast<const uint2*>(src)[i];
-            av[2 * i] = v.x; av[2 * i + 1] = v.y;
+            ap[2 * i] = v.x; ap[2 * i + 1] = v.y;
           }
         }
-        auto a16 = [&](int j, int m) -> uint16_t {
-          const int e = j * MT + m;
-          return (e & 1) ? hi16(av[e >> 1]) : lo16(av[e >> 1]);
-        };
-        using DP = DiffPairs<T, BITS>;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          uint32_t d[DP::kPairs];
-          DP::run((&cur[b][0].x)[c], z[c], d);
+          uint32_t d[NP];
+          DP::run((&cur[b][0].x)[c], kz[c], d);
 #pragma unroll
-          for (int p = 0; p < DP::kPairs; ++p)
+          for (int p = 0; p < NP; ++p)
 #pragma unroll
-            for (int m = 0; m < MT; ++m) {
-              accg[m][c] = fma_mix(a16(DP::lo_k(p), m), lo16(d[p]), accg[m][c], T());
-              accg[m][c] = fma_mix(a16(DP::hi_k(p), m), hi16(d[p]), accg[m][c], T());
-            }
+            for (int m = 0; m < MT; ++m) acch[m][c] = fma2(ap[p * MT + m], d[p], acch[m][c], T());
         }
-      } else {
+        if (kFlushEveryUnit) flush();
+      }
+      if (!kFlushEveryUnit) flush();
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b)
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r) cur[b][r] = nxt[b][r];
+    }
+    if (cur_g >= 0) { flush(); fold(); }
+  } else {
+    // ---------------------------------------------------------------- fp32 path
+    float* sA = reinterpret_cast<float*>(smem);   // sA[(k - kbase) * MT + m]
+    const int kcount = ucount * PER;
+    for (int i = threadIdx.x; i < kcount * MT; i += kThreads) {
+      const int m = i / kcount, kk = i - m * kcount;
+      sA[kk * MT + m] =
+          m < a.M ? F16Traits<T>::to_f32(A[static_cast<long long>(m) * a.K + kbase + kk]) : 0.f;
+    }
+    __syncthreads();
+    float s[4];
+    int z[4];
+    int cur_g = -1;
+    for (int ub = wu0; ub < wu1; ub += kBatch) {
+      if (ub + kBatch < wu1) load(nxt, ub + kBatch);
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        const int u = ub + b;
+        if (u >= wu1) break;
+        const int k0 = u * PER;
+        const int kk0 = k0 - kbase;
 #pragma unroll 4
         for (int j = 0; j < PER; ++j) {
           const int k = k0 + j;
@@ -243,23 +291,15 @@ __global__ void __launch_bounds__(kThreads) k_decode(const Args a) {
           }
         }
       }
-    }
 #pragma unroll
-    for (int b = 0; b < kBatch; ++b)
+      for (int b = 0; b < kBatch; ++b)
 #pragma unroll
-      for (int r = 0; r < ROWS; ++r) cur[b][r] = nxt[b][r];
-  }
-  if constexpr (FACTORED) {
-    if (cur_g >= 0) {
-#pragma unroll
-      for (int m = 0; m < MT; ++m)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) acc[m][c] = fmaf(s[c], accg[m][c], acc[m][c]);
+        for (int r = 0; r < ROWS; ++r) cur[b][r] = nxt[b][r];
     }
   }
 
   // ---- reduction: warps (shared memory), then the cluster (distributed shared memory)
-  __syncthreads();   // every warp is done reading sA
+  __syncthreads();   // every warp is done reading the staged activations
   float* red = reinterpret_cast<float*>(smem);   // [kWarps][MT][kSlab]
 #pragma unroll
   for (int m = 0; m < MT; ++m)
@@ -289,15 +329,19 @@ __global__ void __launch_bounds__(kThreads) k_decode(const Args a) {
 }
 
 // Shared memory bytes for one CTA.
-template <int BITS, int MT, bool FACTORED>
-constexpr size_t smem_bytes(int units_per_cta) {
-  const size_t stage = static_cast<size_t>(units_per_cta) * Pack<BITS>::kPerUnit * MT *
-                       (FACTORED ? 2 : 4);
+template <int BITS, int MT, typename T, bool HALF>
+size_t smem_bytes(int units_per_cta) {
+  size_t stage;
+  if constexpr (HALF) {
+    stage = static_cast<size_t>(units_per_cta) * DiffPairs<T, BITS>::kPairs * MT * 4;
+  } else {
+    stage = static_cast<size_t>(units_per_cta) * Pack<BITS>::kPerUnit * MT * 4;
+  }
   const size_t red = static_cast<size_t>(kWarps) * MT * kSlab * 4;
   return stage > red ? stage : red;
 }
 
-template <int BITS, int MT, typename T, bool FACTORED, bool ACT>
+template <int BITS, int MT, typename T, bool HALF, bool ACT>
 cudaError_t launch_one(const Problem& p, int cs, cudaStream_t stream) {
   Args a;
   a.A = p.A; a.M = p.M; a.K = p.K; a.N = p.N;
@@ -309,8 +353,8 @@ cudaError_t launch_one(const Problem& p, int cs, cudaStream_t stream) {
   a.C = p.out; a.status = p.status;
   const int slabs = (p.N + kSlab - 1) / kSlab;
   const int units_per_cta = (a.units + cs - 1) / cs;
-  const size_t smem = smem_bytes<BITS, MT, FACTORED>(units_per_cta);
-  auto kern = k_decode<BITS, MT, T, FACTORED, ACT>;
+  const size_t smem = smem_bytes<BITS, MT, T, HALF>(units_per_cta);
+  auto kern = k_decode<BITS, MT, T, HALF, ACT>;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
@@ -321,23 +365,25 @@ cudaError_t launch_one(const Problem& p, int cs, cudaStream_t stream) {
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = cs;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
-// Cluster size: enough warps to fill the GPU (about 16 per SM), at least one unit per warp.
+// Cluster size: enough warps to fill the GPU (about 24 per SM), at least two units per warp.
 inline int choose_cluster(const Problem& p, int per_unit) {
   const int slabs = (p.N + kSlab - 1) / kSlab;
   const int units = p.K / per_unit;
-  const int target = device_info().sm_count * 16;
+  const int target = device_info().sm_count * 24;
   int cs = 1;
-  while (cs < 8 && slabs * cs * kWarps < target && units >= 2 * cs * kWarps) cs *= 2;
+  while (cs < 8 && slabs * cs * kWarps < target && units >= 4 * cs * kWarps) cs *= 2;
   return cs;
 }
 

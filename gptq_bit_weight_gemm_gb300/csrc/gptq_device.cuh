@@ -107,18 +107,6 @@ struct F16Traits<__nv_bfloat16> {
   }
 };
 
-// d = a * b + c with a, b 16-bit floats and c, d fp32: exact product, one rounding.
-__device__ __forceinline__ float fma_mix(uint16_t a, uint16_t b, float c, __half) {
-  float d;
-  asm("fma.rn.f32.f16 %0, %1, %2, %3;" : "=f"(d) : "h"(a), "h"(b), "f"(c));
-  return d;
-}
-__device__ __forceinline__ float fma_mix(uint16_t a, uint16_t b, float c, __nv_bfloat16) {
-  float d;
-  asm("fma.rn.f32.bf16 %0, %1, %2, %3;" : "=f"(d) : "h"(a), "h"(b), "f"(c));
-  return d;
-}
-
 __device__ __forceinline__ uint16_t lo16(uint32_t x) { return static_cast<uint16_t>(x & 0xFFFFu); }
 __device__ __forceinline__ uint16_t hi16(uint32_t x) { return static_cast<uint16_t>(x >> 16); }
 
@@ -157,66 +145,136 @@ __device__ __forceinline__ uint32_t splat2(float x) {
 // ------------------------------------------------------------------------------------------
 // Exact (q - zero) pairs from one packed word, as 16-bit floats.
 //
-// DiffPairs<T, BITS>::run(word, z) fills d[kPairs] with two k values each; pair p holds k
-// indices lo_k(p) (low half) and hi_k(p) (high half) of the word's kPerUnit codes.  z is the
-// runtime zero (stored + offset, up to 256).  Valid for T = __half with every width and for
-// T = __nv_bfloat16 with BITS <= 4 (the code must fit in the 7-bit bf16 mantissa).
+// DiffPairs<T, BITS> turns one packed word into kPairs registers of two 16-bit values each;
+// pair p holds the codes of k = lo_k(p) (low half) and k = hi_k(p) (high half) of the word.
+// The code is OR-ed into the mantissa of a magic number M with unit last place (1024 for fp16,
+// 128 for bf16); a code sitting `sh` bits up reads as M + 2^sh q, and one sub or fma with a
+// per-zero constant (consts(), computed once per group) gives q - zero exactly.  Valid for
+// __half with 2, 4 and 8 bits and for __nv_bfloat16 with 2 and 4 bits.
 // ------------------------------------------------------------------------------------------
 template <typename T, int BITS>
 struct DiffPairs;
 
-template <typename T>
-struct DiffPairs<T, 4> {
-  static constexpr int kPairs = 4;
+__device__ __forceinline__ uint32_t fma2(uint32_t a, uint32_t b, uint32_t c, __nv_bfloat16) {
+  __nv_bfloat162 r = __hfma2(*reinterpret_cast<__nv_bfloat162*>(&a),
+                             *reinterpret_cast<__nv_bfloat162*>(&b),
+                             *reinterpret_cast<__nv_bfloat162*>(&c));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
+template <>
+struct DiffPairs<__half, 4> {
+  static constexpr int kPairs = 4, kConsts = 2;
   __device__ static __forceinline__ int lo_k(int p) { return p; }
   __device__ static __forceinline__ int hi_k(int p) { return p + 4; }
-  __device__ static __forceinline__ void run(uint32_t w, int z, uint32_t (&d)[4]) {
-    const uint32_t M2 = F16Traits<T>::kMagic2;
-    const uint32_t zz = splat2<T>(F16Traits<T>::kMagic + static_cast<float>(z));
-    if constexpr (std::is_same<T, __half>::value) {
-      // fp16: nibble pairs at bits (4p, 4p + 16).  A code at bits 4..7 of a half reads as
-      // 1024 + 16 q, so x * (1/16) - (64 + z) = q - z (exact: one fma, representable result).
-      const uint32_t w8 = w >> 8;
-      const uint32_t nz16 = splat2<T>(-(64.0f + static_cast<float>(z)));
-      const uint32_t inv16 = 0x2C002C00u;   // (1/16, 1/16)
-      d[0] = sub2(lop3_and_or(w, 0x000F000Fu, M2), zz, T());
-      d[1] = fma2(lop3_and_or(w, 0x00F000F0u, M2), inv16, nz16, T());
-      d[2] = sub2(lop3_and_or(w8, 0x000F000Fu, M2), zz, T());
-      d[3] = fma2(lop3_and_or(w8, 0x00F000F0u, M2), inv16, nz16, T());
-    } else {
-      d[0] = sub2(lop3_and_or(w, 0x000F000Fu, M2), zz, T());
-      d[1] = sub2(lop3_and_or(w >> 4, 0x000F000Fu, M2), zz, T());
-      d[2] = sub2(lop3_and_or(w >> 8, 0x000F000Fu, M2), zz, T());
-      d[3] = sub2(lop3_and_or(w >> 12, 0x000F000Fu, M2), zz, T());
+  __device__ static __forceinline__ void consts(int z, uint32_t (&k)[kConsts]) {
+    k[0] = splat2<__half>(1024.0f + static_cast<float>(z));
+    k[1] = splat2<__half>(-(64.0f + static_cast<float>(z)));
+  }
+  __device__ static __forceinline__ void run(uint32_t w, const uint32_t (&k)[kConsts],
+                                             uint32_t (&d)[kPairs]) {
+    const uint32_t M2 = 0x64006400u, inv16 = 0x2C002C00u;
+    const uint32_t w8 = w >> 8;
+    d[0] = sub2(lop3_and_or(w, 0x000F000Fu, M2), k[0], __half());
+    d[1] = fma2(lop3_and_or(w, 0x00F000F0u, M2), inv16, k[1], __half());
+    d[2] = sub2(lop3_and_or(w8, 0x000F000Fu, M2), k[0], __half());
+    d[3] = fma2(lop3_and_or(w8, 0x00F000F0u, M2), inv16, k[1], __half());
+  }
+};
+
+template <>
+struct DiffPairs<__nv_bfloat16, 4> {
+  static constexpr int kPairs = 4, kConsts = 1;
+  __device__ static __forceinline__ int lo_k(int p) { return p; }
+  __device__ static __forceinline__ int hi_k(int p) { return p + 4; }
+  __device__ static __forceinline__ void consts(int z, uint32_t (&k)[kConsts]) {
+    k[0] = splat2<__nv_bfloat16>(128.0f + static_cast<float>(z));
+  }
+  __device__ static __forceinline__ void run(uint32_t w, const uint32_t (&k)[kConsts],
+                                             uint32_t (&d)[kPairs]) {
+    const uint32_t M2 = 0x43004300u;
+    d[0] = sub2(lop3_and_or(w, 0x000F000Fu, M2), k[0], __nv_bfloat16());
+    d[1] = sub2(lop3_and_or(w >> 4, 0x000F000Fu, M2), k[0], __nv_bfloat16());
+    d[2] = sub2(lop3_and_or(w >> 8, 0x000F000Fu, M2), k[0], __nv_bfloat16());
+    d[3] = sub2(lop3_and_or(w >> 12, 0x000F000Fu, M2), k[0], __nv_bfloat16());
+  }
+};
+
+template <>
+struct DiffPairs<__half, 2> {
+  static constexpr int kPairs = 8, kConsts = 4;
+  __device__ static __forceinline__ int lo_k(int p) { return p; }
+  __device__ static __forceinline__ int hi_k(int p) { return p + 8; }
+  __device__ static __forceinline__ void consts(int z, uint32_t (&k)[kConsts]) {
+    k[0] = splat2<__half>(1024.0f + static_cast<float>(z));
+    k[1] = splat2<__half>(-(256.0f + static_cast<float>(z)));
+    k[2] = splat2<__half>(-(64.0f + static_cast<float>(z)));
+    k[3] = splat2<__half>(-(16.0f + static_cast<float>(z)));
+  }
+  __device__ static __forceinline__ void run(uint32_t w, const uint32_t (&k)[kConsts],
+                                             uint32_t (&d)[kPairs]) {
+    const uint32_t M2 = 0x64006400u;
+    const uint32_t inv4 = 0x34003400u, inv16 = 0x2C002C00u, inv64 = 0x24002400u;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t x = h ? (w >> 8) : w;
+      d[4 * h + 0] = sub2(lop3_and_or(x, 0x00030003u, M2), k[0], __half());
+      d[4 * h + 1] = fma2(lop3_and_or(x, 0x000C000Cu, M2), inv4, k[1], __half());
+      d[4 * h + 2] = fma2(lop3_and_or(x, 0x00300030u, M2), inv16, k[2], __half());
+      d[4 * h + 3] = fma2(lop3_and_or(x, 0x00C000C0u, M2), inv64, k[3], __half());
     }
   }
 };
 
-template <typename T>
-struct DiffPairs<T, 2> {
-  static constexpr int kPairs = 8;
+template <>
+struct DiffPairs<__nv_bfloat16, 2> {
+  static constexpr int kPairs = 8, kConsts = 3;
   __device__ static __forceinline__ int lo_k(int p) { return p; }
   __device__ static __forceinline__ int hi_k(int p) { return p + 8; }
-  __device__ static __forceinline__ void run(uint32_t w, int z, uint32_t (&d)[8]) {
-    const uint32_t M2 = F16Traits<T>::kMagic2;
-    const uint32_t zz = splat2<T>(F16Traits<T>::kMagic + static_cast<float>(z));
+  __device__ static __forceinline__ void consts(int z, uint32_t (&k)[kConsts]) {
+    k[0] = splat2<__nv_bfloat16>(128.0f + static_cast<float>(z));
+    k[1] = splat2<__nv_bfloat16>(-(32.0f + static_cast<float>(z)));
+    k[2] = splat2<__nv_bfloat16>(-(8.0f + static_cast<float>(z)));
+  }
+  __device__ static __forceinline__ void run(uint32_t w, const uint32_t (&k)[kConsts],
+                                             uint32_t (&d)[kPairs]) {
+    const uint32_t M2 = 0x43004300u;
+    const uint32_t inv4 = 0x3E803E80u, inv16 = 0x3D803D80u;   // 0.25, 0.0625 in bf16
 #pragma unroll
-    for (int p = 0; p < 8; ++p) d[p] = sub2(lop3_and_or(w >> (2 * p), 0x00030003u, M2), zz, T());
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t x = h ? (w >> 8) : w;
+      d[4 * h + 0] = sub2(lop3_and_or(x, 0x00030003u, M2), k[0], __nv_bfloat16());
+      d[4 * h + 1] = fma2(lop3_and_or(x, 0x000C000Cu, M2), inv4, k[1], __nv_bfloat16());
+      d[4 * h + 2] = fma2(lop3_and_or(x, 0x00300030u, M2), inv16, k[2], __nv_bfloat16());
+      d[4 * h + 3] = sub2(lop3_and_or(x >> 6, 0x00030003u, M2), k[0], __nv_bfloat16());
+    }
   }
 };
 
 template <>
 struct DiffPairs<__half, 8> {
-  static constexpr int kPairs = 2;
+  static constexpr int kPairs = 2, kConsts = 1;
   __device__ static __forceinline__ int lo_k(int p) { return p; }
   __device__ static __forceinline__ int hi_k(int p) { return p + 2; }
-  __device__ static __forceinline__ void run(uint32_t w, int z, uint32_t (&d)[2]) {
-    const uint32_t zz = splat2<__half>(1024.0f + static_cast<float>(z));
+  __device__ static __forceinline__ void consts(int z, uint32_t (&k)[kConsts]) {
+    k[0] = splat2<__half>(1024.0f + static_cast<float>(z));
+  }
+  __device__ static __forceinline__ void run(uint32_t w, const uint32_t (&k)[kConsts],
+                                             uint32_t (&d)[kPairs]) {
     // bytes (0, 2) and (1, 3) under the 0x64 exponent byte
-    d[0] = sub2(__byte_perm(w, 0x64646464u, 0x4240u), zz, __half());
-    d[1] = sub2(__byte_perm(w, 0x64646464u, 0x4341u), zz, __half());
+    d[0] = sub2(__byte_perm(w, 0x64646464u, 0x4240u), k[0], __half());
+    d[1] = sub2(__byte_perm(w, 0x64646464u, 0x4341u), k[0], __half());
   }
 };
+
+// Sum of the two halves of a 16-bit pair, in fp32.
+__device__ __forceinline__ float sum2_f32(uint32_t x, __half) {
+  const float2 f = __half22float2(*reinterpret_cast<__half2*>(&x));
+  return f.x + f.y;
+}
+__device__ __forceinline__ float sum2_f32(uint32_t x, __nv_bfloat16) {
+  return __uint_as_float(x << 16) + __uint_as_float(x & 0xFFFF0000u);
+}
 
 // Exact q - z as an fp32 (any width): magic 2^23 has ulp 1.
 __device__ __forceinline__ float diff_f32(uint32_t code, int z) {

@@ -1,21 +1,458 @@
-// prefill.cu -- large-M path (interim): runs the decode kernel on 16-row slices of A.
+// prefill.cu -- compute-bound GPTQ GEMM for many tokens (M > 16) on the 5th-generation tensor
+// cores: C = A @ dequant(W) with tcgen05.mma (kind::f16, fp32 accumulators in TMEM).
+//
+// The page "增强 vLLM 对 GPTQv2 格式的支持：分析与实现" (section "调整细节：根据格式选择处理方
+// 式") describes gptq_gemm's large-M path as a reconstruct kernel (dequantize with
+// zeros[i] + zero_offset) followed by a GEMM.  Here the reconstruction never leaves the SM: each
+// packed weight tile is dequantized straight into the shared-memory layout the tensor core reads,
+// and a 256 x 256 output tile accumulates over K in tensor memory.
+//
+// Per CTA (persistent, one per SM, 448 threads, warp-specialised):
+//   warp 4      TMA producer: A tile [256 x 64] (128-byte swizzle) and the packed qweight tile
+//               [64 k x 256 n] for each k-step into a 3-stage ring;
+//   warps 6-13  dequantizers: thread n reads column n's packed words, forms
+//               w = RN((q - zero) * scale) exactly (q - zero exact in fp32, one fp32 product,
+//               one rounding to A's dtype) and stores the B tile K-major with the 128-byte
+//               swizzle (2-stage ring), then fence.proxy.async + mbarrier arrive;
+//   warp 5      TMEM owner and MMA issuer: per k-step 4 x 2 tcgen05.mma (M=128, N=256, K=16),
+//               one per 128-row half of A, both reading the same B tile; tcgen05.commit frees
+//               the ring slots and signals the accumulators;
+//   warps 0-3   epilogue: tcgen05.ld of the two 128 x 256 fp32 accumulators (512 TMEM
+//               columns), rounding to A's dtype, direct 64-byte row-segment stores.
+// Every mbarrier wait is bounded (2 s of %globaltimer): on expiry the kernel sets
+// GPTQ_DEV_TIMEOUT in the status word, every role stops, in-flight copies and MMAs are waited
+// for (bounded), TMEM is freed and the CTA exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "gptq_device.cuh"
 #include "gptq_internal.h"
+#include "sm100_ptx.cuh"
 
 namespace gptq {
+namespace prefill {
 
-cudaError_t launch_decode(const Problem& p, cudaStream_t stream);
+constexpr int kBM = 256;            // rows of A per tile (two UMMA M=128 halves)
+constexpr int kBN = 256;            // columns per tile (UMMA N=256)
+constexpr int kBK = 64;             // k per stage: one 128-byte swizzle row of 16-bit values
+constexpr int kStages = 3;          // A + packed-W ring
+constexpr int kBStages = 2;         // dequantized-B ring
+constexpr int kEpiWarps = 4;
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int kDqWarp0 = 6;
+constexpr int kDqWarps = 8;         // one thread per tile column
+constexpr int kThreads = (kDqWarp0 + kDqWarps) * 32;
+constexpr uint32_t kTmemCols = 512; // two 128 x 256 fp32 accumulators
+constexpr uint32_t kATileBytes = kBM * kBK * 2;
+constexpr uint32_t kBTileBytes = kBN * kBK * 2;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+template <int BITS>
+struct Geo {
+  static constexpr int kRows = kBK * BITS / 32;                // qweight rows per k-step
+  static constexpr uint32_t kWBytes = kBN * kRows * 4;         // packed tile bytes
+  static constexpr uint32_t kOffW = kStages * kATileBytes;
+  static constexpr uint32_t kOffB = kOffW + kStages * kWBytes;
+  static constexpr uint32_t kOffBar = kOffB + kBStages * kBTileBytes;
+  // barriers: full[S], empty[S], bfull[BS], bempty[BS], acc_full, acc_empty, drain
+  static constexpr uint32_t kNumBars = 2 * kStages + 2 * kBStages + 3;
+  static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag
+  static constexpr uint32_t kBytes = kOffMisc + 16;
+  static constexpr size_t kDynSmem = kBytes + 1024;             // slack to align the base
+};
+
+struct Args {
+  int M, N, K, group, G, zero_offset, zwords;
+  const int32_t* qzeros;
+  const __half* scales;
+  const int32_t* g_idx;
+  void* C;
+  unsigned* status;
+};
+
+struct Sync {
+  uint32_t base;        // shared address of the aligned dynamic shared memory
+  volatile int* abort;
+  unsigned* status;
+};
+
+// Bounded wait on an mbarrier phase; false if the wait ran out or another role aborted.
+__device__ __forceinline__ bool wait_bar(const Sync& s, uint32_t bar, uint32_t parity) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer();
+  while (true) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (*s.abort) return false;
+    if (ptx::globaltimer() - t0 > kWaitLimitNs) {
+      *s.abort = 1;
+      atomicOr(s.status, kStatusTimeout);
+      return false;
+    }
+  }
+}
+
+// Byte offset of (row, 16-byte chunk) in a K-major tile stored with the 128-byte swizzle.
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+  return static_cast<uint32_t>((row >> 3) * 1024 + (row & 7) * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+// Runtime zero of column n in qzeros row g.
+template <int BITS>
+__device__ __forceinline__ int zero_of(const Args& a, int g, int n) {
+  const int32_t* row = a.qzeros + static_cast<long long>(g) * a.zwords;
+  const int bit = BITS * n;
+  uint32_t v = static_cast<uint32_t>(__ldg(row + (bit >> 5))) >> (bit & 31);
+  if ((bit & 31) + BITS > 32) v |= static_cast<uint32_t>(__ldg(row + (bit >> 5) + 1)) << (32 - (bit & 31));
+  return static_cast<int>(v & Pack<BITS>::kMask) + a.zero_offset;
+}
+
+template <int BITS>
+__device__ __forceinline__ int clamp_group(const Args& a, int k) {
+  if (a.g_idx == nullptr) return k / a.group;
+  int g = __ldg(a.g_idx + k);
+  if (g < 0 || g >= a.G) {
+    atomicOr(a.status, kStatusGidxRange);
+    g = g < 0 ? 0 : a.G - 1;
+  }
+  return g;
+}
+
+// Code j (0..7) of 16-byte chunk c (0..7) of this column's packed words for one k-step.
+template <int BITS>
+__device__ __forceinline__ uint32_t chunk_code(const uint32_t (&w)[Geo<BITS>::kRows], int c, int j) {
+  if constexpr (BITS == 4) {
+    return (w[c] >> (4 * j)) & 15u;
+  } else if constexpr (BITS == 2) {
+    return (w[c >> 1] >> (2 * (8 * (c & 1) + j))) & 3u;
+  } else if constexpr (BITS == 8) {
+    return (w[2 * c + (j >> 2)] >> (8 * (j & 3))) & 255u;
+  } else {
+    const int u = c >> 2;
+    return code3(w[3 * u], w[3 * u + 1], w[3 * u + 2], 8 * (c & 3) + j);
+  }
+}
+
+template <int BITS, typename T, bool PERK>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_prefill(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
+              const Args a) {
+  using Gm = Geo<BITS>;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = ptx::smem_addr(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const uint32_t bar0 = sbase + Gm::kOffBar;
+  auto full = [&](int s) { return bar0 + 8u * s; };
+  auto empty = [&](int s) { return bar0 + 8u * (kStages + s); };
+  auto bfull = [&](int s) { return bar0 + 8u * (2 * kStages + s); };
+  auto bempty = [&](int s) { return bar0 + 8u * (2 * kStages + kBStages + s); };
+  const uint32_t acc_full = bar0 + 8u * (2 * kStages + 2 * kBStages);
+  const uint32_t acc_empty = acc_full + 8u;
+  const uint32_t drain = acc_full + 16u;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Gm::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Gm::kOffMisc + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(full(s), 1);
+      ptx::mbar_init(empty(s), 1 + kDqWarps);
+    }
+    for (int s = 0; s < kBStages; ++s) {
+      ptx::mbar_init(bfull(s), kDqWarps * 32);
+      ptx::mbar_init(bempty(s), 1);
+    }
+    ptx::mbar_init(acc_full, 1);
+    ptx::mbar_init(acc_empty, kEpiWarps);
+    ptx::mbar_init(drain, 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    ptx::prefetch_tmap(&tmA);
+    ptx::prefetch_tmap(&tmW);
+  }
+  if (warp == kMmaWarp) {
+    ptx::tmem_alloc(ptx::smem_addr(tmem_slot), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const Sync sy{sbase, abort_flag, a.status};
+
+  const int num_m = (a.M + kBM - 1) / kBM;
+  const int num_n = (a.N + kBN - 1) / kBN;
+  const int num_tiles = num_m * num_n;
+  const int ksteps = (a.K + kBK - 1) / kBK;
+
+  if (warp == kProducerWarp) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      uint32_t issued = 0, last_par[kStages] = {0, 0, 0};
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+        const int mt = t % num_m, nt = t / num_m;
+        for (int ks = 0; ks < ksteps; ++ks) {
+          if (!wait_bar(sy, empty(s), ph ^ 1u)) { ok = false; break; }
+          ptx::mbar_arrive_expect_tx(full(s), kATileBytes + Gm::kWBytes);
+          ptx::tma_load_2d(sbase + s * kATileBytes, &tmA, ks * kBK, mt * kBM, full(s));
+          ptx::tma_load_2d(sbase + Gm::kOffW + s * Gm::kWBytes, &tmW, nt * kBN, ks * Gm::kRows,
+                           full(s));
+          issued |= 1u << s;
+          last_par[s] = ph;
+          if (++s == kStages) { s = 0; ph ^= 1u; }
+        }
+      }
+      if (!ok) {
+        // let the copies already issued land before the CTA's shared memory goes away
+        const uint64_t t0 = ptx::globaltimer();
+        for (int i = 0; i < kStages; ++i)
+          if (issued & (1u << i))
+            while (!ptx::mbar_try_wait(full(i), last_par[i]) && ptx::globaltimer() - t0 < kWaitLimitNs) {}
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc =
+          ptx::umma_idesc_f16(std::is_same<T, __half>::value ? 0u : 1u, 128u, static_cast<uint32_t>(kBN));
+      int s = 0, sb = 0;
+      uint32_t ph = 0, phb = 0, aph = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+        if (!wait_bar(sy, acc_empty, aph ^ 1u)) { ok = false; break; }
+        ptx::tc_fence_after();
+        for (int ks = 0; ks < ksteps; ++ks) {
+          if (!wait_bar(sy, full(s), ph) || !wait_bar(sy, bfull(sb), phb)) { ok = false; break; }
+          ptx::tc_fence_after();
+          const uint32_t a_addr = sbase + s * kATileBytes;
+          const uint32_t b_addr = sbase + Gm::kOffB + sb * kBTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint64_t bd = ptx::umma_desc_sw128_kmajor(b_addr + kk * 32);
+            const uint32_t acc = (ks | kk) != 0;
+            ptx::umma_f16(tmem, ptx::umma_desc_sw128_kmajor(a_addr + kk * 32), bd, idesc, acc);
+            ptx::umma_f16(tmem + 256, ptx::umma_desc_sw128_kmajor(a_addr + 128 * 128 + kk * 32), bd,
+                          idesc, acc);
+          }
+          ptx::umma_commit(empty(s));
+          ptx::umma_commit(bempty(sb));
+          if (++s == kStages) { s = 0; ph ^= 1u; }
+          if (++sb == kBStages) { sb = 0; phb ^= 1u; }
+        }
+        if (!ok) break;
+        ptx::umma_commit(acc_full);
+        aph ^= 1u;
+      }
+      if (!ok) {
+        // wait (bounded) for the MMAs already issued before TMEM is released
+        ptx::umma_commit(drain);
+        const uint64_t t0 = ptx::globaltimer();
+        while (!ptx::mbar_try_wait(drain, 0) && ptx::globaltimer() - t0 < kWaitLimitNs) {}
+      }
+    }
+  } else if (warp >= kDqWarp0) {
+    // ---------------------------------------------------------------- dequantizers
+    const int col = threadIdx.x - kDqWarp0 * 32;   // 0..255: tile column of this thread
+    const int dq_lane = lane;
+    int s = 0, sb = 0;
+    uint32_t ph = 0, phb = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+      const int nt = t / num_m;
+      const int n = nt * kBN + col;
+      const bool n_ok = n < a.N;
+      int cur_g = -1;
+      float sc = 0.f;
+      int z = 0;
+      for (int ks = 0; ks < ksteps; ++ks) {
+        if (!wait_bar(sy, full(s), ph)) { ok = false; break; }
+        uint32_t w[Gm::kRows];
+        const uint32_t* wt = reinterpret_cast<const uint32_t*>(smem + Gm::kOffW + s * Gm::kWBytes);
+#pragma unroll
+        for (int r = 0; r < Gm::kRows; ++r) w[r] = wt[r * kBN + col];
+        __syncwarp();
+        if (dq_lane == 0) ptx::mbar_arrive(empty(s));
+        if (!wait_bar(sy, bempty(sb), phb ^ 1u)) { ok = false; break; }
+        unsigned char* bt = smem + Gm::kOffB + sb * kBTileBytes;
+#pragma unroll
+        for (int c = 0; c < kBK / 8; ++c) {
+          const int k0 = ks * kBK + c * 8;
+          uint4 out = make_uint4(0u, 0u, 0u, 0u);
+          if (n_ok && k0 < a.K) {
+            float v[8];
+            if constexpr (!PERK) {
+              const int g = k0 / a.group;
+              if (g != cur_g) {
+                sc = __half2float(a.scales[static_cast<long long>(g) * a.N + n]);
+                z = zero_of<BITS>(a, g, n);
+                cur_g = g;
+              }
+#pragma unroll
+              for (int j = 0; j < 8; ++j) v[j] = diff_f32(chunk_code<BITS>(w, c, j), z) * sc;
+            } else {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const int g = clamp_group<BITS>(a, k0 + j);
+                const float sj = __half2float(a.scales[static_cast<long long>(g) * a.N + n]);
+                v[j] = diff_f32(chunk_code<BITS>(w, c, j), zero_of<BITS>(a, g, n)) * sj;
+              }
+            }
+            out.x = pack2(v[0], v[1], T());
+            out.y = pack2(v[2], v[3], T());
+            out.z = pack2(v[4], v[5], T());
+            out.w = pack2(v[6], v[7], T());
+          }
+          *reinterpret_cast<uint4*>(bt + swz(col, c)) = out;
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::mbar_arrive(bfull(sb));
+        if (++s == kStages) { s = 0; ph ^= 1u; }
+        if (++sb == kBStages) { sb = 0; phb ^= 1u; }
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue (warps 0-3)
+    const int q = warp;   // TMEM lanes 32q .. 32q + 31
+    uint32_t aph = 0;
+    T* C = static_cast<T*>(a.C);
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+      const int mt = t % num_m, nt = t / num_m;
+      if (!wait_bar(sy, acc_full, aph)) break;
+      ptx::tc_fence_after();
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        const int m = mt * kBM + half * 128 + q * 32 + lane;
+#pragma unroll 1
+        for (int cc = 0; cc < kBN / 32; ++cc) {
+          uint32_t r[32];
+          ptx::tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + half * 256 + cc * 32, r);
+          ptx::tmem_ld_wait();
+          const int n0 = nt * kBN + cc * 32;
+          if (m < a.M && n0 < a.N) {
+            uint4* dst = reinterpret_cast<uint4*>(C + static_cast<long long>(m) * a.N + n0);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint4 o;
+              o.x = pack2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]), T());
+              o.y = pack2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]), T());
+              o.z = pack2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]), T());
+              o.w = pack2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]), T());
+              dst[v] = o;
+            }
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(acc_empty);
+      aph ^= 1u;
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, []() {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+template <int BITS, typename T, bool PERK>
+cudaError_t launch_typed(const Problem& p, cudaStream_t stream) {
+  using Gm = Geo<BITS>;
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  CUtensorMap tmA, tmW;
+  {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.K), static_cast<cuuint64_t>(p.M)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.K) * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(kBM)};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(&tmA, std::is_same<T, __half>::value ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                          : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                     2, const_cast<void*>(p.A), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t rows = static_cast<cuuint64_t>(p.K) * BITS / 32;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.N), rows};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.N) * 4};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBN), static_cast<cuuint32_t>(Gm::kRows)};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(&tmW, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, const_cast<int32_t*>(p.qweight), dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
+  Args a;
+  a.M = p.M; a.N = p.N; a.K = p.K; a.group = p.group; a.G = p.G; a.zero_offset = p.zero_offset;
+  a.zwords = p.N * BITS / 32;
+  a.qzeros = p.qzeros;
+  a.scales = static_cast<const __half*>(p.scales);
+  a.g_idx = p.g_idx;
+  a.C = p.out;
+  a.status = p.status;
+  auto kern = k_prefill<BITS, T, PERK>;
+  static bool attr_set = false;   // per instantiation; the attribute is per function
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(Gm::kDynSmem));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int tiles = ((p.M + kBM - 1) / kBM) * ((p.N + kBN - 1) / kBN);
+  const int grid = tiles < device_info().sm_count ? tiles : device_info().sm_count;
+  kern<<<grid, kThreads, Gm::kDynSmem, stream>>>(tmA, tmW, a);
+  return cudaGetLastError();
+}
+
+template <int BITS, typename T>
+cudaError_t launch_t(const Problem& p, cudaStream_t stream) {
+  const bool perk = p.g_idx != nullptr || (p.group % 8) != 0;
+  return perk ? launch_typed<BITS, T, true>(p, stream) : launch_typed<BITS, T, false>(p, stream);
+}
+
+template <int BITS>
+cudaError_t launch_bits(const Problem& p, cudaStream_t stream) {
+  return p.dtype == 0 ? launch_t<BITS, __half>(p, stream) : launch_t<BITS, __nv_bfloat16>(p, stream);
+}
+
+}  // namespace prefill
 
 cudaError_t launch_prefill(const Problem& p, cudaStream_t stream) {
-  const size_t es = 2;
-  for (int m0 = 0; m0 < p.M; m0 += kDecodeMaxM) {
-    Problem s = p;
-    s.M = p.M - m0 < kDecodeMaxM ? p.M - m0 : kDecodeMaxM;
-    s.A = static_cast<const char*>(p.A) + static_cast<size_t>(m0) * p.K * es;
-    s.out = static_cast<char*>(p.out) + static_cast<size_t>(m0) * p.N * es;
-    cudaError_t e = launch_decode(s, stream);
-    if (e != cudaSuccess) return e;
+  switch (p.bits) {
+    case 2: return prefill::launch_bits<2>(p, stream);
+    case 3: return prefill::launch_bits<3>(p, stream);
+    case 4: return prefill::launch_bits<4>(p, stream);
+    case 8: return prefill::launch_bits<8>(p, stream);
+    default: return cudaErrorInvalidValue;
   }
-  return cudaSuccess;
 }
 
 }  // namespace gptq
