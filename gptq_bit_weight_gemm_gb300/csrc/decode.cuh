@@ -99,6 +99,10 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 template <int BITS, int MT, typename T, bool HALF, bool ACT>
 __global__ void __launch_bounds__(kThreads) k_decode(const Args a) {
   using P = Pack<BITS>;
@@ -113,7 +117,9 @@ __global__ void __launch_bounds__(kThreads) k_decode(const Args a) {
   const int n_base = static_cast<int>(blockIdx.y) * kSlab;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n0 = n_base + lane * 4;
-  const bool col_ok = n0 < a.N;
+  // Lanes past the last column read the last valid columns (N % 4 == 0) and store nothing:
+  // the hot loop needs no per-lane predicate.
+  const int n0c = n0 < a.N ? n0 : a.N - 4;
 
   int cu0, cu1;
   split(a.units, cs, rank, cu0, cu1);
@@ -122,24 +128,26 @@ __global__ void __launch_bounds__(kThreads) k_decode(const Args a) {
   wu0 += cu0;
   wu1 += cu0;
 
-  const int32_t* qw = a.qweight + n0;
-  const long long row_stride = a.N;
-  uint4 cur[kBatch][ROWS], nxt[kBatch][ROWS];
+  const long long ustride = static_cast<long long>(ROWS) * a.N;   // words between units
+  const int32_t* qw = a.qweight + n0c;
+  auto unit_ptr = [&](int u, int r) { return qw + u * ustride + static_cast<long long>(r) * a.N; };
   auto load = [&](uint4 (&dst)[kBatch][ROWS], int ufirst) {
 #pragma unroll
     for (int b = 0; b < kBatch; ++b)
 #pragma unroll
-      for (int r = 0; r < ROWS; ++r) {
-        const int u = ufirst + b;
-        if (col_ok && u < wu1)
-          dst[b][r] = ld_stream_v4(qw + (static_cast<long long>(u) * ROWS + r) * row_stride);
-        else
-          dst[b][r] = make_uint4(0u, 0u, 0u, 0u);
-      }
+      for (int r = 0; r < ROWS; ++r)
+        if (ufirst + b < wu1) dst[b][r] = ld_stream_v4(unit_ptr(ufirst + b, r));
   };
 
+  // Weights are never written by the kernel this one may overlap with through programmatic
+  // launch -- and even if they were, L2 is the coherence point -- so warming L2 with this warp's
+  // first rows before griddepcontrol.wait is safe; every real load happens after the wait.
+  for (int u = wu0; u < wu1 && u < wu0 + 4 * kBatch; ++u)
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r) prefetch_l2(unit_ptr(u, r));
   pdl_wait();            // the previous kernel's writes are visible from here on
-  load(cur, wu0);        // first weights in flight while the activations are staged
+  uint4 bufA[kBatch][ROWS], bufB[kBatch][ROWS];
+  load(bufA, wu0);       // first weights in flight while the activations are staged
 
   const T* A = static_cast<const T*>(a.A);
   const int kbase = cu0 * PER;
@@ -179,8 +187,16 @@ __global__ void __launch_bounds__(kThreads) k_decode(const Args a) {
       for (int c = 0; c < 4; ++c) { accg[m][c] = 0.f; acch[m][c] = 0u; }
     float s[4];
     uint32_t kz[4][DP::kConsts];
-    int cur_g = -1;
+    const int upg = a.group / PER;                 // units per group (group % PER == 0 here)
+    int g = wu0 / upg;
+    int left = upg - (wu0 - g * upg);              // units left in group g
 
+    auto set_group = [&](int gg) {
+      int z[4];
+      load_sz<BITS>(a, gg, n0c, s, z);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) DP::consts(z[c], kz[c]);
+    };
     auto flush = [&]() {
 #pragma unroll
       for (int m = 0; m < MT; ++m)
@@ -199,24 +215,11 @@ __global__ void __launch_bounds__(kThreads) k_decode(const Args a) {
           accg[m][c] = 0.f;
         }
     };
-
-    for (int ub = wu0; ub < wu1; ub += kBatch) {
-      if (ub + kBatch < wu1) load(nxt, ub + kBatch);
+    auto process = [&](const uint4 (&buf)[kBatch][ROWS], int ub) {
 #pragma unroll
       for (int b = 0; b < kBatch; ++b) {
         const int u = ub + b;
         if (u >= wu1) break;
-        const int g = (u * PER) / a.group;
-        if (g != cur_g) {
-          if (cur_g >= 0) { flush(); fold(); }
-          if (col_ok) {
-            int z[4];
-            load_sz<BITS>(a, g, n0, s, z);
-#pragma unroll
-            for (int c = 0; c < 4; ++c) DP::consts(z[c], kz[c]);
-          }
-          cur_g = g;
-        }
         uint32_t ap[NP * MT];
         const uint32_t* src = sAP + (u - cu0) * NP * MT;
         if constexpr ((NP * MT) % 4 == 0) {
@@ -235,21 +238,32 @@ __global__ void __launch_bounds__(kThreads) k_decode(const Args a) {
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t d[NP];
-          DP::run((&cur[b][0].x)[c], kz[c], d);
+          DP::run((&buf[b][0].x)[c], kz[c], d);
 #pragma unroll
           for (int p = 0; p < NP; ++p)
 #pragma unroll
             for (int m = 0; m < MT; ++m) acch[m][c] = fma2(ap[p * MT + m], d[p], acch[m][c], T());
         }
         if (kFlushEveryUnit) flush();
+        if (--left == 0) {                         // group boundary (warp-uniform)
+          if (!kFlushEveryUnit) flush();
+          fold();
+          left = upg;
+          if (u + 1 < wu1) set_group(++g);
+        }
       }
       if (!kFlushEveryUnit) flush();
-#pragma unroll
-      for (int b = 0; b < kBatch; ++b)
-#pragma unroll
-        for (int r = 0; r < ROWS; ++r) cur[b][r] = nxt[b][r];
+    };
+
+    if (wu0 < wu1) set_group(g);
+    for (int ub = wu0; ub < wu1; ub += 2 * kBatch) {
+      if (ub + kBatch < wu1) load(bufB, ub + kBatch);
+      process(bufA, ub);
+      if (ub + kBatch >= wu1) break;
+      if (ub + 2 * kBatch < wu1) load(bufA, ub + 2 * kBatch);
+      process(bufB, ub + kBatch);
     }
-    if (cur_g >= 0) { flush(); fold(); }
+    if (wu0 < wu1 && left != upg) fold();          // range ended inside a group
   } else {
     // ---------------------------------------------------------------- fp32 path
     float* sA = reinterpret_cast<float*>(smem);   // sA[(k - kbase) * MT + m]
@@ -263,8 +277,7 @@ __global__ void __launch_bounds__(kThreads) k_decode(const Args a) {
     float s[4];
     int z[4];
     int cur_g = -1;
-    for (int ub = wu0; ub < wu1; ub += kBatch) {
-      if (ub + kBatch < wu1) load(nxt, ub + kBatch);
+    auto process = [&](const uint4 (&buf)[kBatch][ROWS], int ub) {
 #pragma unroll
       for (int b = 0; b < kBatch; ++b) {
         const int u = ub + b;
@@ -276,12 +289,12 @@ __global__ void __launch_bounds__(kThreads) k_decode(const Args a) {
           const int k = k0 + j;
           const int g = ACT ? checked_group(a, k) : k / a.group;
           if (ACT || g != cur_g) {
-            if (col_ok) load_sz<BITS>(a, g, n0, s, z);
+            load_sz<BITS>(a, g, n0c, s, z);
             cur_g = g;
           }
           float w[4];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) w[c] = diff_f32(unit_code<BITS>(cur[b], c, j), z[c]) * s[c];
+          for (int c = 0; c < 4; ++c) w[c] = diff_f32(unit_code<BITS>(buf[b], c, j), z[c]) * s[c];
           const float* ak = sA + (kk0 + j) * MT;
 #pragma unroll
           for (int m = 0; m < MT; ++m) {
@@ -291,10 +304,13 @@ __global__ void __launch_bounds__(kThreads) k_decode(const Args a) {
           }
         }
       }
-#pragma unroll
-      for (int b = 0; b < kBatch; ++b)
-#pragma unroll
-        for (int r = 0; r < ROWS; ++r) cur[b][r] = nxt[b][r];
+    };
+    for (int ub = wu0; ub < wu1; ub += 2 * kBatch) {
+      if (ub + kBatch < wu1) load(bufB, ub + kBatch);
+      process(bufA, ub);
+      if (ub + kBatch >= wu1) break;
+      if (ub + 2 * kBatch < wu1) load(bufA, ub + 2 * kBatch);
+      process(bufB, ub + kBatch);
     }
   }
 

@@ -84,7 +84,7 @@ __device__ __forceinline__ bool wait_bar(const Sync& s, uint32_t bar, uint32_t p
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer();
   while (true) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (ptx::mbar_try_wait_hint(bar, parity, 200000u)) return true;
     if (*s.abort) return false;
     if (ptx::globaltimer() - t0 > kWaitLimitNs) {
       *s.abort = 1;
@@ -133,6 +133,113 @@ __device__ __forceinline__ uint32_t chunk_code(const uint32_t (&w)[Geo<BITS>::kR
     const int u = c >> 2;
     return code3(w[3 * u], w[3 * u + 1], w[3 * u + 2], 8 * (c & 3) + j);
   }
+}
+
+// ------------------------------------------------------------------------------ dequant
+// Per-group constants of one column: the exact-unpack constants of DiffPairs, the scale as a
+// 16-bit pair (fp16 output) or as fp32 (bf16 output), and the runtime zero.
+template <int BITS, typename T>
+struct ColConsts {
+  using DPT = typename std::conditional<(BITS == 8 || !std::is_same<T, __nv_bfloat16>::value),
+                                        __half, T>::type;   // unpack type (bf16 8-bit: fp16)
+  uint32_t kz[BITS == 3 ? 1 : DiffPairs<DPT, BITS == 3 ? 4 : BITS>::kConsts];
+  uint32_t s2;   // fp16 scale in both halves
+  float s;
+  int z;
+  __device__ __forceinline__ void set(float sc, uint16_t sbits, int zero) {
+    s = sc;
+    z = zero;
+    s2 = static_cast<uint32_t>(sbits) | (static_cast<uint32_t>(sbits) << 16);
+    if constexpr (BITS != 3) DiffPairs<DPT, BITS>::consts(zero, kz);
+  }
+};
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  __half2 r = __hmul2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+__device__ __forceinline__ float bf_lo(uint32_t x) { return __uint_as_float(x << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
+__device__ __forceinline__ float h_lo(uint32_t x) { return __half2float(__ushort_as_half(static_cast<uint16_t>(x & 0xFFFFu))); }
+__device__ __forceinline__ float h_hi(uint32_t x) { return __half2float(__ushort_as_half(static_cast<uint16_t>(x >> 16))); }
+
+// Round (x0, x1) * s to bf16 and pack (x0 low half).
+__device__ __forceinline__ uint32_t scale_pack_bf16(float x0, float x1, float s) {
+  const float2 p = ptx::mul_f32x2(make_float2(x0, x1), make_float2(s, s));
+  return pack2(p.x, p.y, __nv_bfloat16());
+}
+
+// One 16-byte chunk (8 consecutive k of one column) for 4-bit: word w.
+template <typename T>
+__device__ __forceinline__ uint4 dq_chunk4(uint32_t w, const ColConsts<4, T>& cc) {
+  uint32_t d[4];
+  uint4 o;
+  if constexpr (std::is_same<T, __half>::value) {
+    DiffPairs<__half, 4>::run(w, cc.kz, d);              // d[p] = (k p, k p+4) - z, exact
+    uint32_t e[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) e[p] = hmul2(d[p], cc.s2);   // one rounding: RN((q - z) s)
+    o.x = __byte_perm(e[0], e[1], 0x5410);
+    o.y = __byte_perm(e[2], e[3], 0x5410);
+    o.z = __byte_perm(e[0], e[1], 0x7632);
+    o.w = __byte_perm(e[2], e[3], 0x7632);
+  } else {
+    DiffPairs<__nv_bfloat16, 4>::run(w, cc.kz, d);
+    o.x = scale_pack_bf16(bf_lo(d[0]), bf_lo(d[1]), cc.s);
+    o.y = scale_pack_bf16(bf_lo(d[2]), bf_lo(d[3]), cc.s);
+    o.z = scale_pack_bf16(bf_hi(d[0]), bf_hi(d[1]), cc.s);
+    o.w = scale_pack_bf16(bf_hi(d[2]), bf_hi(d[3]), cc.s);
+  }
+  return o;
+}
+
+// Two chunks (16 consecutive k of one column) for 2-bit: word w.
+template <typename T>
+__device__ __forceinline__ void dq_chunks2(uint32_t w, const ColConsts<2, T>& cc, uint4& lo, uint4& hi) {
+  uint32_t d[8];
+  if constexpr (std::is_same<T, __half>::value) {
+    DiffPairs<__half, 2>::run(w, cc.kz, d);              // d[p] = (k p, k p+8) - z
+    uint32_t e[8];
+#pragma unroll
+    for (int p = 0; p < 8; ++p) e[p] = hmul2(d[p], cc.s2);
+    lo = make_uint4(__byte_perm(e[0], e[1], 0x5410), __byte_perm(e[2], e[3], 0x5410),
+                    __byte_perm(e[4], e[5], 0x5410), __byte_perm(e[6], e[7], 0x5410));
+    hi = make_uint4(__byte_perm(e[0], e[1], 0x7632), __byte_perm(e[2], e[3], 0x7632),
+                    __byte_perm(e[4], e[5], 0x7632), __byte_perm(e[6], e[7], 0x7632));
+  } else {
+    DiffPairs<__nv_bfloat16, 2>::run(w, cc.kz, d);
+    lo = make_uint4(scale_pack_bf16(bf_lo(d[0]), bf_lo(d[1]), cc.s),
+                    scale_pack_bf16(bf_lo(d[2]), bf_lo(d[3]), cc.s),
+                    scale_pack_bf16(bf_lo(d[4]), bf_lo(d[5]), cc.s),
+                    scale_pack_bf16(bf_lo(d[6]), bf_lo(d[7]), cc.s));
+    hi = make_uint4(scale_pack_bf16(bf_hi(d[0]), bf_hi(d[1]), cc.s),
+                    scale_pack_bf16(bf_hi(d[2]), bf_hi(d[3]), cc.s),
+                    scale_pack_bf16(bf_hi(d[4]), bf_hi(d[5]), cc.s),
+                    scale_pack_bf16(bf_hi(d[6]), bf_hi(d[7]), cc.s));
+  }
+}
+
+// One chunk for 8-bit: words w0 (k 0..3) and w1 (k 4..7); the unpack is fp16 for both dtypes.
+template <typename T>
+__device__ __forceinline__ uint4 dq_chunk8(uint32_t w0, uint32_t w1, const ColConsts<8, T>& cc) {
+  uint32_t d0[2], d1[2];
+  DiffPairs<__half, 8>::run(w0, cc.kz, d0);              // (k0, k2), (k1, k3) - z
+  DiffPairs<__half, 8>::run(w1, cc.kz, d1);
+  uint4 o;
+  if constexpr (std::is_same<T, __half>::value) {
+    const uint32_t a0 = hmul2(d0[0], cc.s2), a1 = hmul2(d0[1], cc.s2);
+    const uint32_t b0 = hmul2(d1[0], cc.s2), b1 = hmul2(d1[1], cc.s2);
+    o.x = __byte_perm(a0, a1, 0x5410);
+    o.y = __byte_perm(a0, a1, 0x7632);
+    o.z = __byte_perm(b0, b1, 0x5410);
+    o.w = __byte_perm(b0, b1, 0x7632);
+  } else {
+    o.x = scale_pack_bf16(h_lo(d0[0]), h_lo(d0[1]), cc.s);
+    o.y = scale_pack_bf16(h_hi(d0[0]), h_hi(d0[1]), cc.s);
+    o.z = scale_pack_bf16(h_lo(d1[0]), h_lo(d1[1]), cc.s);
+    o.w = scale_pack_bf16(h_hi(d1[0]), h_hi(d1[1]), cc.s);
+  }
+  return o;
 }
 
 template <int BITS, typename T, bool PERK>
@@ -270,9 +377,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nt = t / num_m;
       const int n = nt * kBN + col;
       const bool n_ok = n < a.N;
-      int cur_g = -1;
-      float sc = 0.f;
-      int z = 0;
+      const int nc = n_ok ? n : a.N - 1;      // clamped column for scale/zero reads
+      int gnext = 0;                          // first k of the next group (fast path)
+      ColConsts<BITS, T> cc;
       for (int ks = 0; ks < ksteps; ++ks) {
         if (!wait_bar(sy, full(s), ph)) { ok = false; break; }
         uint32_t w[Gm::kRows];
@@ -283,35 +390,87 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (dq_lane == 0) ptx::mbar_arrive(empty(s));
         if (!wait_bar(sy, bempty(sb), phb ^ 1u)) { ok = false; break; }
         unsigned char* bt = smem + Gm::kOffB + sb * kBTileBytes;
+        const int kst = ks * kBK;
+        if constexpr (!PERK) {
+          // one group per 16 k at least (fast-path condition): track it without division
+          auto group_at = [&](int k) {
+            if (k >= gnext) {
+              const int g = k / a.group;
+              gnext = (g + 1) * a.group;
+              const uint16_t sb16 = __half_as_ushort(a.scales[static_cast<long long>(g) * a.N + nc]);
+              cc.set(__half2float(__ushort_as_half(sb16)), sb16, zero_of<BITS>(a, g, nc));
+            }
+          };
+          if constexpr (BITS == 4) {
 #pragma unroll
-        for (int c = 0; c < kBK / 8; ++c) {
-          const int k0 = ks * kBK + c * 8;
-          uint4 out = make_uint4(0u, 0u, 0u, 0u);
-          if (n_ok && k0 < a.K) {
-            float v[8];
-            if constexpr (!PERK) {
-              const int g = k0 / a.group;
-              if (g != cur_g) {
-                sc = __half2float(a.scales[static_cast<long long>(g) * a.N + n]);
-                z = zero_of<BITS>(a, g, n);
-                cur_g = g;
+            for (int c = 0; c < 8; ++c) {
+              const int k0 = kst + 8 * c;
+              uint4 out = make_uint4(0u, 0u, 0u, 0u);
+              if (k0 < a.K) {
+                group_at(k0);
+                if (n_ok) out = dq_chunk4<T>(w[c], cc);
               }
+              *reinterpret_cast<uint4*>(bt + swz(col, c)) = out;
+            }
+          } else if constexpr (BITS == 2) {
 #pragma unroll
-              for (int j = 0; j < 8; ++j) v[j] = diff_f32(chunk_code<BITS>(w, c, j), z) * sc;
-            } else {
+            for (int i = 0; i < 4; ++i) {
+              const int k0 = kst + 16 * i;
+              uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
+              if (k0 < a.K) {
+                group_at(k0);
+                if (n_ok) dq_chunks2<T>(w[i], cc, lo, hi);
+              }
+              *reinterpret_cast<uint4*>(bt + swz(col, 2 * i)) = lo;
+              *reinterpret_cast<uint4*>(bt + swz(col, 2 * i + 1)) = hi;
+            }
+          } else if constexpr (BITS == 8) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const int k0 = kst + 8 * c;
+              uint4 out = make_uint4(0u, 0u, 0u, 0u);
+              if (k0 < a.K) {
+                group_at(k0);
+                if (n_ok) out = dq_chunk8<T>(w[2 * c], w[2 * c + 1], cc);
+              }
+              *reinterpret_cast<uint4*>(bt + swz(col, c)) = out;
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const int k0 = kst + 8 * c;
+              uint4 out = make_uint4(0u, 0u, 0u, 0u);
+              if (k0 < a.K) {
+                group_at(k0);
+                if (n_ok) {
+                  float v[8];
+#pragma unroll
+                  for (int j = 0; j < 8; ++j) v[j] = diff_f32(chunk_code<BITS>(w, c, j), cc.z) * cc.s;
+                  out = make_uint4(pack2(v[0], v[1], T()), pack2(v[2], v[3], T()),
+                                   pack2(v[4], v[5], T()), pack2(v[6], v[7], T()));
+                }
+              }
+              *reinterpret_cast<uint4*>(bt + swz(col, c)) = out;
+            }
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < kBK / 8; ++c) {
+            const int k0 = kst + c * 8;
+            uint4 out = make_uint4(0u, 0u, 0u, 0u);
+            if (n_ok && k0 < a.K) {
+              float v[8];
 #pragma unroll
               for (int j = 0; j < 8; ++j) {
                 const int g = clamp_group<BITS>(a, k0 + j);
                 const float sj = __half2float(a.scales[static_cast<long long>(g) * a.N + n]);
                 v[j] = diff_f32(chunk_code<BITS>(w, c, j), zero_of<BITS>(a, g, n)) * sj;
               }
+              out = make_uint4(pack2(v[0], v[1], T()), pack2(v[2], v[3], T()),
+                               pack2(v[4], v[5], T()), pack2(v[6], v[7], T()));
             }
-            out.x = pack2(v[0], v[1], T());
-            out.y = pack2(v[2], v[3], T());
-            out.z = pack2(v[4], v[5], T());
-            out.w = pack2(v[6], v[7], T());
+            *reinterpret_cast<uint4*>(bt + swz(col, c)) = out;
           }
-          *reinterpret_cast<uint4*>(bt + swz(col, c)) = out;
         }
         ptx::fence_proxy_async_smem();
         ptx::mbar_arrive(bfull(sb));
@@ -434,7 +593,8 @@ cudaError_t launch_typed(const Problem& p, cudaStream_t stream) {
 
 template <int BITS, typename T>
 cudaError_t launch_t(const Problem& p, cudaStream_t stream) {
-  const bool perk = p.g_idx != nullptr || (p.group % 8) != 0;
+  // fast path: one group per unpacked word (2-bit words hold 16 k) and per 8-k chunk
+  const bool perk = p.g_idx != nullptr || (p.group % (BITS == 2 ? 16 : 8)) != 0;
   return perk ? launch_typed<BITS, T, true>(p, stream) : launch_typed<BITS, T, false>(p, stream);
 }
 
