@@ -253,6 +253,7 @@ def run_ours(args, rank, world, local_rank):
 
     # ---- secondary figure: M = 4096 prefill TFLOP/s
     prefill = run_prefill(g, torch, dev, stream, bf16_peak, peak_src, l2) if not args.skip_prefill else None
+    sweep = run_sweep(g, torch, dev, stream, hbm_peak, bf16_peak, l2) if args.all else None
     del sets
     torch.cuda.synchronize()
     assert g.device_status(stream) == 0, "device status word reported an error"
@@ -290,6 +291,8 @@ def run_ours(args, rank, world, local_rank):
     }
     if prefill is not None:
         line["prefill"] = prefill
+    if sweep is not None:
+        line["all_workloads"] = sweep
     return line
 
 
@@ -323,6 +326,64 @@ def run_prefill(g, torch, dev, stream, bf16_peak, peak_src, l2):
                          "traffic": load_traffic("prefill_4bit"),
                          "peak_source": peak_src + " (bf16_tflops, burst)"},
             "note": "A (33.5 MB) and W (29 MB) fit in L2 but are re-read per tile; timed back to back"}
+
+
+# ------------------------------------------------------------------------------------ sweep
+def time_workload(g, torch, dev, stream, wl, M, fmt, l2, reps=200):
+    """Per-launch time of gptq_gemm on one workload: CUDA graph of `reps` launches over weight
+    copies whose total exceeds 3x L2 (or the whole problem when one copy is larger)."""
+    draw = gptq_inputs.draw_weights(wl)
+    W = torch.from_numpy(draw.W).to(dev)
+    gi = None if draw.g_idx is None else torch.from_numpy(draw.g_idx).to(dev)
+    f = g.V2 if fmt == "v2" else g.V1
+    qw, qz, sc = g.quantize_rtn(W, bits=wl.bits, group=wl.group, g_idx=gi, sym=wl.sym, fmt=f)
+    del W
+    A = gptq_inputs.draw_activations(wl, M).to(dev)
+    nbytes = algorithmic_bytes(wl, M)
+    S = max(1, min(32, int(np.ceil(3 * l2 / nbytes))))
+    sets = [(qw.clone(), qz.clone(), sc.clone(), A.clone(),
+             torch.empty((M, wl.N), dtype=A.dtype, device=dev)) for _ in range(S)]
+    n = max(S, (reps // S) * S) if M <= 64 else S * max(1, 8 // S)
+
+    def launch(i):
+        q, z, s_, a, c = sets[i % S]
+        g.gemm(a, q, z, s_, gi, bits=wl.bits, group=wl.group, fmt=f, out=c, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(2 * S):
+            launch(i)
+    stream.synchronize()
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr, stream=stream):
+        for i in range(n):
+            launch(i)
+    with torch.cuda.stream(stream):
+        gr.replay()
+        st, en = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        st.record(stream)
+        for _ in range(3):
+            gr.replay()
+        en.record(stream)
+    stream.synchronize()
+    ms = st.elapsed_time(en) / (3 * n)
+    del sets, gr
+    return ms, nbytes
+
+
+def run_sweep(g, torch, dev, stream, hbm_peak, bf16_peak, l2):
+    rows = []
+    for name, wl in gptq_inputs.WORKLOADS.items():
+        for M in wl.Ms:
+            for fmt in wl.fmts:
+                ms, nbytes = time_workload(g, torch, dev, stream, wl, M, fmt, l2)
+                gbs = nbytes / (ms * 1e-3) / 1e9
+                tflops = 2.0 * M * wl.N * wl.K / (ms * 1e-3) / 1e12
+                row = {"workload": name, "M": M, "fmt": fmt, "us": round(ms * 1e3, 3),
+                       "GB/s": round(gbs, 1), "hbm_frac": round(gbs / hbm_peak, 4),
+                       "TFLOP/s": round(tflops, 2), "tensor_frac": round(tflops / bf16_peak, 4)}
+                rows.append(row)
+                print(json.dumps(row), file=sys.stderr, flush=True)
+    return rows
 
 
 # ------------------------------------------------------------------------------------ CPU oracle
@@ -407,6 +468,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--skip-prefill", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--all", action="store_true",
+                    help="also time every workload and M (per-launch us, GB/s, TFLOP/s)")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
 

@@ -27,7 +27,7 @@ HEADER = os.path.join(os.path.dirname(HERE), "include", "gptq.h")
 F16, BF16 = 0, 1
 V1, V2 = 1, 2
 DEV_TIMEOUT, DEV_GIDX_RANGE, DEV_SCALE_OVERFLOW = 0x1, 0x2, 0x4
-DECODE_MAX_M = 16
+DECODE_MAX_M = 32
 
 _STATUS = {0: "GPTQ_OK", -1: "GPTQ_ERR_ARG", -2: "GPTQ_ERR_SHAPE", -3: "GPTQ_ERR_ALIGN",
            -4: "GPTQ_ERR_WORKSPACE", -5: "GPTQ_ERR_ZERO_OVERFLOW", -6: "GPTQ_ERR_CUDA",

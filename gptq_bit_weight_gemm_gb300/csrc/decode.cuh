@@ -1,4 +1,4 @@
-// decode.cuh -- memory-bound GPTQ GEMM for few tokens (M <= 16): C = A @ dequant(W).
+// decode.cuh -- memory-bound GPTQ GEMM for few tokens (M <= 32): C = A @ dequant(W).
 //
 // This is the decode case of vLLM's gptq_gemm (page "增强 vLLM 对 GPTQv2 格式的支持：分析与实
 // 现", section "调整细节：根据格式选择处理方式": zeros[i] + zero_offset, zero_offset =
@@ -16,8 +16,8 @@
 //    constant), multiplied by the activation pair and summed with one fp16x2/bf16x2 fma per pair;
 //    the 16-bit partial sums are flushed into fp32 after every unit (bf16) or every 4 units
 //    (fp16), and the scale is applied once per group: acc += scale * sum_k a_k (q_k - zero).
-//  * fp32 path (act-order, 3-bit, bf16 8-bit, M > 4): w = (q - zero) * scale in fp32 (exact)
-//    and fp32 fmas.
+//  * fp32 path (M <= 4 with act-order, 3-bit or bf16 8-bit): w = (q - zero) * scale in fp32
+//    (exact) and fp32 fmas.  4 < M <= 32 runs the tensor-core variant in decode_mma.cuh.
 //  * partial sums are reduced across warps in shared memory and across the cluster through
 //    distributed shared memory, in a fixed order (deterministic), then rounded once to the
 //    output dtype.  No global workspace and no atomics.
@@ -103,14 +103,118 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+
+// Stage activation pairs into shared memory.  Work item = (unit u, real token m < M): one
+// thread reads the unit's PER consecutive activations of row m with 16-byte loads (8-byte for
+// 8-bit units) and writes the NP pairs (lo_k(p), hi_k(p)) through `put(u, m, p, value)`.  A
+// thread's loads for up to kStageBatch items are all issued before any of them is used, so the
+// staging costs about one L2 round trip, not one per item.  Rows m >= M and units past the last
+// one are written as zero by the caller.
+constexpr int kStageBatch = 4;
+
+template <int PER>
+struct UnitVec {   // a unit's activations: PER 16-bit values
+  static constexpr int kWords = PER / 2;
+  uint32_t w[kWords];
+  __device__ __forceinline__ void load(const uint16_t* p) {
+    if constexpr (kWords >= 4) {
+#pragma unroll
+      for (int i = 0; i < kWords / 4; ++i) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(p) + i);
+        w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+      }
+    } else {
+      const uint2 v = __ldg(reinterpret_cast<const uint2*>(p));
+      w[0] = v.x; w[1] = v.y;
+    }
+  }
+  __device__ __forceinline__ uint32_t half(int k) const {
+    return (w[k >> 1] >> (16 * (k & 1))) & 0xFFFFu;
+  }
+};
+
+template <int PER, int NP, class LoK, class HiK, class Put>
+__device__ __forceinline__ void stage_pairs(const uint16_t* A, int M, int K, int ufirst, int nunits,
+                                            int units, LoK lo_k, HiK hi_k, Put put) {
+  const int items = nunits * M;
+  for (int base = 0; base < items; base += kStageBatch * static_cast<int>(blockDim.x)) {
+    UnitVec<PER> v[kStageBatch];
+#pragma unroll
+    for (int j = 0; j < kStageBatch; ++j) {
+      const int it = base + j * static_cast<int>(blockDim.x) + static_cast<int>(threadIdx.x);
+      const int uu = it / M, m = it - uu * M;
+      if (it < items && ufirst + uu < units)
+        v[j].load(A + static_cast<long long>(m) * K + static_cast<long long>(ufirst + uu) * PER);
+    }
+#pragma unroll
+    for (int j = 0; j < kStageBatch; ++j) {
+      const int it = base + j * static_cast<int>(blockDim.x) + static_cast<int>(threadIdx.x);
+      const int uu = it / M, m = it - uu * M;
+      if (it < items) {
+        const bool live = ufirst + uu < units;
+#pragma unroll
+        for (int p = 0; p < NP; ++p)
+          put(uu, m, p, live ? (v[j].half(lo_k(p)) | (v[j].half(hi_k(p)) << 16)) : 0u);
+      }
+    }
+  }
+}
+
+// Raw scale/zero words of columns n0..n0+3 for group g (loads only; decoded later so the
+// loads overlap the activation staging).
+template <int BITS>
+struct SZRaw {
+  uint2 sv;
+  uint32_t zf;
+  __device__ __forceinline__ void load(const Args& a, int g, int n0) {
+    sv = __ldg(reinterpret_cast<const uint2*>(a.scales + static_cast<long long>(g) * a.N + n0));
+    zf = zeros4<BITS>(a.qzeros + static_cast<long long>(g) * a.zwords, n0);
+  }
+  __device__ __forceinline__ void decode(int zero_offset, float (&s)[4], int (&z)[4]) const {
+    s[0] = __half2float(__ushort_as_half(static_cast<uint16_t>(sv.x & 0xFFFFu)));
+    s[1] = __half2float(__ushort_as_half(static_cast<uint16_t>(sv.x >> 16)));
+    s[2] = __half2float(__ushort_as_half(static_cast<uint16_t>(sv.y & 0xFFFFu)));
+    s[3] = __half2float(__ushort_as_half(static_cast<uint16_t>(sv.y >> 16)));
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      z[c] = static_cast<int>((zf >> (BITS * c)) & Pack<BITS>::kMask) + zero_offset;
+  }
+};
+
+// Shared memory of one CTA: [staged activations | per-warp partials] (aliased, one after the
+// other in time), then the receive slots of the cluster reduce-scatter (never aliased).
+template <int BITS, int MT, typename T, bool HALF>
+__host__ __device__ constexpr size_t recv_offset(int units, int cs) {
+  const size_t upc = static_cast<size_t>((units + cs - 1) / cs);
+  const size_t stage = HALF ? upc * DiffPairs<T, (HALF ? BITS : 4)>::kPairs * MT * 4
+                            : upc * Pack<BITS>::kPerUnit * MT * 4;
+  const size_t red = static_cast<size_t>(kWarps) * MT * kSlab * 4;
+  const size_t m = stage > red ? stage : red;
+  return (m + 15) & ~static_cast<size_t>(15);
+}
+template <int BITS, int MT, typename T, bool HALF>
+size_t smem_bytes(int units, int cs) {
+  return recv_offset<BITS, MT, T, HALF>(units, cs) + static_cast<size_t>(MT) * kSlab * 4;
+}
+
+// Few-token instantiations are capped at 102 registers so five CTAs (20 warps) fit on an SM
+// and the whole grid is resident in one wave.
 template <int BITS, int MT, typename T, bool HALF, bool ACT>
-__global__ void __launch_bounds__(kThreads) k_decode(const Args a) {
+__global__ void __launch_bounds__(kThreads, (MT <= 2 ? 5 : 1)) k_decode(const Args a) {
   using P = Pack<BITS>;
   constexpr int PER = P::kPerUnit;
   constexpr int ROWS = P::kRowsPerUnit;
+  constexpr int CH = ROWS == 3 ? 2 : 4;          // register ring: units in flight per warp
   extern __shared__ __align__(16) unsigned char smem[];
 
   pdl_launch_dependents();
+  cluster_arrive_relaxed();                      // matched by cluster_wait() before the reduction
   cg::cluster_group cluster = cg::this_cluster();
   const int cs = static_cast<int>(gridDim.x);   // grid x == cluster x
   const int rank = static_cast<int>(blockIdx.x);
@@ -131,23 +235,26 @@ __global__ void __launch_bounds__(kThreads) k_decode(const Args a) {
   const long long ustride = static_cast<long long>(ROWS) * a.N;   // words between units
   const int32_t* qw = a.qweight + n0c;
   auto unit_ptr = [&](int u, int r) { return qw + u * ustride + static_cast<long long>(r) * a.N; };
-  auto load = [&](uint4 (&dst)[kBatch][ROWS], int ufirst) {
+  auto load_unit = [&](uint4 (&dst)[ROWS], int u) {
 #pragma unroll
-    for (int b = 0; b < kBatch; ++b)
-#pragma unroll
-      for (int r = 0; r < ROWS; ++r)
-        if (ufirst + b < wu1) dst[b][r] = ld_stream_v4(unit_ptr(ufirst + b, r));
+    for (int r = 0; r < ROWS; ++r) dst[r] = ld_stream_v4(unit_ptr(u, r));
   };
 
-  // Weights are never written by the kernel this one may overlap with through programmatic
-  // launch -- and even if they were, L2 is the coherence point -- so warming L2 with this warp's
-  // first rows before griddepcontrol.wait is safe; every real load happens after the wait.
-  for (int u = wu0; u < wu1 && u < wu0 + 4 * kBatch; ++u)
+  // The whole weight range of this warp is requested into L2 up front: the prefetches need no
+  // registers, keep HBM busy, and the register ring below then mostly hits L2.  They are issued
+  // before griddepcontrol.wait; that is safe because L2 is the point of coherence (a line written
+  // by the previous kernel is never served stale from L2) and every real load comes after the
+  // wait.
+  for (int u = wu0; u < wu1; ++u)
 #pragma unroll
     for (int r = 0; r < ROWS; ++r) prefetch_l2(unit_ptr(u, r));
   pdl_wait();            // the previous kernel's writes are visible from here on
-  uint4 bufA[kBatch][ROWS], bufB[kBatch][ROWS];
-  load(bufA, wu0);       // first weights in flight while the activations are staged
+  // Rolling ring: slot b holds unit ub + b; it is refilled with unit ub + b + CH right after
+  // use, so CH units per warp stay in flight for the whole loop.
+  uint4 ring[CH][ROWS];
+#pragma unroll
+  for (int b = 0; b < CH; ++b)
+    if (wu0 + b < wu1) load_unit(ring[b], wu0 + b);
 
   const T* A = static_cast<const T*>(a.A);
   const int kbase = cu0 * PER;
@@ -164,19 +271,25 @@ __global__ void __launch_bounds__(kThreads) k_decode(const Args a) {
     using DP = DiffPairs<T, BITS>;
     constexpr int NP = DP::kPairs;
     constexpr bool kFlushEveryUnit = std::is_same<T, __nv_bfloat16>::value;
+    const int upg = a.group / PER;                 // units per group (group % PER == 0 here)
+    int g = wu0 / upg;
+    int left = upg - (wu0 - g * upg);              // units left in group g
+    // Scale/zero words of the current group and, one group ahead, of the next: no global load
+    // sits on the critical path at a group boundary.
+    SZRaw<BITS> raw, raw_next;
+    const int g_last = (wu1 - 1) / upg;
+    if (wu0 < wu1) raw.load(a, g, n0c);            // in flight during the staging below
+    if (wu0 < wu1 && g < g_last) raw_next.load(a, g + 1, n0c);
+
     // activation pairs: sAP[(unit * NP + p) * MT + m] = (a[m][k0 + lo_k(p)], a[m][k0 + hi_k(p)])
     uint32_t* sAP = reinterpret_cast<uint32_t*>(smem);
     const uint16_t* A16 = reinterpret_cast<const uint16_t*>(A);
-    for (int i = threadIdx.x; i < ucount * NP * MT; i += kThreads) {
-      const int m = i % MT, up = i / MT, p = up % NP, uu = up / NP;
-      uint32_t v = 0u;
-      if (m < a.M) {
-        const long long row = static_cast<long long>(m) * a.K + kbase + uu * PER;
-        v = static_cast<uint32_t>(A16[row + DP::lo_k(p)]) |
-            (static_cast<uint32_t>(A16[row + DP::hi_k(p)]) << 16);
-      }
-      sAP[i] = v;
-    }
+    if (a.M < MT)
+      for (int i = threadIdx.x; i < ucount * NP * MT; i += kThreads)
+        if (i % MT >= a.M) sAP[i] = 0u;
+    stage_pairs<PER, NP>(A16, a.M, a.K, cu0, ucount, a.units,
+                         [](int p) { return DP::lo_k(p); }, [](int p) { return DP::hi_k(p); },
+                         [&](int uu, int m, int p, uint32_t v) { sAP[(uu * NP + p) * MT + m] = v; });
     __syncthreads();
 
     float accg[MT][4];
@@ -187,13 +300,9 @@ __global__ void __launch_bounds__(kThreads) k_decode(const Args a) {
       for (int c = 0; c < 4; ++c) { accg[m][c] = 0.f; acch[m][c] = 0u; }
     float s[4];
     uint32_t kz[4][DP::kConsts];
-    const int upg = a.group / PER;                 // units per group (group % PER == 0 here)
-    int g = wu0 / upg;
-    int left = upg - (wu0 - g * upg);              // units left in group g
-
-    auto set_group = [&](int gg) {
+    auto set_group = [&]() {
       int z[4];
-      load_sz<BITS>(a, gg, n0c, s, z);
+      raw.decode(a.zero_offset, s, z);
 #pragma unroll
       for (int c = 0; c < 4; ++c) DP::consts(z[c], kz[c]);
     };
@@ -215,9 +324,9 @@ __global__ void __launch_bounds__(kThreads) k_decode(const Args a) {
           accg[m][c] = 0.f;
         }
     };
-    auto process = [&](const uint4 (&buf)[kBatch][ROWS], int ub) {
+    auto process = [&](int ub) {
 #pragma unroll
-      for (int b = 0; b < kBatch; ++b) {
+      for (int b = 0; b < CH; ++b) {
         const int u = ub + b;
         if (u >= wu1) break;
         uint32_t ap[NP * MT];
@@ -235,34 +344,35 @@ __global__ void __launch_bounds__(kThreads) k_decode(const Args a) {
             ap[2 * i] = v.x; ap[2 * i + 1] = v.y;
           }
         }
+        const uint4 wv = ring[b][0];
+        if (u + CH < wu1) load_unit(ring[b], u + CH);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t d[NP];
-          DP::run((&buf[b][0].x)[c], kz[c], d);
+          DP::run((&wv.x)[c], kz[c], d);
 #pragma unroll
           for (int p = 0; p < NP; ++p)
 #pragma unroll
             for (int m = 0; m < MT; ++m) acch[m][c] = fma2(ap[p * MT + m], d[p], acch[m][c], T());
         }
-        if (kFlushEveryUnit) flush();
+        if (kFlushEveryUnit || (b & 3) == 3) flush();
         if (--left == 0) {                         // group boundary (warp-uniform)
           if (!kFlushEveryUnit) flush();
           fold();
           left = upg;
-          if (u + 1 < wu1) set_group(++g);
+          if (u + 1 < wu1) {
+            ++g;
+            raw = raw_next;
+            set_group();
+            if (g < g_last) raw_next.load(a, g + 1, n0c);
+          }
         }
       }
       if (!kFlushEveryUnit) flush();
     };
 
-    if (wu0 < wu1) set_group(g);
-    for (int ub = wu0; ub < wu1; ub += 2 * kBatch) {
-      if (ub + kBatch < wu1) load(bufB, ub + kBatch);
-      process(bufA, ub);
-      if (ub + kBatch >= wu1) break;
-      if (ub + 2 * kBatch < wu1) load(bufA, ub + 2 * kBatch);
-      process(bufB, ub + kBatch);
-    }
+    if (wu0 < wu1) set_group();
+    for (int ub = wu0; ub < wu1; ub += CH) process(ub);
     if (wu0 < wu1 && left != upg) fold();          // range ended inside a group
   } else {
     // ---------------------------------------------------------------- fp32 path
@@ -277,13 +387,17 @@ __global__ void __launch_bounds__(kThreads) k_decode(const Args a) {
     float s[4];
     int z[4];
     int cur_g = -1;
-    auto process = [&](const uint4 (&buf)[kBatch][ROWS], int ub) {
+    auto process = [&](int ub) {
 #pragma unroll
-      for (int b = 0; b < kBatch; ++b) {
+      for (int b = 0; b < CH; ++b) {
         const int u = ub + b;
         if (u >= wu1) break;
         const int k0 = u * PER;
         const int kk0 = k0 - kbase;
+        uint4 wv[ROWS];
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r) wv[r] = ring[b][r];
+        if (u + CH < wu1) load_unit(ring[b], u + CH);
 #pragma unroll 4
         for (int j = 0; j < PER; ++j) {
           const int k = k0 + j;
@@ -294,7 +408,7 @@ __global__ void __launch_bounds__(kThreads) k_decode(const Args a) {
           }
           float w[4];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) w[c] = diff_f32(unit_code<BITS>(buf[b], c, j), z[c]) * s[c];
+          for (int c = 0; c < 4; ++c) w[c] = diff_f32(unit_code<BITS>(wv, c, j), z[c]) * s[c];
           const float* ak = sA + (kk0 + j) * MT;
 #pragma unroll
           for (int m = 0; m < MT; ++m) {
@@ -305,56 +419,45 @@ __global__ void __launch_bounds__(kThreads) k_decode(const Args a) {
         }
       }
     };
-    for (int ub = wu0; ub < wu1; ub += 2 * kBatch) {
-      if (ub + kBatch < wu1) load(bufB, ub + kBatch);
-      process(bufA, ub);
-      if (ub + kBatch >= wu1) break;
-      if (ub + 2 * kBatch < wu1) load(bufA, ub + 2 * kBatch);
-      process(bufB, ub + kBatch);
-    }
+    for (int ub = wu0; ub < wu1; ub += CH) process(ub);
   }
 
-  // ---- reduction: warps (shared memory), then the cluster (distributed shared memory)
+  // ---- reduction: warps (shared memory), then a reduce-scatter over the cluster: every CTA
+  // pushes each column's partial sum into the shared memory of the CTA that owns the column
+  // (distributed shared memory), one cluster barrier, and each owner sums its slots in rank
+  // order (deterministic) and writes C.
   __syncthreads();   // every warp is done reading the staged activations
-  float* red = reinterpret_cast<float*>(smem);   // [kWarps][MT][kSlab]
+  float* red = reinterpret_cast<float*>(smem);                        // [kWarps][MT][kSlab]
+  // [cs][MT][kSlab / cs]: a region of its own -- peers may push into it while this CTA is
+  // still reading its staged activations.
+  float* recv = reinterpret_cast<float*>(smem + recv_offset<BITS, MT, T, HALF>(a.units, cs));
 #pragma unroll
   for (int m = 0; m < MT; ++m)
     *reinterpret_cast<float4*>(red + (warp * MT + m) * kSlab + lane * 4) =
         make_float4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]);
   __syncthreads();
+  const int per_rank = kSlab / cs;
+  cluster_wait();    // every CTA of the cluster is running: remote stores are safe
   for (int i = threadIdx.x; i < MT * kSlab; i += kThreads) {
     float v = red[i];
 #pragma unroll
     for (int w = 1; w < kWarps; ++w) v += red[w * MT * kSlab + i];
-    red[i] = v;
+    const int m = i / kSlab, col = i - m * kSlab;
+    const int owner = col / per_rank;
+    float* dst = cluster.map_shared_rank(recv, owner);
+    dst[(rank * MT + m) * per_rank + (col - owner * per_rank)] = v;
   }
-  cluster.sync();
-  const int per_rank = kSlab / cs;
+  cluster.sync();    // all pushes visible to their owners
   T* C = static_cast<T*>(a.C);
   for (int i = threadIdx.x; i < MT * per_rank; i += kThreads) {
-    const int m = i / per_rank;
-    const int col = rank * per_rank + (i - m * per_rank);
-    const int n = n_base + col;
+    const int m = i / per_rank, c = i - m * per_rank;
+    const int n = n_base + rank * per_rank + c;
     if (m < a.M && n < a.N) {
       float v = 0.f;
-      for (int q = 0; q < cs; ++q) v += cluster.map_shared_rank(red, q)[m * kSlab + col];
+      for (int q = 0; q < cs; ++q) v += recv[(q * MT + m) * per_rank + c];
       C[static_cast<long long>(m) * a.N + n] = F16Traits<T>::from_f32(v);
     }
   }
-  cluster.sync();   // keep this CTA's shared memory alive until the cluster has read it
-}
-
-// Shared memory bytes for one CTA.
-template <int BITS, int MT, typename T, bool HALF>
-size_t smem_bytes(int units_per_cta) {
-  size_t stage;
-  if constexpr (HALF) {
-    stage = static_cast<size_t>(units_per_cta) * DiffPairs<T, BITS>::kPairs * MT * 4;
-  } else {
-    stage = static_cast<size_t>(units_per_cta) * Pack<BITS>::kPerUnit * MT * 4;
-  }
-  const size_t red = static_cast<size_t>(kWarps) * MT * kSlab * 4;
-  return stage > red ? stage : red;
 }
 
 template <int BITS, int MT, typename T, bool HALF, bool ACT>
@@ -368,8 +471,7 @@ cudaError_t launch_one(const Problem& p, int cs, cudaStream_t stream) {
   a.units = p.K / Pack<BITS>::kPerUnit;
   a.C = p.out; a.status = p.status;
   const int slabs = (p.N + kSlab - 1) / kSlab;
-  const int units_per_cta = (a.units + cs - 1) / cs;
-  const size_t smem = smem_bytes<BITS, MT, T, HALF>(units_per_cta);
+  const size_t smem = smem_bytes<BITS, MT, T, HALF>(a.units, cs);
   auto kern = k_decode<BITS, MT, T, HALF, ACT>;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -403,32 +505,42 @@ inline int choose_cluster(const Problem& p, int per_unit) {
   return cs;
 }
 
+template <int BITS, int MT, typename T, bool FOLD>
+cudaError_t launch_mma(const Problem& p, int cs, cudaStream_t stream);
+
 template <int BITS, int MT, typename T>
 cudaError_t launch_mt(const Problem& p, cudaStream_t stream) {
   const int cs = choose_cluster(p, Pack<BITS>::kPerUnit);
   constexpr bool kHas16 = (BITS == 2 || BITS == 4 || (BITS == 8 && std::is_same<T, __half>::value));
-  const bool factorable = p.g_idx == nullptr && (p.group % Pack<BITS>::kPerUnit) == 0;
-  if constexpr (kHas16 && MT <= 4) {
-    if (factorable) return launch_one<BITS, MT, T, true, false>(p, cs, stream);
+  if constexpr (MT >= 8) {
+    // tensor cores from registers; the scale folds per group when groups align with k-tiles
+    const bool fold = kHas16 && p.g_idx == nullptr && (p.group % (4 * Pack<BITS>::kPerUnit)) == 0;
+    if constexpr (kHas16) {
+      if (fold) return launch_mma<BITS, MT, T, true>(p, cs, stream);
+    }
+    return launch_mma<BITS, MT, T, false>(p, cs, stream);
+  } else {
+    const bool factorable = p.g_idx == nullptr && (p.group % Pack<BITS>::kPerUnit) == 0;
+    if constexpr (kHas16) {
+      if (factorable) return launch_one<BITS, MT, T, true, false>(p, cs, stream);
+    }
+    if (p.g_idx) return launch_one<BITS, MT, T, false, true>(p, cs, stream);
+    return launch_one<BITS, MT, T, false, false>(p, cs, stream);
   }
-  if (p.g_idx) return launch_one<BITS, MT, T, false, true>(p, cs, stream);
-  return launch_one<BITS, MT, T, false, false>(p, cs, stream);
 }
 
+// Every M <= 32 runs the register-MMA kernel (token blocks of 8): even at one token, handing
+// the multiply-accumulate to the tensor core leaves the SM with only the unpack to issue.
 template <int BITS>
 cudaError_t launch_bits(const Problem& p, cudaStream_t stream) {
   if (p.dtype == 0) {
-    if (p.M <= 1) return launch_mt<BITS, 1, __half>(p, stream);
-    if (p.M <= 2) return launch_mt<BITS, 2, __half>(p, stream);
-    if (p.M <= 4) return launch_mt<BITS, 4, __half>(p, stream);
     if (p.M <= 8) return launch_mt<BITS, 8, __half>(p, stream);
-    return launch_mt<BITS, 16, __half>(p, stream);
+    if (p.M <= 16) return launch_mt<BITS, 16, __half>(p, stream);
+    return launch_mt<BITS, 32, __half>(p, stream);
   }
-  if (p.M <= 1) return launch_mt<BITS, 1, __nv_bfloat16>(p, stream);
-  if (p.M <= 2) return launch_mt<BITS, 2, __nv_bfloat16>(p, stream);
-  if (p.M <= 4) return launch_mt<BITS, 4, __nv_bfloat16>(p, stream);
   if (p.M <= 8) return launch_mt<BITS, 8, __nv_bfloat16>(p, stream);
-  return launch_mt<BITS, 16, __nv_bfloat16>(p, stream);
+  if (p.M <= 16) return launch_mt<BITS, 16, __nv_bfloat16>(p, stream);
+  return launch_mt<BITS, 32, __nv_bfloat16>(p, stream);
 }
 
 }  // namespace decode

@@ -1,0 +1,367 @@
+// decode_mma.cuh -- GPTQ GEMM for 4 < M <= 32 tokens on the tensor cores from registers
+// (mma.sync m16n8k16, fp16/bf16 inputs, fp32 accumulate).
+//
+// At 8-32 tokens the FMA count per weight makes the CUDA-core path ALU-bound, while the whole
+// problem is still a weight stream (page "增强 vLLM 对 GPTQv2 格式的支持：分析与实现", section
+// "调整细节：根据格式选择处理方式", notes gptq_gemm's decode speed as the open item).  This kernel
+// keeps the structure of the CUDA-core decode kernel -- cluster split-K over 128-column slabs,
+// one 16-byte load per packed row for 4 columns, L2 prefetch of the weight range, DSMEM
+// reduce-scatter -- and swaps the multiply: the weights become the 16-row A operand of
+// mma.sync ("swap-AB": rows = output columns), the tokens the 8-column B operand, so the
+// unpacked weights never leave registers.
+//
+// Fragment mapping (PTX m16n8k16, thread = (g, t) = (lane / 4, lane % 4)): a warp owns 32
+// columns; thread (g, t) loads columns 4g .. 4g+3.  Tile 0 maps MMA row g to column 4g and row
+// g+8 to column 4g+1; tile 1 maps them to columns 4g+2 and 4g+3.  A k-tile is 4 packed units:
+// thread t holds unit t.  The K order inside an MMA may be any permutation shared by A and B, so
+// MMA j of a unit takes the unpacked pairs 2j and 2j+1 of thread t's word as the k-slots
+// (2t, 2t+1) and (2t+8, 2t+9) -- and the activations are staged in the same pairing, which makes
+// them exactly the B fragment.
+//
+//  * FOLD (groups aligned to k-tiles, no act-order, 2/4/8-bit): A = q - zero exactly (magic-
+//    number unpack), products exact, a fresh accumulator per group folded with the scale:
+//    acc += scale * sum_k a_k (q_k - zero).
+//  * FULL (act-order, 3-bit, unaligned groups): A = RN((q - zero) * scale) per weight (exact
+//    fp32 product, one rounding), accumulated across groups.
+#pragma once
+
+#include "decode.cuh"
+
+namespace gptq {
+namespace decode {
+
+// Pairing of a unit's codes into the two halves of one register: pair p = (lo_k(p), hi_k(p)).
+template <int BITS>
+struct MmaPairs {
+  static constexpr int kPairs = BITS == 3 ? 16 : 16 / BITS;
+  static constexpr int kHalf = Pack<BITS>::kPerUnit / 2;
+  __device__ static __forceinline__ int lo_k(int p) { return p; }
+  __device__ static __forceinline__ int hi_k(int p) { return p + kHalf; }
+};
+
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1, __half) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1, __nv_bfloat16) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Words of the staged activations for one unit (all MT tokens x NP pairs), padded so that the
+// 16-byte loads of a warp's 4 units x 8 tokens fall in distinct bank groups.
+template <int MT, int NP>
+__host__ __device__ constexpr int unit_words() {
+  return MT * NP + ((8 - (MT * NP) % 32) + 32) % 32;
+}
+
+// Shared memory: [staged activations | partial sums] (aliased in time), then the receive slots.
+template <int BITS, int MT>
+__host__ __device__ constexpr size_t mma_recv_offset(int units, int cs) {
+  const size_t tiles_per_cta = static_cast<size_t>(((units + 3) / 4 + cs - 1) / cs);
+  const size_t stage = tiles_per_cta * 4 * unit_words<MT, MmaPairs<BITS>::kPairs>() * 4;
+  const size_t part = static_cast<size_t>(MT) * kSlab * 4;
+  const size_t m = stage > part ? stage : part;
+  return (m + 15) & ~static_cast<size_t>(15);
+}
+
+template <int BITS, int MT, typename T, bool FOLD>
+__global__ void __launch_bounds__(kThreads) k_decode_mma(const Args a) {
+  using P = Pack<BITS>;
+  using MP = MmaPairs<BITS>;
+  constexpr int PER = P::kPerUnit;
+  constexpr int ROWS = P::kRowsPerUnit;
+  constexpr int NP = MP::kPairs;
+  constexpr int NB = MT / 8;                          // token blocks of 8
+  constexpr int UW = unit_words<MT, NP>();
+  constexpr int RING = ROWS == 3 ? 2 : 4;             // k-tiles of loads in flight per thread
+  extern __shared__ __align__(16) unsigned char smem[];
+
+  pdl_launch_dependents();
+  cluster_arrive_relaxed();
+  cg::cluster_group cluster = cg::this_cluster();
+  const int cs = static_cast<int>(gridDim.x);
+  const int rank = static_cast<int>(blockIdx.x);
+  const int n_base = static_cast<int>(blockIdx.y) * kSlab;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gq = lane >> 2, tq = lane & 3;
+  const int n0 = n_base + warp * 32 + gq * 4;
+  const int n0c = n0 < a.N ? n0 : a.N - 4;
+
+  // CTA range in k-tiles of 4 units (every warp of the CTA covers all of it, 32 columns each)
+  const int tiles_total = (a.units + 3) / 4;
+  int ct0, ct1;
+  split(tiles_total, cs, rank, ct0, ct1);
+  const int cu0 = ct0 * 4;
+  const int ntile = ct1 - ct0;
+
+  const long long ustride = static_cast<long long>(ROWS) * a.N;
+  const int32_t* qw = a.qweight + n0c;
+  auto unit_ptr = [&](int u, int r) { return qw + u * ustride + static_cast<long long>(r) * a.N; };
+  auto load_tile = [&](uint4 (&dst)[ROWS], int kt) {
+    const int u = cu0 + kt * 4 + tq;
+    if (u < a.units) {
+#pragma unroll
+      for (int r = 0; r < ROWS; ++r) dst[r] = ld_stream_v4(unit_ptr(u, r));
+    }
+  };
+  for (int kt = 0; kt < ntile; ++kt) {                 // L2 warm-up, safe before the wait
+    const int u = cu0 + kt * 4 + tq;
+    if (u < a.units) {
+#pragma unroll
+      for (int r = 0; r < ROWS; ++r) prefetch_l2(unit_ptr(u, r));
+    }
+  }
+  pdl_wait();
+  uint4 ring[RING][ROWS];
+#pragma unroll
+  for (int i = 0; i < RING; ++i) {
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r) ring[i][r] = make_uint4(0u, 0u, 0u, 0u);
+    if (i < ntile) load_tile(ring[i], i);
+  }
+
+  // Stage activations: sB[u][m][p] = (a[m][k0 + lo_k(p)], a[m][k0 + hi_k(p)]), zero past K or M.
+  uint32_t* sB = reinterpret_cast<uint32_t*>(smem);
+  const uint16_t* A16 = static_cast<const uint16_t*>(a.A);
+  const int nunits = ntile * 4;
+  if (a.M < MT)                                          // token rows past M are zero
+    for (int i = threadIdx.x; i < nunits * MT * NP; i += kThreads) {
+      const int p = i % NP, um = i / NP, m = um % MT, uu = um / MT;
+      if (m >= a.M) sB[uu * UW + m * NP + p] = 0u;
+    }
+  stage_pairs<PER, NP>(A16, a.M, a.K, cu0, nunits, a.units,
+                       [](int p) { return MP::lo_k(p); }, [](int p) { return MP::hi_k(p); },
+                       [&](int uu, int m, int p, uint32_t v) { sB[uu * UW + m * NP + p] = v; });
+  __syncthreads();
+
+  float acc[2][NB][4];
+#pragma unroll
+  for (int t = 0; t < 2; ++t)
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[t][nb][i] = 0.f;
+
+  // B fragments of k-tile kt for this thread: unit tq, tokens 8 nb + gq, pairs 0..NP-1.
+  auto load_b = [&](int kt, uint32_t (&bf)[NB][NP]) {
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+      const uint32_t* src = sB + (kt * 4 + tq) * UW + (8 * nb + gq) * NP;
+      if constexpr (NP % 4 == 0) {
+#pragma unroll
+        for (int i = 0; i < NP / 4; ++i) {
+          const uint4 v = reinterpret_cast<const uint4*>(src)[i];
+          bf[nb][4 * i] = v.x; bf[nb][4 * i + 1] = v.y; bf[nb][4 * i + 2] = v.z; bf[nb][4 * i + 3] = v.w;
+        }
+      } else {
+        const uint2 v = reinterpret_cast<const uint2*>(src)[0];
+        bf[nb][0] = v.x; bf[nb][1] = v.y;
+      }
+    }
+  };
+
+  if constexpr (FOLD) {
+    using DP = DiffPairs<T, BITS>;
+    static_assert(DP::kPairs == NP, "pairing must match the activation staging");
+    float cg[2][NB][4];
+    float s[4];
+    uint32_t kz[4][DP::kConsts];
+    const int tpg = a.group / (4 * PER);               // k-tiles per group (>= 1 here)
+    int g = (cu0 * PER) / a.group;
+    int left = tpg - ((cu0 / 4) % tpg);
+    const int g_end = ((cu0 + nunits) * PER - 1) / a.group;
+    const int g_last = g_end < a.G - 1 ? g_end : a.G - 1;
+    SZRaw<BITS> raw, raw_next;
+    raw.load(a, g, n0c);
+    if (g < g_last) raw_next.load(a, g + 1, n0c);
+    auto set_group = [&]() {
+      int z[4];
+      raw.decode(a.zero_offset, s, z);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) DP::consts(z[c], kz[c]);
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) cg[t][nb][i] = 0.f;
+    };
+    auto fold = [&]() {
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+          acc[t][nb][0] = fmaf(s[2 * t], cg[t][nb][0], acc[t][nb][0]);
+          acc[t][nb][1] = fmaf(s[2 * t], cg[t][nb][1], acc[t][nb][1]);
+          acc[t][nb][2] = fmaf(s[2 * t + 1], cg[t][nb][2], acc[t][nb][2]);
+          acc[t][nb][3] = fmaf(s[2 * t + 1], cg[t][nb][3], acc[t][nb][3]);
+        }
+    };
+    if (ntile > 0) set_group();
+    for (int kt0 = 0; kt0 < ntile; kt0 += RING) {
+#pragma unroll
+      for (int i = 0; i < RING; ++i) {
+        const int kt = kt0 + i;
+        if (kt >= ntile) break;
+        const uint4 wv = ring[i][0];
+        if (kt + RING < ntile) load_tile(ring[i], kt + RING);
+        uint32_t bf[NB][NP];
+        load_b(kt, bf);
+        uint32_t d[4][NP];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) DP::run((&wv.x)[c], kz[c], d[c]);
+#pragma unroll
+        for (int j = 0; j < NP / 2; ++j)
+#pragma unroll
+          for (int t = 0; t < 2; ++t)
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb)
+              mma16816(cg[t][nb], d[2 * t][2 * j], d[2 * t + 1][2 * j], d[2 * t][2 * j + 1],
+                       d[2 * t + 1][2 * j + 1], bf[nb][2 * j], bf[nb][2 * j + 1], T());
+        if (--left == 0) {                              // group boundary (warp-uniform)
+          fold();
+          left = tpg;
+          if (kt + 1 < ntile) {
+            ++g;
+            raw = raw_next;
+            set_group();
+            if (g < g_last) raw_next.load(a, g + 1, n0c);
+          }
+        }
+      }
+    }
+    if (ntile > 0 && left != tpg) fold();
+  } else {
+    for (int kt0 = 0; kt0 < ntile; kt0 += RING) {
+#pragma unroll
+      for (int i = 0; i < RING; ++i) {
+        const int kt = kt0 + i;
+        if (kt >= ntile) break;
+        uint4 wv[ROWS];
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r) wv[r] = ring[i][r];
+        if (kt + RING < ntile) load_tile(ring[i], kt + RING);
+        uint32_t bf[NB][NP];
+        load_b(kt, bf);
+        const int u = cu0 + kt * 4 + tq;
+        const int uk = (u < a.units ? u : a.units - 1) * PER;
+        // dequantize this unit for 4 columns: w[c][p] = RN((q - z) * s) pairs
+        uint32_t w[4][NP];
+        float s[4];
+        int z[4];
+        int cur_g = -1;
+#pragma unroll
+        for (int p = 0; p < NP; ++p) {
+          float v[4][2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int j = h ? MP::hi_k(p) : MP::lo_k(p);
+            const int k = uk + j;
+            const int gg = a.g_idx ? checked_group(a, k) : k / a.group;
+            if (gg != cur_g) {
+              load_sz<BITS>(a, gg, n0c, s, z);
+              cur_g = gg;
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c) v[c][h] = diff_f32(unit_code<BITS>(wv, c, j), z[c]) * s[c];
+          }
+#pragma unroll
+          for (int c = 0; c < 4; ++c) w[c][p] = pack2(v[c][0], v[c][1], T());
+        }
+#pragma unroll
+        for (int j = 0; j < NP / 2; ++j)
+#pragma unroll
+          for (int t = 0; t < 2; ++t)
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb)
+              mma16816(acc[t][nb], w[2 * t][2 * j], w[2 * t + 1][2 * j], w[2 * t][2 * j + 1],
+                       w[2 * t + 1][2 * j + 1], bf[nb][2 * j], bf[nb][2 * j + 1], T());
+      }
+    }
+  }
+
+  // ---- this CTA's partial sums -> shared memory, then the cluster reduce-scatter
+  __syncthreads();                                      // done with the staged activations
+  float* part = reinterpret_cast<float*>(smem);         // [MT][kSlab]
+  // [cs][MT][kSlab / cs]: a region of its own -- peers may push into it while this CTA is
+  // still reading its staged activations.
+  float* recv = reinterpret_cast<float*>(smem + mma_recv_offset<BITS, MT>(a.units, cs));
+#pragma unroll
+  for (int t = 0; t < 2; ++t)
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+      const int col = warp * 32 + gq * 4 + 2 * t;
+      const int m = nb * 8 + 2 * tq;
+      part[m * kSlab + col] = acc[t][nb][0];
+      part[(m + 1) * kSlab + col] = acc[t][nb][1];
+      part[m * kSlab + col + 1] = acc[t][nb][2];
+      part[(m + 1) * kSlab + col + 1] = acc[t][nb][3];
+    }
+  __syncthreads();
+  const int per_rank = kSlab / cs;
+  cluster_wait();
+  for (int i = threadIdx.x; i < MT * kSlab; i += kThreads) {
+    const int m = i / kSlab, col = i - m * kSlab;
+    const int owner = col / per_rank;
+    float* dst = cluster.map_shared_rank(recv, owner);
+    dst[(rank * MT + m) * per_rank + (col - owner * per_rank)] = part[i];
+  }
+  cluster.sync();
+  T* C = static_cast<T*>(a.C);
+  for (int i = threadIdx.x; i < MT * per_rank; i += kThreads) {
+    const int m = i / per_rank, c = i - m * per_rank;
+    const int n = n_base + rank * per_rank + c;
+    if (m < a.M && n < a.N) {
+      float v = 0.f;
+      for (int q = 0; q < cs; ++q) v += recv[(q * MT + m) * per_rank + c];
+      C[static_cast<long long>(m) * a.N + n] = F16Traits<T>::from_f32(v);
+    }
+  }
+}
+
+template <int BITS, int MT, typename T, bool FOLD>
+cudaError_t launch_mma(const Problem& p, int cs, cudaStream_t stream) {
+  Args a;
+  a.A = p.A; a.M = p.M; a.K = p.K; a.N = p.N;
+  a.qweight = p.qweight; a.qzeros = p.qzeros;
+  a.scales = static_cast<const __half*>(p.scales);
+  a.g_idx = p.g_idx; a.group = p.group; a.G = p.G; a.zero_offset = p.zero_offset;
+  a.zwords = p.N * BITS / 32;
+  a.units = p.K / Pack<BITS>::kPerUnit;
+  a.C = p.out; a.status = p.status;
+  const int slabs = (p.N + kSlab - 1) / kSlab;
+  const size_t smem = mma_recv_offset<BITS, MT>(a.units, cs) + static_cast<size_t>(MT) * kSlab * 4;
+  auto kern = k_decode_mma<BITS, MT, T, FOLD>;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cs, slabs, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+}  // namespace decode
+}  // namespace gptq

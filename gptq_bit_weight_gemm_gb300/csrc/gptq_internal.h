@@ -50,7 +50,8 @@ struct QuantProblem {
 };
 cudaError_t launch_quantize(const QuantProblem& q, cudaStream_t stream);
 
-// Largest M handled by the decode (split-K GEMV) kernel.
-constexpr int kDecodeMaxM = 16;
+// Largest M handled by the decode (split-K, weight-streaming) kernels; larger M goes to the
+// tensor-core tile kernel.
+constexpr int kDecodeMaxM = 32;
 
 }  // namespace gptq

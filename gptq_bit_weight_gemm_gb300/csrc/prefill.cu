@@ -38,12 +38,11 @@ constexpr int kBM = 256;            // rows of A per tile (two UMMA M=128 halves
 constexpr int kBN = 256;            // columns per tile (UMMA N=256)
 constexpr int kBK = 64;             // k per stage: one 128-byte swizzle row of 16-bit values
 constexpr int kStages = 3;          // A + packed-W ring
-constexpr int kBStages = 2;         // dequantized-B ring
 constexpr int kEpiWarps = 4;
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr int kDqWarp0 = 6;
-constexpr int kDqWarps = 8;         // one thread per tile column
+constexpr int kDqWarps = 16;        // two threads per tile column (4 chunks each)
 constexpr int kThreads = (kDqWarp0 + kDqWarps) * 32;
 constexpr uint32_t kTmemCols = 512; // two 128 x 256 fp32 accumulators
 constexpr uint32_t kATileBytes = kBM * kBK * 2;
@@ -54,11 +53,12 @@ template <int BITS>
 struct Geo {
   static constexpr int kRows = kBK * BITS / 32;                // qweight rows per k-step
   static constexpr uint32_t kWBytes = kBN * kRows * 4;         // packed tile bytes
+  static constexpr int kBStages = BITS == 8 ? 2 : 3;           // dequantized-B ring depth
   static constexpr uint32_t kOffW = kStages * kATileBytes;
   static constexpr uint32_t kOffB = kOffW + kStages * kWBytes;
-  static constexpr uint32_t kOffBar = kOffB + kBStages * kBTileBytes;
+  static constexpr uint32_t kOffBar = kOffB + Geo::kBStages * kBTileBytes;
   // barriers: full[S], empty[S], bfull[BS], bempty[BS], acc_full, acc_empty, drain
-  static constexpr uint32_t kNumBars = 2 * kStages + 2 * kBStages + 3;
+  static constexpr uint32_t kNumBars = 2 * kStages + 2 * Geo::kBStages + 3;
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag
   static constexpr uint32_t kBytes = kOffMisc + 16;
   static constexpr size_t kDynSmem = kBytes + 1024;             // slack to align the base
@@ -109,6 +109,24 @@ __device__ __forceinline__ int zero_of(const Args& a, int g, int n) {
   return static_cast<int>(v & Pack<BITS>::kMask) + a.zero_offset;
 }
 
+// The qzeros word(s) holding column n's field in row g (loads only; decoded by zero_from).
+template <int BITS>
+__device__ __forceinline__ uint2 zero_words(const Args& a, int g, int n) {
+  const int32_t* row = a.qzeros + static_cast<long long>(g) * a.zwords;
+  const int bit = BITS * n;
+  uint2 w;
+  w.x = static_cast<uint32_t>(__ldg(row + (bit >> 5)));
+  w.y = ((bit & 31) + BITS > 32) ? static_cast<uint32_t>(__ldg(row + (bit >> 5) + 1)) : 0u;
+  return w;
+}
+template <int BITS>
+__device__ __forceinline__ int zero_from(const Args& a, uint2 w, int n) {
+  const int bit = BITS * n;
+  uint32_t v = w.x >> (bit & 31);
+  if ((bit & 31) + BITS > 32) v |= w.y << (32 - (bit & 31));
+  return static_cast<int>(v & Pack<BITS>::kMask) + a.zero_offset;
+}
+
 template <int BITS>
 __device__ __forceinline__ int clamp_group(const Args& a, int k) {
   if (a.g_idx == nullptr) return k / a.group;
@@ -120,9 +138,11 @@ __device__ __forceinline__ int clamp_group(const Args& a, int k) {
   return g;
 }
 
-// Code j (0..7) of 16-byte chunk c (0..7) of this column's packed words for one k-step.
+// Code j (0..7) of local chunk c (0..3) of one thread's half k-step (32 consecutive k), whose
+// packed words are w[0 .. R/2 - 1].
 template <int BITS>
-__device__ __forceinline__ uint32_t chunk_code(const uint32_t (&w)[Geo<BITS>::kRows], int c, int j) {
+__device__ __forceinline__ uint32_t local_code(const uint32_t (&w)[Geo<BITS>::kRows / 2], int c,
+                                               int j) {
   if constexpr (BITS == 4) {
     return (w[c] >> (4 * j)) & 15u;
   } else if constexpr (BITS == 2) {
@@ -130,8 +150,7 @@ __device__ __forceinline__ uint32_t chunk_code(const uint32_t (&w)[Geo<BITS>::kR
   } else if constexpr (BITS == 8) {
     return (w[2 * c + (j >> 2)] >> (8 * (j & 3))) & 255u;
   } else {
-    const int u = c >> 2;
-    return code3(w[3 * u], w[3 * u + 1], w[3 * u + 2], 8 * (c & 3) + j);
+    return code3(w[0], w[1], w[2], 8 * c + j);
   }
 }
 
@@ -247,6 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     k_prefill(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
               const Args a) {
   using Gm = Geo<BITS>;
+  constexpr int kBStages = Gm::kBStages;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -368,8 +388,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= kDqWarp0) {
     // ---------------------------------------------------------------- dequantizers
-    const int col = threadIdx.x - kDqWarp0 * 32;   // 0..255: tile column of this thread
-    const int dq_lane = lane;
+    // Two threads per tile column: thread (col, hf) dequantizes chunks 4 hf .. 4 hf + 3 of
+    // column col (k = 32 hf .. 32 hf + 31 of the k-step), i.e. words hf R/2 .. hf R/2 + R/2 - 1.
+    constexpr int kHalfRows = Gm::kRows / 2;
+    const int dq = threadIdx.x - kDqWarp0 * 32;
+    const int col = dq % kBN;
+    const int hf = dq / kBN;
     int s = 0, sb = 0;
     uint32_t ph = 0, phb = 0;
     bool ok = true;
@@ -379,65 +403,79 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool n_ok = n < a.N;
       const int nc = n_ok ? n : a.N - 1;      // clamped column for scale/zero reads
       int gnext = 0;                          // first k of the next group (fast path)
+      int pf_g = -1;                          // group whose scale/zero are prefetched
+      uint16_t pf_s = 0;
+      uint2 pf_z = make_uint2(0u, 0u);
       ColConsts<BITS, T> cc;
       for (int ks = 0; ks < ksteps; ++ks) {
         if (!wait_bar(sy, full(s), ph)) { ok = false; break; }
-        uint32_t w[Gm::kRows];
+        uint32_t wl[kHalfRows];
         const uint32_t* wt = reinterpret_cast<const uint32_t*>(smem + Gm::kOffW + s * Gm::kWBytes);
 #pragma unroll
-        for (int r = 0; r < Gm::kRows; ++r) w[r] = wt[r * kBN + col];
+        for (int r = 0; r < kHalfRows; ++r) wl[r] = wt[(hf * kHalfRows + r) * kBN + col];
         __syncwarp();
-        if (dq_lane == 0) ptx::mbar_arrive(empty(s));
+        if (lane == 0) ptx::mbar_arrive(empty(s));
         if (!wait_bar(sy, bempty(sb), phb ^ 1u)) { ok = false; break; }
         unsigned char* bt = smem + Gm::kOffB + sb * kBTileBytes;
-        const int kst = ks * kBK;
+        const int kst = ks * kBK + 32 * hf;     // first k of this thread's half of the k-step
         if constexpr (!PERK) {
-          // one group per 16 k at least (fast-path condition): track it without division
+          // One group per 16 k at least (fast-path condition), tracked without division.  The
+          // next group's scale and zero word are prefetched into registers one group ahead so
+          // that no global load sits on the dequant critical path.
           auto group_at = [&](int k) {
             if (k >= gnext) {
-              const int g = k / a.group;
+              if (pf_g < 0 || k >= (pf_g + 1) * a.group || k < pf_g * a.group) {
+                pf_g = k / a.group;                      // first group of the tile: load now
+                pf_s = __half_as_ushort(__ldg(a.scales + static_cast<long long>(pf_g) * a.N + nc));
+                pf_z = zero_words<BITS>(a, pf_g, nc);
+              }
+              const int g = pf_g;
               gnext = (g + 1) * a.group;
-              const uint16_t sb16 = __half_as_ushort(a.scales[static_cast<long long>(g) * a.N + nc]);
-              cc.set(__half2float(__ushort_as_half(sb16)), sb16, zero_of<BITS>(a, g, nc));
+              cc.set(__half2float(__ushort_as_half(pf_s)), pf_s, zero_from<BITS>(a, pf_z, nc));
+              if (gnext < a.K) {                          // prefetch group g + 1
+                pf_g = g + 1;
+                pf_s = __half_as_ushort(__ldg(a.scales + static_cast<long long>(pf_g) * a.N + nc));
+                pf_z = zero_words<BITS>(a, pf_g, nc);
+              }
             }
           };
           if constexpr (BITS == 4) {
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
+            for (int c = 0; c < 4; ++c) {
               const int k0 = kst + 8 * c;
               uint4 out = make_uint4(0u, 0u, 0u, 0u);
               if (k0 < a.K) {
                 group_at(k0);
-                if (n_ok) out = dq_chunk4<T>(w[c], cc);
+                if (n_ok) out = dq_chunk4<T>(wl[c], cc);
               }
-              *reinterpret_cast<uint4*>(bt + swz(col, c)) = out;
+              *reinterpret_cast<uint4*>(bt + swz(col, 4 * hf + c)) = out;
             }
           } else if constexpr (BITS == 2) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            for (int i = 0; i < 2; ++i) {
               const int k0 = kst + 16 * i;
               uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
               if (k0 < a.K) {
                 group_at(k0);
-                if (n_ok) dq_chunks2<T>(w[i], cc, lo, hi);
+                if (n_ok) dq_chunks2<T>(wl[i], cc, lo, hi);
               }
-              *reinterpret_cast<uint4*>(bt + swz(col, 2 * i)) = lo;
-              *reinterpret_cast<uint4*>(bt + swz(col, 2 * i + 1)) = hi;
+              *reinterpret_cast<uint4*>(bt + swz(col, 4 * hf + 2 * i)) = lo;
+              *reinterpret_cast<uint4*>(bt + swz(col, 4 * hf + 2 * i + 1)) = hi;
             }
           } else if constexpr (BITS == 8) {
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
+            for (int c = 0; c < 4; ++c) {
               const int k0 = kst + 8 * c;
               uint4 out = make_uint4(0u, 0u, 0u, 0u);
               if (k0 < a.K) {
                 group_at(k0);
-                if (n_ok) out = dq_chunk8<T>(w[2 * c], w[2 * c + 1], cc);
+                if (n_ok) out = dq_chunk8<T>(wl[2 * c], wl[2 * c + 1], cc);
               }
-              *reinterpret_cast<uint4*>(bt + swz(col, c)) = out;
+              *reinterpret_cast<uint4*>(bt + swz(col, 4 * hf + c)) = out;
             }
           } else {
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
+            for (int c = 0; c < 4; ++c) {
               const int k0 = kst + 8 * c;
               uint4 out = make_uint4(0u, 0u, 0u, 0u);
               if (k0 < a.K) {
@@ -445,17 +483,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (n_ok) {
                   float v[8];
 #pragma unroll
-                  for (int j = 0; j < 8; ++j) v[j] = diff_f32(chunk_code<BITS>(w, c, j), cc.z) * cc.s;
+                  for (int j = 0; j < 8; ++j) v[j] = diff_f32(local_code<BITS>(wl, c, j), cc.z) * cc.s;
                   out = make_uint4(pack2(v[0], v[1], T()), pack2(v[2], v[3], T()),
                                    pack2(v[4], v[5], T()), pack2(v[6], v[7], T()));
                 }
               }
-              *reinterpret_cast<uint4*>(bt + swz(col, c)) = out;
+              *reinterpret_cast<uint4*>(bt + swz(col, 4 * hf + c)) = out;
             }
           }
         } else {
 #pragma unroll
-          for (int c = 0; c < kBK / 8; ++c) {
+          for (int c = 0; c < 4; ++c) {
             const int k0 = kst + c * 8;
             uint4 out = make_uint4(0u, 0u, 0u, 0u);
             if (n_ok && k0 < a.K) {
@@ -464,12 +502,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int j = 0; j < 8; ++j) {
                 const int g = clamp_group<BITS>(a, k0 + j);
                 const float sj = __half2float(a.scales[static_cast<long long>(g) * a.N + n]);
-                v[j] = diff_f32(chunk_code<BITS>(w, c, j), zero_of<BITS>(a, g, n)) * sj;
+                v[j] = diff_f32(local_code<BITS>(wl, c, j), zero_of<BITS>(a, g, n)) * sj;
               }
               out = make_uint4(pack2(v[0], v[1], T()), pack2(v[2], v[3], T()),
                                pack2(v[4], v[5], T()), pack2(v[6], v[7], T()));
             }
-            *reinterpret_cast<uint4*>(bt + swz(col, c)) = out;
+            *reinterpret_cast<uint4*>(bt + swz(col, 4 * hf + c)) = out;
           }
         }
         ptx::fence_proxy_async_smem();

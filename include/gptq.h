@@ -91,9 +91,9 @@ int gptq_dequant(const int32_t* qweight, const int32_t* qzeros, const void* scal
  * gptq_gemm -- C[M, N] = A[M, K] @ W[K, N] with W dequantized on the fly, the operation
  * vLLM's gptq_gemm(..., use_v2_format) performs (page section "调整细节：根据格式选择处理
  * 方式"; fmt == GPTQ_FMT_V2 is use_v2_format = true).  Products are accumulated in fp32 and
- * C is rounded once to A's dtype.  M <= 16 runs the memory-bound decode kernel (split-K
- * over a thread-block cluster, reduced through distributed shared memory); larger M runs
- * the tcgen05 tensor-core kernel.
+ * C is rounded once to A's dtype.  M <= 32 runs the memory-bound decode kernels (split-K
+ * over a thread-block cluster, reduced through distributed shared memory; CUDA cores for
+ * M <= 4, mma.sync from registers above); larger M runs the tcgen05 tensor-core kernel.
  * Device pointers: A, qweight, qzeros, scales, g_idx (nullable), C.  `workspace` may be NULL
  * when gptq_gemm_workspace_size() returns 0 (every current path); otherwise it must be a
  * device buffer of at least that many bytes, owned by the caller.
