@@ -25,7 +25,10 @@
 //    fp32 product, one rounding), accumulated across groups.
 #pragma once
 
+#include <cuda.h>
+
 #include "decode.cuh"
+#include "sm100_ptx.cuh"
 
 namespace gptq {
 namespace decode {
@@ -56,34 +59,66 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Words of the staged activations for one unit (all MT tokens x NP pairs), padded so that the
-// 16-byte loads of a warp's 4 units x 8 tokens fall in distinct bank groups.
-template <int MT, int NP>
-__host__ __device__ constexpr int unit_words() {
-  return MT * NP + ((8 - (MT * NP) % 32) + 32) % 32;
+// Words of the staged activations for one unit (the M real tokens x NP pairs), padded so that
+// the 16-byte loads of a warp's 4 units fall in distinct bank groups.
+__host__ __device__ constexpr int unit_words(int M, int NP) {
+  return M * NP + ((8 - (M * NP) % 32) + 32) % 32;
 }
 
-// Shared memory: [staged activations | partial sums] (aliased in time), then the receive slots.
-template <int BITS, int MT>
-__host__ __device__ constexpr size_t mma_recv_offset(int units, int cs) {
-  const size_t tiles_per_cta = static_cast<size_t>(((units + 3) / 4 + cs - 1) / cs);
-  const size_t stage = tiles_per_cta * 4 * unit_words<MT, MmaPairs<BITS>::kPairs>() * 4;
-  const size_t part = static_cast<size_t>(MT) * kSlab * 4;
-  const size_t m = stage > part ? stage : part;
-  return (m + 15) & ~static_cast<size_t>(15);
+// Launch geometry shared by host and device.
+struct TmaGeo {
+  int cs;              // CTAs per cluster (K split)
+  int tiles_per_cta;   // k-tiles (4 units each) of the largest CTA range
+  int chunk_tiles;     // k-tiles per TMA chunk
+  int nbuf;            // chunk buffers (all chunks in flight when nbuf == chunks)
+  int chunk_bytes;     // 128 columns x chunk rows x 4 bytes
+};
+
+// Shared memory of one CTA: [weight chunk buffers][activation pairs | partial sums (aliased in
+// time)][receive slots][mbarriers + abort flag].
+// Activations, partial sums and receive slots are sized by the real token count M, not by the
+// MMA token block: at one token the slice of weights dominates and five CTAs fit on an SM.
+template <int BITS>
+struct TmaSmem {
+  __host__ __device__ static size_t stage_bytes(const TmaGeo& g, int M) {
+    const size_t stage = static_cast<size_t>(g.tiles_per_cta) * 4 * unit_words(M, MmaPairs<BITS>::kPairs) * 4;
+    const size_t part = static_cast<size_t>(M) * kSlab * 4;
+    return ((stage > part ? stage : part) + 127) & ~static_cast<size_t>(127);
+  }
+  __host__ __device__ static size_t off_stage(const TmaGeo& g) {
+    return static_cast<size_t>(g.nbuf) * g.chunk_bytes;
+  }
+  __host__ __device__ static size_t bytes(const TmaGeo& g, int M) {
+    return off_stage(g) + stage_bytes(g, M) + static_cast<size_t>(M) * kSlab * 4 + 8 * 16 + 4 * 17;
+  }
+};
+
+__device__ __forceinline__ bool tma_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                         unsigned* status) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer();
+  while (true) {
+    if (ptx::mbar_try_wait_hint(bar, parity, 100000u)) return true;
+    if (*abort_flag) return false;
+    if (ptx::globaltimer() - t0 > 2000000000ull) {
+      *abort_flag = 1;
+      atomicOr(status, kStatusTimeout);
+      return false;
+    }
+  }
 }
 
 template <int BITS, int MT, typename T, bool FOLD>
-__global__ void __launch_bounds__(kThreads) k_decode_mma(const Args a) {
+__global__ void __launch_bounds__(kThreads, (MT <= 8 && BITS != 3 ? 5 : 1))
+    k_decode_mma(const __grid_constant__ CUtensorMap tmW, const Args a, const TmaGeo geo) {
   using P = Pack<BITS>;
   using MP = MmaPairs<BITS>;
   constexpr int PER = P::kPerUnit;
   constexpr int ROWS = P::kRowsPerUnit;
   constexpr int NP = MP::kPairs;
   constexpr int NB = MT / 8;                          // token blocks of 8
-  constexpr int UW = unit_words<MT, NP>();
-  constexpr int RING = ROWS == 3 ? 2 : 4;             // k-tiles of loads in flight per thread
-  extern __shared__ __align__(16) unsigned char smem[];
+  const int UW = unit_words(a.M, NP);
+  extern __shared__ __align__(128) unsigned char smem[];
 
   pdl_launch_dependents();
   cluster_arrive_relaxed();
@@ -102,42 +137,42 @@ __global__ void __launch_bounds__(kThreads) k_decode_mma(const Args a) {
   split(tiles_total, cs, rank, ct0, ct1);
   const int cu0 = ct0 * 4;
   const int ntile = ct1 - ct0;
+  const int nchunk = (ntile + geo.chunk_tiles - 1) / geo.chunk_tiles;
+  const int chunk_rows = geo.chunk_tiles * 4 * ROWS;
 
-  const long long ustride = static_cast<long long>(ROWS) * a.N;
-  const int32_t* qw = a.qweight + n0c;
-  auto unit_ptr = [&](int u, int r) { return qw + u * ustride + static_cast<long long>(r) * a.N; };
-  auto load_tile = [&](uint4 (&dst)[ROWS], int kt) {
-    const int u = cu0 + kt * 4 + tq;
-    if (u < a.units) {
-#pragma unroll
-      for (int r = 0; r < ROWS; ++r) dst[r] = ld_stream_v4(unit_ptr(u, r));
-    }
+  uint8_t* sbuf = smem;                                               // weight chunks
+  uint32_t* sB = reinterpret_cast<uint32_t*>(smem + TmaSmem<BITS>::off_stage(geo));
+  float* recv = reinterpret_cast<float*>(smem + TmaSmem<BITS>::off_stage(geo) +
+                                         TmaSmem<BITS>::stage_bytes(geo, a.M));
+  uint8_t* misc = reinterpret_cast<uint8_t*>(recv + a.M * kSlab);
+  const uint32_t bar0 = ptx::smem_addr(misc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 8 * 16);
+
+  // Issue the packed slice into shared memory: chunk c of this CTA lands in buffer c % nbuf.
+  // The copies read weights only; they are issued before griddepcontrol.wait because global
+  // memory (through L2) is coherent for them and the weights are not produced by the kernel
+  // this one may overlap with.
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < geo.nbuf; ++b) ptx::mbar_init(bar0 + 8 * b, 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  volatile int* last_issued = abort_flag + 1;          // [nbuf] last chunk issued per buffer
+  auto issue = [&](int c) {
+    const int b = c % geo.nbuf;
+    last_issued[b] = c;
+    ptx::mbar_arrive_expect_tx(bar0 + 8 * b, static_cast<uint32_t>(geo.chunk_bytes));
+    ptx::tma_load_2d(ptx::smem_addr(sbuf + static_cast<size_t>(b) * geo.chunk_bytes), &tmW, n_base,
+                     (cu0 + c * geo.chunk_tiles * 4) * ROWS, bar0 + 8 * b);
   };
-  for (int kt = 0; kt < ntile; ++kt) {                 // L2 warm-up, safe before the wait
-    const int u = cu0 + kt * 4 + tq;
-    if (u < a.units) {
-#pragma unroll
-      for (int r = 0; r < ROWS; ++r) prefetch_l2(unit_ptr(u, r));
-    }
-  }
+  if (threadIdx.x == 0)
+    for (int c = 0; c < nchunk && c < geo.nbuf; ++c) issue(c);
   pdl_wait();
-  uint4 ring[RING][ROWS];
-#pragma unroll
-  for (int i = 0; i < RING; ++i) {
-#pragma unroll
-    for (int r = 0; r < ROWS; ++r) ring[i][r] = make_uint4(0u, 0u, 0u, 0u);
-    if (i < ntile) load_tile(ring[i], i);
-  }
 
   // Stage activations: sB[u][m][p] = (a[m][k0 + lo_k(p)], a[m][k0 + hi_k(p)]), zero past K or M.
-  uint32_t* sB = reinterpret_cast<uint32_t*>(smem);
   const uint16_t* A16 = static_cast<const uint16_t*>(a.A);
   const int nunits = ntile * 4;
-  if (a.M < MT)                                          // token rows past M are zero
-    for (int i = threadIdx.x; i < nunits * MT * NP; i += kThreads) {
-      const int p = i % NP, um = i / NP, m = um % MT, uu = um / MT;
-      if (m >= a.M) sB[uu * UW + m * NP + p] = 0u;
-    }
   stage_pairs<PER, NP>(A16, a.M, a.K, cu0, nunits, a.units,
                        [](int p) { return MP::lo_k(p); }, [](int p) { return MP::hi_k(p); },
                        [&](int uu, int m, int p, uint32_t v) { sB[uu * UW + m * NP + p] = v; });
@@ -155,6 +190,11 @@ __global__ void __launch_bounds__(kThreads) k_decode_mma(const Args a) {
   auto load_b = [&](int kt, uint32_t (&bf)[NB][NP]) {
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) {
+      if (8 * nb + gq >= a.M) {                         // absent token: zero B column
+#pragma unroll
+        for (int i = 0; i < NP; ++i) bf[nb][i] = 0u;
+        continue;
+      }
       const uint32_t* src = sB + (kt * 4 + tq) * UW + (8 * nb + gq) * NP;
       if constexpr (NP % 4 == 0) {
 #pragma unroll
@@ -207,18 +247,19 @@ __global__ void __launch_bounds__(kThreads) k_decode_mma(const Args a) {
         }
     };
     if (ntile > 0) set_group();
-    for (int kt0 = 0; kt0 < ntile; kt0 += RING) {
-#pragma unroll
-      for (int i = 0; i < RING; ++i) {
-        const int kt = kt0 + i;
-        if (kt >= ntile) break;
-        const uint4 wv = ring[i][0];
-        if (kt + RING < ntile) load_tile(ring[i], kt + RING);
+    for (int c = 0; c < nchunk; ++c) {
+      const bool ok = tma_wait(bar0 + 8 * (c % geo.nbuf), (c / geo.nbuf) & 1, abort_flag, a.status);
+      const uint8_t* cb = sbuf + static_cast<size_t>(c % geo.nbuf) * geo.chunk_bytes;
+      const int kt_end = (c + 1) * geo.chunk_tiles < ntile ? (c + 1) * geo.chunk_tiles : ntile;
+      for (int kt = c * geo.chunk_tiles; ok && kt < kt_end; ++kt) {
+        const int rl = (kt - c * geo.chunk_tiles) * 4 + tq;          // unit row in the chunk
+        const uint4 wv = *reinterpret_cast<const uint4*>(cb + static_cast<size_t>(rl) * (kSlab * 4) +
+                                                         (warp * 32 + gq * 4) * 4);
         uint32_t bf[NB][NP];
         load_b(kt, bf);
         uint32_t d[4][NP];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) DP::run((&wv.x)[c], kz[c], d[c]);
+        for (int cc = 0; cc < 4; ++cc) DP::run((&wv.x)[cc], kz[cc], d[cc]);
 #pragma unroll
         for (int j = 0; j < NP / 2; ++j)
 #pragma unroll
@@ -238,18 +279,24 @@ __global__ void __launch_bounds__(kThreads) k_decode_mma(const Args a) {
           }
         }
       }
+      if (c + geo.nbuf < nchunk) {                      // refill this buffer with chunk c + nbuf
+        __syncthreads();
+        if (threadIdx.x == 0 && !*abort_flag) { ptx::fence_proxy_async_smem(); issue(c + geo.nbuf); }
+      }
     }
     if (ntile > 0 && left != tpg) fold();
   } else {
-    for (int kt0 = 0; kt0 < ntile; kt0 += RING) {
-#pragma unroll
-      for (int i = 0; i < RING; ++i) {
-        const int kt = kt0 + i;
-        if (kt >= ntile) break;
+    for (int c = 0; c < nchunk; ++c) {
+      const bool ok = tma_wait(bar0 + 8 * (c % geo.nbuf), (c / geo.nbuf) & 1, abort_flag, a.status);
+      const uint8_t* cb = sbuf + static_cast<size_t>(c % geo.nbuf) * geo.chunk_bytes;
+      const int kt_end = (c + 1) * geo.chunk_tiles < ntile ? (c + 1) * geo.chunk_tiles : ntile;
+      for (int kt = c * geo.chunk_tiles; ok && kt < kt_end; ++kt) {
+        const int rl = ((kt - c * geo.chunk_tiles) * 4 + tq) * ROWS;  // first row of the unit
         uint4 wv[ROWS];
 #pragma unroll
-        for (int r = 0; r < ROWS; ++r) wv[r] = ring[i][r];
-        if (kt + RING < ntile) load_tile(ring[i], kt + RING);
+        for (int r = 0; r < ROWS; ++r)
+          wv[r] = *reinterpret_cast<const uint4*>(cb + static_cast<size_t>(rl + r) * (kSlab * 4) +
+                                                  (warp * 32 + gq * 4) * 4);
         uint32_t bf[NB][NP];
         load_b(kt, bf);
         const int u = cu0 + kt * 4 + tq;
@@ -272,10 +319,10 @@ __global__ void __launch_bounds__(kThreads) k_decode_mma(const Args a) {
               cur_g = gg;
             }
 #pragma unroll
-            for (int c = 0; c < 4; ++c) v[c][h] = diff_f32(unit_code<BITS>(wv, c, j), z[c]) * s[c];
+            for (int cc = 0; cc < 4; ++cc) v[cc][h] = diff_f32(unit_code<BITS>(wv, cc, j), z[cc]) * s[cc];
           }
 #pragma unroll
-          for (int c = 0; c < 4; ++c) w[c][p] = pack2(v[c][0], v[c][1], T());
+          for (int cc = 0; cc < 4; ++cc) w[cc][p] = pack2(v[cc][0], v[cc][1], T());
         }
 #pragma unroll
         for (int j = 0; j < NP / 2; ++j)
@@ -286,46 +333,86 @@ __global__ void __launch_bounds__(kThreads) k_decode_mma(const Args a) {
               mma16816(acc[t][nb], w[2 * t][2 * j], w[2 * t + 1][2 * j], w[2 * t][2 * j + 1],
                        w[2 * t + 1][2 * j + 1], bf[nb][2 * j], bf[nb][2 * j + 1], T());
       }
+      if (c + geo.nbuf < nchunk) {
+        __syncthreads();
+        if (threadIdx.x == 0 && !*abort_flag) { ptx::fence_proxy_async_smem(); issue(c + geo.nbuf); }
+      }
     }
   }
 
   // ---- this CTA's partial sums -> shared memory, then the cluster reduce-scatter
   __syncthreads();                                      // done with the staged activations
-  float* part = reinterpret_cast<float*>(smem);         // [MT][kSlab]
-  // [cs][MT][kSlab / cs]: a region of its own -- peers may push into it while this CTA is
-  // still reading its staged activations.
-  float* recv = reinterpret_cast<float*>(smem + mma_recv_offset<BITS, MT>(a.units, cs));
+  float* part = reinterpret_cast<float*>(sB);           // [M][kSlab], aliases the staging
+  // recv ([cs][M][kSlab / cs]) has a region of its own: peers may push into it while this CTA
+  // is still reading its staged activations.
+  const int Mr = a.M;
 #pragma unroll
   for (int t = 0; t < 2; ++t)
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) {
       const int col = warp * 32 + gq * 4 + 2 * t;
       const int m = nb * 8 + 2 * tq;
-      part[m * kSlab + col] = acc[t][nb][0];
-      part[(m + 1) * kSlab + col] = acc[t][nb][1];
-      part[m * kSlab + col + 1] = acc[t][nb][2];
-      part[(m + 1) * kSlab + col + 1] = acc[t][nb][3];
+      if (m < Mr) {
+        part[m * kSlab + col] = acc[t][nb][0];
+        part[m * kSlab + col + 1] = acc[t][nb][2];
+      }
+      if (m + 1 < Mr) {
+        part[(m + 1) * kSlab + col] = acc[t][nb][1];
+        part[(m + 1) * kSlab + col + 1] = acc[t][nb][3];
+      }
     }
   __syncthreads();
   const int per_rank = kSlab / cs;
   cluster_wait();
-  for (int i = threadIdx.x; i < MT * kSlab; i += kThreads) {
+  for (int i = threadIdx.x; i < Mr * kSlab; i += kThreads) {
     const int m = i / kSlab, col = i - m * kSlab;
     const int owner = col / per_rank;
     float* dst = cluster.map_shared_rank(recv, owner);
-    dst[(rank * MT + m) * per_rank + (col - owner * per_rank)] = part[i];
+    dst[(rank * Mr + m) * per_rank + (col - owner * per_rank)] = part[i];
   }
   cluster.sync();
   T* C = static_cast<T*>(a.C);
-  for (int i = threadIdx.x; i < MT * per_rank; i += kThreads) {
+  for (int i = threadIdx.x; i < Mr * per_rank; i += kThreads) {
     const int m = i / per_rank, c = i - m * per_rank;
     const int n = n_base + rank * per_rank + c;
-    if (m < a.M && n < a.N) {
+    if (n < a.N) {
       float v = 0.f;
-      for (int q = 0; q < cs; ++q) v += recv[(q * MT + m) * per_rank + c];
+      for (int q = 0; q < cs; ++q) v += recv[(q * Mr + m) * per_rank + c];
       C[static_cast<long long>(m) * a.N + n] = F16Traits<T>::from_f32(v);
     }
   }
+  if (*abort_flag && threadIdx.x == 0) {
+    // after a timeout, let every copy already issued land before shared memory is released
+    const uint64_t t0 = ptx::globaltimer();
+    for (int b = 0; b < nchunk && b < geo.nbuf; ++b) {
+      const int last = last_issued[b];
+      while (!ptx::mbar_try_wait(bar0 + 8 * b, (last / geo.nbuf) & 1) &&
+             ptx::globaltimer() - t0 < 2000000000ull) {}
+    }
+  }
+}
+
+// Chunking of a CTA range of `tiles` k-tiles: chunks of at most ~16 KB (128 columns x rows),
+// as many buffers as fit in about 48 KB; the chunk divides the range when it can so the boxes
+// do not read past it.
+template <int BITS>
+TmaGeo make_geo(int units, int cs) {
+  constexpr int ROWS = Pack<BITS>::kRowsPerUnit;
+  TmaGeo g;
+  g.cs = cs;
+  const int tiles_total = (units + 3) / 4;
+  g.tiles_per_cta = (tiles_total + cs - 1) / cs;
+  const int max_tiles = (16 * 1024) / (4 * ROWS * kSlab * 4);   // k-tiles per 16 KB chunk
+  int ct = 1;
+  for (int d = 1; d <= max_tiles && d <= g.tiles_per_cta; ++d)
+    if (g.tiles_per_cta % d == 0) ct = d;
+  g.chunk_tiles = ct;
+  g.chunk_bytes = ct * 4 * ROWS * kSlab * 4;
+  const int chunks = (g.tiles_per_cta + ct - 1) / ct;
+  const int fit = (48 * 1024) / g.chunk_bytes;
+  g.nbuf = chunks < fit ? chunks : (fit < 1 ? 1 : fit);
+  if (g.nbuf > 16) g.nbuf = 16;
+  return g;
 }
 
 template <int BITS, int MT, typename T, bool FOLD>
@@ -338,8 +425,21 @@ cudaError_t launch_mma(const Problem& p, int cs, cudaStream_t stream) {
   a.zwords = p.N * BITS / 32;
   a.units = p.K / Pack<BITS>::kPerUnit;
   a.C = p.out; a.status = p.status;
+  const TmaGeo geo = make_geo<BITS>(a.units, cs);
+  CUtensorMap tmW;
+  {
+    constexpr int ROWS = Pack<BITS>::kRowsPerUnit;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.N), static_cast<cuuint64_t>(a.units) * ROWS};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.N) * 4};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kSlab),
+                               static_cast<cuuint32_t>(geo.chunk_tiles * 4 * ROWS)};
+    const cuuint32_t estr[2] = {1, 1};
+    if (!encode_tensor_map(&tmW, CU_TENSOR_MAP_DATA_TYPE_INT32, const_cast<int32_t*>(p.qweight), dims,
+                           strides, box, estr, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return cudaErrorInvalidValue;
+  }
   const int slabs = (p.N + kSlab - 1) / kSlab;
-  const size_t smem = mma_recv_offset<BITS, MT>(a.units, cs) + static_cast<size_t>(MT) * kSlab * 4;
+  const size_t smem = TmaSmem<BITS>::bytes(geo, p.M);
   auto kern = k_decode_mma<BITS, MT, T, FOLD>;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -360,7 +460,7 @@ cudaError_t launch_mma(const Problem& p, int cs, cudaStream_t stream) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kern, a);
+  return cudaLaunchKernelEx(&cfg, kern, tmW, a, geo);
 }
 
 }  // namespace decode

@@ -1,5 +1,7 @@
 // gptq_api.cu -- the C ABI (include/gptq.h): host-side validation, dispatch, the host v1 -> v2
 // zero repack and the device status word.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -110,6 +112,26 @@ int device_ready(Problem* p) {
 int from_cuda(cudaError_t e) { return e == cudaSuccess ? GPTQ_OK : GPTQ_ERR_CUDA; }
 
 }  // namespace
+
+bool encode_tensor_map(void* tmap, int dtype, void* base, const uint64_t* dims,
+                       const uint64_t* strides, const uint32_t* box, const uint32_t* estr,
+                       int swizzle) {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, []() {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  if (!fn) return false;
+  return fn(static_cast<CUtensorMap*>(tmap), static_cast<CUtensorMapDataType>(dtype), 2, base,
+            reinterpret_cast<const cuuint64_t*>(dims), reinterpret_cast<const cuuint64_t*>(strides),
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, static_cast<CUtensorMapSwizzle>(swizzle),
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 const DeviceInfo& device_info() {
   cudaError_t err;

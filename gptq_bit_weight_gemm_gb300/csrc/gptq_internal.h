@@ -50,6 +50,12 @@ struct QuantProblem {
 };
 cudaError_t launch_quantize(const QuantProblem& q, cudaStream_t stream);
 
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link); false if
+// the driver refuses the map.  `dtype` is a CUtensorMapDataType, `swizzle` a CUtensorMapSwizzle.
+bool encode_tensor_map(void* tmap, int dtype, void* base, const uint64_t* dims,
+                       const uint64_t* strides, const uint32_t* box, const uint32_t* estr,
+                       int swizzle);
+
 // Largest M handled by the decode (split-K, weight-streaming) kernels; larger M goes to the
 // tensor-core tile kernel.
 constexpr int kDecodeMaxM = 32;
