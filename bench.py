@@ -131,6 +131,23 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(sel), "window": window}
 
 
+# ------------------------------------------------------------------------------------ ranks
+def max_over_ranks(x, dist, device):
+    """The largest value of x over all ranks (x itself on one rank)."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(world, bytes_per_step, steps, seconds):
+    """Throughput of the whole job: every rank processed `steps` steps of `bytes_per_step`
+    (weak scaling: per-rank work is fixed), timed by the slowest rank."""
+    return world * bytes_per_step * steps / seconds / 1e9
+
+
 # ------------------------------------------------------------------------------------ our arm
 def run_ours(args, rank, world, local_rank):
     import torch
@@ -213,13 +230,9 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     t1 = time.time()
     barrier()
-    ms_total = start.elapsed_time(end)
-    if dist is not None:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(start.elapsed_time(end), dist, dev)
     ms_per_step = ms_total / args.steps
-    value = world * set_bytes * args.steps / (ms_total * 1e-3) / 1e9    # GB/s over all ranks
+    value = whole_job_gbs(world, set_bytes, args.steps, ms_total * 1e-3)   # GB/s over all ranks
     kernel_gbs = set_bytes / (ms_per_step * 1e-3) / 1e9                 # per launch, this GPU
 
     # ---- end to end through the public API: A from pinned host memory, C read back
@@ -242,12 +255,8 @@ def run_ours(args, rank, world, local_rank):
             c_host.copy_(c, non_blocking=True)
             stream.synchronize()
         te1 = time.perf_counter()
-    e2e_s = te1 - te0
-    if dist is not None:
-        t = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
-    e2e_value = world * set_bytes * n_e2e / e2e_s / 1e9
+    e2e_s = max_over_ranks(te1 - te0, dist, dev)
+    e2e_value = whole_job_gbs(world, set_bytes, n_e2e, e2e_s)
     sampler.stop()
     clocks = sampler.summary(t0, t1)
 

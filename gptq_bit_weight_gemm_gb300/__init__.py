@@ -56,6 +56,7 @@ _SIGNATURES = {
     "gptq_quantize_rtn": (_I, [_P, _I, _I, _I, _I, _P, _I, _I, _P, _P, _P, _P]),
     "gptq_get_device_status": (_I, [_P, ctypes.POINTER(ctypes.c_uint)]),
     "gptq_strerror": (ctypes.c_char_p, [_I]),
+    "gptq_selftest_wait_timeout": (_I, [ctypes.c_ulonglong, _P, _P]),
 }
 
 
@@ -80,6 +81,16 @@ def header_functions():
     with open(HEADER) as f:
         text = f.read()
     return sorted(set(re.findall(r"^\s*(?:int|size_t|const char\s*\*)\s+(gptq_\w+)\s*\(", text, re.M)))
+
+
+def selftest_wait_timeout(limit_ns=50_000_000, stream=None):
+    """Run the bounded-wait self-test; returns (waited_out, status bits)."""
+    torch = _torch()
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    _check(lib().gptq_selftest_wait_timeout(int(limit_ns), _ptr(flag), _stream(stream)),
+           "gptq_selftest_wait_timeout")
+    status = device_status(stream)
+    return int(flag.item()), status
 
 
 def _check(rc, what):

@@ -133,14 +133,14 @@ __device__ __forceinline__ void stage_pairs(const uint16_t* A, int M, int K, int
 #pragma unroll
     for (int j = 0; j < kStageBatch; ++j) {
       const int it = base + j * static_cast<int>(blockDim.x) + static_cast<int>(threadIdx.x);
-      const int uu = it / M, m = it - uu * M;
+      const int uu = M == 1 ? it : it / M, m = it - uu * M;
       if (it < items && ufirst + uu < units)
         v[j].load(A + static_cast<long long>(m) * K + static_cast<long long>(ufirst + uu) * PER);
     }
 #pragma unroll
     for (int j = 0; j < kStageBatch; ++j) {
       const int it = base + j * static_cast<int>(blockDim.x) + static_cast<int>(threadIdx.x);
-      const int uu = it / M, m = it - uu * M;
+      const int uu = M == 1 ? it : it / M, m = it - uu * M;
       if (it < items) {
         const bool live = ufirst + uu < units;
 #pragma unroll

@@ -65,13 +65,18 @@ __host__ __device__ constexpr int unit_words(int M, int NP) {
   return M * NP + ((8 - (M * NP) % 32) + 32) % 32;
 }
 
+// Shared-memory row stride of a staged weight row: 128 columns, unpadded, because a tiled TMA
+// copy must land on a 128-byte aligned shared address (one box covers a whole chunk).
+constexpr int kRowStride = kSlab * 4;
+
 // Launch geometry shared by host and device.
 struct TmaGeo {
   int cs;              // CTAs per cluster (K split)
   int tiles_per_cta;   // k-tiles (4 units each) of the largest CTA range
   int chunk_tiles;     // k-tiles per TMA chunk
   int nbuf;            // chunk buffers (all chunks in flight when nbuf == chunks)
-  int chunk_bytes;     // 128 columns x chunk rows x 4 bytes
+  int chunk_bytes;     // chunk rows x kRowStride (bytes of shared memory per buffer)
+  int chunk_rows;      // rows per chunk
 };
 
 // Shared memory of one CTA: [weight chunk buffers][activation pairs | partial sums (aliased in
@@ -162,9 +167,10 @@ __global__ void __launch_bounds__(kThreads, (MT <= 8 && BITS != 3 ? 5 : 1))
   auto issue = [&](int c) {
     const int b = c % geo.nbuf;
     last_issued[b] = c;
-    ptx::mbar_arrive_expect_tx(bar0 + 8 * b, static_cast<uint32_t>(geo.chunk_bytes));
-    ptx::tma_load_2d(ptx::smem_addr(sbuf + static_cast<size_t>(b) * geo.chunk_bytes), &tmW, n_base,
-                     (cu0 + c * geo.chunk_tiles * 4) * ROWS, bar0 + 8 * b);
+    const uint32_t dst = ptx::smem_addr(sbuf + static_cast<size_t>(b) * geo.chunk_bytes);
+    const int row0 = (cu0 + c * geo.chunk_tiles * 4) * ROWS;
+    ptx::mbar_arrive_expect_tx(bar0 + 8 * b, static_cast<uint32_t>(geo.chunk_rows * kSlab * 4));
+    ptx::tma_load_2d(dst, &tmW, n_base, row0, bar0 + 8 * b);
   };
   if (threadIdx.x == 0)
     for (int c = 0; c < nchunk && c < geo.nbuf; ++c) issue(c);
@@ -253,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, (MT <= 8 && BITS != 3 ? 5 : 1))
       const int kt_end = (c + 1) * geo.chunk_tiles < ntile ? (c + 1) * geo.chunk_tiles : ntile;
       for (int kt = c * geo.chunk_tiles; ok && kt < kt_end; ++kt) {
         const int rl = (kt - c * geo.chunk_tiles) * 4 + tq;          // unit row in the chunk
-        const uint4 wv = *reinterpret_cast<const uint4*>(cb + static_cast<size_t>(rl) * (kSlab * 4) +
+        const uint4 wv = *reinterpret_cast<const uint4*>(cb + static_cast<size_t>(rl) * kRowStride +
                                                          (warp * 32 + gq * 4) * 4);
         uint32_t bf[NB][NP];
         load_b(kt, bf);
@@ -295,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, (MT <= 8 && BITS != 3 ? 5 : 1))
         uint4 wv[ROWS];
 #pragma unroll
         for (int r = 0; r < ROWS; ++r)
-          wv[r] = *reinterpret_cast<const uint4*>(cb + static_cast<size_t>(rl + r) * (kSlab * 4) +
+          wv[r] = *reinterpret_cast<const uint4*>(cb + static_cast<size_t>(rl + r) * kRowStride +
                                                   (warp * 32 + gq * 4) * 4);
         uint32_t bf[NB][NP];
         load_b(kt, bf);
@@ -362,18 +368,19 @@ __global__ void __launch_bounds__(kThreads, (MT <= 8 && BITS != 3 ? 5 : 1))
       }
     }
   __syncthreads();
-  const int per_rank = kSlab / cs;
+  const int per_rank = kSlab / cs;                      // cs is a power of two
+  const int pr_shift = __ffs(per_rank) - 1;
   cluster_wait();
   for (int i = threadIdx.x; i < Mr * kSlab; i += kThreads) {
     const int m = i / kSlab, col = i - m * kSlab;
-    const int owner = col / per_rank;
+    const int owner = col >> pr_shift;
     float* dst = cluster.map_shared_rank(recv, owner);
     dst[(rank * Mr + m) * per_rank + (col - owner * per_rank)] = part[i];
   }
   cluster.sync();
   T* C = static_cast<T*>(a.C);
   for (int i = threadIdx.x; i < Mr * per_rank; i += kThreads) {
-    const int m = i / per_rank, c = i - m * per_rank;
+    const int m = i >> pr_shift, c = i - (m << pr_shift);
     const int n = n_base + rank * per_rank + c;
     if (n < a.N) {
       float v = 0.f;
@@ -392,9 +399,9 @@ __global__ void __launch_bounds__(kThreads, (MT <= 8 && BITS != 3 ? 5 : 1))
   }
 }
 
-// Chunking of a CTA range of `tiles` k-tiles: chunks of at most ~16 KB (128 columns x rows),
-// as many buffers as fit in about 48 KB; the chunk divides the range when it can so the boxes
-// do not read past it.
+// Chunking of a CTA range: chunks of up to 2 k-tiles (each its own mbarrier, so compute starts
+// as soon as the first rows land), as many buffers as fit in about 40 KB (all of them for the
+// common shapes: the whole slice is then in flight from the first cycle).
 template <int BITS>
 TmaGeo make_geo(int units, int cs) {
   constexpr int ROWS = Pack<BITS>::kRowsPerUnit;
@@ -402,14 +409,11 @@ TmaGeo make_geo(int units, int cs) {
   g.cs = cs;
   const int tiles_total = (units + 3) / 4;
   g.tiles_per_cta = (tiles_total + cs - 1) / cs;
-  const int max_tiles = (16 * 1024) / (4 * ROWS * kSlab * 4);   // k-tiles per 16 KB chunk
-  int ct = 1;
-  for (int d = 1; d <= max_tiles && d <= g.tiles_per_cta; ++d)
-    if (g.tiles_per_cta % d == 0) ct = d;
-  g.chunk_tiles = ct;
-  g.chunk_bytes = ct * 4 * ROWS * kSlab * 4;
-  const int chunks = (g.tiles_per_cta + ct - 1) / ct;
-  const int fit = (48 * 1024) / g.chunk_bytes;
+  g.chunk_tiles = (g.tiles_per_cta >= 2 && BITS != 8) ? 2 : 1;    // chunks of at most 16 KB
+  g.chunk_rows = g.chunk_tiles * 4 * ROWS;
+  g.chunk_bytes = g.chunk_rows * kRowStride;
+  const int chunks = (g.tiles_per_cta + g.chunk_tiles - 1) / g.chunk_tiles;
+  const int fit = (40 * 1024) / g.chunk_bytes;
   g.nbuf = chunks < fit ? chunks : (fit < 1 ? 1 : fit);
   if (g.nbuf > 16) g.nbuf = 16;
   return g;
@@ -431,8 +435,7 @@ cudaError_t launch_mma(const Problem& p, int cs, cudaStream_t stream) {
     constexpr int ROWS = Pack<BITS>::kRowsPerUnit;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.N), static_cast<cuuint64_t>(a.units) * ROWS};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.N) * 4};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kSlab),
-                               static_cast<cuuint32_t>(geo.chunk_tiles * 4 * ROWS)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kSlab), static_cast<cuuint32_t>(geo.chunk_rows)};
     const cuuint32_t estr[2] = {1, 1};
     if (!encode_tensor_map(&tmW, CU_TENSOR_MAP_DATA_TYPE_INT32, const_cast<int32_t*>(p.qweight), dims,
                            strides, box, estr, CU_TENSOR_MAP_SWIZZLE_NONE))

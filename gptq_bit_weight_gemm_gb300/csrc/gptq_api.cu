@@ -252,6 +252,16 @@ extern "C" int gptq_get_device_status(void* stream, unsigned int* out) {
   return gptq::from_cuda(err);
 }
 
+extern "C" int gptq_selftest_wait_timeout(unsigned long long limit_ns, int* waited_out, void* stream) {
+  if (!waited_out || limit_ns == 0 || limit_ns > 10000000000ull) return GPTQ_ERR_ARG;
+  if (!gptq::aligned(waited_out, 4)) return GPTQ_ERR_ALIGN;
+  Problem p = {};
+  int rc = gptq::device_ready(&p);
+  if (rc) return rc;
+  return gptq::from_cuda(gptq::launch_wait_selftest(p.status, limit_ns, waited_out,
+                                                    static_cast<cudaStream_t>(stream)));
+}
+
 extern "C" const char* gptq_strerror(int code) {
   switch (code) {
     case GPTQ_OK: return "GPTQ_OK";

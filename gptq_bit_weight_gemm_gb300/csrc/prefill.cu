@@ -80,13 +80,14 @@ struct Sync {
 };
 
 // Bounded wait on an mbarrier phase; false if the wait ran out or another role aborted.
-__device__ __forceinline__ bool wait_bar(const Sync& s, uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool wait_bar(const Sync& s, uint32_t bar, uint32_t parity,
+                                         uint64_t limit_ns = kWaitLimitNs) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer();
   while (true) {
     if (ptx::mbar_try_wait_hint(bar, parity, 200000u)) return true;
     if (*s.abort) return false;
-    if (ptx::globaltimer() - t0 > kWaitLimitNs) {
+    if (ptx::globaltimer() - t0 > limit_ns) {
       *s.abort = 1;
       atomicOr(s.status, kStatusTimeout);
       return false;
@@ -563,6 +564,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Self-test of the bounded wait: one CTA waits, with the kernels' own wait routine, on an
+// mbarrier phase that nothing completes.  The wait must give up after `limit_ns`, raise the abort
+// flag and set the timeout bit of the status word; the kernel then returns normally.
+__global__ void k_wait_selftest(unsigned* status, uint64_t limit_ns, int* waited_out) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  const uint32_t b = ptx::smem_addr(&bar);
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(b, 1);
+    abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  const Sync sy{0u, &abort_flag, status};
+  const bool ok = wait_bar(sy, b, 0u, limit_ns);   // no arrival will ever come
+  if (threadIdx.x == 0) *waited_out = ok ? 0 : 1;
+}
+
 // ------------------------------------------------------------------------------ host side
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -642,6 +661,11 @@ cudaError_t launch_bits(const Problem& p, cudaStream_t stream) {
 }
 
 }  // namespace prefill
+
+cudaError_t launch_wait_selftest(unsigned* status, uint64_t limit_ns, int* flag, cudaStream_t stream) {
+  prefill::k_wait_selftest<<<1, 32, 0, stream>>>(status, limit_ns, flag);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_prefill(const Problem& p, cudaStream_t stream) {
   switch (p.bits) {

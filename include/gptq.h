@@ -139,6 +139,16 @@ int gptq_quantize_rtn(const float* W, int K, int N, int bits, int group, const i
  */
 int gptq_get_device_status(void* stream, unsigned int* out);
 
+/*
+ * gptq_selftest_wait_timeout -- exercise the failure path of the kernels' bounded waits without
+ * faulting the GPU: one CTA waits, with the same wait routine the tensor-core kernel uses, on an
+ * mbarrier phase that nothing completes.  After `limit_ns` (1 ns .. 10 s) the wait gives up,
+ * sets GPTQ_DEV_TIMEOUT in the device status word and writes 1 to *waited_out (a device int,
+ * 4-byte aligned); the kernel then returns and the context stays usable.  Read the status with
+ * gptq_get_device_status().  No counterpart on the pages: this is the library's own test hook.
+ */
+int gptq_selftest_wait_timeout(unsigned long long limit_ns, int* waited_out, void* stream);
+
 /* Human-readable name of a gptq_status code (static string). */
 const char* gptq_strerror(int code);
 

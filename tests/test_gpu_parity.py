@@ -126,6 +126,10 @@ SMALL = [
     (2, 64, False, "f16", 300, 576, 800),
     (3, 128, True, "bf16", 129, 1024, 288),
     (4, -1, False, "bf16", 257, 256, 1024),
+    (4, 128, False, "f16", 24, 640, 416),
+    (2, 64, False, "bf16", 32, 512, 288),
+    (3, 128, True, "f16", 20, 640, 288),
+    (8, 128, False, "bf16", 31, 384, 160),
 ]
 
 
@@ -261,3 +265,20 @@ def test_misaligned_pointer_rejected():
     with pytest.raises(g.GPTQError) as e:    # the C ABI refuses the 2-byte offset
         g.gemm(flat, qw, qz, sc, bits=4, group=64)
     assert e.value.code == -3
+
+
+# ------------------------------------------------------------------------------ failure detection
+def test_bounded_wait_times_out_and_context_survives():
+    """A bounded wait on a phase nothing completes gives up, flags GPTQ_DEV_TIMEOUT, and the
+    context stays usable (no trap, no fault)."""
+    assert g.device_status() == 0
+    waited, status = g.selftest_wait_timeout(50_000_000)
+    assert waited == 1
+    assert status & g.DEV_TIMEOUT
+    assert g.device_status() == 0          # read-and-clear
+    wl = WL["tiny_4bit_g64"]
+    _, ck = checkpoint(wl, "v2")
+    A = gptq_inputs.draw_activations(wl, 64)
+    C = _gpu_gemm(wl, ck, A)
+    Cref, B = _oracle_gemm(wl, ck, A)
+    assert_gemm_close(C.float().cpu().numpy(), Cref, B, "after timeout self-test")

@@ -21,7 +21,8 @@ def test_exports_every_declared_symbol(lib):
     declared = g.header_functions()
     assert declared == sorted(["gptq_dequant", "gptq_gemm", "gptq_gemm_workspace_size",
                                "gptq_repack_zeros_v1_to_v2", "gptq_quantize_rtn",
-                               "gptq_get_device_status", "gptq_strerror"])
+                               "gptq_get_device_status", "gptq_strerror",
+                               "gptq_selftest_wait_timeout"])
     for name in declared:
         assert hasattr(lib, name), name
 
@@ -55,6 +56,12 @@ def test_gemm_validation_without_gpu(lib, kw, code):
 def test_gemm_m0_is_noop(lib):
     rc = lib.gptq_gemm(None, 0, 256, 0, FAKE, FAKE, FAKE, None, 256, 4, 128, 2, None, None, 0, None)
     assert rc == 0
+
+
+def test_selftest_validation_without_gpu(lib):
+    assert lib.gptq_selftest_wait_timeout(0, FAKE, None) == -1
+    assert lib.gptq_selftest_wait_timeout(100, None, None) == -1
+    assert lib.gptq_selftest_wait_timeout(100, P(0x10002), None) == -3
 
 
 def test_dequant_and_quantize_validation_without_gpu(lib):
