@@ -142,6 +142,14 @@ __device__ __forceinline__ uint32_t splat2(float x) {
   return h | (h << 16);
 }
 
+// Both halves set to the 16-bit float with bit pattern base + mult * z.  Above a power of two
+// 2^e the 16-bit formats step by 2^(e - 10) (fp16) or 2^(e - 7) (bf16), so 2^e + z (or its
+// negative) has the pattern bits(2^e) + z * 2^(10 - e) (fp16) while that stays below the next
+// power of two; DiffPairs uses this for its per-zero constants, all exact for 0 <= z <= 2^BITS.
+__device__ __forceinline__ uint32_t splat_bits(uint32_t base, uint32_t mult, int z) {
+  return (base + mult * static_cast<uint32_t>(z)) * 0x00010001u;
+}
+
 // ------------------------------------------------------------------------------------------
 // Exact (q - zero) pairs from one packed word, as 16-bit floats.
 //
@@ -168,8 +176,8 @@ struct DiffPairs<__half, 4> {
   __device__ static __forceinline__ int lo_k(int p) { return p; }
   __device__ static __forceinline__ int hi_k(int p) { return p + 4; }
   __device__ static __forceinline__ void consts(int z, uint32_t (&k)[kConsts]) {
-    k[0] = splat2<__half>(1024.0f + static_cast<float>(z));
-    k[1] = splat2<__half>(-(64.0f + static_cast<float>(z)));
+    k[0] = splat_bits(0x6400u, 1u, z);     // 1024 + z
+    k[1] = splat_bits(0xD400u, 16u, z);    // -(64 + z)
   }
   __device__ static __forceinline__ void run(uint32_t w, const uint32_t (&k)[kConsts],
                                              uint32_t (&d)[kPairs]) {
@@ -188,7 +196,7 @@ struct DiffPairs<__nv_bfloat16, 4> {
   __device__ static __forceinline__ int lo_k(int p) { return p; }
   __device__ static __forceinline__ int hi_k(int p) { return p + 4; }
   __device__ static __forceinline__ void consts(int z, uint32_t (&k)[kConsts]) {
-    k[0] = splat2<__nv_bfloat16>(128.0f + static_cast<float>(z));
+    k[0] = splat_bits(0x4300u, 1u, z);     // 128 + z
   }
   __device__ static __forceinline__ void run(uint32_t w, const uint32_t (&k)[kConsts],
                                              uint32_t (&d)[kPairs]) {
@@ -206,10 +214,10 @@ struct DiffPairs<__half, 2> {
   __device__ static __forceinline__ int lo_k(int p) { return p; }
   __device__ static __forceinline__ int hi_k(int p) { return p + 8; }
   __device__ static __forceinline__ void consts(int z, uint32_t (&k)[kConsts]) {
-    k[0] = splat2<__half>(1024.0f + static_cast<float>(z));
-    k[1] = splat2<__half>(-(256.0f + static_cast<float>(z)));
-    k[2] = splat2<__half>(-(64.0f + static_cast<float>(z)));
-    k[3] = splat2<__half>(-(16.0f + static_cast<float>(z)));
+    k[0] = splat_bits(0x6400u, 1u, z);     // 1024 + z
+    k[1] = splat_bits(0xDC00u, 4u, z);     // -(256 + z)
+    k[2] = splat_bits(0xD400u, 16u, z);    // -(64 + z)
+    k[3] = splat_bits(0xCC00u, 64u, z);    // -(16 + z)
   }
   __device__ static __forceinline__ void run(uint32_t w, const uint32_t (&k)[kConsts],
                                              uint32_t (&d)[kPairs]) {
@@ -232,9 +240,9 @@ struct DiffPairs<__nv_bfloat16, 2> {
   __device__ static __forceinline__ int lo_k(int p) { return p; }
   __device__ static __forceinline__ int hi_k(int p) { return p + 8; }
   __device__ static __forceinline__ void consts(int z, uint32_t (&k)[kConsts]) {
-    k[0] = splat2<__nv_bfloat16>(128.0f + static_cast<float>(z));
-    k[1] = splat2<__nv_bfloat16>(-(32.0f + static_cast<float>(z)));
-    k[2] = splat2<__nv_bfloat16>(-(8.0f + static_cast<float>(z)));
+    k[0] = splat_bits(0x4300u, 1u, z);     // 128 + z
+    k[1] = splat_bits(0xC200u, 4u, z);     // -(32 + z)
+    k[2] = splat_bits(0xC100u, 16u, z);    // -(8 + z)
   }
   __device__ static __forceinline__ void run(uint32_t w, const uint32_t (&k)[kConsts],
                                              uint32_t (&d)[kPairs]) {
@@ -257,7 +265,7 @@ struct DiffPairs<__half, 8> {
   __device__ static __forceinline__ int lo_k(int p) { return p; }
   __device__ static __forceinline__ int hi_k(int p) { return p + 2; }
   __device__ static __forceinline__ void consts(int z, uint32_t (&k)[kConsts]) {
-    k[0] = splat2<__half>(1024.0f + static_cast<float>(z));
+    k[0] = splat_bits(0x6400u, 1u, z);     // 1024 + z
   }
   __device__ static __forceinline__ void run(uint32_t w, const uint32_t (&k)[kConsts],
                                              uint32_t (&d)[kPairs]) {
