@@ -27,6 +27,8 @@
 
 #include <cuda.h>
 
+#include <atomic>
+
 #include "decode.cuh"
 #include "sm100_ptx.cuh"
 
@@ -88,12 +90,12 @@ struct TmaGeo {
 };
 
 // Shared memory of one CTA: [alignment pad][weight chunk buffers][activation pairs | partial
-// sums (aliased in time)][receive slots][group scales][group zero words][mbarriers, flags].
+// sums (aliased in time)][receive slots][per group and column: scale, scale * zero][per group
+// and token: kMagic * sum b, sum 2^shift b][mbarriers, flags].
 // Activations, partial sums and receive slots are sized by the real token count M, not by the
 // MMA token block.
 template <int BITS>
 struct TmaSmem {
-  static constexpr int kZW = kSlab * BITS / 32;        // zero words of a slab per group
   __host__ __device__ static size_t stage_bytes(const TmaGeo& g, int M) {
     const size_t stage = static_cast<size_t>(g.tiles_per_cta) * 4 * unit_words(M, MmaPairs<BITS>::kPairs) * 4;
     const size_t part = static_cast<size_t>(M) * kSlab * 4;
@@ -103,14 +105,14 @@ struct TmaSmem {
     return static_cast<size_t>(g.nbuf) * g.chunk_bytes;
   }
   __host__ __device__ static size_t off_recv(const TmaGeo& g, int M) { return off_stage(g) + stage_bytes(g, M); }
-  __host__ __device__ static size_t off_scales(const TmaGeo& g, int M) {
+  __host__ __device__ static size_t off_gconst(const TmaGeo& g, int M) {
     return off_recv(g, M) + static_cast<size_t>(M) * kSlab * 4;
   }
-  __host__ __device__ static size_t off_zeros(const TmaGeo& g, int M) {
-    return off_scales(g, M) + static_cast<size_t>(g.max_groups) * kSlab * 2;
+  __host__ __device__ static size_t off_sums(const TmaGeo& g, int M) {
+    return off_gconst(g, M) + static_cast<size_t>(g.max_groups) * kSlab * 8;
   }
   __host__ __device__ static size_t off_misc(const TmaGeo& g, int M) {
-    return off_zeros(g, M) + static_cast<size_t>(g.max_groups) * kZW * 4;
+    return off_sums(g, M) + static_cast<size_t>(g.max_groups) * M * 8;
   }
   // bytes past the 1024-aligned base, plus the worst-case alignment pad
   __host__ __device__ static size_t bytes(const TmaGeo& g, int M) {
@@ -134,7 +136,7 @@ __device__ __forceinline__ bool tma_wait(uint32_t bar, uint32_t parity, volatile
 }
 
 template <int BITS, int MT, typename T, bool FOLD>
-__global__ void __launch_bounds__(kThreads, (MT <= 8 && BITS != 3 ? 5 : 1))
+__global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
     k_decode_mma(const __grid_constant__ CUtensorMap tmW, const Args a, const TmaGeo geo) {
   using P = Pack<BITS>;
   using MP = MmaPairs<BITS>;
@@ -143,7 +145,6 @@ __global__ void __launch_bounds__(kThreads, (MT <= 8 && BITS != 3 ? 5 : 1))
   constexpr int ROWS = P::kRowsPerUnit;
   constexpr int NP = MP::kPairs;
   constexpr int NB = MT / 8;                          // token blocks of 8
-  constexpr int ZW = SM::kZW;
   const int UW = unit_words(a.M, NP);
   extern __shared__ __align__(128) unsigned char smem_raw[];
 
@@ -173,11 +174,56 @@ __global__ void __launch_bounds__(kThreads, (MT <= 8 && BITS != 3 ? 5 : 1))
   uint8_t* sbuf = smem;                                               // weight chunks
   uint32_t* sB = reinterpret_cast<uint32_t*>(smem + SM::off_stage(geo));
   float* recv = reinterpret_cast<float*>(smem + SM::off_recv(geo, a.M));
-  uint16_t* sS = reinterpret_cast<uint16_t*>(smem + SM::off_scales(geo, a.M));
-  uint32_t* sZ = reinterpret_cast<uint32_t*>(smem + SM::off_zeros(geo, a.M));
+  float2* sK = reinterpret_cast<float2*>(smem + SM::off_gconst(geo, a.M));   // [group][column]
+  float* sT = reinterpret_cast<float*>(smem + SM::off_sums(geo, a.M));       // [group][M]
+  float* sQ = sT + geo.max_groups * a.M;                                      // [group][M]
   uint8_t* misc = smem + SM::off_misc(geo, a.M);
   const uint32_t bar0 = ptx::smem_addr(misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 8 * 16);
+
+  // Scales and zeros of the groups this range touches (FOLD): their loads go out first, ahead
+  // of the weight stream (behind it they would wait for the whole slice), and land in shared
+  // memory as (scale, scale * zero) per group and column.
+  const int g_lo = (cu0 * PER) / a.group;
+  const int g_end = (ct1 * 4 * PER - 1) / a.group;
+  const int ngrp = ntile > 0 ? (g_end < a.G - 1 ? g_end : a.G - 1) - g_lo + 1 : 0;
+  constexpr int kGB = 4;                               // group items per thread in flight
+  uint2 gsv[kGB];
+  uint32_t gzf[kGB];
+  auto group_loads = [&](int base) {
+#pragma unroll
+    for (int j = 0; j < kGB; ++j) {
+      const int i = base + j * kThreads + static_cast<int>(threadIdx.x);
+      gsv[j] = make_uint2(0u, 0u);
+      gzf[j] = 0u;
+      const int n = n_base + 4 * (i & 31);
+      if (i < ngrp * 32 && n < a.N) {
+        const int g = g_lo + (i >> 5);
+        gsv[j] = __ldg(reinterpret_cast<const uint2*>(a.scales + static_cast<long long>(g) * a.N + n));
+        gzf[j] = zeros4<BITS>(a.qzeros + static_cast<long long>(g) * a.zwords, n);
+      }
+    }
+  };
+  auto group_stores = [&](int base) {
+#pragma unroll
+    for (int j = 0; j < kGB; ++j) {
+      const int i = base + j * kThreads + static_cast<int>(threadIdx.x);
+      if (i < ngrp * 32) {
+        float2 v[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint16_t h = c & 1 ? hi16(c < 2 ? gsv[j].x : gsv[j].y) : lo16(c < 2 ? gsv[j].x : gsv[j].y);
+          const float sc = __half2float(__ushort_as_half(h));
+          const int z = static_cast<int>((gzf[j] >> (BITS * c)) & P::kMask) + a.zero_offset;
+          v[c] = make_float2(sc, sc * static_cast<float>(z));
+        }
+        float4* dst = reinterpret_cast<float4*>(sK + (i >> 5) * kSlab + 4 * (i & 31));
+        dst[0] = make_float4(v[0].x, v[0].y, v[1].x, v[1].y);
+        dst[1] = make_float4(v[2].x, v[2].y, v[3].x, v[3].y);
+      }
+    }
+  };
+  if constexpr (FOLD) group_loads(0);
 
   // Issue the packed slice into shared memory: chunk c of this CTA lands in buffer c % nbuf.
   // The copies read weights only; they are issued before griddepcontrol.wait because global
@@ -203,37 +249,73 @@ __global__ void __launch_bounds__(kThreads, (MT <= 8 && BITS != 3 ? 5 : 1))
   if (threadIdx.x == 0)
     for (int c = 0; c < nchunk && c < geo.nbuf; ++c) issue(c);
 
-  // Scales and zero words of the groups this range touches (FOLD): staged once, so the loop
-  // below reads them from shared memory.  Like the weights they come before griddepcontrol.wait.
-  const int g_lo = (cu0 * PER) / a.group;
   if constexpr (FOLD) {
-    const int g_end = (ct1 * 4 * PER - 1) / a.group;
-    const int ngrp = ntile > 0 ? (g_end < a.G - 1 ? g_end : a.G - 1) - g_lo + 1 : 0;
-    for (int i = threadIdx.x; i < ngrp * (kSlab / 4); i += kThreads) {
-      const int gi = i >> 5, q = i & 31;
-      const int n = n_base + 4 * q;
-      uint2 v = make_uint2(0u, 0u);
-      if (n < a.N)
-        v = __ldg(reinterpret_cast<const uint2*>(a.scales + static_cast<long long>(g_lo + gi) * a.N + n));
-      *reinterpret_cast<uint2*>(sS + gi * kSlab + 4 * q) = v;
-    }
-    for (int i = threadIdx.x; i < ngrp * ZW; i += kThreads) {
-      const int gi = i / ZW, w = i - gi * ZW;
-      const int wg = n_base * BITS / 32 + w;
-      sZ[gi * ZW + w] = wg < a.zwords
-                            ? static_cast<uint32_t>(__ldg(a.qzeros + static_cast<long long>(g_lo + gi) * a.zwords + wg))
-                            : 0u;
+    group_stores(0);
+    for (int base = kGB * kThreads; base < ngrp * 32; base += kGB * kThreads) {
+      group_loads(base);
+      group_stores(base);
     }
   }
   pdl_wait();
 
-  // Stage activations: sB[u][m][p] = (a[m][k0 + lo_k(p)], a[m][k0 + hi_k(p)]), zero past K or M.
+  // Stage activations: sB[u][m][p] = (a[m][k0 + lo_k(p)], a[m][k0 + hi_k(p)]), zero past K or M
+  // (FOLD: times 2^-shift(p), matching the raw codes of CodePairs).
   const uint16_t* A16 = static_cast<const uint16_t*>(a.A);
   const int nunits = ntile * 4;
   stage_pairs<PER, NP>(A16, a.M, a.K, cu0, nunits, a.units,
                        [](int p) { return MP::lo_k(p); }, [](int p) { return MP::hi_k(p); },
-                       [&](int uu, int m, int p, uint32_t v) { sB[uu * UW + m * NP + p] = v; });
+                       [&](int uu, int m, int p, uint32_t v) {
+                         if constexpr (FOLD) v = scale_pow2(v, CodePairs<T, BITS>::shift(p), T());
+                         sB[uu * UW + m * NP + p] = v;
+                       });
   __syncthreads();
+  if constexpr (FOLD) {
+    // Per group and token: kMagic * T and Q, with T = sum_k b_k and Q = sum_k 2^shift b_k over
+    // the staged activations (the two corrections of the raw-code MMA).  One warp per group;
+    // the lanes of a token split its pairs and meet in a fixed shuffle order (deterministic).
+    using CP = CodePairs<T, BITS>;
+    const int upg = a.group / PER;
+    const int lps = a.M <= 1 ? 5 : a.M <= 2 ? 4 : a.M <= 4 ? 3 : a.M <= 8 ? 2 : a.M <= 16 ? 1 : 0;
+    const int m = lane >> lps, sub = lane & ((1 << lps) - 1);
+    for (int gi = warp; gi < ngrp; gi += kWarps) {
+      int u_lo = (g_lo + gi) * upg - cu0, u_hi = u_lo + upg;
+      u_lo = u_lo < 0 ? 0 : u_lo;
+      u_hi = u_hi > nunits ? nunits : u_hi;
+      float t = 0.f, q = 0.f;
+      if (m < a.M) {
+        for (int uu = u_lo + sub; uu < u_hi; uu += (1 << lps)) {
+          uint32_t v[NP];
+          const uint32_t* src = sB + uu * UW + m * NP;
+          if constexpr (NP % 4 == 0) {
+#pragma unroll
+            for (int i = 0; i < NP / 4; ++i) {
+              const uint4 x = reinterpret_cast<const uint4*>(src)[i];
+              v[4 * i] = x.x; v[4 * i + 1] = x.y; v[4 * i + 2] = x.z; v[4 * i + 3] = x.w;
+            }
+          } else {
+            const uint2 x = reinterpret_cast<const uint2*>(src)[0];
+            v[0] = x.x; v[1] = x.y;
+          }
+#pragma unroll
+          for (int pp = 0; pp < NP; ++pp) {
+            const float f = F16Traits<T>::to_f32(F16Traits<T>::from_bits(lo16(v[pp]))) +
+                            F16Traits<T>::to_f32(F16Traits<T>::from_bits(hi16(v[pp])));
+            t += f;
+            q = fmaf(f, static_cast<float>(1 << CP::shift(pp)), q);
+          }
+        }
+      }
+      for (int o = (1 << lps) >> 1; o > 0; o >>= 1) {
+        t += __shfl_xor_sync(0xFFFFFFFFu, t, o);
+        q += __shfl_xor_sync(0xFFFFFFFFu, q, o);
+      }
+      if (sub == 0 && m < a.M) {
+        sT[gi * a.M + m] = CP::kMagic * t;
+        sQ[gi * a.M + m] = q;
+      }
+    }
+    __syncthreads();
+  }
 
   float acc[2][NB][4];
 #pragma unroll
@@ -272,25 +354,15 @@ __global__ void __launch_bounds__(kThreads, (MT <= 8 && BITS != 3 ? 5 : 1))
   };
 
   if constexpr (FOLD) {
-    using DP = DiffPairs<T, BITS>;
-    static_assert(DP::kPairs == NP, "pairing must match the activation staging");
+    using CP = CodePairs<T, BITS>;
+    static_assert(CP::kPairs == NP, "pairing must match the activation staging");
+    // Raw-code MMAs into a per-group accumulator cg; at each group end
+    //   acc += scale * (cg - kMagic T) - scale * zero * Q.
+    // Tiles go in blocks of 4 where a block stays inside one chunk and one group (shared-memory
+    // offsets then are immediates); absent tokens read token M-1's activations (their outputs
+    // are never stored).
     float cg[2][NB][4];
-    float s[4];
-    uint32_t kz[4][DP::kConsts];
-    const int tpg = a.group / (4 * PER);               // k-tiles per group (>= 1 here)
-    int gi = 0;                                        // group of the current tile, from g_lo
-    int left = tpg - (ct0 % tpg);
-    const int zwi = (col0 * BITS) >> 5, zsh = (col0 * BITS) & 31;
-    auto set_group = [&]() {
-      const uint2 sv = *reinterpret_cast<const uint2*>(sS + gi * kSlab + col0);
-      s[0] = __half2float(__ushort_as_half(lo16(sv.x)));
-      s[1] = __half2float(__ushort_as_half(hi16(sv.x)));
-      s[2] = __half2float(__ushort_as_half(lo16(sv.y)));
-      s[3] = __half2float(__ushort_as_half(hi16(sv.y)));
-      const uint32_t zf = sZ[gi * ZW + zwi] >> zsh;
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        DP::consts(static_cast<int>((zf >> (BITS * c)) & P::kMask) + a.zero_offset, kz[c]);
+    auto clear_cg = [&]() {
 #pragma unroll
       for (int t = 0; t < 2; ++t)
 #pragma unroll
@@ -298,53 +370,106 @@ __global__ void __launch_bounds__(kThreads, (MT <= 8 && BITS != 3 ? 5 : 1))
 #pragma unroll
           for (int i = 0; i < 4; ++i) cg[t][nb][i] = 0.f;
     };
-    auto fold = [&]() {
+    auto fold = [&](int gi) {
+      const float4 k01 = *reinterpret_cast<const float4*>(sK + gi * kSlab + col0);
+      const float4 k23 = *reinterpret_cast<const float4*>(sK + gi * kSlab + col0 + 2);
+      const float ks[4] = {k01.x, k01.z, k23.x, k23.z}, kz[4] = {k01.y, k01.w, k23.y, k23.w};
 #pragma unroll
-      for (int t = 0; t < 2; ++t)
+      for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
-        for (int nb = 0; nb < NB; ++nb) {
-          acc[t][nb][0] = fmaf(s[2 * t], cg[t][nb][0], acc[t][nb][0]);
-          acc[t][nb][1] = fmaf(s[2 * t], cg[t][nb][1], acc[t][nb][1]);
-          acc[t][nb][2] = fmaf(s[2 * t + 1], cg[t][nb][2], acc[t][nb][2]);
-          acc[t][nb][3] = fmaf(s[2 * t + 1], cg[t][nb][3], acc[t][nb][3]);
-        }
-    };
-    if (ntile > 0) set_group();
-    for (int c = 0; c < nchunk; ++c) {
-      const bool ok = tma_wait(bar0 + 8 * (c % geo.nbuf), (c / geo.nbuf) & 1, abort_flag, a.status);
-      const uint8_t* cb = wslot + static_cast<size_t>(c % geo.nbuf) * geo.chunk_bytes;
-      const int kt0 = c * geo.chunk_tiles;
-      const int kt_end = kt0 + geo.chunk_tiles < ntile ? kt0 + geo.chunk_tiles : ntile;
-      for (int kt = kt0; ok && kt < kt_end; ++kt) {
-        const uint4 wv = wrow(cb, (kt - kt0) * 4 + tq);
-        uint32_t bf[NB][NP];
-        load_b(kt, bf);
-        uint32_t d[4][NP];
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) DP::run((&wv.x)[cc], kz[cc], d[cc]);
-#pragma unroll
-        for (int j = 0; j < NP / 2; ++j)
+        for (int h = 0; h < 2; ++h) {
+          int m = nb * 8 + 2 * tq + h;
+          m = m < a.M ? m : a.M - 1;
+          const float mt = sT[gi * a.M + m], q = sQ[gi * a.M + m];
 #pragma unroll
           for (int t = 0; t < 2; ++t)
 #pragma unroll
-            for (int nb = 0; nb < NB; ++nb)
-              mma16816(cg[t][nb], d[2 * t][2 * j], d[2 * t + 1][2 * j], d[2 * t][2 * j + 1],
-                       d[2 * t + 1][2 * j + 1], bf[nb][2 * j], bf[nb][2 * j + 1], T());
-        if (--left == 0) {                              // group boundary (warp-uniform)
-          fold();
-          left = tpg;
-          if (kt + 1 < ntile) {
-            ++gi;
-            set_group();
+            for (int r = 0; r < 2; ++r) {
+              const int i = 2 * r + h, c = 2 * t + r;
+              acc[t][nb][i] = fmaf(-kz[c], q, fmaf(ks[c], cg[t][nb][i] - mt, acc[t][nb][i]));
+            }
+        }
+    };
+    int boff[NB];                                      // word offset of this thread's tokens
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+      const int m = 8 * nb + gq;
+      boff[nb] = (m < a.M ? m : a.M - 1) * NP + tq * UW;
+    }
+    auto tile = [&](const uint8_t* wp, int kt) {
+      const uint4 wv = *reinterpret_cast<const uint4*>(wp);
+      uint32_t bf[NB][NP];
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) {
+        const uint32_t* src = sB + kt * 4 * UW + boff[nb];
+        if constexpr (NP % 4 == 0) {
+#pragma unroll
+          for (int i = 0; i < NP / 4; ++i) {
+            const uint4 v = reinterpret_cast<const uint4*>(src)[i];
+            bf[nb][4 * i] = v.x; bf[nb][4 * i + 1] = v.y; bf[nb][4 * i + 2] = v.z; bf[nb][4 * i + 3] = v.w;
           }
+        } else {
+          const uint2 v = reinterpret_cast<const uint2*>(src)[0];
+          bf[nb][0] = v.x; bf[nb][1] = v.y;
         }
       }
-      if (c + geo.nbuf < nchunk) {                      // refill this buffer with chunk c + nbuf
-        __syncthreads();
-        if (threadIdx.x == 0 && !*abort_flag) { ptx::fence_proxy_async_smem(); issue(c + geo.nbuf); }
+      uint32_t d[4][NP];
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) CP::run((&wv.x)[cc], d[cc]);
+#pragma unroll
+      for (int j = 0; j < NP / 2; ++j)
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb)
+            mma16816(cg[t][nb], d[2 * t][2 * j], d[2 * t + 1][2 * j], d[2 * t][2 * j + 1],
+                     d[2 * t + 1][2 * j + 1], bf[nb][2 * j], bf[nb][2 * j + 1], T());
+    };
+    const int tpg = a.group / (4 * PER);               // k-tiles per group (>= 1 here)
+    int gi = 0, g_end_kt = tpg - (ct0 % tpg);          // local group, tile where it ends
+    int c = -1, chunk_kt = 0, chunk_end = 0;
+    bool ok = true, dirty = false;
+    const uint8_t* we = wslot;                         // rows of even / odd k-tiles of the chunk
+    const uint8_t* wo = wslot;
+    clear_cg();
+    for (int kt = 0; kt < ntile;) {                    // control flow is uniform over the CTA
+      if (kt == chunk_end) {
+        if (c >= 0 && c + geo.nbuf < nchunk) {         // refill the buffer just consumed
+          __syncthreads();
+          if (threadIdx.x == 0 && !*abort_flag) { ptx::fence_proxy_async_smem(); issue(c + geo.nbuf); }
+        }
+        ++c;
+        ok = tma_wait(bar0 + 8 * (c % geo.nbuf), (c / geo.nbuf) & 1, abort_flag, a.status);
+        const uint8_t* cb = wslot + static_cast<size_t>(c % geo.nbuf) * geo.chunk_bytes + tq * kBoxRowBytes;
+        we = cb + ((quad ^ tq) << 4);
+        wo = cb + ((quad ^ tq ^ 4) << 4);
+        chunk_kt = c * geo.chunk_tiles;
+        chunk_end = chunk_kt + geo.chunk_tiles < ntile ? chunk_kt + geo.chunk_tiles : ntile;
+      }
+      const int lim = chunk_end < g_end_kt ? chunk_end : g_end_kt;
+      const int l0 = kt - chunk_kt;
+      if (lim - kt >= 4) {
+        if (ok) {
+          const uint8_t* e = (l0 & 1) ? wo : we;
+          const uint8_t* o = (l0 & 1) ? we : wo;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) tile(((u & 1) ? o : e) + (l0 + u) * 4 * kBoxRowBytes, kt + u);
+        }
+        kt += 4;
+      } else {
+        if (ok) tile(((l0 & 1) ? wo : we) + l0 * 4 * kBoxRowBytes, kt);
+        kt += 1;
+      }
+      dirty = true;
+      if (kt == g_end_kt) {
+        fold(gi);
+        clear_cg();
+        dirty = false;
+        ++gi;
+        g_end_kt += tpg;
       }
     }
-    if (ntile > 0 && left != tpg) fold();
+    if (dirty) fold(gi);
   } else {
     for (int c = 0; c < nchunk; ++c) {
       const bool ok = tma_wait(bar0 + 8 * (c % geo.nbuf), (c / geo.nbuf) & 1, abort_flag, a.status);
@@ -478,7 +603,9 @@ TmaGeo make_geo(int units, int cs, int M, int group, int ctas, int sm_count, int
     const int chunks = (g.tiles_per_cta + ct - 1) / ct;
     g.nbuf = 0;
     const size_t fixed = TmaSmem<BITS>::bytes(g, M);          // everything but the buffers
-    const long long budget = static_cast<long long>(233472 / per_sm) - 1024 - static_cast<long long>(fixed);
+    // an SM holds 228 KB; each CTA takes its size rounded up to 1 KB plus 1 KB reserved
+    const long long cap = (static_cast<long long>(233472 / per_sm) - 1024) & ~1023LL;
+    const long long budget = cap - static_cast<long long>(fixed);
     int fit = budget > 0 ? static_cast<int>(budget / g.chunk_bytes) : 0;
     if (fit > 16) fit = 16;
     g.nbuf = chunks < fit ? chunks : fit;
@@ -520,6 +647,17 @@ cudaError_t launch_mma(const Problem& p, int cs, cudaStream_t stream) {
   }
   const size_t smem = TmaSmem<BITS>::bytes(geo, p.M);
   auto kern = k_decode_mma<BITS, MT, T, FOLD>;
+  // once per device, FOLD only: the full shared-memory carveout (left to the driver, it may pick
+  // a smaller one and fit fewer CTAs per SM than the one-wave budget above assumes).  The FULL
+  // path keeps the driver's choice: it re-reads scales through L1, which the carveout would shrink.
+  static std::atomic<unsigned long long> carveout_set{0};
+  const int dev = device_info().device;
+  if (FOLD && (dev >= 64 || !(carveout_set.load(std::memory_order_relaxed) & (1ull << dev)))) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         static_cast<int>(cudaSharedmemCarveoutMaxShared));
+    if (e != cudaSuccess) return e;
+    if (dev < 64) carveout_set.fetch_or(1ull << dev, std::memory_order_relaxed);
+  }
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));

@@ -91,6 +91,7 @@ struct F16Traits<__half> {
   __device__ static __forceinline__ float to_f32(__half x) { return __half2float(x); }
   __device__ static __forceinline__ __half from_f32(float x) { return __float2half_rn(x); }
   __device__ static __forceinline__ uint16_t bits(__half x) { return __half_as_ushort(x); }
+  __device__ static __forceinline__ __half from_bits(uint16_t b) { return __ushort_as_half(b); }
 };
 
 template <>
@@ -105,6 +106,7 @@ struct F16Traits<__nv_bfloat16> {
   __device__ static __forceinline__ uint16_t bits(__nv_bfloat16 x) {
     return __bfloat16_as_ushort(x);
   }
+  __device__ static __forceinline__ __nv_bfloat16 from_bits(uint16_t b) { return __ushort_as_bfloat16(b); }
 };
 
 __device__ __forceinline__ uint16_t lo16(uint32_t x) { return static_cast<uint16_t>(x & 0xFFFFu); }
@@ -274,6 +276,109 @@ struct DiffPairs<__half, 8> {
     d[1] = sub2(__byte_perm(w, 0x64646464u, 0x4341u), k[0], __half());
   }
 };
+
+// ------------------------------------------------------------------------------------------
+// Raw codes as 16-bit floats, zero not subtracted (decode kernels).
+//
+// CodePairs<T, BITS> is DiffPairs without the per-pair sub/fma: pair p of a word holds
+// kMagic + 2^shift(p) * q for the codes lo_k(p), hi_k(p) (the DiffPairs pairing), i.e. only the
+// masks (plus one shared shift).  With the matching activation pair scaled by 2^-shift(p),
+//   sum_k b_k (kMagic + 2^shift q_k) = kMagic * sum_k b_k + sum_k (2^shift b_k) q_k,
+// so sum_k (2^shift b_k)(q_k - z) is the MMA result minus kMagic * sum_k b_k and minus
+// z * sum_k 2^shift b_k -- two sums per quantization group and token.
+// ------------------------------------------------------------------------------------------
+template <typename T, int BITS>
+struct CodePairs;
+
+template <>
+struct CodePairs<__half, 4> {
+  static constexpr int kPairs = 4;
+  static constexpr float kMagic = 1024.0f;
+  __host__ __device__ static constexpr int shift(int p) { return (p & 1) ? 4 : 0; }
+  __device__ static __forceinline__ void run(uint32_t w, uint32_t (&d)[kPairs]) {
+    const uint32_t M2 = 0x64006400u, w8 = w >> 8;
+    d[0] = lop3_and_or(w, 0x000F000Fu, M2);
+    d[1] = lop3_and_or(w, 0x00F000F0u, M2);
+    d[2] = lop3_and_or(w8, 0x000F000Fu, M2);
+    d[3] = lop3_and_or(w8, 0x00F000F0u, M2);
+  }
+};
+
+template <>
+struct CodePairs<__nv_bfloat16, 4> {
+  static constexpr int kPairs = 4;
+  static constexpr float kMagic = 128.0f;
+  __host__ __device__ static constexpr int shift(int) { return 0; }
+  __device__ static __forceinline__ void run(uint32_t w, uint32_t (&d)[kPairs]) {
+    const uint32_t M2 = 0x43004300u;
+    d[0] = lop3_and_or(w, 0x000F000Fu, M2);
+    d[1] = lop3_and_or(w >> 4, 0x000F000Fu, M2);
+    d[2] = lop3_and_or(w >> 8, 0x000F000Fu, M2);
+    d[3] = lop3_and_or(w >> 12, 0x000F000Fu, M2);
+  }
+};
+
+template <>
+struct CodePairs<__half, 2> {
+  static constexpr int kPairs = 8;
+  static constexpr float kMagic = 1024.0f;
+  __host__ __device__ static constexpr int shift(int p) { return 2 * (p & 3); }
+  __device__ static __forceinline__ void run(uint32_t w, uint32_t (&d)[kPairs]) {
+    const uint32_t M2 = 0x64006400u;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t x = h ? (w >> 8) : w;
+      d[4 * h + 0] = lop3_and_or(x, 0x00030003u, M2);
+      d[4 * h + 1] = lop3_and_or(x, 0x000C000Cu, M2);
+      d[4 * h + 2] = lop3_and_or(x, 0x00300030u, M2);
+      d[4 * h + 3] = lop3_and_or(x, 0x00C000C0u, M2);
+    }
+  }
+};
+
+template <>
+struct CodePairs<__nv_bfloat16, 2> {
+  static constexpr int kPairs = 8;
+  static constexpr float kMagic = 128.0f;
+  __host__ __device__ static constexpr int shift(int p) { return (p & 3) == 3 ? 0 : 2 * (p & 3); }
+  __device__ static __forceinline__ void run(uint32_t w, uint32_t (&d)[kPairs]) {
+    const uint32_t M2 = 0x43004300u;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t x = h ? (w >> 8) : w;
+      d[4 * h + 0] = lop3_and_or(x, 0x00030003u, M2);
+      d[4 * h + 1] = lop3_and_or(x, 0x000C000Cu, M2);
+      d[4 * h + 2] = lop3_and_or(x, 0x00300030u, M2);
+      d[4 * h + 3] = lop3_and_or(x >> 6, 0x00030003u, M2);
+    }
+  }
+};
+
+template <>
+struct CodePairs<__half, 8> {
+  static constexpr int kPairs = 2;
+  static constexpr float kMagic = 1024.0f;
+  __host__ __device__ static constexpr int shift(int) { return 0; }
+  __device__ static __forceinline__ void run(uint32_t w, uint32_t (&d)[kPairs]) {
+    d[0] = __byte_perm(w, 0x64646464u, 0x4240u);
+    d[1] = __byte_perm(w, 0x64646464u, 0x4341u);
+  }
+};
+
+// A 16-bit pair times 2^-s (exact unless the result is subnormal, where it rounds).
+__device__ __forceinline__ uint32_t scale_pow2(uint32_t v, int s, __half) {
+  if (s == 0) return v;
+  const uint16_t f = static_cast<uint16_t>((15 - s) << 10);
+  __half2 r = __hmul2(*reinterpret_cast<__half2*>(&v), __halves2half2(__ushort_as_half(f), __ushort_as_half(f)));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+__device__ __forceinline__ uint32_t scale_pow2(uint32_t v, int s, __nv_bfloat16) {
+  if (s == 0) return v;
+  const uint16_t f = static_cast<uint16_t>((127 - s) << 7);
+  __nv_bfloat162 r = __hmul2(*reinterpret_cast<__nv_bfloat162*>(&v),
+                             __halves2bfloat162(__ushort_as_bfloat16(f), __ushort_as_bfloat16(f)));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
 
 // Sum of the two halves of a 16-bit pair, in fp32.
 __device__ __forceinline__ float sum2_f32(uint32_t x, __half) {
