@@ -18,11 +18,20 @@
 // thread t's word as the k-slots (2t, 2t+1) and (2t+8, 2t+9) -- and the activations are staged
 // in the same pairing, which makes them exactly the B fragment.
 //
-//  * FOLD (groups aligned to k-tiles, no act-order, 2/4/8-bit): A = q - zero exactly (magic-
-//    number unpack), products exact, a fresh accumulator per group folded with the scale:
-//    acc += scale * sum_k a_k (q_k - zero).
+//  * FOLD (groups aligned to k-tiles, no act-order, 2/4/8-bit): A = the raw code as a 16-bit
+//    float kMagic + 2^shift q (masks only, CodePairs), B = the activation times 2^-shift, a fresh
+//    fp32 accumulator R per group; at the group end
+//      acc += scale * (R - kMagic * T) - scale * zero * Q,
+//    with T = sum_k b_k and Q = sum_k 2^shift b_k per group and token, summed once from the
+//    staged activations.  Tiles go in blocks of 4 inside one chunk and one group.
 //  * FULL (act-order, 3-bit, unaligned groups): A = RN((q - zero) * scale) per weight (exact
 //    fp32 product, one rounding), accumulated across groups.
+//
+// Cost model that shaped it (measured on GB300): a k-tile of 4 packed words per warp costs the
+// dispatch of its integer-pipe ops (16 lanes, 2 cycles each), its mma.sync (about 8 cycles per
+// m16n8k16 per SM sub-partition) and its fp16 ops, added rather than overlapped; the raw-code
+// unpack (4 masks + 1 shift per 4-bit word) and the per-group constants staged in shared
+// memory keep the count per word low.
 #pragma once
 
 #include <cuda.h>

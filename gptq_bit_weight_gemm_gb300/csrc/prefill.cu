@@ -7,13 +7,15 @@
 // packed weight tile is dequantized straight into the shared-memory layout the tensor core reads,
 // and a 256 x 256 output tile accumulates over K in tensor memory.
 //
-// Per CTA (persistent, one per SM, 448 threads, warp-specialised):
+// Per CTA (persistent, one per SM, 704 threads, warp-specialised):
 //   warp 4      TMA producer: A tile [256 x 64] (128-byte swizzle) and the packed qweight tile
 //               [64 k x 256 n] for each k-step into a 3-stage ring;
-//   warps 6-13  dequantizers: thread n reads column n's packed words, forms
-//               w = RN((q - zero) * scale) exactly (q - zero exact in fp32, one fp32 product,
-//               one rounding to A's dtype) and stores the B tile K-major with the 128-byte
-//               swizzle (2-stage ring), then fence.proxy.async + mbarrier arrive;
+//   warps 6-21  dequantizers, two threads per tile column (4 chunks of 8 k each): exact
+//               q - zero as 16-bit floats (DiffPairs), then one rounding of (q - zero) * scale --
+//               fp16: HMUL2 (an exact product rounded once); bf16: fp32 products (f32x2) rounded
+//               once -- stored K-major with the 128-byte swizzle into a 3-stage B ring (2 for
+//               8-bit), then fence.proxy.async + mbarrier arrive.  The next group's scale and
+//               zero words are loaded one group ahead;
 //   warp 5      TMEM owner and MMA issuer: per k-step 4 x 2 tcgen05.mma (M=128, N=256, K=16),
 //               one per 128-row half of A, both reading the same B tile; tcgen05.commit frees
 //               the ring slots and signals the accumulators;
