@@ -96,11 +96,14 @@ struct TmaGeo {
   int chunk_bytes;     // 4 slots
   int nbuf;            // chunk buffers (all chunks in flight when nbuf == chunks)
   int max_groups;      // quantization groups a CTA range can touch (FOLD staging)
+  int full_groups;     // FULL: groups staged in shared memory (all G with g_idx), 0 = read via L1
+  int full_k;          // FULL: k values of the largest CTA range (their group indices are staged)
 };
 
 // Shared memory of one CTA: [alignment pad][weight chunk buffers][activation pairs | partial
 // sums (aliased in time)][receive slots][per group and column: scale, scale * zero][per group
-// and token: kMagic * sum b, sum 2^shift b][mbarriers, flags].
+// and token: kMagic * sum b, sum 2^shift b][FULL: per group and column scale and zero, per k
+// its group][mbarriers, flags].
 // Activations, partial sums and receive slots are sized by the real token count M, not by the
 // MMA token block.
 template <int BITS>
@@ -120,8 +123,17 @@ struct TmaSmem {
   __host__ __device__ static size_t off_sums(const TmaGeo& g, int M) {
     return off_gconst(g, M) + static_cast<size_t>(g.max_groups) * kSlab * 8;
   }
+  __host__ __device__ static size_t off_full(const TmaGeo& g, int M) {
+    return (off_sums(g, M) + static_cast<size_t>(g.max_groups) * M * 8 + 15) & ~static_cast<size_t>(15);
+  }
+  // FULL staging: (scale bits | zero << 16) per group and column, then a group index per k
+  __host__ __device__ static size_t full_bytes(const TmaGeo& g) {
+    return g.full_groups > 0
+               ? ((static_cast<size_t>(g.full_groups) * kSlab * 4 + static_cast<size_t>(g.full_k) * 2 + 15) & ~static_cast<size_t>(15))
+               : 0;
+  }
   __host__ __device__ static size_t off_misc(const TmaGeo& g, int M) {
-    return off_sums(g, M) + static_cast<size_t>(g.max_groups) * M * 8;
+    return off_full(g, M) + full_bytes(g);
   }
   // bytes past the 1024-aligned base, plus the worst-case alignment pad
   __host__ __device__ static size_t bytes(const TmaGeo& g, int M) {
@@ -186,6 +198,8 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
   float2* sK = reinterpret_cast<float2*>(smem + SM::off_gconst(geo, a.M));   // [group][column]
   float* sT = reinterpret_cast<float*>(smem + SM::off_sums(geo, a.M));       // [group][M]
   float* sQ = sT + geo.max_groups * a.M;                                      // [group][M]
+  uint32_t* sSZ = reinterpret_cast<uint32_t*>(smem + SM::off_full(geo, a.M));  // [group][column]
+  uint16_t* sG = reinterpret_cast<uint16_t*>(sSZ + geo.full_groups * kSlab);    // [k of the range]
   uint8_t* misc = smem + SM::off_misc(geo, a.M);
   const uint32_t bar0 = ptx::smem_addr(misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 8 * 16);
@@ -263,6 +277,33 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
     for (int base = kGB * kThreads; base < ngrp * 32; base += kGB * kThreads) {
       group_loads(base);
       group_stores(base);
+    }
+  } else if (geo.full_groups > 0) {
+    // FULL: scales, runtime zeros and the group of every k of the range, read once into shared
+    // memory (with g_idx every group may occur, so all G are staged).  Checkpoint data, like the
+    // weights, so this too precedes griddepcontrol.wait.
+    const int g_base = a.g_idx ? 0 : g_lo;
+    const int ng = a.g_idx ? a.G : ngrp;
+    for (int i = threadIdx.x; i < ng * 32; i += kThreads) {
+      const int gi = i >> 5, n = n_base + 4 * (i & 31);
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (n < a.N) {
+        const int g = g_base + gi;
+        const uint2 sv = __ldg(reinterpret_cast<const uint2*>(a.scales + static_cast<long long>(g) * a.N + n));
+        const uint32_t zf = zeros4<BITS>(a.qzeros + static_cast<long long>(g) * a.zwords, n);
+        const uint32_t zz[4] = {((zf >> 0) & P::kMask) + a.zero_offset, ((zf >> BITS) & P::kMask) + a.zero_offset,
+                                ((zf >> (2 * BITS)) & P::kMask) + a.zero_offset,
+                                ((zf >> (3 * BITS)) & P::kMask) + a.zero_offset};
+        v = make_uint4(lo16(sv.x) | (zz[0] << 16), hi16(sv.x) | (zz[1] << 16), lo16(sv.y) | (zz[2] << 16),
+                       hi16(sv.y) | (zz[3] << 16));
+      }
+      *reinterpret_cast<uint4*>(sSZ + gi * kSlab + 4 * (i & 31)) = v;
+    }
+    const int k0 = cu0 * PER, nk = ntile * 4 * PER;
+    for (int i = threadIdx.x; i < nk; i += kThreads) {
+      const int k = k0 + i < a.K ? k0 + i : a.K - 1;
+      const int g = a.g_idx ? checked_group(a, k) : k / a.group;
+      sG[i] = static_cast<uint16_t>(g - g_base);
     }
   }
   pdl_wait();
@@ -494,10 +535,10 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
         load_b(kt, bf);
         const int u = cu0 + kt * 4 + tq;
         const int uk = (u < a.units ? u : a.units - 1) * PER;
+        const uint16_t* gk = sG + (kt * 4 + tq) * PER;   // staged groups of this unit's k
         // dequantize this unit for 4 columns: w[c][p] = RN((q - z) * s) pairs
         uint32_t w[4][NP];
-        float s[4];
-        int z[4];
+        float s[4], zf[4];
         int cur_g = -1;
 #pragma unroll
         for (int p = 0; p < NP; ++p) {
@@ -506,13 +547,29 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
           for (int h = 0; h < 2; ++h) {
             const int j = h ? MP::hi_k(p) : MP::lo_k(p);
             const int k = uk + j;
-            const int gg = a.g_idx ? checked_group(a, k) : k / a.group;
+            const int gg = geo.full_groups > 0 ? static_cast<int>(gk[j])
+                                               : (a.g_idx ? checked_group(a, k) : k / a.group);
             if (gg != cur_g) {
-              load_sz<BITS>(a, gg, n0c, s, z);
+              if (geo.full_groups > 0) {
+                const uint4 sz = *reinterpret_cast<const uint4*>(sSZ + gg * kSlab + col0);
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                  const uint32_t e = (&sz.x)[cc];
+                  s[cc] = __half2float(__ushort_as_half(lo16(e)));
+                  zf[cc] = __uint_as_float(0x4B000000u | (e >> 16));   // 2^23 + zero
+                }
+              } else {
+                int z[4];
+                load_sz<BITS>(a, gg, n0c, s, z);
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) zf[cc] = 8388608.0f + static_cast<float>(z[cc]);
+              }
               cur_g = gg;
             }
+            // q - z exactly (magic 2^23 has ulp 1), one fp32 product, rounded once below
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) v[cc][h] = diff_f32(unit_code<BITS>(wv, cc, j), z[cc]) * s[cc];
+            for (int cc = 0; cc < 4; ++cc)
+              v[cc][h] = (__uint_as_float(0x4B000000u | unit_code<BITS>(wv, cc, j)) - zf[cc]) * s[cc];
           }
 #pragma unroll
           for (int cc = 0; cc < 4; ++cc) w[cc][p] = pack2(v[cc][0], v[cc][1], T());
@@ -591,7 +648,8 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
 // is resident at once (one wave), at least 2 -- all of them for the common one-token shapes, so
 // the whole slice is in flight from the first cycle.
 template <int BITS>
-TmaGeo make_geo(int units, int cs, int M, int group, int ctas, int sm_count, int max_per_sm) {
+TmaGeo make_geo(int units, int cs, int M, int group, int ctas, int sm_count, int max_per_sm, bool full,
+                bool has_gidx, int G) {
   constexpr int ROWS = Pack<BITS>::kRowsPerUnit;
   constexpr int PER = Pack<BITS>::kPerUnit;
   TmaGeo g;
@@ -601,6 +659,15 @@ TmaGeo make_geo(int units, int cs, int M, int group, int ctas, int sm_count, int
   const int tile_bytes = 4 * ROWS * kSlab * 4;
   const int tpg = group / (4 * PER);
   g.max_groups = (tpg >= 1 ? (g.tiles_per_cta + tpg - 1) / tpg : g.tiles_per_cta) + 1;
+  if (full) g.max_groups = 0;                                  // no FOLD constants or sums
+  // FULL path: stage scales/zeros (all G with g_idx) and per-k groups when they take <= 24 KB
+  g.full_groups = 0;
+  g.full_k = g.tiles_per_cta * 4 * PER;
+  if (full) {
+    const int range_groups = (g.tiles_per_cta * 4 * PER + group - 1) / group + 1;
+    const int ng = has_gidx ? G : (range_groups < G ? range_groups : G);
+    if (static_cast<size_t>(ng) * kSlab * 4 + static_cast<size_t>(g.full_k) * 2 <= 24 * 1024) g.full_groups = ng;
+  }
   int per_sm = (ctas + sm_count - 1) / sm_count;
   if (per_sm > max_per_sm) per_sm = max_per_sm;
   if (per_sm < 1) per_sm = 1;
@@ -642,7 +709,8 @@ cudaError_t launch_mma(const Problem& p, int cs, cudaStream_t stream) {
   a.C = p.out; a.status = p.status;
   const int slabs = (p.N + kSlab - 1) / kSlab;
   constexpr int kMaxPerSm = (MT <= 16 && BITS != 3) ? 5 : 4;   // register-limited residency
-  const TmaGeo geo = make_geo<BITS>(a.units, cs, p.M, p.group, slabs * cs, device_info().sm_count, kMaxPerSm);
+  const TmaGeo geo = make_geo<BITS>(a.units, cs, p.M, p.group, slabs * cs, device_info().sm_count, kMaxPerSm,
+                                    !FOLD, p.g_idx != nullptr, p.G);
   CUtensorMap tmW;
   {
     constexpr int ROWS = Pack<BITS>::kRowsPerUnit;
