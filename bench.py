@@ -338,15 +338,22 @@ def run_prefill(g, torch, dev, stream, bf16_peak, peak_src, l2):
 
 
 # ------------------------------------------------------------------------------------ sweep
-def time_workload(g, torch, dev, stream, wl, M, fmt, l2, reps=200):
+def time_workload(g, torch, dev, stream, wl, M, fmt, l2, reps=200, prepacked=False):
     """Per-launch time of gptq_gemm on one workload: CUDA graph of `reps` launches over weight
-    copies whose total exceeds 3x L2 (or the whole problem when one copy is larger)."""
+    copies whose total exceeds 3x L2 (or the whole problem when one copy is larger).
+    prepacked: an act-order checkpoint with its rows sorted by group (gptq_prepack_act_order),
+    multiplied by gptq_gemm_perm."""
     draw = gptq_inputs.draw_weights(wl)
     W = torch.from_numpy(draw.W).to(dev)
     gi = None if draw.g_idx is None else torch.from_numpy(draw.g_idx).to(dev)
     f = g.V2 if fmt == "v2" else g.V1
     qw, qz, sc = g.quantize_rtn(W, bits=wl.bits, group=wl.group, g_idx=gi, sym=wl.sym, fmt=f)
     del W
+    perm = None
+    if prepacked:
+        qw2, p = g.prepack_act_order(qw.cpu().numpy(), draw.g_idx, K=wl.K, N=wl.N, bits=wl.bits,
+                                     group=wl.group)
+        qw, perm = torch.from_numpy(qw2).to(dev), torch.from_numpy(p).to(dev)
     A = gptq_inputs.draw_activations(wl, M).to(dev)
     nbytes = algorithmic_bytes(wl, M)
     S = max(1, min(32, int(np.ceil(3 * l2 / nbytes))))
@@ -356,7 +363,10 @@ def time_workload(g, torch, dev, stream, wl, M, fmt, l2, reps=200):
 
     def launch(i):
         q, z, s_, a, c = sets[i % S]
-        g.gemm(a, q, z, s_, gi, bits=wl.bits, group=wl.group, fmt=f, out=c, stream=stream)
+        if prepacked:
+            g.gemm_perm(a, perm, q, z, s_, bits=wl.bits, group=wl.group, fmt=f, out=c, stream=stream)
+        else:
+            g.gemm(a, q, z, s_, gi, bits=wl.bits, group=wl.group, fmt=f, out=c, stream=stream)
 
     with torch.cuda.stream(stream):
         for i in range(2 * S):
@@ -382,9 +392,15 @@ def time_workload(g, torch, dev, stream, wl, M, fmt, l2, reps=200):
 def run_sweep(g, torch, dev, stream, hbm_peak, bf16_peak, l2):
     rows = []
     for name, wl in gptq_inputs.WORKLOADS.items():
+        variants = [(fmt, False) for fmt in wl.fmts]
+        if wl.act_order:
+            variants += [(fmt + "+prepacked", True) for fmt in wl.fmts]
         for M in wl.Ms:
-            for fmt in wl.fmts:
-                ms, nbytes = time_workload(g, torch, dev, stream, wl, M, fmt, l2)
+            for fmt, pre in variants:
+                if pre and M > g.DECODE_MAX_M:
+                    continue
+                ms, nbytes = time_workload(g, torch, dev, stream, wl, M, fmt.split("+")[0], l2,
+                                           prepacked=pre)
                 gbs = nbytes / (ms * 1e-3) / 1e9
                 tflops = 2.0 * M * wl.N * wl.K / (ms * 1e-3) / 1e12
                 row = {"workload": name, "M": M, "fmt": fmt, "us": round(ms * 1e3, 3),

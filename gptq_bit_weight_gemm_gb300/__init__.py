@@ -12,6 +12,8 @@ Operations (page "增强 vLLM 对 GPTQv2 格式的支持：分析与实现", sec
   dequant(qweight, qzeros, scales, g_idx, K, bits, group, fmt, dtype) -> W [K, N]
   quantize_rtn(W, bits, group, g_idx, sym, fmt)              -> (qweight, qzeros, scales)
   repack_zeros_v1_to_v2(qzeros_v1, N, bits)                  (host memory)
+  prepack_act_order(qweight, g_idx, K, N, bits, group)      (host memory) -> (qweight', perm)
+  gemm_perm(A, perm, qweight', qzeros, scales, bits, group) -> A[:, perm] @ dequant(W'), M <= 32
   device_status(stream)                                      -> GPTQ_DEV_* bits
 """
 import ctypes
@@ -57,6 +59,8 @@ _SIGNATURES = {
     "gptq_get_device_status": (_I, [_P, ctypes.POINTER(ctypes.c_uint)]),
     "gptq_strerror": (ctypes.c_char_p, [_I]),
     "gptq_selftest_wait_timeout": (_I, [ctypes.c_ulonglong, _P, _P]),
+    "gptq_prepack_act_order": (_I, [_P, _P, _I, _I, _I, _I, _P, _P]),
+    "gptq_gemm_perm": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
 }
 
 
@@ -183,6 +187,34 @@ def repack_zeros_v1_to_v2(qzeros_v1, N, bits):
     G = src.shape[0]
     rc = lib().gptq_repack_zeros_v1_to_v2(src.ctypes.data_as(_P), out.ctypes.data_as(_P), G, N, bits)
     _check(rc, "gptq_repack_zeros_v1_to_v2")
+    return out
+
+
+def prepack_act_order(qweight, g_idx, *, K, N, bits, group):
+    """Host: sort an act-order checkpoint's rows by group.  qweight (numpy int32 [K*bits/32, N])
+    and g_idx (numpy int32 [K]) -> (qweight_out, perm), with A @ W == A[:, perm] @ W_out."""
+    qw = np.ascontiguousarray(qweight, dtype=np.int32)
+    gi = np.ascontiguousarray(g_idx, dtype=np.int32)
+    out = np.empty_like(qw)
+    perm = np.empty(K, dtype=np.int32)
+    rc = lib().gptq_prepack_act_order(qw.ctypes.data_as(_P), gi.ctypes.data_as(_P), K, N, bits, group,
+                                      out.ctypes.data_as(_P), perm.ctypes.data_as(_P))
+    _check(rc, "gptq_prepack_act_order")
+    return out, perm
+
+
+def gemm_perm(A, perm, qweight, qzeros, scales, *, bits, group, fmt=V2, out=None, stream=None):
+    """C[M, N] = A[:, perm] @ dequant(prepacked qweight), M <= 32."""
+    torch = _torch()
+    M, K = A.shape
+    N = qweight.shape[1]
+    if out is None:
+        out = torch.empty((M, N), dtype=A.dtype, device=A.device)
+    rc = lib().gptq_gemm_perm(_ptr(A, name="A"), M, K, _dtype_code(A), _ptr(perm, torch.int32, "perm"),
+                              _ptr(qweight, torch.int32, "qweight"), _ptr(qzeros, torch.int32, "qzeros"),
+                              _ptr(scales, torch.float16, "scales"), N, bits, group, fmt,
+                              _ptr(out, A.dtype, "out"), _stream(stream))
+    _check(rc, "gptq_gemm_perm")
     return out
 
 

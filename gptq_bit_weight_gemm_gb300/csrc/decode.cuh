@@ -33,6 +33,7 @@ struct Args {
   const int32_t* qzeros;
   const __half* scales;
   const int32_t* g_idx;
+  const int32_t* perm;       // nullable: activation column of each (prepacked) weight row
   int group, G, zero_offset, zwords, units;
   void* C;
   unsigned* status;
@@ -119,14 +120,30 @@ struct UnitVec {   // a unit's activations: PER 16-bit values
       w[0] = v.x; w[1] = v.y;
     }
   }
+  // the same, gathered: value i is row[pk[i]] (prepacked act-order rows); an index outside
+  // [0, K) is clamped so that a bad permutation cannot read outside the row
+  __device__ __forceinline__ void load_perm(const uint16_t* row, const int32_t* pk, int K) {
+    int idx[PER];
+#pragma unroll
+    for (int i = 0; i < PER / 4; ++i) {
+      const int4 v = __ldg(reinterpret_cast<const int4*>(pk) + i);
+      idx[4 * i] = v.x; idx[4 * i + 1] = v.y; idx[4 * i + 2] = v.z; idx[4 * i + 3] = v.w;
+    }
+#pragma unroll
+    for (int i = 0; i < PER; ++i) idx[i] = idx[i] < 0 ? 0 : (idx[i] >= K ? K - 1 : idx[i]);
+#pragma unroll
+    for (int i = 0; i < kWords; ++i)
+      w[i] = static_cast<uint32_t>(__ldg(row + idx[2 * i])) | (static_cast<uint32_t>(__ldg(row + idx[2 * i + 1])) << 16);
+  }
   __device__ __forceinline__ uint32_t half(int k) const {
     return (w[k >> 1] >> (16 * (k & 1))) & 0xFFFFu;
   }
 };
 
 template <int PER, int NP, class LoK, class HiK, class Put>
-__device__ __forceinline__ void stage_pairs(const uint16_t* A, int M, int K, int ufirst, int nunits,
-                                            int units, LoK lo_k, HiK hi_k, Put put) {
+__device__ __forceinline__ void stage_pairs(const uint16_t* A, const int32_t* perm, int M, int K,
+                                            int ufirst, int nunits, int units, LoK lo_k, HiK hi_k,
+                                            Put put) {
   const int items = nunits * M;
   for (int base = 0; base < items; base += kStageBatch * static_cast<int>(blockDim.x)) {
     UnitVec<PER> v[kStageBatch];
@@ -134,8 +151,12 @@ __device__ __forceinline__ void stage_pairs(const uint16_t* A, int M, int K, int
     for (int j = 0; j < kStageBatch; ++j) {
       const int it = base + j * static_cast<int>(blockDim.x) + static_cast<int>(threadIdx.x);
       const int uu = M == 1 ? it : it / M, m = it - uu * M;
-      if (it < items && ufirst + uu < units)
-        v[j].load(A + static_cast<long long>(m) * K + static_cast<long long>(ufirst + uu) * PER);
+      if (it < items && ufirst + uu < units) {
+        if (perm)
+          v[j].load_perm(A + static_cast<long long>(m) * K, perm + static_cast<long long>(ufirst + uu) * PER, K);
+        else
+          v[j].load(A + static_cast<long long>(m) * K + static_cast<long long>(ufirst + uu) * PER);
+      }
     }
 #pragma unroll
     for (int j = 0; j < kStageBatch; ++j) {
@@ -150,27 +171,6 @@ __device__ __forceinline__ void stage_pairs(const uint16_t* A, int M, int K, int
     }
   }
 }
-
-// Raw scale/zero words of columns n0..n0+3 for group g (loads only; decoded later so the
-// loads overlap the activation staging).
-template <int BITS>
-struct SZRaw {
-  uint2 sv;
-  uint32_t zf;
-  __device__ __forceinline__ void load(const Args& a, int g, int n0) {
-    sv = __ldg(reinterpret_cast<const uint2*>(a.scales + static_cast<long long>(g) * a.N + n0));
-    zf = zeros4<BITS>(a.qzeros + static_cast<long long>(g) * a.zwords, n0);
-  }
-  __device__ __forceinline__ void decode(int zero_offset, float (&s)[4], int (&z)[4]) const {
-    s[0] = __half2float(__ushort_as_half(static_cast<uint16_t>(sv.x & 0xFFFFu)));
-    s[1] = __half2float(__ushort_as_half(static_cast<uint16_t>(sv.x >> 16)));
-    s[2] = __half2float(__ushort_as_half(static_cast<uint16_t>(sv.y & 0xFFFFu)));
-    s[3] = __half2float(__ushort_as_half(static_cast<uint16_t>(sv.y >> 16)));
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-      z[c] = static_cast<int>((zf >> (BITS * c)) & Pack<BITS>::kMask) + zero_offset;
-  }
-};
 
 // Cluster size: enough warps to fill the GPU (about 24 per SM), at least two units per warp.
 inline int choose_cluster(const Problem& p, int per_unit) {

@@ -312,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
   // (FOLD: times 2^-shift(p), matching the raw codes of CodePairs).
   const uint16_t* A16 = static_cast<const uint16_t*>(a.A);
   const int nunits = ntile * 4;
-  stage_pairs<PER, NP>(A16, a.M, a.K, cu0, nunits, a.units,
+  stage_pairs<PER, NP>(A16, a.perm, a.M, a.K, cu0, nunits, a.units,
                        [](int p) { return MP::lo_k(p); }, [](int p) { return MP::hi_k(p); },
                        [&](int uu, int m, int p, uint32_t v) {
                          if constexpr (FOLD) v = scale_pow2(v, CodePairs<T, BITS>::shift(p), T());
@@ -703,7 +703,7 @@ cudaError_t launch_mma(const Problem& p, int cs, cudaStream_t stream) {
   a.A = p.A; a.M = p.M; a.K = p.K; a.N = p.N;
   a.qweight = p.qweight; a.qzeros = p.qzeros;
   a.scales = static_cast<const __half*>(p.scales);
-  a.g_idx = p.g_idx; a.group = p.group; a.G = p.G; a.zero_offset = p.zero_offset;
+  a.g_idx = p.g_idx; a.perm = p.perm; a.group = p.group; a.G = p.G; a.zero_offset = p.zero_offset;
   a.zwords = p.N * BITS / 32;
   a.units = p.K / Pack<BITS>::kPerUnit;
   a.C = p.out; a.status = p.status;

@@ -194,6 +194,69 @@ extern "C" int gptq_gemm(const void* A, int M, int K, int a_dtype, const int32_t
   return gptq::from_cuda(gptq::launch_prefill(p, s));
 }
 
+extern "C" int gptq_gemm_perm(const void* A, int M, int K, int a_dtype, const int32_t* perm,
+                              const int32_t* qweight, const int32_t* qzeros, const void* scales,
+                              int N, int bits, int group, int fmt, void* C, void* stream) {
+  Problem p = {};
+  if (group == -1) return GPTQ_ERR_SHAPE;                 // act-order always has real groups
+  int rc = gptq::check_common(qweight, qzeros, scales, nullptr, K, N, bits, group, &p);
+  if (rc) return rc;
+  if (fmt != GPTQ_FMT_V1 && fmt != GPTQ_FMT_V2) return GPTQ_ERR_ARG;
+  if (a_dtype != GPTQ_F16 && a_dtype != GPTQ_BF16) return GPTQ_ERR_ARG;
+  if (M < 0 || M > gptq::kDecodeMaxM) return GPTQ_ERR_SHAPE;
+  if (M == 0) return GPTQ_OK;
+  if (!A || !C || !perm) return GPTQ_ERR_ARG;
+  if (!gptq::aligned(A, 16) || !gptq::aligned(C, 16) || !gptq::aligned(perm, 16)) return GPTQ_ERR_ALIGN;
+  rc = gptq::device_ready(&p);
+  if (rc) return rc;
+  p.A = A;
+  p.M = M;
+  p.dtype = a_dtype;
+  p.perm = perm;
+  p.zero_offset = fmt == GPTQ_FMT_V1 ? 1 : 0;
+  p.out = C;
+  return gptq::from_cuda(gptq::launch_decode(p, static_cast<cudaStream_t>(stream)));
+}
+
+extern "C" int gptq_prepack_act_order(const int32_t* qweight, const int32_t* g_idx, int K, int N,
+                                      int bits, int group, int32_t* qweight_out, int32_t* perm) {
+  if (!gptq::bits_ok(bits) || !qweight || !g_idx || !qweight_out || !perm) return GPTQ_ERR_ARG;
+  if (K <= 0 || N <= 0 || K % 32 || N % 32 || group <= 0 || K % group) return GPTQ_ERR_SHAPE;
+  const int G = K / group;
+  // stable counting sort of the rows by group; every group must hold exactly `group` rows
+  std::vector<int> next(G, 0);
+  for (int k = 0; k < K; ++k) {
+    const int g = g_idx[k];
+    if (g < 0 || g >= G) return GPTQ_ERR_SHAPE;
+    if (++next[g] > group) return GPTQ_ERR_SHAPE;
+  }
+  for (int g = 0; g < G; ++g) next[g] = g * group;
+  std::vector<int32_t> order(K);
+  for (int k = 0; k < K; ++k) order[next[g_idx[k]]++] = k;
+  // rewrite every column's LSB-first code stream in the new row order
+  const int rows = K * bits / 32;
+  const uint32_t mask = (1u << bits) - 1u;
+  const uint32_t* in = reinterpret_cast<const uint32_t*>(qweight);
+  std::vector<uint32_t> out(static_cast<size_t>(rows) * N, 0u);
+  for (int n = 0; n < N; ++n) {
+    auto code = [&](int k) {
+      const int bit = bits * k, w = bit >> 5, sh = bit & 31;
+      uint64_t v = in[static_cast<size_t>(w) * N + n];
+      if (sh + bits > 32) v |= static_cast<uint64_t>(in[static_cast<size_t>(w + 1) * N + n]) << 32;
+      return static_cast<uint32_t>(v >> sh) & mask;
+    };
+    for (int k = 0; k < K; ++k) {
+      const uint64_t v = static_cast<uint64_t>(code(order[k])) << ((bits * k) & 31);
+      const int w = (bits * k) >> 5;
+      out[static_cast<size_t>(w) * N + n] |= static_cast<uint32_t>(v);
+      if (((bits * k) & 31) + bits > 32) out[static_cast<size_t>(w + 1) * N + n] |= static_cast<uint32_t>(v >> 32);
+    }
+  }
+  for (size_t i = 0; i < out.size(); ++i) qweight_out[i] = static_cast<int32_t>(out[i]);
+  for (int k = 0; k < K; ++k) perm[k] = order[k];
+  return GPTQ_OK;
+}
+
 extern "C" int gptq_quantize_rtn(const float* W, int K, int N, int bits, int group,
                                  const int32_t* g_idx, int sym, int fmt, int32_t* qweight,
                                  int32_t* qzeros, void* scales, void* stream) {

@@ -17,6 +17,7 @@ struct Problem {
   const int32_t* qzeros;     // [G, N*bits/32]
   const void* scales;        // [G, N] fp16
   const int32_t* g_idx;      // [K] or nullptr
+  const int32_t* perm;       // [K] or nullptr: A column of each weight row (prepacked act-order)
   int bits;
   int group;                 // K when the caller passed -1
   int G;

@@ -91,9 +91,9 @@ int gptq_dequant(const int32_t* qweight, const int32_t* qzeros, const void* scal
  * gptq_gemm -- C[M, N] = A[M, K] @ W[K, N] with W dequantized on the fly, the operation
  * vLLM's gptq_gemm(..., use_v2_format) performs (page section "调整细节：根据格式选择处理
  * 方式"; fmt == GPTQ_FMT_V2 is use_v2_format = true).  Products are accumulated in fp32 and
- * C is rounded once to A's dtype.  M <= 32 runs the memory-bound decode kernels (split-K
- * over a thread-block cluster, reduced through distributed shared memory; CUDA cores for
- * M <= 4, mma.sync from registers above); larger M runs the tcgen05 tensor-core kernel.
+ * C is rounded once to A's dtype.  M <= 32 runs the memory-bound decode kernel (TMA-streamed
+ * weights, mma.sync from registers, split-K over a thread-block cluster reduced through
+ * distributed shared memory); larger M runs the tcgen05 tensor-core kernel.
  * Device pointers: A, qweight, qzeros, scales, g_idx (nullable), C.  `workspace` may be NULL
  * when gptq_gemm_workspace_size() returns 0 (every current path); otherwise it must be a
  * device buffer of at least that many bytes, owned by the caller.
@@ -103,6 +103,34 @@ int gptq_gemm(const void* A, int M, int K, int a_dtype, const int32_t* qweight,
               const int32_t* qzeros, const void* scales, const int32_t* g_idx, int N, int bits,
               int group, int fmt, void* C, void* workspace, size_t workspace_bytes,
               void* stream);
+
+/*
+ * gptq_prepack_act_order -- HOST function: rewrite an act-order checkpoint (page section
+ * "LLM 的权重量化": the quantization groups are the row sets {k : g_idx[k] == g}) so that the
+ * groups are contiguous row ranges.  perm[k'] (the stable sort of the rows by g_idx) is the
+ * original row now at row k'; qweight_out holds W[perm[k'], n] in the layout above, so rows
+ * [g*group, (g+1)*group) belong to group g and qzeros/scales stay valid unchanged.  Then
+ * A @ W == A[:, perm] @ W_out: gptq_gemm_perm computes it, gathering A through perm.
+ * Host memory: qweight [K*bits/32, N], g_idx [K], qweight_out (same size, must not alias
+ * qweight), perm [K].  Every group must hold exactly `group` rows (as GPTQ's act-order does),
+ * else GPTQ_ERR_SHAPE; an entry outside [0, K/group) is GPTQ_ERR_SHAPE too.
+ */
+int gptq_prepack_act_order(const int32_t* qweight, const int32_t* g_idx, int K, int N, int bits,
+                           int group, int32_t* qweight_out, int32_t* perm);
+
+/*
+ * gptq_gemm_perm -- C[M, N] = A[:, perm] @ W[K, N] for a checkpoint prepacked by
+ * gptq_prepack_act_order (W = its qweight_out, contiguous groups of `group` rows), i.e. the
+ * act-order GEMM of page section "调整细节：根据格式选择处理方式" without a per-row group
+ * lookup.  The decode kernel gathers A's columns through perm while staging them.  Tokens:
+ * 0 <= M <= 32 (larger M: GPTQ_ERR_SHAPE; gptq_gemm with g_idx serves that range).
+ * Device pointers: A [M, K], perm [K] int32 (16-byte aligned; an entry outside [0, K) is
+ * clamped, never read past A), qweight, qzeros, scales, C.
+ * Returns GPTQ_OK or a negative gptq_status.
+ */
+int gptq_gemm_perm(const void* A, int M, int K, int a_dtype, const int32_t* perm,
+                   const int32_t* qweight, const int32_t* qzeros, const void* scales, int N,
+                   int bits, int group, int fmt, void* C, void* stream);
 
 /* Bytes of device workspace gptq_gemm needs for this problem (0 for every current path). */
 size_t gptq_gemm_workspace_size(int M, int K, int N, int bits, int group);

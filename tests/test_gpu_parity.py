@@ -201,6 +201,54 @@ def test_act_order_permutation_invariance():
     assert torch.equal(Wp.view(torch.int16), W[torch.from_numpy(p).to(DEV)].view(torch.int16))
 
 
+# ------------------------------------------------------------------------------ prepacked act-order
+PERM_CASES = [
+    # (bits, group, dtype, M, K, N): act-order checkpoints, rows sorted by group on the host
+    (3, 128, "f16", 16, 640, 416),
+    (3, 128, "bf16", 20, 640, 288),
+    (2, 16, "f16", 4, 512, 128),
+    (2, 64, "bf16", 13, 1024, 160),
+    (4, 128, "f16", 1, 1024, 544),
+    (4, 64, "bf16", 8, 512, 352),
+    (8, 128, "f16", 32, 384, 288),
+    (8, 128, "bf16", 3, 384, 160),
+]
+
+
+def _gemm_perm(wl, ck, A):
+    qw2, perm = g.prepack_act_order(ck["qweight"], ck["g_idx"], K=wl.K, N=wl.N, bits=wl.bits,
+                                    group=wl.group)
+    _, qz, sc, _ = to_device(ck)
+    C = g.gemm_perm(A.to(DEV), torch.from_numpy(perm).to(DEV), torch.from_numpy(qw2).to(DEV), qz, sc,
+                    bits=wl.bits, group=wl.group, fmt=ck["fmt"])
+    torch.cuda.synchronize()
+    return C
+
+
+@pytest.mark.parametrize("case", PERM_CASES, ids=lambda c: "b%d_g%d_%s_M%d_K%d_N%d" % c)
+@pytest.mark.parametrize("fmt", ["v2", "v1"])
+def test_gemm_perm_prepacked_act_order(case, fmt):
+    """A[:, perm] @ W_prepacked equals the act-order GEMM of the original checkpoint."""
+    bits, group, dt, M, K, N = case
+    wl = gptq_inputs.Workload("small", K, N, bits, group, dt, (M,), (fmt,), seed=M * 11 + bits,
+                              act_order=True)
+    _, ck = checkpoint(wl, fmt)
+    A = gptq_inputs.draw_activations(wl, M)
+    C = _gemm_perm(wl, ck, A)
+    Cref, B = _oracle_gemm(wl, ck, A)
+    assert_gemm_close(C.float().cpu().numpy(), Cref, B, str(case))
+
+
+def test_gemm_perm_full_size_act_order():
+    wl = WL["act_order_3bit_g128"]
+    _, ck = checkpoint(wl, "v2")
+    A = gptq_inputs.draw_activations(wl, 16)
+    C = _gemm_perm(wl, ck, A)
+    Cref, B = _oracle_gemm(wl, ck, A)
+    assert_gemm_close(C.float().cpu().numpy(), Cref, B, "act_order_3bit_g128 prepacked")
+    assert g.device_status() == 0
+
+
 # ------------------------------------------------------------------------------ edge cases
 def test_m0_leaves_output_untouched():
     wl = WL["tiny_4bit_g64"]

@@ -22,7 +22,8 @@ def test_exports_every_declared_symbol(lib):
     assert declared == sorted(["gptq_dequant", "gptq_gemm", "gptq_gemm_workspace_size",
                                "gptq_repack_zeros_v1_to_v2", "gptq_quantize_rtn",
                                "gptq_get_device_status", "gptq_strerror",
-                               "gptq_selftest_wait_timeout"])
+                               "gptq_selftest_wait_timeout", "gptq_prepack_act_order",
+                               "gptq_gemm_perm"])
     for name in declared:
         assert hasattr(lib, name), name
 
@@ -102,6 +103,60 @@ def test_host_repack_in_place(lib):
     rc = lib.gptq_repack_zeros_v1_to_v2(qz.ctypes.data_as(P), qz.ctypes.data_as(P), 1, 64, 4)
     assert rc == 0
     assert np.array_equal(oracle.unpack_n(qz, 1, 64, 4), z + 1)
+
+
+def _act_order_checkpoint(bits, K=256, N=64, group=32, seed=0):
+    rng = np.random.default_rng(seed)
+    W = (rng.standard_normal((K, N)) * 0.02).astype(np.float32)
+    g_idx = (rng.permutation(K) // group).astype(np.int32)
+    return oracle.make_checkpoint(W, bits, group, g_idx=g_idx), g_idx
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4, 8])
+def test_prepack_act_order_matches_oracle(lib, bits):
+    """Row k' of the prepacked checkpoint, read with contiguous groups, dequantizes exactly like
+    row perm[k'] of the act-order original (the oracle reads both)."""
+    K, N, group = 256, 64, 32
+    ck, g_idx = _act_order_checkpoint(bits, K, N, group)
+    qw2, perm = g.prepack_act_order(ck["qweight"], g_idx, K=K, N=N, bits=bits, group=group)
+    assert sorted(perm.tolist()) == list(range(K))
+    assert np.all(np.diff(g_idx[perm]) >= 0)                       # groups now contiguous
+    assert np.all(np.diff(perm[g_idx[perm] == 3]) > 0)             # stable inside a group
+    w_orig = oracle.dequant(ck["qweight"], ck["qzeros"], ck["scales"], g_idx, K, N, bits, group, 2, 0)
+    w_new = oracle.dequant(qw2, ck["qzeros"], ck["scales"], None, K, N, bits, group, 2, 0)
+    assert np.array_equal(w_new, w_orig[perm])
+    assert np.array_equal(oracle.unpack_k(qw2, K, N, bits), ck["q"][perm])
+
+
+def test_prepack_act_order_validation(lib):
+    K, N, group = 256, 64, 32
+    ck, g_idx = _act_order_checkpoint(4, K, N, group)
+    qw = ck["qweight"]
+    bad = g_idx.copy()
+    bad[np.flatnonzero(g_idx == 1)[0]] = 0                         # group 0: group + 1 rows
+    for gi, code in ((bad, -2), (np.full(K, 8, np.int32), -2), (np.full(K, -1, np.int32), -2)):
+        out, perm = np.empty_like(qw), np.empty(K, np.int32)
+        rc = lib.gptq_prepack_act_order(qw.ctypes.data_as(P), gi.ctypes.data_as(P), K, N, 4, group,
+                                        out.ctypes.data_as(P), perm.ctypes.data_as(P))
+        assert rc == code
+    out, perm = np.empty_like(qw), np.empty(K, np.int32)
+    assert lib.gptq_prepack_act_order(qw.ctypes.data_as(P), g_idx.ctypes.data_as(P), K, N, 4, 48,
+                                      out.ctypes.data_as(P), perm.ctypes.data_as(P)) == -2
+    assert lib.gptq_prepack_act_order(None, g_idx.ctypes.data_as(P), K, N, 4, group,
+                                      out.ctypes.data_as(P), perm.ctypes.data_as(P)) == -1
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(M=33), -2), (dict(M=-1), -2), (dict(group=-1), -2), (dict(perm=None), -1),
+    (dict(perm=P(0x10004)), -3), (dict(bits=5), -1), (dict(K=48), -2),
+])
+def test_gemm_perm_validation_without_gpu(lib, kw, code):
+    a = dict(A=FAKE, M=1, K=256, dtype=0, perm=FAKE, qweight=FAKE, qzeros=FAKE, scales=FAKE,
+             N=256, bits=4, group=128, fmt=2, C=FAKE)
+    a.update(kw)
+    rc = lib.gptq_gemm_perm(a["A"], a["M"], a["K"], a["dtype"], a["perm"], a["qweight"], a["qzeros"],
+                            a["scales"], a["N"], a["bits"], a["group"], a["fmt"], a["C"], None)
+    assert rc == code
 
 
 def test_product_does_not_import_oracle():
