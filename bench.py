@@ -354,6 +354,7 @@ def time_workload(g, torch, dev, stream, wl, M, fmt, l2, reps=200, prepacked=Fal
         qw2, p = g.prepack_act_order(qw.cpu().numpy(), draw.g_idx, K=wl.K, N=wl.N, bits=wl.bits,
                                      group=wl.group)
         qw, perm = torch.from_numpy(qw2).to(dev), torch.from_numpy(p).to(dev)
+        ws = torch.empty(max(1, g.gemm_perm_workspace_size(M, wl.K)), dtype=torch.uint8, device=dev)
     A = gptq_inputs.draw_activations(wl, M).to(dev)
     nbytes = algorithmic_bytes(wl, M)
     S = max(1, min(32, int(np.ceil(3 * l2 / nbytes))))
@@ -364,7 +365,8 @@ def time_workload(g, torch, dev, stream, wl, M, fmt, l2, reps=200, prepacked=Fal
     def launch(i):
         q, z, s_, a, c = sets[i % S]
         if prepacked:
-            g.gemm_perm(a, perm, q, z, s_, bits=wl.bits, group=wl.group, fmt=f, out=c, stream=stream)
+            g.gemm_perm(a, perm, q, z, s_, bits=wl.bits, group=wl.group, fmt=f, out=c, workspace=ws,
+                        stream=stream)
         else:
             g.gemm(a, q, z, s_, gi, bits=wl.bits, group=wl.group, fmt=f, out=c, stream=stream)
 

@@ -60,7 +60,8 @@ _SIGNATURES = {
     "gptq_strerror": (ctypes.c_char_p, [_I]),
     "gptq_selftest_wait_timeout": (_I, [ctypes.c_ulonglong, _P, _P]),
     "gptq_prepack_act_order": (_I, [_P, _P, _I, _I, _I, _I, _P, _P]),
-    "gptq_gemm_perm": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
+    "gptq_gemm_perm": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P]),
+    "gptq_gemm_perm_workspace_size": (_SZ, [_I, _I]),
 }
 
 
@@ -203,17 +204,28 @@ def prepack_act_order(qweight, g_idx, *, K, N, bits, group):
     return out, perm
 
 
-def gemm_perm(A, perm, qweight, qzeros, scales, *, bits, group, fmt=V2, out=None, stream=None):
-    """C[M, N] = A[:, perm] @ dequant(prepacked qweight), M <= 32."""
+def gemm_perm_workspace_size(M, K):
+    return int(lib().gptq_gemm_perm_workspace_size(M, K))
+
+
+def gemm_perm(A, perm, qweight, qzeros, scales, *, bits, group, fmt=V2, out=None, workspace=None,
+              stream=None):
+    """C[M, N] = A[:, perm] @ dequant(prepacked qweight), M <= 32.  For M > 1 a workspace of
+    gemm_perm_workspace_size(M, K) bytes is used (allocated here when not given)."""
     torch = _torch()
     M, K = A.shape
     N = qweight.shape[1]
     if out is None:
         out = torch.empty((M, N), dtype=A.dtype, device=A.device)
+    ws_bytes = gemm_perm_workspace_size(M, K)
+    if ws_bytes and workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=A.device)
+    ws_ptr = _ptr(workspace, name="workspace") if ws_bytes else None
+    ws_len = workspace.numel() * workspace.element_size() if ws_bytes else 0
     rc = lib().gptq_gemm_perm(_ptr(A, name="A"), M, K, _dtype_code(A), _ptr(perm, torch.int32, "perm"),
                               _ptr(qweight, torch.int32, "qweight"), _ptr(qzeros, torch.int32, "qzeros"),
                               _ptr(scales, torch.float16, "scales"), N, bits, group, fmt,
-                              _ptr(out, A.dtype, "out"), _stream(stream))
+                              _ptr(out, A.dtype, "out"), ws_ptr, ws_len, _stream(stream))
     _check(rc, "gptq_gemm_perm")
     return out
 

@@ -188,7 +188,8 @@ cudaError_t launch_mma(const Problem& p, int cs, cudaStream_t stream);
 template <int BITS, int MT, typename T>
 cudaError_t launch_mt(const Problem& p, cudaStream_t stream) {
   const int cs = choose_cluster(p, Pack<BITS>::kPerUnit);
-  constexpr bool kHas16 = (BITS == 2 || BITS == 4 || (BITS == 8 && std::is_same<T, __half>::value));
+  constexpr bool kHas16 = (BITS == 2 || BITS == 4 ||
+                           ((BITS == 8 || BITS == 3) && std::is_same<T, __half>::value));
   // the scale folds per group when groups align with k-tiles (4 units)
   const bool fold = kHas16 && p.g_idx == nullptr && (p.group % (4 * Pack<BITS>::kPerUnit)) == 0;
   if constexpr (kHas16) {

@@ -47,10 +47,17 @@ namespace decode {
 // Pairing of a unit's codes into the two halves of one register: pair p = (lo_k(p), hi_k(p)).
 template <int BITS>
 struct MmaPairs {
-  static constexpr int kPairs = BITS == 3 ? 16 : 16 / BITS;
+  static constexpr int kPairs = 16 / BITS;
   static constexpr int kHalf = Pack<BITS>::kPerUnit / 2;
   __device__ static __forceinline__ int lo_k(int p) { return p; }
   __device__ static __forceinline__ int hi_k(int p) { return p + kHalf; }
+};
+// 3-bit: the pairing under which every pair is one mask of one stream window (CodePairs<half, 3>)
+template <>
+struct MmaPairs<3> {
+  static constexpr int kPairs = 16;
+  __device__ static __forceinline__ int lo_k(int p) { return code3_pair(p, 0); }
+  __device__ static __forceinline__ int hi_k(int p) { return code3_pair(p, 1); }
 };
 
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
@@ -315,7 +322,8 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
   stage_pairs<PER, NP>(A16, a.perm, a.M, a.K, cu0, nunits, a.units,
                        [](int p) { return MP::lo_k(p); }, [](int p) { return MP::hi_k(p); },
                        [&](int uu, int m, int p, uint32_t v) {
-                         if constexpr (FOLD) v = scale_pow2(v, CodePairs<T, BITS>::shift(p), T());
+                         if constexpr (FOLD)
+                           v = scale_pow2_pair(v, CodePairs<T, BITS>::shift_lo(p), CodePairs<T, BITS>::shift_hi(p), T());
                          sB[uu * UW + m * NP + p] = v;
                        });
   __syncthreads();
@@ -348,10 +356,10 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
           }
 #pragma unroll
           for (int pp = 0; pp < NP; ++pp) {
-            const float f = F16Traits<T>::to_f32(F16Traits<T>::from_bits(lo16(v[pp]))) +
-                            F16Traits<T>::to_f32(F16Traits<T>::from_bits(hi16(v[pp])));
-            t += f;
-            q = fmaf(f, static_cast<float>(1 << CP::shift(pp)), q);
+            const float fl = F16Traits<T>::to_f32(F16Traits<T>::from_bits(lo16(v[pp])));
+            const float fh = F16Traits<T>::to_f32(F16Traits<T>::from_bits(hi16(v[pp])));
+            t += fl + fh;
+            q = fmaf(fl, static_cast<float>(1 << CP::shift_lo(pp)), fmaf(fh, static_cast<float>(1 << CP::shift_hi(pp)), q));
           }
         }
       }
@@ -446,6 +454,36 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
       const int m = 8 * nb + gq;
       boff[nb] = (m < a.M ? m : a.M - 1) * NP + tq * UW;
     }
+    // 3-bit: unit tq of local tile l is rows 3 (4 l + tq) .. +2 of the chunk; pairs per column
+    auto tile3 = [&](const uint8_t* cslot, int l, int kt) {
+      uint4 wv[3];
+#pragma unroll
+      for (int r = 0; r < 3; ++r) wv[r] = wrow(cslot, (l * 4 + tq) * 3 + r);
+      uint32_t bf[NB][NP];
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) {
+        const uint32_t* src = sB + kt * 4 * UW + boff[nb];
+#pragma unroll
+        for (int i = 0; i < NP / 4; ++i) {
+          const uint4 v = reinterpret_cast<const uint4*>(src)[i];
+          bf[nb][4 * i] = v.x; bf[nb][4 * i + 1] = v.y; bf[nb][4 * i + 2] = v.z; bf[nb][4 * i + 3] = v.w;
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        uint32_t d0[NP], d1[NP];
+        if constexpr (BITS == 3) {
+          CP::run3((&wv[0].x)[2 * t], (&wv[1].x)[2 * t], (&wv[2].x)[2 * t], d0);
+          CP::run3((&wv[0].x)[2 * t + 1], (&wv[1].x)[2 * t + 1], (&wv[2].x)[2 * t + 1], d1);
+        }
+#pragma unroll
+        for (int j = 0; j < NP / 2; ++j)
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb)
+            mma16816(cg[t][nb], d0[2 * j], d1[2 * j], d0[2 * j + 1], d1[2 * j + 1], bf[nb][2 * j],
+                     bf[nb][2 * j + 1], T());
+      }
+    };
     auto tile = [&](const uint8_t* wp, int kt) {
       const uint4 wv = *reinterpret_cast<const uint4*>(wp);
       uint32_t bf[NB][NP];
@@ -465,7 +503,9 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
       }
       uint32_t d[4][NP];
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) CP::run((&wv.x)[cc], d[cc]);
+      for (int cc = 0; cc < 4; ++cc) {
+        if constexpr (BITS != 3) CP::run((&wv.x)[cc], d[cc]);
+      }
 #pragma unroll
       for (int j = 0; j < NP / 2; ++j)
 #pragma unroll
@@ -481,6 +521,7 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
     bool ok = true, dirty = false;
     const uint8_t* we = wslot;                         // rows of even / odd k-tiles of the chunk
     const uint8_t* wo = wslot;
+    const uint8_t* cslot = wslot;                      // this warp's box slot of the chunk
     clear_cg();
     for (int kt = 0; kt < ntile;) {                    // control flow is uniform over the CTA
       if (kt == chunk_end) {
@@ -490,7 +531,8 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
         }
         ++c;
         ok = tma_wait(bar0 + 8 * (c % geo.nbuf), (c / geo.nbuf) & 1, abort_flag, a.status);
-        const uint8_t* cb = wslot + static_cast<size_t>(c % geo.nbuf) * geo.chunk_bytes + tq * kBoxRowBytes;
+        cslot = wslot + static_cast<size_t>(c % geo.nbuf) * geo.chunk_bytes;
+        const uint8_t* cb = cslot + tq * kBoxRowBytes;
         we = cb + ((quad ^ tq) << 4);
         wo = cb + ((quad ^ tq ^ 4) << 4);
         chunk_kt = c * geo.chunk_tiles;
@@ -498,7 +540,10 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
       }
       const int lim = chunk_end < g_end_kt ? chunk_end : g_end_kt;
       const int l0 = kt - chunk_kt;
-      if (lim - kt >= 4) {
+      if constexpr (BITS == 3) {
+        if (ok) tile3(cslot, l0, kt);
+        kt += 1;
+      } else if (lim - kt >= 4) {
         if (ok) {
           const uint8_t* e = (l0 & 1) ? wo : we;
           const uint8_t* o = (l0 & 1) ? we : wo;
@@ -708,9 +753,36 @@ cudaError_t launch_mma(const Problem& p, int cs, cudaStream_t stream) {
   a.units = p.K / Pack<BITS>::kPerUnit;
   a.C = p.out; a.status = p.status;
   const int slabs = (p.N + kSlab - 1) / kSlab;
-  constexpr int kMaxPerSm = (MT <= 16 && BITS != 3) ? 5 : 4;   // register-limited residency
-  const TmaGeo geo = make_geo<BITS>(a.units, cs, p.M, p.group, slabs * cs, device_info().sm_count, kMaxPerSm,
-                                    !FOLD, p.g_idx != nullptr, p.G);
+  const int sms = device_info().sm_count;
+  auto kern = k_decode_mma<BITS, MT, T, FOLD>;
+  // CTAs per SM the registers allow (read once per kernel from its attributes)
+  static std::atomic<int> regs_cache{-1};
+  int regs = regs_cache.load(std::memory_order_relaxed);
+  if (regs < 0) {
+    cudaFuncAttributes fa;
+    regs = cudaFuncGetAttributes(&fa, kern) == cudaSuccess ? fa.numRegs : 0;
+    regs_cache.store(regs, std::memory_order_relaxed);
+  }
+  const int by_regs = regs > 0 ? 65536 / (((regs + 7) & ~7) * kThreads) : 5;
+  const int max_per_sm = by_regs < 1 ? 1 : (by_regs > 5 ? 5 : by_regs);
+  // FOLD: one wave when it can be had -- the largest K split (at most the chosen one) whose grid
+  // is resident at once; halving stops where a CTA's shared memory would no longer fit (a
+  // smaller split stages more activations), and the chosen split stays when no split gives one
+  // wave.  FULL keeps the chosen split: it is latency-bound and gains from every extra CTA.
+  auto geo_for = [&](int c) {
+    return make_geo<BITS>(a.units, c, p.M, p.group, slabs * c, sms, max_per_sm, !FOLD, p.g_idx != nullptr, p.G);
+  };
+  for (int c = cs; FOLD && c >= 1; c /= 2) {
+    const size_t bytes = (TmaSmem<BITS>::bytes(geo_for(c), p.M) + 1023) & ~static_cast<size_t>(1023);
+    if (bytes > 227 * 1024) break;
+    int per_sm = static_cast<int>(233472 / (bytes + 1024));
+    per_sm = per_sm < max_per_sm ? per_sm : max_per_sm;
+    if (slabs * c <= per_sm * sms) {
+      cs = c;
+      break;
+    }
+  }
+  const TmaGeo geo = geo_for(cs);
   CUtensorMap tmW;
   {
     constexpr int ROWS = Pack<BITS>::kRowsPerUnit;
@@ -723,7 +795,6 @@ cudaError_t launch_mma(const Problem& p, int cs, cudaStream_t stream) {
       return cudaErrorInvalidValue;
   }
   const size_t smem = TmaSmem<BITS>::bytes(geo, p.M);
-  auto kern = k_decode_mma<BITS, MT, T, FOLD>;
   // once per device, FOLD only: the full shared-memory carveout (left to the driver, it may pick
   // a smaller one and fit fewer CTAs per SM than the one-wave budget above assumes).  The FULL
   // path keeps the driver's choice: it re-reads scales through L1, which the carveout would shrink.

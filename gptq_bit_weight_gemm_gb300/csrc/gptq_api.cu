@@ -194,9 +194,15 @@ extern "C" int gptq_gemm(const void* A, int M, int K, int a_dtype, const int32_t
   return gptq::from_cuda(gptq::launch_prefill(p, s));
 }
 
+extern "C" size_t gptq_gemm_perm_workspace_size(int M, int K) {
+  if (M <= 1 || K <= 0) return 0;
+  return (static_cast<size_t>(M) * K * 2 + 255) & ~static_cast<size_t>(255);
+}
+
 extern "C" int gptq_gemm_perm(const void* A, int M, int K, int a_dtype, const int32_t* perm,
                               const int32_t* qweight, const int32_t* qzeros, const void* scales,
-                              int N, int bits, int group, int fmt, void* C, void* stream) {
+                              int N, int bits, int group, int fmt, void* C, void* workspace,
+                              size_t workspace_bytes, void* stream) {
   Problem p = {};
   if (group == -1) return GPTQ_ERR_SHAPE;                 // act-order always has real groups
   int rc = gptq::check_common(qweight, qzeros, scales, nullptr, K, N, bits, group, &p);
@@ -204,18 +210,31 @@ extern "C" int gptq_gemm_perm(const void* A, int M, int K, int a_dtype, const in
   if (fmt != GPTQ_FMT_V1 && fmt != GPTQ_FMT_V2) return GPTQ_ERR_ARG;
   if (a_dtype != GPTQ_F16 && a_dtype != GPTQ_BF16) return GPTQ_ERR_ARG;
   if (M < 0 || M > gptq::kDecodeMaxM) return GPTQ_ERR_SHAPE;
+  const size_t ws = gptq_gemm_perm_workspace_size(M, K);
+  if (workspace_bytes < ws) return GPTQ_ERR_WORKSPACE;
   if (M == 0) return GPTQ_OK;
-  if (!A || !C || !perm) return GPTQ_ERR_ARG;
+  if (!A || !C || !perm || (ws && !workspace)) return GPTQ_ERR_ARG;
   if (!gptq::aligned(A, 16) || !gptq::aligned(C, 16) || !gptq::aligned(perm, 16)) return GPTQ_ERR_ALIGN;
+  if (ws && !gptq::aligned(workspace, 16)) return GPTQ_ERR_ALIGN;
   rc = gptq::device_ready(&p);
   if (rc) return rc;
-  p.A = A;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
   p.M = M;
   p.dtype = a_dtype;
-  p.perm = perm;
   p.zero_offset = fmt == GPTQ_FMT_V1 ? 1 : 0;
   p.out = C;
-  return gptq::from_cuda(gptq::launch_decode(p, static_cast<cudaStream_t>(stream)));
+  if (ws) {
+    // several tokens: gather A[:, perm] once into the workspace, then a plain decode GEMM
+    cudaError_t e = gptq::launch_gather_cols(A, perm, M, K, workspace, s);
+    if (e != cudaSuccess) return gptq::from_cuda(e);
+    p.A = workspace;
+    p.perm = nullptr;
+  } else {
+    // one token: each CTA gathers its own k range while staging (no workspace)
+    p.A = A;
+    p.perm = perm;
+  }
+  return gptq::from_cuda(gptq::launch_decode(p, s));
 }
 
 extern "C" int gptq_prepack_act_order(const int32_t* qweight, const int32_t* g_idx, int K, int N,

@@ -281,8 +281,9 @@ struct DiffPairs<__half, 8> {
 // Raw codes as 16-bit floats, zero not subtracted (decode kernels).
 //
 // CodePairs<T, BITS> is DiffPairs without the per-pair sub/fma: pair p of a word holds
-// kMagic + 2^shift(p) * q for the codes lo_k(p), hi_k(p) (the DiffPairs pairing), i.e. only the
-// masks (plus one shared shift).  With the matching activation pair scaled by 2^-shift(p),
+// kMagic + 2^shift_lo(p) * q (low half) and kMagic + 2^shift_hi(p) * q (high half) for the codes
+// lo_k(p), hi_k(p) (2/4/8-bit: the DiffPairs pairing), i.e. only masks (plus shared shifts).
+// With the matching activation halves scaled by 2^-shift,
 //   sum_k b_k (kMagic + 2^shift q_k) = kMagic * sum_k b_k + sum_k (2^shift b_k) q_k,
 // so sum_k (2^shift b_k)(q_k - z) is the MMA result minus kMagic * sum_k b_k and minus
 // z * sum_k 2^shift b_k -- two sums per quantization group and token.
@@ -294,7 +295,8 @@ template <>
 struct CodePairs<__half, 4> {
   static constexpr int kPairs = 4;
   static constexpr float kMagic = 1024.0f;
-  __host__ __device__ static constexpr int shift(int p) { return (p & 1) ? 4 : 0; }
+  __host__ __device__ static constexpr int shift_lo(int p) { return (p & 1) ? 4 : 0; }
+  __host__ __device__ static constexpr int shift_hi(int p) { return shift_lo(p); }
   __device__ static __forceinline__ void run(uint32_t w, uint32_t (&d)[kPairs]) {
     const uint32_t M2 = 0x64006400u, w8 = w >> 8;
     d[0] = lop3_and_or(w, 0x000F000Fu, M2);
@@ -308,7 +310,8 @@ template <>
 struct CodePairs<__nv_bfloat16, 4> {
   static constexpr int kPairs = 4;
   static constexpr float kMagic = 128.0f;
-  __host__ __device__ static constexpr int shift(int) { return 0; }
+  __host__ __device__ static constexpr int shift_lo(int) { return 0; }
+  __host__ __device__ static constexpr int shift_hi(int) { return 0; }
   __device__ static __forceinline__ void run(uint32_t w, uint32_t (&d)[kPairs]) {
     const uint32_t M2 = 0x43004300u;
     d[0] = lop3_and_or(w, 0x000F000Fu, M2);
@@ -322,7 +325,8 @@ template <>
 struct CodePairs<__half, 2> {
   static constexpr int kPairs = 8;
   static constexpr float kMagic = 1024.0f;
-  __host__ __device__ static constexpr int shift(int p) { return 2 * (p & 3); }
+  __host__ __device__ static constexpr int shift_lo(int p) { return 2 * (p & 3); }
+  __host__ __device__ static constexpr int shift_hi(int p) { return shift_lo(p); }
   __device__ static __forceinline__ void run(uint32_t w, uint32_t (&d)[kPairs]) {
     const uint32_t M2 = 0x64006400u;
 #pragma unroll
@@ -340,7 +344,8 @@ template <>
 struct CodePairs<__nv_bfloat16, 2> {
   static constexpr int kPairs = 8;
   static constexpr float kMagic = 128.0f;
-  __host__ __device__ static constexpr int shift(int p) { return (p & 3) == 3 ? 0 : 2 * (p & 3); }
+  __host__ __device__ static constexpr int shift_lo(int p) { return (p & 3) == 3 ? 0 : 2 * (p & 3); }
+  __host__ __device__ static constexpr int shift_hi(int p) { return shift_lo(p); }
   __device__ static __forceinline__ void run(uint32_t w, uint32_t (&d)[kPairs]) {
     const uint32_t M2 = 0x43004300u;
 #pragma unroll
@@ -358,25 +363,69 @@ template <>
 struct CodePairs<__half, 8> {
   static constexpr int kPairs = 2;
   static constexpr float kMagic = 1024.0f;
-  __host__ __device__ static constexpr int shift(int) { return 0; }
+  __host__ __device__ static constexpr int shift_lo(int) { return 0; }
+  __host__ __device__ static constexpr int shift_hi(int) { return 0; }
   __device__ static __forceinline__ void run(uint32_t w, uint32_t (&d)[kPairs]) {
     d[0] = __byte_perm(w, 0x64646464u, 0x4240u);
     d[1] = __byte_perm(w, 0x64646464u, 0x4341u);
   }
 };
 
-// A 16-bit pair times 2^-s (exact unless the result is subnormal, where it rounds).
-__device__ __forceinline__ uint32_t scale_pow2(uint32_t v, int s, __half) {
-  if (s == 0) return v;
-  const uint16_t f = static_cast<uint16_t>((15 - s) << 10);
-  __half2 r = __hmul2(*reinterpret_cast<__half2*>(&v), __halves2half2(__ushort_as_half(f), __ushort_as_half(f)));
+// 3-bit, fp16: a unit is 32 codes in a 96-bit LSB-first stream of 3 words (code j at bit 3j).
+// A pair can be read by one mask when its two codes sit at bits [p, p+3) and [16+p', 16+p'+3)
+// (p, p' <= 7: inside the fp16 mantissa) of one 32-bit window of the stream, i.e. a window
+// starting at bit s with p = 3 lo - s and p' = 3 hi - s - 16.  This pairing of the 32 codes
+// uses 9 windows: the 3 words themselves and 6 shifts (s = 4, 10, 35, 38, 58, 70).
+__host__ __device__ constexpr int code3_pair(int p, int which) {   // which: 0 lo, 1 hi, 2 window
+  constexpr int t[16][3] = {{0, 6, 0},    {1, 7, 0},    {2, 9, 4},    {3, 8, 4},
+                            {4, 11, 10},  {5, 10, 10},  {12, 16, 32}, {13, 17, 32},
+                            {14, 18, 35}, {15, 19, 38}, {20, 27, 58}, {21, 26, 58},
+                            {22, 28, 64}, {23, 29, 64}, {24, 31, 70}, {25, 30, 70}};
+  return t[p][which];
+}
+
+template <>
+struct CodePairs<__half, 3> {
+  static constexpr int kPairs = 16;
+  static constexpr float kMagic = 1024.0f;
+  __host__ __device__ static constexpr int lo_k(int p) { return code3_pair(p, 0); }
+  __host__ __device__ static constexpr int hi_k(int p) { return code3_pair(p, 1); }
+  __host__ __device__ static constexpr int shift_lo(int p) { return 3 * lo_k(p) - code3_pair(p, 2); }
+  __host__ __device__ static constexpr int shift_hi(int p) { return 3 * hi_k(p) - code3_pair(p, 2) - 16; }
+  __device__ static __forceinline__ void run3(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t (&d)[kPairs]) {
+    const uint32_t x[9] = {w0,
+                           w0 >> 4,
+                           __funnelshift_r(w0, w1, 10),
+                           w1,
+                           w1 >> 3,
+                           w1 >> 6,
+                           __funnelshift_r(w1, w2, 26),
+                           w2,
+                           w2 >> 6};
+#pragma unroll
+    for (int p = 0; p < kPairs; ++p) {
+      const int s = code3_pair(p, 2);
+      const int xi = s == 0 ? 0 : s == 4 ? 1 : s == 10 ? 2 : s == 32 ? 3 : s == 35 ? 4
+                   : s == 38 ? 5 : s == 58 ? 6 : s == 64 ? 7 : 8;
+      const uint32_t mask = (7u << shift_lo(p)) | (7u << (16 + shift_hi(p)));
+      d[p] = lop3_and_or(x[xi], mask, 0x64006400u);
+    }
+  }
+};
+
+// A 16-bit pair times (2^-slo, 2^-shi) (exact unless a result is subnormal, where it rounds).
+__device__ __forceinline__ uint32_t scale_pow2_pair(uint32_t v, int slo, int shi, __half) {
+  if (slo == 0 && shi == 0) return v;
+  const __half2 f = __halves2half2(__ushort_as_half(static_cast<uint16_t>((15 - slo) << 10)),
+                                   __ushort_as_half(static_cast<uint16_t>((15 - shi) << 10)));
+  __half2 r = __hmul2(*reinterpret_cast<__half2*>(&v), f);
   return *reinterpret_cast<uint32_t*>(&r);
 }
-__device__ __forceinline__ uint32_t scale_pow2(uint32_t v, int s, __nv_bfloat16) {
-  if (s == 0) return v;
-  const uint16_t f = static_cast<uint16_t>((127 - s) << 7);
-  __nv_bfloat162 r = __hmul2(*reinterpret_cast<__nv_bfloat162*>(&v),
-                             __halves2bfloat162(__ushort_as_bfloat16(f), __ushort_as_bfloat16(f)));
+__device__ __forceinline__ uint32_t scale_pow2_pair(uint32_t v, int slo, int shi, __nv_bfloat16) {
+  if (slo == 0 && shi == 0) return v;
+  const __nv_bfloat162 f = __halves2bfloat162(__ushort_as_bfloat16(static_cast<uint16_t>((127 - slo) << 7)),
+                                              __ushort_as_bfloat16(static_cast<uint16_t>((127 - shi) << 7)));
+  __nv_bfloat162 r = __hmul2(*reinterpret_cast<__nv_bfloat162*>(&v), f);
   return *reinterpret_cast<uint32_t*>(&r);
 }
 

@@ -38,6 +38,8 @@ const DeviceInfo& device_info();   // current device, cached
 cudaError_t launch_dequant(const Problem& p, cudaStream_t stream);
 cudaError_t launch_decode(const Problem& p, cudaStream_t stream);
 cudaError_t launch_prefill(const Problem& p, cudaStream_t stream);
+cudaError_t launch_gather_cols(const void* A, const int32_t* perm, int M, int K, void* out,
+                               cudaStream_t stream);
 cudaError_t launch_wait_selftest(unsigned* status, uint64_t limit_ns, int* flag, cudaStream_t stream);
 
 struct QuantProblem {

@@ -122,15 +122,22 @@ int gptq_prepack_act_order(const int32_t* qweight, const int32_t* g_idx, int K, 
  * gptq_gemm_perm -- C[M, N] = A[:, perm] @ W[K, N] for a checkpoint prepacked by
  * gptq_prepack_act_order (W = its qweight_out, contiguous groups of `group` rows), i.e. the
  * act-order GEMM of page section "调整细节：根据格式选择处理方式" without a per-row group
- * lookup.  The decode kernel gathers A's columns through perm while staging them.  Tokens:
- * 0 <= M <= 32 (larger M: GPTQ_ERR_SHAPE; gptq_gemm with g_idx serves that range).
+ * lookup.  One token: the decode kernel gathers A's columns through perm while staging them.
+ * Several tokens: A[:, perm] is first gathered once into `workspace` (a device buffer of at least
+ * gptq_gemm_perm_workspace_size(M, K) bytes, 16-byte aligned, owned by the caller; it is
+ * overwritten), then the decode kernel reads it.  Tokens: 0 <= M <= 32 (larger M:
+ * GPTQ_ERR_SHAPE; gptq_gemm with g_idx serves that range).
  * Device pointers: A [M, K], perm [K] int32 (16-byte aligned; an entry outside [0, K) is
- * clamped, never read past A), qweight, qzeros, scales, C.
- * Returns GPTQ_OK or a negative gptq_status.
+ * clamped, never read past A), qweight, qzeros, scales, C, workspace.
+ * Returns GPTQ_OK or a negative gptq_status (GPTQ_ERR_WORKSPACE if the workspace is too small).
  */
 int gptq_gemm_perm(const void* A, int M, int K, int a_dtype, const int32_t* perm,
                    const int32_t* qweight, const int32_t* qzeros, const void* scales, int N,
-                   int bits, int group, int fmt, void* C, void* stream);
+                   int bits, int group, int fmt, void* C, void* workspace,
+                   size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace gptq_gemm_perm needs: M * K * 2 rounded up to 256 for M > 1, else 0. */
+size_t gptq_gemm_perm_workspace_size(int M, int K);
 
 /* Bytes of device workspace gptq_gemm needs for this problem (0 for every current path). */
 size_t gptq_gemm_workspace_size(int M, int K, int N, int bits, int group);

@@ -23,7 +23,7 @@ def test_exports_every_declared_symbol(lib):
                                "gptq_repack_zeros_v1_to_v2", "gptq_quantize_rtn",
                                "gptq_get_device_status", "gptq_strerror",
                                "gptq_selftest_wait_timeout", "gptq_prepack_act_order",
-                               "gptq_gemm_perm"])
+                               "gptq_gemm_perm", "gptq_gemm_perm_workspace_size"])
     for name in declared:
         assert hasattr(lib, name), name
 
@@ -149,14 +149,24 @@ def test_prepack_act_order_validation(lib):
 @pytest.mark.parametrize("kw,code", [
     (dict(M=33), -2), (dict(M=-1), -2), (dict(group=-1), -2), (dict(perm=None), -1),
     (dict(perm=P(0x10004)), -3), (dict(bits=5), -1), (dict(K=48), -2),
+    (dict(M=4), -4), (dict(M=4, ws=FAKE, ws_bytes=4 * 256 * 2 - 1), -4),
+    (dict(M=4, ws=P(0x10008), ws_bytes=4 * 256 * 2), -3),
 ])
 def test_gemm_perm_validation_without_gpu(lib, kw, code):
     a = dict(A=FAKE, M=1, K=256, dtype=0, perm=FAKE, qweight=FAKE, qzeros=FAKE, scales=FAKE,
-             N=256, bits=4, group=128, fmt=2, C=FAKE)
+             N=256, bits=4, group=128, fmt=2, C=FAKE, ws=None, ws_bytes=0)
     a.update(kw)
     rc = lib.gptq_gemm_perm(a["A"], a["M"], a["K"], a["dtype"], a["perm"], a["qweight"], a["qzeros"],
-                            a["scales"], a["N"], a["bits"], a["group"], a["fmt"], a["C"], None)
+                            a["scales"], a["N"], a["bits"], a["group"], a["fmt"], a["C"], a["ws"],
+                            a["ws_bytes"], None)
     assert rc == code
+
+
+def test_gemm_perm_workspace_size(lib):
+    assert g.gemm_perm_workspace_size(1, 4096) == 0
+    assert g.gemm_perm_workspace_size(0, 4096) == 0
+    assert g.gemm_perm_workspace_size(16, 5120) == 16 * 5120 * 2
+    assert g.gemm_perm_workspace_size(3, 96) == 768        # 576 rounded up to 256
 
 
 def test_product_does_not_import_oracle():
