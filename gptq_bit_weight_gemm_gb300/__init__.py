@@ -62,6 +62,7 @@ _SIGNATURES = {
     "gptq_prepack_act_order": (_I, [_P, _P, _I, _I, _I, _I, _P, _P]),
     "gptq_gemm_perm": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P]),
     "gptq_gemm_perm_workspace_size": (_SZ, [_I, _I]),
+    "gptq_gemm_perm_noalloc": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
 }
 
 

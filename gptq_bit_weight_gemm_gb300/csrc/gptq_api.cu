@@ -237,6 +237,74 @@ extern "C" int gptq_gemm_perm(const void* A, int M, int K, int a_dtype, const in
   return gptq::from_cuda(gptq::launch_decode(p, s));
 }
 
+// ---------------------------------------------------------------------------------------------
+// Allocation-free variant of gptq_gemm_perm.  Its only scratch (the gathered activations
+// A[:, perm] for M > 1) is this file-scope device array; its device address is looked up once
+// per device, with that device current, and handed to the gather kernel.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = static_cast<size_t>(1) << 20;   // 1 MiB per device
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+struct ScratchState {
+  std::once_flag once;
+  void* ptr = nullptr;
+  cudaError_t err = cudaSuccess;
+};
+ScratchState g_noalloc_state[gptq::kMaxDevices];
+
+// Device address of g_noalloc_scratch on the current device (set up on first use), or nullptr.
+void* noalloc_scratch() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= gptq::kMaxDevices) return nullptr;
+  ScratchState& st = g_noalloc_state[dev];
+  std::call_once(st.once, [&st]() {
+    void* ptr = nullptr;
+    st.err = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    st.ptr = st.err == cudaSuccess ? ptr : nullptr;
+  });
+  return st.ptr;
+}
+
+}  // namespace
+
+extern "C" int gptq_gemm_perm_noalloc(const void* A, int M, int K, int a_dtype, const int32_t* perm,
+                                      const int32_t* qweight, const int32_t* qzeros,
+                                      const void* scales, int N, int bits, int group, int fmt,
+                                      void* C, void* stream) {
+  Problem p = {};
+  if (group == -1) return GPTQ_ERR_SHAPE;
+  int rc = gptq::check_common(qweight, qzeros, scales, nullptr, K, N, bits, group, &p);
+  if (rc) return rc;
+  if (fmt != GPTQ_FMT_V1 && fmt != GPTQ_FMT_V2) return GPTQ_ERR_ARG;
+  if (a_dtype != GPTQ_F16 && a_dtype != GPTQ_BF16) return GPTQ_ERR_ARG;
+  if (M < 0 || M > gptq::kDecodeMaxM) return GPTQ_ERR_SHAPE;
+  const size_t need = gptq_gemm_perm_workspace_size(M, K);
+  if (need > kNoAllocScratchBytes) return GPTQ_ERR_WORKSPACE;   // beyond the built-in scratch
+  if (M == 0) return GPTQ_OK;
+  if (!A || !C || !perm) return GPTQ_ERR_ARG;
+  if (!gptq::aligned(A, 16) || !gptq::aligned(C, 16) || !gptq::aligned(perm, 16)) return GPTQ_ERR_ALIGN;
+  rc = gptq::device_ready(&p);
+  if (rc) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  p.M = M;
+  p.dtype = a_dtype;
+  p.zero_offset = fmt == GPTQ_FMT_V1 ? 1 : 0;
+  p.out = C;
+  if (need) {
+    void* scratch = noalloc_scratch();
+    if (!scratch) return GPTQ_ERR_CUDA;
+    cudaError_t e = gptq::launch_gather_cols(A, perm, M, K, scratch, s);
+    if (e != cudaSuccess) return gptq::from_cuda(e);
+    p.A = scratch;
+    p.perm = nullptr;
+  } else {
+    p.A = A;
+    p.perm = perm;
+  }
+  return gptq::from_cuda(gptq::launch_decode(p, s));
+}
+
 extern "C" int gptq_prepack_act_order(const int32_t* qweight, const int32_t* g_idx, int K, int N,
                                       int bits, int group, int32_t* qweight_out, int32_t* perm) {
   if (!gptq::bits_ok(bits) || !qweight || !g_idx || !qweight_out || !perm) return GPTQ_ERR_ARG;

@@ -139,6 +139,24 @@ int gptq_gemm_perm(const void* A, int M, int K, int a_dtype, const int32_t* perm
 /* Bytes of workspace gptq_gemm_perm needs: M * K * 2 rounded up to 256 for M > 1, else 0. */
 size_t gptq_gemm_perm_workspace_size(int M, int K);
 
+/*
+ * gptq_gemm_perm_noalloc -- gptq_gemm_perm for callers that cannot allocate device memory: a
+ * serving runtime or framework plug-in whose allocator has reserved the GPU's memory up front
+ * and forbids further allocations, or code for which the synchronisation of cudaMalloc is not
+ * allowed.  Same arguments and result as gptq_gemm_perm, without the workspace: the gathered
+ * activations live in a static device buffer of 1 MiB that every GPU loading this library holds
+ * until the process exits.  Limit: M * K * 2 bytes <= 1 MiB (e.g. M = 32 with K <= 16384);
+ * larger problems return GPTQ_ERR_WORKSPACE.  The call allocates nothing (no cudaMalloc or
+ * cudaFree, no allocating library routine).  The first call on a device looks up the buffer's
+ * device address there (cudaGetSymbolAddress); make that first call before any stream capture.
+ * All calls share the buffer and leave their contents in it (each call writes every element it
+ * later reads): calls that overlap on the GPU, on any streams, race.  The pages have no
+ * counterpart for this entry point.
+ */
+int gptq_gemm_perm_noalloc(const void* A, int M, int K, int a_dtype, const int32_t* perm,
+                           const int32_t* qweight, const int32_t* qzeros, const void* scales,
+                           int N, int bits, int group, int fmt, void* C, void* stream);
+
 /* Bytes of device workspace gptq_gemm needs for this problem (0 for every current path). */
 size_t gptq_gemm_workspace_size(int M, int K, int N, int bits, int group);
 

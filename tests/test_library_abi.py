@@ -23,7 +23,8 @@ def test_exports_every_declared_symbol(lib):
                                "gptq_repack_zeros_v1_to_v2", "gptq_quantize_rtn",
                                "gptq_get_device_status", "gptq_strerror",
                                "gptq_selftest_wait_timeout", "gptq_prepack_act_order",
-                               "gptq_gemm_perm", "gptq_gemm_perm_workspace_size"])
+                               "gptq_gemm_perm", "gptq_gemm_perm_workspace_size",
+                               "gptq_gemm_perm_noalloc"])
     for name in declared:
         assert hasattr(lib, name), name
 
