@@ -172,13 +172,15 @@ __device__ __forceinline__ void stage_pairs(const uint16_t* A, const int32_t* pe
   }
 }
 
-// Cluster size: enough warps to fill the GPU (about 24 per SM), at least two units per warp.
+// Cluster size: enough warps to fill the GPU (about 24 per SM), at least one k-tile per warp
+// and CTA.  Up to 16 (a non-portable cluster size, opted into at launch) for narrow matrices;
+// the launcher may halve it again to keep the grid within one wave.
 inline int choose_cluster(const Problem& p, int per_unit) {
   const int slabs = (p.N + kSlab - 1) / kSlab;
   const int units = p.K / per_unit;
   const int target = device_info().sm_count * 24;
   int cs = 1;
-  while (cs < 8 && slabs * cs * kWarps < target && units >= 4 * cs * kWarps) cs *= 2;
+  while (cs < 16 && slabs * cs * kWarps < target && units >= 4 * cs * kWarps) cs *= 2;
   return cs;
 }
 

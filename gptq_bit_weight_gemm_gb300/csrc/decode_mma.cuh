@@ -772,7 +772,10 @@ cudaError_t launch_mma(const Problem& p, int cs, cudaStream_t stream) {
   auto geo_for = [&](int c) {
     return make_geo<BITS>(a.units, c, p.M, p.group, slabs * c, sms, max_per_sm, !FOLD, p.g_idx != nullptr, p.G);
   };
-  for (int c = cs; FOLD && c >= 1; c /= 2) {
+  // A 16-CTA cluster is used only when it gives one wave; otherwise (and for FULL) at most 8.
+  const int cs0 = cs;
+  cs = cs0 < 8 ? cs0 : 8;
+  for (int c = cs0; FOLD && c >= 1; c /= 2) {
     const size_t bytes = (TmaSmem<BITS>::bytes(geo_for(c), p.M) + 1023) & ~static_cast<size_t>(1023);
     if (bytes > 227 * 1024) break;
     int per_sm = static_cast<int>(233472 / (bytes + 1024));
@@ -810,6 +813,14 @@ cudaError_t launch_mma(const Problem& p, int cs, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
+  }
+  if (cs > 8) {                                 // 16-CTA clusters are a non-portable size
+    static std::atomic<unsigned long long> nonportable_set{0};
+    if (dev >= 64 || !(nonportable_set.load(std::memory_order_relaxed) & (1ull << dev))) {
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return e;
+      if (dev < 64) nonportable_set.fetch_or(1ull << dev, std::memory_order_relaxed);
+    }
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(cs, slabs, 1);

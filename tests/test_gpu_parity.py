@@ -130,6 +130,10 @@ SMALL = [
     (2, 64, False, "bf16", 32, 512, 288),
     (3, 128, True, "f16", 20, 640, 288),
     (8, 128, False, "bf16", 31, 384, 160),
+    # narrow and deep: 16-CTA clusters
+    (4, 128, False, "f16", 1, 4096, 256),
+    (2, 64, False, "bf16", 8, 4096, 640),
+    (3, 128, True, "f16", 4, 4096, 128),
 ]
 
 
