@@ -357,7 +357,7 @@ def time_workload(g, torch, dev, stream, wl, M, fmt, l2, reps=200, prepacked=Fal
         ws = torch.empty(max(1, g.gemm_perm_workspace_size(M, wl.K)), dtype=torch.uint8, device=dev)
     A = gptq_inputs.draw_activations(wl, M).to(dev)
     nbytes = algorithmic_bytes(wl, M)
-    S = max(1, min(32, int(np.ceil(3 * l2 / nbytes))))
+    S = max(1, min(256, int(np.ceil(3 * l2 / nbytes))))   # > 3x L2 of weights (the tiny case: L2)
     sets = [(qw.clone(), qz.clone(), sc.clone(), A.clone(),
              torch.empty((M, wl.N), dtype=A.dtype, device=dev)) for _ in range(S)]
     n = max(S, (reps // S) * S) if M <= 64 else S * max(1, 8 // S)

@@ -200,15 +200,18 @@ cudaError_t launch_mt(const Problem& p, cudaStream_t stream) {
   return launch_mma<BITS, MT, T, false>(p, cs, stream);
 }
 
-// Every M <= 32 runs the tensor-core decode kernel (token blocks of 8): even at one token,
+// Every M <= 32 runs the tensor-core decode kernel (token blocks of 8; one token has an
+// instantiation of its own, where the token count is a compile-time constant): even at one token,
 // handing the multiply-accumulate to the tensor core leaves the SM with only the unpack to issue.
 template <int BITS>
 cudaError_t launch_bits(const Problem& p, cudaStream_t stream) {
   if (p.dtype == 0) {
+    if (p.M == 1) return launch_mt<BITS, 1, __half>(p, stream);
     if (p.M <= 8) return launch_mt<BITS, 8, __half>(p, stream);
     if (p.M <= 16) return launch_mt<BITS, 16, __half>(p, stream);
     return launch_mt<BITS, 32, __half>(p, stream);
   }
+  if (p.M == 1) return launch_mt<BITS, 1, __nv_bfloat16>(p, stream);
   if (p.M <= 8) return launch_mt<BITS, 8, __nv_bfloat16>(p, stream);
   if (p.M <= 16) return launch_mt<BITS, 16, __nv_bfloat16>(p, stream);
   return launch_mt<BITS, 32, __nv_bfloat16>(p, stream);

@@ -144,7 +144,7 @@ struct TmaSmem {
   }
   // bytes past the 1024-aligned base, plus the worst-case alignment pad
   __host__ __device__ static size_t bytes(const TmaGeo& g, int M) {
-    return off_misc(g, M) + 8 * 16 + 4 * 17 + 1024;
+    return off_misc(g, M) + 8 * kWarps * g.nbuf + 4 * (kWarps * g.nbuf + 1) + 1024;
   }
 };
 
@@ -172,8 +172,9 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
   constexpr int PER = P::kPerUnit;
   constexpr int ROWS = P::kRowsPerUnit;
   constexpr int NP = MP::kPairs;
-  constexpr int NB = MT / 8;                          // token blocks of 8
-  const int UW = unit_words(a.M, NP);
+  constexpr int NB = (MT + 7) / 8;                    // token blocks of 8
+  const int Mtok = MT == 1 ? 1 : a.M;                 // tokens (a compile-time 1 for MT = 1)
+  const int UW = unit_words(Mtok, NP);
   extern __shared__ __align__(128) unsigned char smem_raw[];
 
   pdl_launch_dependents();
@@ -201,15 +202,20 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
   uint8_t* smem = smem_raw + ((1024u - (ptx::smem_addr(smem_raw) & 1023u)) & 1023u);
   uint8_t* sbuf = smem;                                               // weight chunks
   uint32_t* sB = reinterpret_cast<uint32_t*>(smem + SM::off_stage(geo));
-  float* recv = reinterpret_cast<float*>(smem + SM::off_recv(geo, a.M));
-  float2* sK = reinterpret_cast<float2*>(smem + SM::off_gconst(geo, a.M));   // [group][column]
-  float* sT = reinterpret_cast<float*>(smem + SM::off_sums(geo, a.M));       // [group][M]
-  float* sQ = sT + geo.max_groups * a.M;                                      // [group][M]
-  uint32_t* sSZ = reinterpret_cast<uint32_t*>(smem + SM::off_full(geo, a.M));  // [group][column]
+  float* recv = reinterpret_cast<float*>(smem + SM::off_recv(geo, Mtok));
+  float2* sK = reinterpret_cast<float2*>(smem + SM::off_gconst(geo, Mtok));   // [group][column]
+  float* sT = reinterpret_cast<float*>(smem + SM::off_sums(geo, Mtok));       // [group][M]
+  float* sQ = sT + geo.max_groups * Mtok;                                      // [group][M]
+  uint32_t* sSZ = reinterpret_cast<uint32_t*>(smem + SM::off_full(geo, Mtok));  // [group][column]
   uint16_t* sG = reinterpret_cast<uint16_t*>(sSZ + geo.full_groups * kSlab);    // [k of the range]
-  uint8_t* misc = smem + SM::off_misc(geo, a.M);
+  uint8_t* misc = smem + SM::off_misc(geo, Mtok);
   const uint32_t bar0 = ptx::smem_addr(misc);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 8 * 16);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 8 * kWarps * geo.nbuf);
+  // With refills (more chunks than buffers) and 2 to 8 tokens, warp w's box slot of buffer b
+  // arrives on its own mbarrier, so warps refill and stream independently; otherwise one mbarrier
+  // per chunk, refilled by the whole CTA at once (all 512 bytes of each row together, which
+  // measured faster for 16 and 32 tokens).
+  auto bar = [&](int w, int b) { return bar0 + 8u * static_cast<uint32_t>(w * geo.nbuf + b); };
 
   // Scales and zeros of the groups this range touches (FOLD): their loads go out first, ahead
   // of the weight stream (behind it they would wait for the whole slice), and land in shared
@@ -259,25 +265,57 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
   // The copies read weights only; they are issued before griddepcontrol.wait because global
   // memory (through L2) is coherent for them and the weights are not produced by the kernel
   // this one may overlap with.
+  const bool per_warp = MT == 8 && geo.nbuf < nchunk;
+  const int bw = per_warp ? warp : 0;                  // this warp's mbarrier row
   if (threadIdx.x == 0) {
-    for (int b = 0; b < geo.nbuf; ++b) ptx::mbar_init(bar0 + 8 * b, 1);
+    for (int w = 0; w < (per_warp ? kWarps : 1); ++w)
+      for (int b = 0; b < geo.nbuf; ++b) ptx::mbar_init(bar(w, b), 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
   __syncthreads();
-  volatile int* last_issued = abort_flag + 1;          // [nbuf] last chunk issued per buffer
-  auto issue = [&](int c) {
+  volatile int* last_issued = abort_flag + 1;          // [warp][nbuf] last chunk issued per buffer
+  // copy warp w's 32 columns of chunk c into buffer c % nbuf (its own slot and mbarrier)
+  auto issue_for = [&](int w, int c) {
+    const int b = c % geo.nbuf;
+    last_issued[w * geo.nbuf + b] = c;
+    const uint32_t dst = ptx::smem_addr(sbuf + static_cast<size_t>(b) * geo.chunk_bytes +
+                                        static_cast<size_t>(w) * geo.slot_bytes);
+    const int row0 = (cu0 + c * geo.chunk_tiles * 4) * ROWS;
+    ptx::mbar_arrive_expect_tx(bar(w, b), static_cast<uint32_t>(geo.chunk_rows * kBoxRowBytes));
+    ptx::tma_load_2d(dst, &tmW, n_base + w * kBoxCols, row0, bar(w, b));
+  };
+  // all four slots of chunk c on one mbarrier (single-barrier mode)
+  auto issue_chunk = [&](int c) {
     const int b = c % geo.nbuf;
     last_issued[b] = c;
-    const uint32_t dst = ptx::smem_addr(sbuf + static_cast<size_t>(b) * geo.chunk_bytes);
     const int row0 = (cu0 + c * geo.chunk_tiles * 4) * ROWS;
-    ptx::mbar_arrive_expect_tx(bar0 + 8 * b, static_cast<uint32_t>(4 * geo.chunk_rows * kBoxRowBytes));
-#pragma unroll
-    for (int w = 0; w < 4; ++w)
-      ptx::tma_load_2d(dst + w * geo.slot_bytes, &tmW, n_base + w * kBoxCols, row0, bar0 + 8 * b);
+    ptx::mbar_arrive_expect_tx(bar(0, b), static_cast<uint32_t>(kWarps * geo.chunk_rows * kBoxRowBytes));
+    for (int w = 0; w < kWarps; ++w)
+      ptx::tma_load_2d(ptx::smem_addr(sbuf + static_cast<size_t>(b) * geo.chunk_bytes +
+                                      static_cast<size_t>(w) * geo.slot_bytes),
+                       &tmW, n_base + w * kBoxCols, row0, bar(0, b));
   };
-  if (threadIdx.x == 0)
-    for (int c = 0; c < nchunk && c < geo.nbuf; ++c) issue(c);
+  // refill after chunk c_next - nbuf was consumed: per warp (its slot) or by the whole CTA
+  // (per_warp is uniform over the CTA, and so is the loop's chunk sequence)
+  auto refill = [&](int c_next) {
+    if (per_warp) {
+      __syncwarp();
+      if (lane == 0 && !*abort_flag) { ptx::fence_proxy_async_smem(); issue_for(warp, c_next); }
+    } else {
+      __syncthreads();
+      if (threadIdx.x == 0 && !*abort_flag) { ptx::fence_proxy_async_smem(); issue_chunk(c_next); }
+    }
+  };
+  if (threadIdx.x == 0) {                                // the first chunks in one burst
+    for (int c = 0; c < nchunk && c < geo.nbuf; ++c) {
+      if (per_warp) {
+        for (int w = 0; w < kWarps; ++w) issue_for(w, c);
+      } else {
+        issue_chunk(c);
+      }
+    }
+  }
 
   if constexpr (FOLD) {
     group_stores(0);
@@ -319,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
   // (FOLD: times 2^-shift(p), matching the raw codes of CodePairs).
   const uint16_t* A16 = static_cast<const uint16_t*>(a.A);
   const int nunits = ntile * 4;
-  stage_pairs<PER, NP>(A16, a.perm, a.M, a.K, cu0, nunits, a.units,
+  stage_pairs<PER, NP>(A16, a.perm, Mtok, a.K, cu0, nunits, a.units,
                        [](int p) { return MP::lo_k(p); }, [](int p) { return MP::hi_k(p); },
                        [&](int uu, int m, int p, uint32_t v) {
                          if constexpr (FOLD)
@@ -333,14 +371,14 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
     // the lanes of a token split its pairs and meet in a fixed shuffle order (deterministic).
     using CP = CodePairs<T, BITS>;
     const int upg = a.group / PER;
-    const int lps = a.M <= 1 ? 5 : a.M <= 2 ? 4 : a.M <= 4 ? 3 : a.M <= 8 ? 2 : a.M <= 16 ? 1 : 0;
+    const int lps = Mtok <= 1 ? 5 : Mtok <= 2 ? 4 : Mtok <= 4 ? 3 : Mtok <= 8 ? 2 : Mtok <= 16 ? 1 : 0;
     const int m = lane >> lps, sub = lane & ((1 << lps) - 1);
     for (int gi = warp; gi < ngrp; gi += kWarps) {
       int u_lo = (g_lo + gi) * upg - cu0, u_hi = u_lo + upg;
       u_lo = u_lo < 0 ? 0 : u_lo;
       u_hi = u_hi > nunits ? nunits : u_hi;
       float t = 0.f, q = 0.f;
-      if (m < a.M) {
+      if (m < Mtok) {
         for (int uu = u_lo + sub; uu < u_hi; uu += (1 << lps)) {
           uint32_t v[NP];
           const uint32_t* src = sB + uu * UW + m * NP;
@@ -367,9 +405,9 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
         t += __shfl_xor_sync(0xFFFFFFFFu, t, o);
         q += __shfl_xor_sync(0xFFFFFFFFu, q, o);
       }
-      if (sub == 0 && m < a.M) {
-        sT[gi * a.M + m] = CP::kMagic * t;
-        sQ[gi * a.M + m] = q;
+      if (sub == 0 && m < Mtok) {
+        sT[gi * Mtok + m] = CP::kMagic * t;
+        sQ[gi * Mtok + m] = q;
       }
     }
     __syncthreads();
@@ -387,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
   auto load_b = [&](int kt, uint32_t (&bf)[NB][NP]) {
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) {
-      if (8 * nb + gq >= a.M) {                         // absent token: zero B column
+      if (8 * nb + gq >= Mtok) {                         // absent token: zero B column
 #pragma unroll
         for (int i = 0; i < NP; ++i) bf[nb][i] = 0u;
         continue;
@@ -437,8 +475,8 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           int m = nb * 8 + 2 * tq + h;
-          m = m < a.M ? m : a.M - 1;
-          const float mt = sT[gi * a.M + m], q = sQ[gi * a.M + m];
+          m = m < Mtok ? m : Mtok - 1;
+          const float mt = sT[gi * Mtok + m], q = sQ[gi * Mtok + m];
 #pragma unroll
           for (int t = 0; t < 2; ++t)
 #pragma unroll
@@ -452,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) {
       const int m = 8 * nb + gq;
-      boff[nb] = (m < a.M ? m : a.M - 1) * NP + tq * UW;
+      boff[nb] = (m < Mtok ? m : Mtok - 1) * NP + tq * UW;
     }
     // 3-bit: unit tq of local tile l is rows 3 (4 l + tq) .. +2 of the chunk; pairs per column
     auto tile3 = [&](const uint8_t* cslot, int l, int kt) {
@@ -525,12 +563,9 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
     clear_cg();
     for (int kt = 0; kt < ntile;) {                    // control flow is uniform over the CTA
       if (kt == chunk_end) {
-        if (c >= 0 && c + geo.nbuf < nchunk) {         // refill the buffer just consumed
-          __syncthreads();
-          if (threadIdx.x == 0 && !*abort_flag) { ptx::fence_proxy_async_smem(); issue(c + geo.nbuf); }
-        }
+        if (c >= 0 && c + geo.nbuf < nchunk) refill(c + geo.nbuf);   // the buffer just consumed
         ++c;
-        ok = tma_wait(bar0 + 8 * (c % geo.nbuf), (c / geo.nbuf) & 1, abort_flag, a.status);
+        ok = __all_sync(0xFFFFFFFFu, tma_wait(bar(bw, c % geo.nbuf), (c / geo.nbuf) & 1, abort_flag, a.status));
         cslot = wslot + static_cast<size_t>(c % geo.nbuf) * geo.chunk_bytes;
         const uint8_t* cb = cslot + tq * kBoxRowBytes;
         we = cb + ((quad ^ tq) << 4);
@@ -567,7 +602,7 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
     if (dirty) fold(gi);
   } else {
     for (int c = 0; c < nchunk; ++c) {
-      const bool ok = tma_wait(bar0 + 8 * (c % geo.nbuf), (c / geo.nbuf) & 1, abort_flag, a.status);
+      const bool ok = __all_sync(0xFFFFFFFFu, tma_wait(bar(bw, c % geo.nbuf), (c / geo.nbuf) & 1, abort_flag, a.status));
       const uint8_t* cb = wslot + static_cast<size_t>(c % geo.nbuf) * geo.chunk_bytes;
       const int kt0 = c * geo.chunk_tiles;
       const int kt_end = kt0 + geo.chunk_tiles < ntile ? kt0 + geo.chunk_tiles : ntile;
@@ -628,10 +663,7 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
               mma16816(acc[t][nb], w[2 * t][2 * j], w[2 * t + 1][2 * j], w[2 * t][2 * j + 1],
                        w[2 * t + 1][2 * j + 1], bf[nb][2 * j], bf[nb][2 * j + 1], T());
       }
-      if (c + geo.nbuf < nchunk) {
-        __syncthreads();
-        if (threadIdx.x == 0 && !*abort_flag) { ptx::fence_proxy_async_smem(); issue(c + geo.nbuf); }
-      }
+      if (c + geo.nbuf < nchunk) refill(c + geo.nbuf);   // the buffer just consumed
     }
   }
 
@@ -640,7 +672,7 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
   float* part = reinterpret_cast<float*>(sB);           // [M][kSlab], aliases the staging
   // recv ([cs][M][kSlab / cs]) has a region of its own: peers may push into it while this CTA
   // is still reading its staged activations.
-  const int Mr = a.M;
+  const int Mr = Mtok;
 #pragma unroll
   for (int t = 0; t < 2; ++t)
 #pragma unroll
@@ -677,12 +709,13 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
       C[static_cast<long long>(m) * a.N + n] = F16Traits<T>::from_f32(v);
     }
   }
-  if (*abort_flag && threadIdx.x == 0) {
-    // after a timeout, let every copy already issued land before shared memory is released
+  if (*abort_flag && lane == 0 && (per_warp || warp == 0)) {
+    // after a timeout, let every copy issued on this warp's mbarriers land before shared memory
+    // is released
     const uint64_t t0 = ptx::globaltimer();
     for (int b = 0; b < nchunk && b < geo.nbuf; ++b) {
-      const int last = last_issued[b];
-      while (!ptx::mbar_try_wait(bar0 + 8 * b, (last / geo.nbuf) & 1) &&
+      const int last = last_issued[bw * geo.nbuf + b];
+      while (!ptx::mbar_try_wait(bar(bw, b), (last / geo.nbuf) & 1) &&
              ptx::globaltimer() - t0 < 2000000000ull) {}
     }
   }
@@ -727,7 +760,9 @@ TmaGeo make_geo(int units, int cs, int M, int group, int ctas, int sm_count, int
     // an SM holds 228 KB; each CTA takes its size rounded up to 1 KB plus 1 KB reserved
     const long long cap = (static_cast<long long>(233472 / per_sm) - 1024) & ~1023LL;
     const long long budget = cap - static_cast<long long>(fixed);
-    int fit = budget > 0 ? static_cast<int>(budget / g.chunk_bytes) : 0;
+    // each buffer also takes an mbarrier and a bookkeeping word per warp
+    const long long per_buf = g.chunk_bytes + kWarps * (8 + 4);
+    int fit = budget > 0 ? static_cast<int>(budget / per_buf) : 0;
     if (fit > 16) fit = 16;
     g.nbuf = chunks < fit ? chunks : fit;
     return chunks;
