@@ -184,10 +184,12 @@ inline int choose_cluster(const Problem& p, int per_unit) {
   return cs;
 }
 
-template <int BITS, int MT, typename T, bool FOLD>
+template <int BITS, int MT, int MX, typename T, bool FOLD>
 cudaError_t launch_mma(const Problem& p, int cs, cudaStream_t stream);
 
-template <int BITS, int MT, typename T>
+// MT: token block bound (1, 8, 16, 32); MX: the exact token count when it is MT (0 = read at run
+// time), so the common batch sizes run with every token loop sized at compile time.
+template <int BITS, int MT, int MX, typename T>
 cudaError_t launch_mt(const Problem& p, cudaStream_t stream) {
   const int cs = choose_cluster(p, Pack<BITS>::kPerUnit);
   constexpr bool kHas16 = (BITS == 2 || BITS == 4 ||
@@ -195,26 +197,32 @@ cudaError_t launch_mt(const Problem& p, cudaStream_t stream) {
   // the scale folds per group when groups align with k-tiles (4 units)
   const bool fold = kHas16 && p.g_idx == nullptr && (p.group % (4 * Pack<BITS>::kPerUnit)) == 0;
   if constexpr (kHas16) {
-    if (fold) return launch_mma<BITS, MT, T, true>(p, cs, stream);
+    if (fold) return launch_mma<BITS, MT, MX, T, true>(p, cs, stream);
   }
-  return launch_mma<BITS, MT, T, false>(p, cs, stream);
+  return launch_mma<BITS, MT, MX, T, false>(p, cs, stream);
 }
 
 // Every M <= 32 runs the tensor-core decode kernel (token blocks of 8; one token has an
 // instantiation of its own, where the token count is a compile-time constant): even at one token,
 // handing the multiply-accumulate to the tensor core leaves the SM with only the unpack to issue.
+template <int BITS, typename T>
+cudaError_t launch_tokens(const Problem& p, cudaStream_t stream) {
+  switch (p.M) {
+    case 1: return launch_mt<BITS, 1, 1, T>(p, stream);
+    case 8: return launch_mt<BITS, 8, 8, T>(p, stream);
+    case 16: return launch_mt<BITS, 16, 16, T>(p, stream);
+    case 32: return launch_mt<BITS, 32, 32, T>(p, stream);
+    default: break;
+  }
+  if (p.M <= 8) return launch_mt<BITS, 8, 0, T>(p, stream);
+  if (p.M <= 16) return launch_mt<BITS, 16, 0, T>(p, stream);
+  return launch_mt<BITS, 32, 0, T>(p, stream);
+}
+
 template <int BITS>
 cudaError_t launch_bits(const Problem& p, cudaStream_t stream) {
-  if (p.dtype == 0) {
-    if (p.M == 1) return launch_mt<BITS, 1, __half>(p, stream);
-    if (p.M <= 8) return launch_mt<BITS, 8, __half>(p, stream);
-    if (p.M <= 16) return launch_mt<BITS, 16, __half>(p, stream);
-    return launch_mt<BITS, 32, __half>(p, stream);
-  }
-  if (p.M == 1) return launch_mt<BITS, 1, __nv_bfloat16>(p, stream);
-  if (p.M <= 8) return launch_mt<BITS, 8, __nv_bfloat16>(p, stream);
-  if (p.M <= 16) return launch_mt<BITS, 16, __nv_bfloat16>(p, stream);
-  return launch_mt<BITS, 32, __nv_bfloat16>(p, stream);
+  if (p.dtype == 0) return launch_tokens<BITS, __half>(p, stream);
+  return launch_tokens<BITS, __nv_bfloat16>(p, stream);
 }
 
 }  // namespace decode

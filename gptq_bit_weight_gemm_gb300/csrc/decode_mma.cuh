@@ -163,7 +163,7 @@ __device__ __forceinline__ bool tma_wait(uint32_t bar, uint32_t parity, volatile
   }
 }
 
-template <int BITS, int MT, typename T, bool FOLD>
+template <int BITS, int MT, int MX, typename T, bool FOLD>
 __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
     k_decode_mma(const __grid_constant__ CUtensorMap tmW, const Args a, const TmaGeo geo) {
   using P = Pack<BITS>;
@@ -173,7 +173,7 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
   constexpr int ROWS = P::kRowsPerUnit;
   constexpr int NP = MP::kPairs;
   constexpr int NB = (MT + 7) / 8;                    // token blocks of 8
-  const int Mtok = MT == 1 ? 1 : a.M;                 // tokens (a compile-time 1 for MT = 1)
+  const int Mtok = MX > 0 ? MX : a.M;                 // tokens (compile-time when MX > 0)
   const int UW = unit_words(Mtok, NP);
   extern __shared__ __align__(128) unsigned char smem_raw[];
 
@@ -777,7 +777,7 @@ TmaGeo make_geo(int units, int cs, int M, int group, int ctas, int sm_count, int
   return g;
 }
 
-template <int BITS, int MT, typename T, bool FOLD>
+template <int BITS, int MT, int MX, typename T, bool FOLD>
 cudaError_t launch_mma(const Problem& p, int cs, cudaStream_t stream) {
   Args a;
   a.A = p.A; a.M = p.M; a.K = p.K; a.N = p.N;
@@ -789,7 +789,7 @@ cudaError_t launch_mma(const Problem& p, int cs, cudaStream_t stream) {
   a.C = p.out; a.status = p.status;
   const int slabs = (p.N + kSlab - 1) / kSlab;
   const int sms = device_info().sm_count;
-  auto kern = k_decode_mma<BITS, MT, T, FOLD>;
+  auto kern = k_decode_mma<BITS, MT, MX, T, FOLD>;
   // CTAs per SM the registers allow (read once per kernel from its attributes)
   static std::atomic<int> regs_cache{-1};
   int regs = regs_cache.load(std::memory_order_relaxed);
@@ -821,6 +821,12 @@ cudaError_t launch_mma(const Problem& p, int cs, cudaStream_t stream) {
     }
   }
   const TmaGeo geo = geo_for(cs);
+  if constexpr (MT == 8 && MX > 0) {
+    // refills ahead: the runtime-count instantiation, whose warps refill independently, is faster
+    // there (measured); the exact one wins when the whole slice is in flight
+    const int chunks = (geo.tiles_per_cta + geo.chunk_tiles - 1) / geo.chunk_tiles;
+    if (geo.nbuf < chunks) return launch_mma<BITS, MT, 0, T, FOLD>(p, cs0, stream);
+  }
   CUtensorMap tmW;
   {
     constexpr int ROWS = Pack<BITS>::kRowsPerUnit;
