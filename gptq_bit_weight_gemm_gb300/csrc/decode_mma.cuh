@@ -275,6 +275,9 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
   }
   __syncthreads();
   volatile int* last_issued = abort_flag + 1;          // [warp][nbuf] last chunk issued per buffer
+  // the packed weights are read once: evict them first, so that activations and other reused
+  // data keep their place in L2
+  const uint64_t stream_policy = ptx::policy_evict_first();
   // copy warp w's 32 columns of chunk c into buffer c % nbuf (its own slot and mbarrier)
   auto issue_for = [&](int w, int c) {
     const int b = c % geo.nbuf;
@@ -283,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
                                         static_cast<size_t>(w) * geo.slot_bytes);
     const int row0 = (cu0 + c * geo.chunk_tiles * 4) * ROWS;
     ptx::mbar_arrive_expect_tx(bar(w, b), static_cast<uint32_t>(geo.chunk_rows * kBoxRowBytes));
-    ptx::tma_load_2d(dst, &tmW, n_base + w * kBoxCols, row0, bar(w, b));
+    ptx::tma_load_2d_hint(dst, &tmW, n_base + w * kBoxCols, row0, bar(w, b), stream_policy);
   };
   // all four slots of chunk c on one mbarrier (single-barrier mode)
   auto issue_chunk = [&](int c) {
@@ -292,9 +295,9 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
     const int row0 = (cu0 + c * geo.chunk_tiles * 4) * ROWS;
     ptx::mbar_arrive_expect_tx(bar(0, b), static_cast<uint32_t>(kWarps * geo.chunk_rows * kBoxRowBytes));
     for (int w = 0; w < kWarps; ++w)
-      ptx::tma_load_2d(ptx::smem_addr(sbuf + static_cast<size_t>(b) * geo.chunk_bytes +
-                                      static_cast<size_t>(w) * geo.slot_bytes),
-                       &tmW, n_base + w * kBoxCols, row0, bar(0, b));
+      ptx::tma_load_2d_hint(ptx::smem_addr(sbuf + static_cast<size_t>(b) * geo.chunk_bytes +
+                                           static_cast<size_t>(w) * geo.slot_bytes),
+                            &tmW, n_base + w * kBoxCols, row0, bar(0, b), stream_policy);
   };
   // refill after chunk c_next - nbuf was consumed: per warp (its slot) or by the whole CTA
   // (per_warp is uniform over the CTA, and so is the loop's chunk sequence)
