@@ -108,7 +108,7 @@ struct TmaGeo {
 };
 
 // Shared memory of one CTA: [alignment pad][weight chunk buffers][activation pairs | partial
-// sums (aliased in time)][receive slots][per group and column: scale, scale * zero][per group
+// sums, several tokens (aliased in time)][receive slots][per group and column: scale, scale * zero][per group
 // and token: kMagic * sum b, sum 2^shift b][FULL: per group and column scale and zero, per k
 // its group][mbarriers, flags].
 // Activations, partial sums and receive slots are sized by the real token count M, not by the
@@ -117,7 +117,7 @@ template <int BITS>
 struct TmaSmem {
   __host__ __device__ static size_t stage_bytes(const TmaGeo& g, int M) {
     const size_t stage = static_cast<size_t>(g.tiles_per_cta) * 4 * unit_words(M, MmaPairs<BITS>::kPairs) * 4;
-    const size_t part = static_cast<size_t>(M) * kSlab * 4;
+    const size_t part = M > 1 ? static_cast<size_t>(M) * kSlab * 4 : 0;   // partial sums (M > 1)
     return ((stage > part ? stage : part) + 127) & ~static_cast<size_t>(127);
   }
   __host__ __device__ static size_t off_stage(const TmaGeo& g) {
@@ -670,36 +670,48 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
     }
   }
 
-  // ---- this CTA's partial sums -> shared memory, then the cluster reduce-scatter
-  __syncthreads();                                      // done with the staged activations
-  float* part = reinterpret_cast<float*>(sB);           // [M][kSlab], aliases the staging
-  // recv ([cs][M][kSlab / cs]) has a region of its own: peers may push into it while this CTA
-  // is still reading its staged activations.
+  // ---- the cluster reduce-scatter into the receive slots ([cs][M][kSlab / cs], a region of its
+  // own: peers may push while this CTA still reads its staged activations) of the CTA that owns
+  // each column.  Fragment element i of acc[t][nb] is column 2t + (i >> 1) of the thread's quad
+  // and token 8 nb + 2 tq + (i & 1).
   const int Mr = Mtok;
-#pragma unroll
-  for (int t = 0; t < 2; ++t)
-#pragma unroll
-    for (int nb = 0; nb < NB; ++nb) {
-      const int col = col0 + 2 * t;
-      const int m = nb * 8 + 2 * tq;
-      if (m < Mr) {
-        part[m * kSlab + col] = acc[t][nb][0];
-        part[m * kSlab + col + 1] = acc[t][nb][2];
-      }
-      if (m + 1 < Mr) {
-        part[(m + 1) * kSlab + col] = acc[t][nb][1];
-        part[(m + 1) * kSlab + col + 1] = acc[t][nb][3];
-      }
-    }
-  __syncthreads();
   const int per_rank = kSlab / cs;                      // cs is a power of two
   const int pr_shift = __ffs(per_rank) - 1;
-  cluster_wait();
-  for (int i = threadIdx.x; i < Mr * kSlab; i += kThreads) {
-    const int m = i / kSlab, col = i - m * kSlab;
-    const int owner = col >> pr_shift;
-    float* dst = cluster.map_shared_rank(recv, owner);
-    dst[(rank * Mr + m) * per_rank + (col - owner * per_rank)] = part[i];
+  if constexpr (MX == 1) {
+    // one token: 128 sums per CTA, pushed straight from registers
+    cluster_wait();
+#pragma unroll
+    for (int t = 0; t < 2; ++t)
+#pragma unroll
+      for (int r = 0; r < 2; ++r)
+        if (tq == 0) {
+          const int col = col0 + 2 * t + r;
+          const int owner = col >> pr_shift;
+          float* dst = cluster.map_shared_rank(recv, owner);
+          dst[rank * per_rank + (col - owner * per_rank)] = acc[t][0][2 * r];
+        }
+  } else {
+    // several tokens: through shared memory first, so that consecutive threads push consecutive
+    // columns (coalesced remote stores)
+    __syncthreads();                                    // done with the staged activations
+    float* part = reinterpret_cast<float*>(sB);         // [M][kSlab], aliases the staging
+#pragma unroll
+    for (int t = 0; t < 2; ++t)
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int col = col0 + 2 * t + (i >> 1), m = nb * 8 + 2 * tq + (i & 1);
+          if (m < Mr) part[m * kSlab + col] = acc[t][nb][i];
+        }
+    __syncthreads();
+    cluster_wait();
+    for (int i = threadIdx.x; i < Mr * kSlab; i += kThreads) {
+      const int m = i / kSlab, col = i - m * kSlab;
+      const int owner = col >> pr_shift;
+      float* dst = cluster.map_shared_rank(recv, owner);
+      dst[(rank * Mr + m) * per_rank + (col - owner * per_rank)] = part[i];
+    }
   }
   cluster.sync();
   T* C = static_cast<T*>(a.C);
