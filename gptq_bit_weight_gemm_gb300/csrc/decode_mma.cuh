@@ -783,7 +783,7 @@ TmaGeo make_geo(int units, int cs, int M, int group, int ctas, int sm_count, int
     return chunks;
   };
   int ct = 1;
-  for (int d = 1; d * tile_bytes <= 16 * 1024 && d <= g.tiles_per_cta; ++d)
+  for (int d = 1; d * tile_bytes <= 32 * 1024 && d <= g.tiles_per_cta; ++d)
     if (g.tiles_per_cta % d == 0) ct = d;
   int chunks = layout(ct);
   while (g.nbuf < 2 && g.nbuf < chunks && ct > 1) chunks = layout(ct = (ct + 1) / 2);
