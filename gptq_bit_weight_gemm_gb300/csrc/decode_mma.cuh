@@ -736,7 +736,7 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
   }
 }
 
-// Chunking of a CTA range: chunks of at most 16 KB whose k-tile count divides the range when it
+// Chunking of a CTA range: chunks of at most 32 KB whose k-tile count divides the range when it
 // can; as many buffers as the shared-memory share of one CTA allows when every CTA of the grid
 // is resident at once (one wave), at least 2 -- all of them for the common one-token shapes, so
 // the whole slice is in flight from the first cycle.
