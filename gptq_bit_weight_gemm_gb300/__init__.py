@@ -14,6 +14,8 @@ Operations (page "增强 vLLM 对 GPTQv2 格式的支持：分析与实现", sec
   repack_zeros_v1_to_v2(qzeros_v1, N, bits)                  (host memory)
   prepack_act_order(qweight, g_idx, K, N, bits, group)      (host memory) -> (qweight', perm)
   gemm_perm(A, perm, qweight', qzeros, scales, bits, group) -> A[:, perm] @ dequant(W'), M <= 32
+  gemm_grouped(A, offsets, qweight[E], qzeros[E], scales[E], bits, group, max_m)
+                                                             -> rows of expert e times W_e
   device_status(stream)                                      -> GPTQ_DEV_* bits
 """
 import ctypes
@@ -28,7 +30,7 @@ HEADER = os.path.join(os.path.dirname(HERE), "include", "gptq.h")
 
 F16, BF16 = 0, 1
 V1, V2 = 1, 2
-DEV_TIMEOUT, DEV_GIDX_RANGE, DEV_SCALE_OVERFLOW = 0x1, 0x2, 0x4
+DEV_TIMEOUT, DEV_GIDX_RANGE, DEV_SCALE_OVERFLOW, DEV_EXPERT_ROWS = 0x1, 0x2, 0x4, 0x8
 DECODE_MAX_M = 32
 
 _STATUS = {0: "GPTQ_OK", -1: "GPTQ_ERR_ARG", -2: "GPTQ_ERR_SHAPE", -3: "GPTQ_ERR_ALIGN",
@@ -63,6 +65,7 @@ _SIGNATURES = {
     "gptq_gemm_perm": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P]),
     "gptq_gemm_perm_workspace_size": (_SZ, [_I, _I]),
     "gptq_gemm_perm_noalloc": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
+    "gptq_gemm_grouped": (_I, [_P, _I, _I, _I, _P, _I, _I, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
 }
 
 
@@ -228,6 +231,26 @@ def gemm_perm(A, perm, qweight, qzeros, scales, *, bits, group, fmt=V2, out=None
                               _ptr(scales, torch.float16, "scales"), N, bits, group, fmt,
                               _ptr(out, A.dtype, "out"), ws_ptr, ws_len, _stream(stream))
     _check(rc, "gptq_gemm_perm")
+    return out
+
+
+def gemm_grouped(A, offsets, qweight, qzeros, scales, *, bits, group, max_m, fmt=V2, out=None,
+                 stream=None):
+    """Mixture-of-experts GEMM: rows [offsets[e], offsets[e+1]) of A [rows, K] times expert e's
+    weight, into the same rows of C [rows, N].  qweight [E, K*bits/32, N], qzeros
+    [E, G, N*bits/32], scales [E, G, N] fp16; offsets [E+1] int32 on the device; every expert
+    has at most max_m (<= 32) rows."""
+    torch = _torch()
+    rows, K = A.shape
+    E, _, N = qweight.shape
+    if out is None:
+        out = torch.empty((rows, N), dtype=A.dtype, device=A.device)
+    rc = lib().gptq_gemm_grouped(_ptr(A, name="A"), rows, K, _dtype_code(A),
+                                 _ptr(offsets, torch.int32, "offsets"), E, max_m,
+                                 _ptr(qweight, torch.int32, "qweight"), _ptr(qzeros, torch.int32, "qzeros"),
+                                 _ptr(scales, torch.float16, "scales"), N, bits, group, fmt,
+                                 _ptr(out, A.dtype, "out"), _stream(stream))
+    _check(rc, "gptq_gemm_grouped")
     return out
 
 

@@ -37,6 +37,10 @@ struct Args {
   int group, G, zero_offset, zwords, units;
   void* C;
   unsigned* status;
+  // grouped (one weight per expert): rows [offsets[e], offsets[e + 1]) of A and C belong to
+  // expert e (blockIdx.z); `rows` bounds them.  nullptr for a single weight.
+  const int32_t* offsets;
+  int rows;
 };
 
 __device__ __forceinline__ void split(int total, int parts, int idx, int& b, int& e) {
@@ -179,17 +183,19 @@ inline int choose_cluster(const Problem& p, int per_unit) {
   const int slabs = (p.N + kSlab - 1) / kSlab;
   const int units = p.K / per_unit;
   const int target = device_info().sm_count * 24;
+  const long long weights = p.E > 1 ? p.E : 1;        // every expert's slabs run side by side
   int cs = 1;
-  while (cs < 16 && slabs * cs * kWarps < target && units >= 4 * cs * kWarps) cs *= 2;
+  while (cs < 16 && slabs * weights * cs * kWarps < target && units >= 4 * cs * kWarps) cs *= 2;
   return cs;
 }
 
-template <int BITS, int MT, int MX, typename T, bool FOLD>
+template <int BITS, int MT, int MX, typename T, bool FOLD, bool GROUPED>
 cudaError_t launch_mma(const Problem& p, int cs, cudaStream_t stream);
 
 // MT: token block bound (1, 8, 16, 32); MX: the exact token count when it is MT (0 = read at run
-// time), so the common batch sizes run with every token loop sized at compile time.
-template <int BITS, int MT, int MX, typename T>
+// time), so the common batch sizes run with every token loop sized at compile time.  GROUPED:
+// one weight per expert (blockIdx.z), each with its own rows of A and C.
+template <int BITS, int MT, int MX, typename T, bool GROUPED = false>
 cudaError_t launch_mt(const Problem& p, cudaStream_t stream) {
   const int cs = choose_cluster(p, Pack<BITS>::kPerUnit);
   constexpr bool kHas16 = (BITS == 2 || BITS == 4 ||
@@ -197,9 +203,9 @@ cudaError_t launch_mt(const Problem& p, cudaStream_t stream) {
   // the scale folds per group when groups align with k-tiles (4 units)
   const bool fold = kHas16 && p.g_idx == nullptr && (p.group % (4 * Pack<BITS>::kPerUnit)) == 0;
   if constexpr (kHas16) {
-    if (fold) return launch_mma<BITS, MT, MX, T, true>(p, cs, stream);
+    if (fold) return launch_mma<BITS, MT, MX, T, true, GROUPED>(p, cs, stream);
   }
-  return launch_mma<BITS, MT, MX, T, false>(p, cs, stream);
+  return launch_mma<BITS, MT, MX, T, false, GROUPED>(p, cs, stream);
 }
 
 // Every M <= 32 runs the tensor-core decode kernel (token blocks of 8; one token has an
@@ -223,6 +229,22 @@ template <int BITS>
 cudaError_t launch_bits(const Problem& p, cudaStream_t stream) {
   if (p.dtype == 0) return launch_tokens<BITS, __half>(p, stream);
   return launch_tokens<BITS, __nv_bfloat16>(p, stream);
+}
+
+// Grouped: p.M is the bound on any expert's rows (the per-expert counts live on the device);
+// one token keeps its compile-time instantiation, more take the run-time token count.
+template <int BITS, typename T>
+cudaError_t launch_grouped_tokens(const Problem& p, cudaStream_t stream) {
+  if (p.M == 1) return launch_mt<BITS, 1, 1, T, true>(p, stream);
+  if (p.M <= 8) return launch_mt<BITS, 8, 0, T, true>(p, stream);
+  if (p.M <= 16) return launch_mt<BITS, 16, 0, T, true>(p, stream);
+  return launch_mt<BITS, 32, 0, T, true>(p, stream);
+}
+
+template <int BITS>
+cudaError_t launch_grouped_bits(const Problem& p, cudaStream_t stream) {
+  if (p.dtype == 0) return launch_grouped_tokens<BITS, __half>(p, stream);
+  return launch_grouped_tokens<BITS, __nv_bfloat16>(p, stream);
 }
 
 }  // namespace decode

@@ -1,0 +1,10 @@
+// decode_grouped_b2.cu -- 2-bit instantiations of the grouped (one weight per expert) decode
+// kernel, in their own translation unit so that they compile in parallel with the rest.
+#include "decode.cuh"
+#include "decode_mma.cuh"
+
+namespace gptq {
+cudaError_t launch_decode_grouped_b2(const Problem& p, cudaStream_t stream) {
+  return decode::launch_grouped_bits<2>(p, stream);
+}
+}  // namespace gptq

@@ -117,7 +117,8 @@ template <int BITS>
 struct TmaSmem {
   __host__ __device__ static size_t stage_bytes(const TmaGeo& g, int M) {
     const size_t stage = static_cast<size_t>(g.tiles_per_cta) * 4 * unit_words(M, MmaPairs<BITS>::kPairs) * 4;
-    const size_t part = M > 1 ? static_cast<size_t>(M) * kSlab * 4 : 0;   // partial sums (M > 1)
+    // partial sums of several tokens (one token pushes them from registers)
+    const size_t part = M > 1 ? static_cast<size_t>(M) * kSlab * 4 : 0;
     return ((stage > part ? stage : part) + 127) & ~static_cast<size_t>(127);
   }
   __host__ __device__ static size_t off_stage(const TmaGeo& g) {
@@ -163,9 +164,9 @@ __device__ __forceinline__ bool tma_wait(uint32_t bar, uint32_t parity, volatile
   }
 }
 
-template <int BITS, int MT, int MX, typename T, bool FOLD>
+template <int BITS, int MT, int MX, typename T, bool FOLD, bool GROUPED = false>
 __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
-    k_decode_mma(const __grid_constant__ CUtensorMap tmW, const Args a, const TmaGeo geo) {
+    k_decode_mma(const __grid_constant__ CUtensorMap tmW, const Args args, const TmaGeo geo) {
   using P = Pack<BITS>;
   using MP = MmaPairs<BITS>;
   using SM = TmaSmem<BITS>;
@@ -173,11 +174,35 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
   constexpr int ROWS = P::kRowsPerUnit;
   constexpr int NP = MP::kPairs;
   constexpr int NB = (MT + 7) / 8;                    // token blocks of 8
-  const int Mtok = MX > 0 ? MX : a.M;                 // tokens (compile-time when MX > 0)
-  const int UW = unit_words(Mtok, NP);
   extern __shared__ __align__(128) unsigned char smem_raw[];
 
   pdl_launch_dependents();
+  // Grouped: expert e = blockIdx.z multiplies rows [offsets[e], offsets[e + 1]) of A into the
+  // same rows of C, with its own scales, zeros and packed rows (e * K * bits / 32 onward in the
+  // stacked weight).  The offsets come from the kernel before this one, so they are read after
+  // griddepcontrol.wait; an expert without rows, the same for every CTA of its cluster, leaves
+  // before any cluster barrier or copy.
+  Args ga = args;                                     // the expert's view (grouped only)
+  int w_row0 = 0;
+  if constexpr (GROUPED) {
+    pdl_wait();
+    const int e = static_cast<int>(blockIdx.z);
+    const int o0 = ga.offsets[e], o1 = ga.offsets[e + 1];
+    if (o0 == o1) return;
+    if (o0 < 0 || o1 < o0 || o1 > ga.rows || o1 - o0 > ga.M) {   // ga.M: the caller's max_m (<= MT)
+      if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) atomicOr(ga.status, kStatusExpertRows);
+      return;
+    }
+    ga.M = o1 - o0;
+    ga.A = static_cast<const uint16_t*>(ga.A) + static_cast<long long>(o0) * ga.K;
+    ga.C = static_cast<uint16_t*>(ga.C) + static_cast<long long>(o0) * ga.N;
+    ga.qzeros += static_cast<long long>(e) * ga.G * ga.zwords;
+    ga.scales += static_cast<long long>(e) * ga.G * ga.N;
+    w_row0 = e * ga.units * ROWS;
+  }
+  const Args& a = GROUPED ? ga : args;
+  const int Mtok = MX > 0 ? MX : a.M;                 // tokens (compile-time when MX > 0)
+  const int UW = unit_words(Mtok, NP);
   cluster_arrive_relaxed();
   cg::cluster_group cluster = cg::this_cluster();
   const int cs = static_cast<int>(gridDim.x);
@@ -284,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
     last_issued[w * geo.nbuf + b] = c;
     const uint32_t dst = ptx::smem_addr(sbuf + static_cast<size_t>(b) * geo.chunk_bytes +
                                         static_cast<size_t>(w) * geo.slot_bytes);
-    const int row0 = (cu0 + c * geo.chunk_tiles * 4) * ROWS;
+    const int row0 = w_row0 + (cu0 + c * geo.chunk_tiles * 4) * ROWS;
     ptx::mbar_arrive_expect_tx(bar(w, b), static_cast<uint32_t>(geo.chunk_rows * kBoxRowBytes));
     ptx::tma_load_2d_hint(dst, &tmW, n_base + w * kBoxCols, row0, bar(w, b), stream_policy);
   };
@@ -292,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
   auto issue_chunk = [&](int c) {
     const int b = c % geo.nbuf;
     last_issued[b] = c;
-    const int row0 = (cu0 + c * geo.chunk_tiles * 4) * ROWS;
+    const int row0 = w_row0 + (cu0 + c * geo.chunk_tiles * 4) * ROWS;
     ptx::mbar_arrive_expect_tx(bar(0, b), static_cast<uint32_t>(kWarps * geo.chunk_rows * kBoxRowBytes));
     for (int w = 0; w < kWarps; ++w)
       ptx::tma_load_2d_hint(ptx::smem_addr(sbuf + static_cast<size_t>(b) * geo.chunk_bytes +
@@ -677,8 +702,10 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
   const int Mr = Mtok;
   const int per_rank = kSlab / cs;                      // cs is a power of two
   const int pr_shift = __ffs(per_rank) - 1;
-  if constexpr (MX == 1) {
-    // one token: 128 sums per CTA, pushed straight from registers
+  if (MX == 1 || Mtok == 1) {
+    // one token: 128 sums per CTA, pushed straight from registers (so the staging needs no room
+    // for partial sums; the run-time token count takes this branch too when a grouped expert
+    // holds one row)
     cluster_wait();
 #pragma unroll
     for (int t = 0; t < 2; ++t)
@@ -792,7 +819,7 @@ TmaGeo make_geo(int units, int cs, int M, int group, int ctas, int sm_count, int
   return g;
 }
 
-template <int BITS, int MT, int MX, typename T, bool FOLD>
+template <int BITS, int MT, int MX, typename T, bool FOLD, bool GROUPED>
 cudaError_t launch_mma(const Problem& p, int cs, cudaStream_t stream) {
   Args a;
   a.A = p.A; a.M = p.M; a.K = p.K; a.N = p.N;
@@ -802,9 +829,12 @@ cudaError_t launch_mma(const Problem& p, int cs, cudaStream_t stream) {
   a.zwords = p.N * BITS / 32;
   a.units = p.K / Pack<BITS>::kPerUnit;
   a.C = p.out; a.status = p.status;
+  a.offsets = GROUPED ? p.offsets : nullptr;
+  a.rows = p.rows;
+  const int E = GROUPED ? p.E : 1;                     // weights side by side (grid z)
   const int slabs = (p.N + kSlab - 1) / kSlab;
   const int sms = device_info().sm_count;
-  auto kern = k_decode_mma<BITS, MT, MX, T, FOLD>;
+  auto kern = k_decode_mma<BITS, MT, MX, T, FOLD, GROUPED>;
   // CTAs per SM the registers allow (read once per kernel from its attributes)
   static std::atomic<int> regs_cache{-1};
   int regs = regs_cache.load(std::memory_order_relaxed);
@@ -820,7 +850,8 @@ cudaError_t launch_mma(const Problem& p, int cs, cudaStream_t stream) {
   // smaller split stages more activations), and the chosen split stays when no split gives one
   // wave.  FULL keeps the chosen split: it is latency-bound and gains from every extra CTA.
   auto geo_for = [&](int c) {
-    return make_geo<BITS>(a.units, c, p.M, p.group, slabs * c, sms, max_per_sm, !FOLD, p.g_idx != nullptr, p.G);
+    return make_geo<BITS>(a.units, c, p.M, p.group, slabs * c * E, sms, max_per_sm, !FOLD, p.g_idx != nullptr,
+                          p.G);
   };
   // A 16-CTA cluster is used only when it gives one wave; otherwise (and for FULL) at most 8.
   const int cs0 = cs;
@@ -830,7 +861,7 @@ cudaError_t launch_mma(const Problem& p, int cs, cudaStream_t stream) {
     if (bytes > 227 * 1024) break;
     int per_sm = static_cast<int>(233472 / (bytes + 1024));
     per_sm = per_sm < max_per_sm ? per_sm : max_per_sm;
-    if (slabs * c <= per_sm * sms) {
+    if (static_cast<long long>(slabs) * c * E <= static_cast<long long>(per_sm) * sms) {
       cs = c;
       break;
     }
@@ -840,12 +871,12 @@ cudaError_t launch_mma(const Problem& p, int cs, cudaStream_t stream) {
     // refills ahead: the runtime-count instantiation, whose warps refill independently, is faster
     // there (measured); the exact one wins when the whole slice is in flight
     const int chunks = (geo.tiles_per_cta + geo.chunk_tiles - 1) / geo.chunk_tiles;
-    if (geo.nbuf < chunks) return launch_mma<BITS, MT, 0, T, FOLD>(p, cs0, stream);
+    if (geo.nbuf < chunks) return launch_mma<BITS, MT, 0, T, FOLD, GROUPED>(p, cs0, stream);
   }
   CUtensorMap tmW;
   {
     constexpr int ROWS = Pack<BITS>::kRowsPerUnit;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.N), static_cast<cuuint64_t>(a.units) * ROWS};
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.N), static_cast<cuuint64_t>(a.units) * ROWS * E};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.N) * 4};
     const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBoxCols), static_cast<cuuint32_t>(geo.chunk_rows)};
     const cuuint32_t estr[2] = {1, 1};
@@ -879,7 +910,7 @@ cudaError_t launch_mma(const Problem& p, int cs, cudaStream_t stream) {
     }
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(cs, slabs, 1);
+  cfg.gridDim = dim3(cs, slabs, E);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;

@@ -27,6 +27,21 @@ cudaError_t launch_decode(const Problem& p, cudaStream_t stream) {
   }
 }
 
+cudaError_t launch_decode_grouped_b2(const Problem& p, cudaStream_t stream);
+cudaError_t launch_decode_grouped_b3(const Problem& p, cudaStream_t stream);
+cudaError_t launch_decode_grouped_b4(const Problem& p, cudaStream_t stream);
+cudaError_t launch_decode_grouped_b8(const Problem& p, cudaStream_t stream);
+
+cudaError_t launch_decode_grouped(const Problem& p, cudaStream_t stream) {
+  switch (p.bits) {
+    case 2: return launch_decode_grouped_b2(p, stream);
+    case 3: return launch_decode_grouped_b3(p, stream);
+    case 4: return launch_decode_grouped_b4(p, stream);
+    case 8: return launch_decode_grouped_b8(p, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -192,6 +207,34 @@ extern "C" int gptq_gemm(const void* A, int M, int K, int a_dtype, const int32_t
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (M <= gptq::kDecodeMaxM) return gptq::from_cuda(gptq::launch_decode(p, s));
   return gptq::from_cuda(gptq::launch_prefill(p, s));
+}
+
+extern "C" int gptq_gemm_grouped(const void* A, int rows, int K, int a_dtype, const int32_t* offsets,
+                                 int E, int max_m, const int32_t* qweight, const int32_t* qzeros,
+                                 const void* scales, int N, int bits, int group, int fmt, void* C,
+                                 void* stream) {
+  Problem p = {};
+  int rc = gptq::check_common(qweight, qzeros, scales, nullptr, K, N, bits, group, &p);
+  if (rc) return rc;
+  if (fmt != GPTQ_FMT_V1 && fmt != GPTQ_FMT_V2) return GPTQ_ERR_ARG;
+  if (a_dtype != GPTQ_F16 && a_dtype != GPTQ_BF16) return GPTQ_ERR_ARG;
+  if (rows < 0 || E < 0 || E > 65535 || max_m < 1 || max_m > gptq::kDecodeMaxM) return GPTQ_ERR_SHAPE;
+  // the stacked weight is one tensor map of E * K * bits / 32 rows (32-bit coordinates)
+  if (static_cast<long long>(E) * K * bits / 32 > 0x7FFFFFFFLL) return GPTQ_ERR_SHAPE;
+  if (rows == 0 || E == 0) return GPTQ_OK;
+  if (!A || !C || !offsets) return GPTQ_ERR_ARG;
+  if (!gptq::aligned(A, 16) || !gptq::aligned(C, 16) || !gptq::aligned(offsets, 4)) return GPTQ_ERR_ALIGN;
+  rc = gptq::device_ready(&p);
+  if (rc) return rc;
+  p.A = A;
+  p.M = max_m;
+  p.dtype = a_dtype;
+  p.zero_offset = fmt == GPTQ_FMT_V1 ? 1 : 0;
+  p.out = C;
+  p.offsets = offsets;
+  p.E = E;
+  p.rows = rows;
+  return gptq::from_cuda(gptq::launch_decode_grouped(p, static_cast<cudaStream_t>(stream)));
 }
 
 extern "C" size_t gptq_gemm_perm_workspace_size(int M, int K) {

@@ -23,6 +23,7 @@ namespace gptq {
 
 constexpr unsigned kStatusTimeout = 0x1u;
 constexpr unsigned kStatusGidxRange = 0x2u;
+constexpr unsigned kStatusExpertRows = 0x8u;   // grouped GEMM: an expert's row range was invalid
 
 template <int BITS>
 struct Pack {

@@ -24,6 +24,11 @@ struct Problem {
   int zero_offset;           // 1 for GPTQv1, 0 for GPTQv2
   void* out;                 // C [M, N] or W [K, N]
   unsigned* status;          // device status word of the current device
+  // grouped GEMM (one weight per expert, stacked [E][...]): device row offsets [E + 1] into A
+  // and C, E experts, `rows` rows in A and C; M is then the bound on any expert's rows
+  const int32_t* offsets;
+  int E;
+  int rows;
 };
 
 struct DeviceInfo {
@@ -37,6 +42,7 @@ const DeviceInfo& device_info();   // current device, cached
 
 cudaError_t launch_dequant(const Problem& p, cudaStream_t stream);
 cudaError_t launch_decode(const Problem& p, cudaStream_t stream);
+cudaError_t launch_decode_grouped(const Problem& p, cudaStream_t stream);
 cudaError_t launch_prefill(const Problem& p, cudaStream_t stream);
 cudaError_t launch_gather_cols(const void* A, const int32_t* perm, int M, int K, void* out,
                                cudaStream_t stream);

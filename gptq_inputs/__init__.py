@@ -26,6 +26,17 @@ and not present -- these seeded draws stand in for them):
 Seeds: the weights of a workload use numpy default_rng(seed); activations with M rows use
 default_rng(seed * 100 + M).  Draw order inside a seed: W, then shifts, then outlier
 positions, then the act-order permutation.
+
+Mixture-of-experts workloads (MOE_WORKLOADS; the grouped GEMM):
+
+  moe_mixtral_4bit_g128     E = 8 experts, each W [4096, 14336] 4-bit, group 128, v2 (the
+                            expert up-projection shape of a Mixtral-8x7B-class model); A fp16;
+                            T tokens in {1, 8}, each routed to 2 distinct experts
+
+Expert e's weights use default_rng(seed * 1000 + e); the routing of T tokens uses
+default_rng(seed * 100 + T) (each token draws its top-k experts without replacement), and the
+token activations default_rng(seed * 100 + T + 50).  Rows of the grouped A are the
+(token, expert) pairs sorted by expert, then by token.
 """
 from dataclasses import dataclass, field, replace
 from typing import Optional, Tuple
@@ -122,3 +133,64 @@ def bits16(t) -> np.ndarray:
     """uint16 bit patterns of a CPU fp16/bf16 torch tensor."""
     import torch
     return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+# ------------------------------------------------------------------ mixture of experts
+@dataclass(frozen=True)
+class MoeWorkload:
+    name: str
+    E: int
+    K: int
+    N: int
+    bits: int
+    group: int
+    act_dtype: str
+    Ts: Tuple[int, ...]        # tokens per batch
+    topk: int
+    seed: int
+
+    @property
+    def G(self) -> int:
+        return 1 if self.group == -1 else self.K // self.group
+
+    def resized(self, E: int, K: int, N: int, Ts: Tuple[int, ...], name: Optional[str] = None):
+        return replace(self, E=E, K=K, N=N, Ts=tuple(Ts), name=name or "%s@%dx%dx%d" % (self.name, E, K, N))
+
+
+MOE_WORKLOADS = {
+    w.name: w for w in [
+        MoeWorkload("moe_mixtral_4bit_g128", 8, 4096, 14336, 4, 128, "f16", (1, 8), 2, seed=6),
+    ]
+}
+
+
+def draw_expert_weights(mw: MoeWorkload, e: int) -> np.ndarray:
+    """fp32 weights [K, N] of expert e."""
+    rng = np.random.default_rng(mw.seed * 1000 + e)
+    W = rng.standard_normal((mw.K, mw.N), dtype=np.float32)
+    W *= np.float32(0.02)
+    return W
+
+
+@dataclass
+class Routing:
+    row_token: np.ndarray     # int32 [T * topk]: the token of each grouped row
+    offsets: np.ndarray       # int32 [E + 1]: rows [offsets[e], offsets[e + 1]) go to expert e
+
+
+def draw_routing(mw: MoeWorkload, T: int) -> Routing:
+    rng = np.random.default_rng(mw.seed * 100 + T)
+    experts = np.stack([rng.choice(mw.E, size=mw.topk, replace=False) for _ in range(T)])
+    pairs = sorted((int(experts[t, j]), t) for t in range(T) for j in range(mw.topk))
+    row_token = np.array([t for _, t in pairs], np.int32)
+    counts = np.bincount([e for e, _ in pairs], minlength=mw.E)
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    return Routing(row_token=row_token, offsets=offsets)
+
+
+def draw_token_activations(mw: MoeWorkload, T: int):
+    """Token activations [T, K] as a CPU torch tensor of the workload's dtype."""
+    import torch
+    rng = np.random.default_rng(mw.seed * 100 + T + 50)
+    a32 = torch.from_numpy(rng.standard_normal((T, mw.K), dtype=np.float32))
+    return a32.to(torch.float16 if mw.act_dtype == "f16" else torch.bfloat16)

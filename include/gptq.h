@@ -73,6 +73,9 @@ typedef enum {
 #define GPTQ_DEV_TIMEOUT 0x1u     /* a bounded wait inside a kernel ran out; output invalid */
 #define GPTQ_DEV_GIDX_RANGE 0x2u  /* an act-order g_idx entry was outside [0, G)            */
 #define GPTQ_DEV_SCALE_OVERFLOW 0x4u /* gptq_quantize_rtn: a group's scale overflowed fp16   */
+#define GPTQ_DEV_EXPERT_ROWS 0x8u /* gptq_gemm_grouped: an expert's row range was decreasing,
+                                     outside [0, rows] or longer than max_m; its rows of C
+                                     were not written                                        */
 
 /*
  * gptq_dequant -- write the dequantized weights W[k][n] = RN((q - zero) * scale).
@@ -138,6 +141,32 @@ int gptq_gemm_perm(const void* A, int M, int K, int a_dtype, const int32_t* perm
 
 /* Bytes of workspace gptq_gemm_perm needs: M * K * 2 rounded up to 256 for M > 1, else 0. */
 size_t gptq_gemm_perm_workspace_size(int M, int K);
+
+/*
+ * gptq_gemm_grouped -- the quantized mixture-of-experts GEMM: for every expert e in [0, E),
+ * C[r, :] = A[r, :] @ W_e for the rows r in [offsets[e], offsets[e + 1]), with W_e expert e's
+ * GPTQ weight dequantized on the fly exactly as in gptq_gemm.  Page "4.3 Weight-only INT4 量化：
+ * GPTQ、AWQ 与 Marlin Kernel", section 7 ("vLLM 生态：GPTQ/AWQ 的工程现状"): GPTQ checkpoints of
+ * MoE models quantize every expert's weights, and vLLM runs them through a fused MoE path.  The
+ * pages fix no layout; the one here is the plainest: the rows of A are already grouped by expert
+ * (the caller gathers and orders them), and every expert has the same K, N, bits and group.
+ * One launch covers all experts (one decode kernel, the expert as the third grid dimension).
+ * Device pointers:
+ *   A        [rows, K] fp16/bf16 (a_dtype), 16-byte aligned;
+ *   offsets  [E + 1] int32, nondecreasing, offsets[0] = 0, offsets[E] <= rows, 4-byte aligned;
+ *            read on the device after the previous kernel on the stream has finished, so a
+ *            routing kernel may write them just before;
+ *   qweight  [E][K * bits / 32][N], qzeros [E][G][N * bits / 32], scales [E][G][N] fp16
+ *            (each expert's tensors laid out as for gptq_gemm, experts back to back);
+ *   C        [rows, N] of a_dtype; rows outside every expert's range are left untouched.
+ * max_m (1..32) bounds every expert's row count; it selects the kernel's token tile.  An expert
+ * whose range is decreasing, leaves [0, rows] or exceeds max_m is skipped and flagged with
+ * GPTQ_DEV_EXPERT_ROWS.  No g_idx (act-order experts: prepack them, one gptq_gemm_perm each).
+ * Returns GPTQ_OK (also for rows == 0 or E == 0, with no launch) or a negative gptq_status.
+ */
+int gptq_gemm_grouped(const void* A, int rows, int K, int a_dtype, const int32_t* offsets, int E,
+                      int max_m, const int32_t* qweight, const int32_t* qzeros, const void* scales,
+                      int N, int bits, int group, int fmt, void* C, void* stream);
 
 /*
  * gptq_gemm_perm_noalloc -- gptq_gemm_perm for callers that cannot allocate device memory: a

@@ -188,6 +188,23 @@ class Oracle:
                                    group, fmt, _p(r), nr, _p(C), _p(B)), "gemm")
         return C, B
 
+    def gemm_grouped(self, A, a_dtype, offsets, qweight, qzeros, scales, N, bits, group, fmt):
+        """Mixture-of-experts reference: expert e multiplies rows [offsets[e], offsets[e + 1]) of
+        A by its own dequantized weight, exactly as gemm() does for one weight (page "4.3
+        Weight-only INT4 量化：GPTQ、AWQ 与 Marlin Kernel", section 7: the expert weights of a
+        MoE model are GPTQ checkpoints like any other).  qweight, qzeros and scales are indexed
+        by expert first.  Returns (C, B) over every row of A; rows no expert owns stay NaN."""
+        A = _c(A, np.uint16)
+        rows = A.shape[0]
+        C = np.full((rows, N), np.nan, np.float32)
+        B = np.full((rows, N), np.nan, np.float64)
+        for e in range(len(offsets) - 1):
+            lo, hi = int(offsets[e]), int(offsets[e + 1])
+            if hi > lo:
+                C[lo:hi], B[lo:hi] = self.gemm(A[lo:hi], a_dtype, qweight[e], qzeros[e], scales[e],
+                                               None, N, bits, group, fmt)
+        return C, B
+
     def repack_v1_to_v2(self, qz_v1, G, N, bits):
         qz = _c(qz_v1, np.int32)
         out = np.empty_like(qz)

@@ -24,7 +24,7 @@ def test_exports_every_declared_symbol(lib):
                                "gptq_get_device_status", "gptq_strerror",
                                "gptq_selftest_wait_timeout", "gptq_prepack_act_order",
                                "gptq_gemm_perm", "gptq_gemm_perm_workspace_size",
-                               "gptq_gemm_perm_noalloc"])
+                               "gptq_gemm_perm_noalloc", "gptq_gemm_grouped"])
     for name in declared:
         assert hasattr(lib, name), name
 
@@ -160,6 +160,23 @@ def test_gemm_perm_validation_without_gpu(lib, kw, code):
     rc = lib.gptq_gemm_perm(a["A"], a["M"], a["K"], a["dtype"], a["perm"], a["qweight"], a["qzeros"],
                             a["scales"], a["N"], a["bits"], a["group"], a["fmt"], a["C"], a["ws"],
                             a["ws_bytes"], None)
+    assert rc == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(max_m=0), -2), (dict(max_m=33), -2), (dict(E=-1), -2), (dict(E=65536), -2),
+    (dict(rows=-1), -2), (dict(offsets=None), -1), (dict(A=None), -1), (dict(C=None), -1),
+    (dict(offsets=P(0x10002)), -3), (dict(A=P(0x10008)), -3), (dict(bits=5), -1),
+    (dict(fmt=3), -1), (dict(dtype=2), -1), (dict(K=48), -2), (dict(group=100), -2),
+    (dict(rows=0), 0), (dict(E=0), 0),
+])
+def test_gemm_grouped_validation_without_gpu(lib, kw, code):
+    a = dict(A=FAKE, rows=16, K=256, dtype=0, offsets=FAKE, E=4, max_m=8, qweight=FAKE,
+             qzeros=FAKE, scales=FAKE, N=256, bits=4, group=128, fmt=2, C=FAKE)
+    a.update(kw)
+    rc = lib.gptq_gemm_grouped(a["A"], a["rows"], a["K"], a["dtype"], a["offsets"], a["E"], a["max_m"],
+                               a["qweight"], a["qzeros"], a["scales"], a["N"], a["bits"], a["group"],
+                               a["fmt"], a["C"], None)
     assert rc == code
 
 

@@ -8,6 +8,9 @@ Page: "增强 vLLM 对 GPTQv2 格式的支持：分析与实现" (xxxxyu.github.
   section "调整细节：根据格式选择处理方式" -- zero_offset = use_v2_format ? 0 : 1; 16 two-bit
                                        codes per int32 word.
 
+Page: "4.3 Weight-only INT4 量化：GPTQ、AWQ 与 Marlin Kernel", section 7 -- the expert weights
+  of a MoE model are GPTQ checkpoints like any other (the grouped GEMM).
+
 Kinds of pin used (each check below names its kind):
   golden     hand-worked values in tests/golden/ (with their derivation);
   closed     closed forms and invariants (error bound, losslessness, permutation invariance);
@@ -371,6 +374,65 @@ def check_brute_force_tiny(orc):
                     (bits, fmt, act, dtype, m, n, float(C[m, n]), exact)
 
 
+def check_grouped(orc):
+    """brute + closed: the grouped (mixture-of-experts) GEMM.  Three experts (one without
+    rows) plus a row no expert owns, every width x format x dtype; each expert's checkpoint is
+    built from chosen codes with the independent packer and every sum recomputed with math.fsum.
+    Then: one expert equals gemm() bit for bit, and reordering the experts (moving their row
+    blocks with them) leaves every row bit-identical."""
+    rng = np.random.default_rng(31)
+    K, N, group = 64, 32, 32
+    offsets = np.array([0, 2, 2, 5], np.int32)           # expert 1 has no rows; row 5 none
+    rows = 6
+    for bits, fmt, dtype in itertools.product((2, 3, 4, 8), (V1, V2), (F16, BF16)):
+        E, G, L = 3, K // group, 1 << bits
+        q = rng.integers(0, L, (E, K, N)).astype(np.uint8)
+        stored = rng.integers(0, L, (E, G, N)).astype(np.int32)
+        s16 = rng.uniform(1e-3, 1e-1, (E, G, N)).astype(np.float16)
+        a32 = rng.standard_normal((rows, K)).astype(np.float32)
+        if dtype == F16:
+            A = a32.astype(np.float16).view(np.uint16)
+            a64 = A.view(np.float16).astype(np.float64)
+        else:
+            t = torch.from_numpy(a32).to(torch.bfloat16)
+            A = t.view(torch.int16).numpy().view(np.uint16)
+            a64 = t.double().numpy()
+        qw = np.stack([_py_pack_k(q[e], bits) for e in range(E)])
+        qz = np.stack([_py_pack_n(stored[e], bits) for e in range(E)])
+        sc = s16.view(np.uint16)
+        off = 1 if fmt == V1 else 0
+        C, B = orc.gemm_grouped(A, dtype, offsets, qw, qz, sc, N, bits, group, fmt)
+        owner = [None] * rows
+        for e in range(E):
+            for r in range(offsets[e], offsets[e + 1]):
+                owner[r] = e
+        for r in range(rows):
+            e = owner[r]
+            if e is None:
+                assert np.all(np.isnan(C[r])) and np.all(np.isnan(B[r])), (bits, fmt, r)
+                continue
+            for n in range(N):
+                terms = [float(a64[r, k]) * (int(q[e, k, n]) - (int(stored[e, k // group, n]) + off))
+                         * float(s16[e, k // group, n]) for k in range(K)]
+                exact = math.fsum(terms)
+                babs = math.fsum(abs(x) for x in terms)
+                assert abs(B[r, n] - babs) <= 1e-12 * babs, (bits, fmt, dtype, r, n)
+                assert abs(float(C[r, n]) - exact) <= 1.01 * K * 2.0 ** -24 * babs, \
+                    (bits, fmt, dtype, r, n, float(C[r, n]), exact)
+        # one expert: the plain GEMM
+        C1, B1 = orc.gemm_grouped(A[:4], dtype, np.array([0, 4], np.int32), qw[:1], qz[:1], sc[:1],
+                                  N, bits, group, fmt)
+        Cg, Bg = orc.gemm(A[:4], dtype, qw[0], qz[0], sc[0], None, N, bits, group, fmt)
+        assert np.array_equal(C1, Cg) and np.array_equal(B1, Bg), (bits, fmt, dtype)
+        # experts in the order (2, 0, 1): rows 2..4 first, then 0..1
+        perm = [2, 0, 1]
+        blocks = [A[offsets[e]:offsets[e + 1]] for e in perm]
+        A2 = np.concatenate(blocks + [A[5:]])
+        off2 = np.concatenate([[0], np.cumsum([len(b) for b in blocks])]).astype(np.int32)
+        C2, _ = orc.gemm_grouped(A2, dtype, off2, qw[perm], qz[perm], sc[perm], N, bits, group, fmt)
+        assert np.array_equal(C2[:3], C[2:5]) and np.array_equal(C2[3:5], C[0:2]), (bits, fmt, dtype)
+
+
 PIN_CHECKS = [
     check_hand_worked_groups,
     check_symmetric_zero,
@@ -384,6 +446,7 @@ PIN_CHECKS = [
     check_identity_and_one_hot,
     check_group_index_forms,
     check_brute_force_tiny,
+    check_grouped,
 ]
 
 
@@ -453,3 +516,32 @@ def test_planted_mistakes_fail_a_pin():
         assert not survivors, "planted mistakes that no pin caught: %s" % survivors
     finally:
         shutil.rmtree(tmpdir, ignore_errors=True)
+
+
+# Plausible mistakes in the grouped composition (Python), planted in copies of its source.
+GROUPED_MUTATIONS = [
+    ("previous expert's weight", "qweight[e], qzeros[e], scales[e]", "qweight[e - 1], qzeros[e - 1], scales[e - 1]"),
+    ("expert 0's scales for all", "qzeros[e], scales[e]", "qzeros[e], scales[0]"),
+    ("row range shifted", "lo, hi = int(offsets[e]), int(offsets[e + 1])",
+     "lo, hi = int(offsets[e]) + 1, int(offsets[e + 1]) + 1"),
+    ("format ignored", "None, N, bits, group, fmt)", "None, N, bits, group, V2)"),
+]
+
+
+def test_planted_mistakes_in_grouped_fail_a_pin():
+    import inspect
+    import textwrap
+    src = textwrap.dedent(inspect.getsource(oracle.Oracle.gemm_grouped))
+    survivors = []
+    for what, old, new in GROUPED_MUTATIONS:
+        assert src.count(old) == 1, old
+        ns = {"np": np, "_c": oracle._c, "V2": V2}
+        exec(src.replace(old, new), ns)
+        orc = oracle.Oracle(oracle.default()._lib)
+        orc.gemm_grouped = ns["gemm_grouped"].__get__(orc)
+        try:
+            check_grouped(orc)
+            survivors.append(what)
+        except (AssertionError, oracle.OracleError, ValueError, IndexError):
+            pass
+    assert not survivors, "planted mistakes that no pin caught: %s" % survivors
