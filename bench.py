@@ -46,6 +46,14 @@ def algorithmic_bytes(wl, M):
     return qweight + scales + qzeros + acts + gidx
 
 
+def grouped_bytes(mw, offsets):
+    """Mixture of experts: every expert that holds rows reads its whole weight (qweight, scales,
+    qzeros) once; plus the grouped activations and the offsets."""
+    active = int(np.count_nonzero(np.diff(offsets)))
+    per_expert = (mw.K * mw.bits // 32 * mw.N * 4 + mw.G * mw.N * 2 + mw.G * (mw.N * mw.bits // 32) * 4)
+    return active * per_expert + int(offsets[-1]) * mw.K * 2 + (mw.E + 1) * 4, active
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -391,6 +399,57 @@ def time_workload(g, torch, dev, stream, wl, M, fmt, l2, reps=200, prepacked=Fal
     return ms, nbytes
 
 
+def time_grouped(g, torch, dev, stream, mw, T, l2, reps=200):
+    """Per-launch time of gptq_gemm_grouped on a mixture-of-experts layer: T tokens routed to
+    top-k experts (rows grouped by expert), CUDA graph of launches over expert-weight copies
+    whose total exceeds 3x L2."""
+    r = gptq_inputs.draw_routing(mw, T)
+    toks = gptq_inputs.draw_token_activations(mw, T)
+    A = toks[torch.from_numpy(r.row_token).long()].contiguous().to(dev)
+    offsets = torch.from_numpy(r.offsets).to(dev)
+    max_m = int(np.diff(r.offsets).max())
+    qws, qzs, scs = [], [], []
+    for e in range(mw.E):
+        W = torch.from_numpy(gptq_inputs.draw_expert_weights(mw, e)).to(dev)
+        qw, qz, sc = g.quantize_rtn(W, bits=mw.bits, group=mw.group, fmt=g.V2)
+        qws.append(qw); qzs.append(qz); scs.append(sc)
+        del W
+    qw, qz, sc = torch.stack(qws), torch.stack(qzs), torch.stack(scs)
+    del qws, qzs, scs
+    nbytes, active = grouped_bytes(mw, r.offsets)
+    weight_bytes = qw.numel() * 4 + qz.numel() * 4 + sc.numel() * 2
+    S = max(1, min(64, int(np.ceil(3 * l2 / weight_bytes))))
+    sets = [(qw.clone(), qz.clone(), sc.clone(), torch.empty((A.shape[0], mw.N), dtype=A.dtype, device=dev))
+            for _ in range(S)]
+    del qw, qz, sc
+    n = max(S, (reps // S) * S)
+
+    def launch(i):
+        q, z, s_, c = sets[i % S]
+        g.gemm_grouped(A, offsets, q, z, s_, bits=mw.bits, group=mw.group, max_m=max_m, fmt=g.V2, out=c,
+                       stream=stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(2 * S):
+            launch(i)
+    stream.synchronize()
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr, stream=stream):
+        for i in range(n):
+            launch(i)
+    with torch.cuda.stream(stream):
+        gr.replay()
+        st, en = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        st.record(stream)
+        for _ in range(3):
+            gr.replay()
+        en.record(stream)
+    stream.synchronize()
+    ms = st.elapsed_time(en) / (3 * n)
+    del sets, gr
+    return ms, nbytes, active, int(r.offsets[-1]), max_m
+
+
 def run_sweep(g, torch, dev, stream, hbm_peak, bf16_peak, l2):
     rows = []
     for name, wl in gptq_inputs.WORKLOADS.items():
@@ -410,6 +469,16 @@ def run_sweep(g, torch, dev, stream, hbm_peak, bf16_peak, l2):
                        "TFLOP/s": round(tflops, 2), "tensor_frac": round(tflops / bf16_peak, 4)}
                 rows.append(row)
                 print(json.dumps(row), file=sys.stderr, flush=True)
+    for name, mw in gptq_inputs.MOE_WORKLOADS.items():
+        for T in mw.Ts:
+            ms, nbytes, active, nrows, max_m = time_grouped(g, torch, dev, stream, mw, T, l2)
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            row = {"workload": name, "M": T, "fmt": "v2 grouped", "rows": nrows, "experts_active": active,
+                   "max_m": max_m, "us": round(ms * 1e3, 3), "GB/s": round(gbs, 1),
+                   "hbm_frac": round(gbs / hbm_peak, 4),
+                   "TFLOP/s": round(2.0 * nrows * mw.N * mw.K / (ms * 1e-3) / 1e12, 2), "tensor_frac": None}
+            rows.append(row)
+            print(json.dumps(row), file=sys.stderr, flush=True)
     return rows
 
 
