@@ -270,7 +270,7 @@ def run_ours(args, rank, world, local_rank):
 
     # ---- secondary figure: M = 4096 prefill TFLOP/s
     prefill = run_prefill(g, torch, dev, stream, bf16_peak, peak_src, l2) if not args.skip_prefill else None
-    sweep = run_sweep(g, torch, dev, stream, hbm_peak, bf16_peak, l2) if args.all else None
+    sweep = run_sweep(g, torch, dev, stream, hbm_peak, bf16_peak, l2, args.sweep_filter) if args.all else None
     del sets
     torch.cuda.synchronize()
     assert g.device_status(stream) == 0, "device status word reported an error"
@@ -450,9 +450,11 @@ def time_grouped(g, torch, dev, stream, mw, T, l2, reps=200):
     return ms, nbytes, active, int(r.offsets[-1]), max_m
 
 
-def run_sweep(g, torch, dev, stream, hbm_peak, bf16_peak, l2):
+def run_sweep(g, torch, dev, stream, hbm_peak, bf16_peak, l2, only=""):
     rows = []
     for name, wl in gptq_inputs.WORKLOADS.items():
+        if only not in name:
+            continue
         variants = [(fmt, False) for fmt in wl.fmts]
         if wl.act_order:
             variants += [(fmt + "+prepacked", True) for fmt in wl.fmts]
@@ -470,6 +472,8 @@ def run_sweep(g, torch, dev, stream, hbm_peak, bf16_peak, l2):
                 rows.append(row)
                 print(json.dumps(row), file=sys.stderr, flush=True)
     for name, mw in gptq_inputs.MOE_WORKLOADS.items():
+        if only not in name:
+            continue
         for T in mw.Ts:
             ms, nbytes, active, nrows, max_m = time_grouped(g, torch, dev, stream, mw, T, l2)
             gbs = nbytes / (ms * 1e-3) / 1e9
@@ -566,6 +570,8 @@ def main():
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--all", action="store_true",
                     help="also time every workload and M (per-launch us, GB/s, TFLOP/s)")
+    ap.add_argument("--sweep-filter", default="",
+                    help="with --all: only the workloads whose name contains this string")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
 

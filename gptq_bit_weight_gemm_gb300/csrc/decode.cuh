@@ -6,7 +6,9 @@
 // 现", section "调整细节：根据格式选择处理方式": zeros[i] + zero_offset, zero_offset =
 // use_v2_format ? 0 : 1); the same page notes that the 2-bit GEMV case is slower than the
 // GEMM case and lists "improve gptq_gemm decode speed" as follow-up work.  Every weight is read
-// from HBM exactly once; the grid is (cluster of CS CTAs splitting K) x (slabs of 128 columns),
+// from HBM exactly once; the grid is (cluster of CS CTAs splitting K) x (slabs of 128 columns)
+// (x experts, for the grouped mixture-of-experts GEMM of page "4.3 Weight-only INT4 量化：GPTQ、
+// AWQ 与 Marlin Kernel", section 7),
 // partial sums meet through distributed shared memory in a fixed order (deterministic, no
 // workspace, no atomics), and launches use programmatic dependent launch so a kernel's prologue
 // overlaps the previous kernel's tail.
