@@ -86,6 +86,7 @@ __host__ __device__ constexpr int unit_words(int M, int NP) {
 // Staged weight chunks: the 128 columns of a slab are 4 TMA boxes of 32 columns (128 bytes per
 // row), each landing in its own 1024-byte aligned slot with the 128-byte swizzle -- the 16-byte
 // piece j of row r sits at piece j ^ (r % 8).  A warp reads its 32 columns from one slot.
+constexpr size_t kMaxCtaSmem = 227 * 1024;   // dynamic shared memory one CTA may opt into
 constexpr int kBoxCols = 32;
 constexpr int kBoxRowBytes = kBoxCols * 4;
 
@@ -866,7 +867,15 @@ cudaError_t launch_mma(const Problem& p, int cs, cudaStream_t stream) {
       break;
     }
   }
-  const TmaGeo geo = geo_for(cs);
+  TmaGeo geo = geo_for(cs);
+  // A layout that does not fit one CTA (a long K range with many tokens stages many activations):
+  // widen the split while every warp of a CTA keeps a k-tile of its own; beyond 16 CTAs nothing is
+  // launched and the caller takes another path.
+  while (TmaSmem<BITS>::bytes(geo, p.M) > kMaxCtaSmem && cs < 16 && a.units >= 4 * (2 * cs) * kWarps) {
+    cs *= 2;
+    geo = geo_for(cs);
+  }
+  if (TmaSmem<BITS>::bytes(geo, p.M) > kMaxCtaSmem) return cudaErrorInvalidConfiguration;
   if constexpr (MT == 8 && MX > 0) {
     // refills ahead: the runtime-count instantiation, whose warps refill independently, is faster
     // there (measured); the exact one wins when the whole slice is in flight

@@ -126,6 +126,9 @@ int device_ready(Problem* p) {
 
 int from_cuda(cudaError_t e) { return e == cudaSuccess ? GPTQ_OK : GPTQ_ERR_CUDA; }
 
+// decode-only paths: a layout that fits no CTA (nothing was launched) is a shape the call refuses
+int from_decode(cudaError_t e) { return e == cudaErrorInvalidConfiguration ? GPTQ_ERR_SHAPE : from_cuda(e); }
+
 }  // namespace
 
 bool encode_tensor_map(void* tmap, int dtype, void* base, const uint64_t* dims,
@@ -205,7 +208,12 @@ extern "C" int gptq_gemm(const void* A, int M, int K, int a_dtype, const int32_t
   p.zero_offset = fmt == GPTQ_FMT_V1 ? 1 : 0;
   p.out = C;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (M <= gptq::kDecodeMaxM) return gptq::from_cuda(gptq::launch_decode(p, s));
+  if (M <= gptq::kDecodeMaxM) {
+    const cudaError_t e = gptq::launch_decode(p, s);
+    // cudaErrorInvalidConfiguration: nothing launched, the decode layout does not fit this K at
+    // this M even split 16 ways; the tensor-core kernel takes the problem (any M)
+    if (e != cudaErrorInvalidConfiguration) return gptq::from_cuda(e);
+  }
   return gptq::from_cuda(gptq::launch_prefill(p, s));
 }
 
@@ -234,7 +242,7 @@ extern "C" int gptq_gemm_grouped(const void* A, int rows, int K, int a_dtype, co
   p.offsets = offsets;
   p.E = E;
   p.rows = rows;
-  return gptq::from_cuda(gptq::launch_decode_grouped(p, static_cast<cudaStream_t>(stream)));
+  return gptq::from_decode(gptq::launch_decode_grouped(p, static_cast<cudaStream_t>(stream)));
 }
 
 extern "C" size_t gptq_gemm_perm_workspace_size(int M, int K) {
@@ -277,7 +285,7 @@ extern "C" int gptq_gemm_perm(const void* A, int M, int K, int a_dtype, const in
     p.A = A;
     p.perm = perm;
   }
-  return gptq::from_cuda(gptq::launch_decode(p, s));
+  return gptq::from_decode(gptq::launch_decode(p, s));
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -345,7 +353,7 @@ extern "C" int gptq_gemm_perm_noalloc(const void* A, int M, int K, int a_dtype, 
     p.A = A;
     p.perm = perm;
   }
-  return gptq::from_cuda(gptq::launch_decode(p, s));
+  return gptq::from_decode(gptq::launch_decode(p, s));
 }
 
 extern "C" int gptq_prepack_act_order(const int32_t* qweight, const int32_t* g_idx, int K, int N,

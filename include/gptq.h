@@ -96,7 +96,9 @@ int gptq_dequant(const int32_t* qweight, const int32_t* qzeros, const void* scal
  * 方式"; fmt == GPTQ_FMT_V2 is use_v2_format = true).  Products are accumulated in fp32 and
  * C is rounded once to A's dtype.  M <= 32 runs the memory-bound decode kernel (TMA-streamed
  * weights, mma.sync from registers, split-K over a thread-block cluster reduced through
- * distributed shared memory); larger M runs the tcgen05 tensor-core kernel.
+ * distributed shared memory); larger M runs the tcgen05 tensor-core kernel, and so does M <= 32
+ * when K is so long that the decode kernel's staged activations fit no CTA even split 16 ways
+ * (K beyond 28672 with many tokens).
  * Device pointers: A, qweight, qzeros, scales, g_idx (nullable), C.  `workspace` may be NULL
  * when gptq_gemm_workspace_size() returns 0 (every current path); otherwise it must be a
  * device buffer of at least that many bytes, owned by the caller.
@@ -132,7 +134,9 @@ int gptq_prepack_act_order(const int32_t* qweight, const int32_t* g_idx, int K, 
  * GPTQ_ERR_SHAPE; gptq_gemm with g_idx serves that range).
  * Device pointers: A [M, K], perm [K] int32 (16-byte aligned; an entry outside [0, K) is
  * clamped, never read past A), qweight, qzeros, scales, C, workspace.
- * Returns GPTQ_OK or a negative gptq_status (GPTQ_ERR_WORKSPACE if the workspace is too small).
+ * Returns GPTQ_OK or a negative gptq_status (GPTQ_ERR_WORKSPACE if the workspace is too small;
+ * GPTQ_ERR_SHAPE, with nothing computed, if K is so long that the decode kernel's staged
+ * activations for M tokens fit no CTA even split 16 ways, which only K beyond 28672 reaches).
  */
 int gptq_gemm_perm(const void* A, int M, int K, int a_dtype, const int32_t* perm,
                    const int32_t* qweight, const int32_t* qzeros, const void* scales, int N,
@@ -162,7 +166,9 @@ size_t gptq_gemm_perm_workspace_size(int M, int K);
  * max_m (1..32) bounds every expert's row count; it selects the kernel's token tile.  An expert
  * whose range is decreasing, leaves [0, rows] or exceeds max_m is skipped and flagged with
  * GPTQ_DEV_EXPERT_ROWS.  No g_idx (act-order experts: prepack them, one gptq_gemm_perm each).
- * Returns GPTQ_OK (also for rows == 0 or E == 0, with no launch) or a negative gptq_status.
+ * Returns GPTQ_OK (also for rows == 0 or E == 0, with no launch) or a negative gptq_status
+ * (GPTQ_ERR_SHAPE, with nothing launched, if K is so long that max_m tokens' staged activations
+ * fit no CTA even split 16 ways: K beyond 28672).
  */
 int gptq_gemm_grouped(const void* A, int rows, int K, int a_dtype, const int32_t* offsets, int E,
                       int max_m, const int32_t* qweight, const int32_t* qzeros, const void* scales,

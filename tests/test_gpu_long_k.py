@@ -1,0 +1,73 @@
+"""GPU parity for long K at many tokens, where the decode kernels' staged activations outgrow one
+CTA's shared memory at the usual K split: the launcher widens the split (up to 16-CTA clusters),
+and where even that does not fit, gptq_gemm runs the tensor-core kernel while the decode-only
+calls (gptq_gemm_perm, gptq_gemm_grouped) refuse the shape with GPTQ_ERR_SHAPE.  Shapes follow the
+down projections of 70B- and 405B-class models (K = 28672, 53248) on a narrow column slice."""
+import numpy as np
+import pytest
+import torch
+
+import gptq_bit_weight_gemm_gb300 as g
+import gptq_inputs
+import oracle
+from helpers import assert_gemm_close, bits16
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+BASE = gptq_inputs.WORKLOADS["llama7b_decode_4bit_g128"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from gptq_bit_weight_gemm_gb300 import build as lib_build
+    lib_build.build()
+    assert torch.cuda.is_available()
+    yield
+    assert g.device_status() == 0
+
+
+def _checkpoint(K, N, bits, group):
+    import dataclasses
+    wl = dataclasses.replace(BASE.resized(K, N, (32,), name="long_k_%d_%d_b%d_g%d" % (K, N, bits, group)),
+                             bits=bits, group=group)
+    draw = gptq_inputs.draw_weights(wl)
+    return wl, oracle.make_checkpoint(draw.W, bits, group, None, False, oracle.V2)
+
+
+def _dev(ck):
+    return (torch.from_numpy(ck["qweight"]).to(DEV), torch.from_numpy(ck["qzeros"]).to(DEV),
+            torch.from_numpy(ck["scales"].view(np.int16)).view(torch.float16).to(DEV))
+
+
+@pytest.mark.parametrize("K,bits,group", [
+    (16384, 4, 32),      # the usual 8-way split would need 248 KB per CTA: widened to 16
+    (28672, 4, 128),     # 70B-class down projection
+    (28672, 8, 128),
+    (53248, 2, 128),     # 405B-class: no split fits, the tensor-core kernel runs
+])
+def test_gemm_long_k_many_tokens(K, bits, group):
+    N, M = 256, 32
+    wl, ck = _checkpoint(K, N, bits, group)
+    A = gptq_inputs.draw_activations(wl, M)
+    qw, qz, sc = _dev(ck)
+    C = g.gemm(A.to(DEV), qw, qz, sc, bits=bits, group=group, fmt=g.V2)
+    torch.cuda.synchronize()
+    Cref, B = oracle.gemm(bits16(A), oracle.F16, ck["qweight"], ck["qzeros"], ck["scales"], None, N, bits,
+                          group, oracle.V2)
+    assert_gemm_close(C.float().cpu().numpy(), Cref, B, "K=%d bits=%d group=%d" % (K, bits, group))
+
+
+def test_decode_only_calls_refuse_what_fits_no_cta():
+    K, N, M, bits, group = 53248, 256, 32, 2, 128
+    wl, ck = _checkpoint(K, N, bits, group)
+    A = gptq_inputs.draw_activations(wl, M).to(DEV)
+    qw, qz, sc = _dev(ck)
+    perm = torch.arange(K, dtype=torch.int32, device=DEV)
+    with pytest.raises(g.GPTQError) as e:
+        g.gemm_perm(A, perm, qw, qz, sc, bits=bits, group=group)
+    assert e.value.code == -2
+    offsets = torch.tensor([0, M], dtype=torch.int32, device=DEV)
+    with pytest.raises(g.GPTQError) as e:
+        g.gemm_grouped(A, offsets, qw[None], qz[None], sc[None], bits=bits, group=group, max_m=M)
+    assert e.value.code == -2
