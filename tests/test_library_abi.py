@@ -2,6 +2,9 @@
 paths (argument validation, the v1 -> v2 zero repack, error strings) behave as documented.
 No compute call is made here: these tests run without a GPU."""
 import ctypes
+import os
+import shutil
+import subprocess
 
 import numpy as np
 import pytest
@@ -9,6 +12,8 @@ import pytest
 import gptq_bit_weight_gemm_gb300 as g
 import oracle
 from gptq_bit_weight_gemm_gb300 import build as lib_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 @pytest.fixture(scope="module")
@@ -197,3 +202,43 @@ def test_product_does_not_import_oracle():
                 text = open(os.path.join(root, f)).read()
                 assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), f
                 assert "gptq_oracle" not in text, f
+
+
+C_CONSUMER = r"""
+#include <stdio.h>
+#include <string.h>
+#include "gptq.h"
+
+int main(void) {
+  int32_t qz[2][8];
+  int rc, i;
+  /* host-only entry points, called from plain C */
+  for (i = 0; i < 8; ++i) qz[0][i] = 0x11111111;          /* 4-bit v1 zeros 1..1 */
+  rc = gptq_repack_zeros_v1_to_v2(qz[0], qz[1], 1, 64, 4);
+  if (rc != GPTQ_OK || qz[1][0] != 0x22222222) { printf("repack %d %x\n", rc, qz[1][0]); return 1; }
+  /* validation happens before any device work */
+  if (gptq_gemm(NULL, 1, 256, GPTQ_F16, NULL, NULL, NULL, NULL, 256, 4, 128, GPTQ_FMT_V2, NULL, NULL, 0,
+                NULL) != GPTQ_ERR_ARG) return 2;
+  if (gptq_gemm_grouped(NULL, 0, 256, GPTQ_F16, NULL, 1, 8, NULL, NULL, NULL, 256, 4, 128,
+                        GPTQ_FMT_V2, NULL, NULL) != GPTQ_ERR_ARG) return 3;
+  if (gptq_gemm_workspace_size(1, 4096, 11008, 4, 128) != 0) return 4;
+  if (strlen(gptq_strerror(GPTQ_ERR_SHAPE)) == 0) return 5;
+  printf("c consumer ok\n");
+  return 0;
+}
+"""
+
+
+@pytest.mark.skipif(shutil.which("gcc") is None, reason="needs gcc")
+def test_header_is_plain_c_and_links(lib, tmp_path):
+    """The boundary is a C ABI: a C99 program (no C++ compiler) includes include/gptq.h, links the
+    built library and calls its host entry points and argument checks."""
+    src = tmp_path / "consumer.c"
+    src.write_text(C_CONSUMER)
+    exe = tmp_path / "consumer"
+    libdir = os.path.dirname(g.LIB_PATH)
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), str(src),
+                    "-o", str(exe), "-L", libdir, "-l:" + os.path.basename(g.LIB_PATH),
+                    "-Wl,-rpath," + libdir], check=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0 and "c consumer ok" in r.stdout, (r.returncode, r.stdout, r.stderr)
