@@ -72,7 +72,7 @@ def _compare(mw, fmt, A, offsets, C, ck, skip=()):
         if e in skip or hi <= lo:
             continue
         owned[lo:hi] = True
-        assert_gemm_close(C[lo:hi].float().cpu().numpy(), Cref[lo:hi], B[lo:hi],
+        assert_gemm_close(C[lo:hi], Cref[lo:hi], B[lo:hi],
                           "%s %s expert %d rows %d..%d" % (mw.name, fmt, e, lo, hi))
     assert np.all(got[~owned] == sentinel), "rows outside every expert's range were written"
 

@@ -55,7 +55,26 @@ def test_gemm_long_k_many_tokens(K, bits, group):
     torch.cuda.synchronize()
     Cref, B = oracle.gemm(bits16(A), oracle.F16, ck["qweight"], ck["qzeros"], ck["scales"], None, N, bits,
                           group, oracle.V2)
-    assert_gemm_close(C.float().cpu().numpy(), Cref, B, "K=%d bits=%d group=%d" % (K, bits, group))
+    assert_gemm_close(C, Cref, B, "K=%d bits=%d group=%d" % (K, bits, group))
+
+
+def test_gemm_long_k_act_order_on_the_tensor_core_fallback():
+    """K = 53248 at 32 tokens fits no decode layout, so gptq_gemm runs the tensor-core kernel; with
+    act-order its per-k group lookup (g_idx) must match the oracle too."""
+    K, N, M, bits, group = 53248, 256, 32, 4, 128
+    import dataclasses
+    wl = dataclasses.replace(BASE.resized(K, N, (M,), name="long_k_act"), bits=bits, group=group,
+                             act_order=True)
+    draw = gptq_inputs.draw_weights(wl)
+    ck = oracle.make_checkpoint(draw.W, bits, group, draw.g_idx, False, oracle.V2)
+    A = gptq_inputs.draw_activations(wl, M)
+    qw, qz, sc = _dev(ck)
+    C = g.gemm(A.to(DEV), qw, qz, sc, torch.from_numpy(ck["g_idx"]).to(DEV), bits=bits, group=group,
+               fmt=g.V2)
+    torch.cuda.synchronize()
+    Cref, B = oracle.gemm(bits16(A), oracle.F16, ck["qweight"], ck["qzeros"], ck["scales"], ck["g_idx"], N,
+                          bits, group, oracle.V2)
+    assert_gemm_close(C, Cref, B, "K=%d act-order" % K)
 
 
 def test_decode_only_calls_refuse_what_fits_no_cta():
