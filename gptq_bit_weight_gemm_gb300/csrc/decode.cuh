@@ -194,22 +194,21 @@ inline int choose_cluster(const Problem& p, int per_unit) {
 }
 
 template <int BITS, int MT, int MX, typename T, bool FOLD, bool GROUPED>
-cudaError_t launch_mma(const Problem& p, int cs, cudaStream_t stream);
+cudaError_t launch_mma(const Problem& p, cudaStream_t stream);
 
 // MT: token block bound (1, 8, 16, 32); MX: the exact token count when it is MT (0 = read at run
 // time), so the common batch sizes run with every token loop sized at compile time.  GROUPED:
 // one weight per expert (blockIdx.z), each with its own rows of A and C.
 template <int BITS, int MT, int MX, typename T, bool GROUPED = false>
 cudaError_t launch_mt(const Problem& p, cudaStream_t stream) {
-  const int cs = choose_cluster(p, Pack<BITS>::kPerUnit);
   constexpr bool kHas16 = (BITS == 2 || BITS == 4 ||
                            ((BITS == 8 || BITS == 3) && std::is_same<T, __half>::value));
   // the scale folds per group when groups align with k-tiles (4 units)
   const bool fold = kHas16 && p.g_idx == nullptr && (p.group % (4 * Pack<BITS>::kPerUnit)) == 0;
   if constexpr (kHas16) {
-    if (fold) return launch_mma<BITS, MT, MX, T, true, GROUPED>(p, cs, stream);
+    if (fold) return launch_mma<BITS, MT, MX, T, true, GROUPED>(p, stream);
   }
-  return launch_mma<BITS, MT, MX, T, false, GROUPED>(p, cs, stream);
+  return launch_mma<BITS, MT, MX, T, false, GROUPED>(p, stream);
 }
 
 // Every M <= 32 runs the tensor-core decode kernel (token blocks of 8; one token has an

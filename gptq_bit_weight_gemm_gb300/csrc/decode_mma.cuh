@@ -18,20 +18,20 @@
 // thread t's word as the k-slots (2t, 2t+1) and (2t+8, 2t+9) -- and the activations are staged
 // in the same pairing, which makes them exactly the B fragment.
 //
-//  * FOLD (groups aligned to k-tiles, no act-order, 2/4/8-bit): A = the raw code as a 16-bit
-//    float kMagic + 2^shift q (masks only, CodePairs), B = the activation times 2^-shift, a fresh
-//    fp32 accumulator R per group; at the group end
-//      acc += scale * (R - kMagic * T) - scale * zero * Q,
-//    with T = sum_k b_k and Q = sum_k 2^shift b_k per group and token, summed once from the
-//    staged activations.  Tiles go in blocks of 4 inside one chunk and one group.
+//  * FOLD (groups aligned to k-tiles, no act-order, 2/4/8-bit and fp16 3-bit): A = the exact
+//    difference q - zero as a 16-bit float (masks into the mantissa of a magic number, then one
+//    sub or fma with a per-group constant, DiffPairs), B = the activations, a fresh fp32
+//    accumulator R per group; at the group end acc += scale * R.  A group whose codes all equal
+//    its zero contributes exactly 0, whatever the scale and the activations.  Tiles go in blocks
+//    of 4 inside one chunk and one group.
 //  * FULL (act-order, 3-bit, unaligned groups): A = RN((q - zero) * scale) per weight (exact
 //    fp32 product, one rounding), accumulated across groups.
 //
 // Cost model that shaped it (measured on GB300): a k-tile of 4 packed words per warp costs the
 // dispatch of its integer-pipe ops (16 lanes, 2 cycles each), its mma.sync (about 8 cycles per
 // m16n8k16 per SM sub-partition) and its fp16 ops, added rather than overlapped; the raw-code
-// unpack (4 masks + 1 shift per 4-bit word) and the per-group constants staged in shared
-// memory keep the count per word low.
+// unpack (4 masks + 1 shift + 4 fp16 sub/fma per 4-bit word) and the per-group constants staged
+// in shared memory keep the count per word low.
 #pragma once
 
 #include <cuda.h>
@@ -109,9 +109,9 @@ struct TmaGeo {
 };
 
 // Shared memory of one CTA: [alignment pad][weight chunk buffers][activation pairs | partial
-// sums, several tokens (aliased in time)][receive slots][per group and column: scale, scale * zero][per group
-// and token: kMagic * sum b, sum 2^shift b][FULL: per group and column scale and zero, per k
-// its group][mbarriers, flags].
+// sums, several tokens (aliased in time)][receive slots][FOLD: per group and column, the scale
+// bits and the runtime zero][FULL: per group and column scale and zero, per k its group]
+// [mbarriers, flags].
 // Activations, partial sums and receive slots are sized by the real token count M, not by the
 // MMA token block.
 template <int BITS>
@@ -129,11 +129,8 @@ struct TmaSmem {
   __host__ __device__ static size_t off_gconst(const TmaGeo& g, int M) {
     return off_recv(g, M) + static_cast<size_t>(M) * kSlab * 4;
   }
-  __host__ __device__ static size_t off_sums(const TmaGeo& g, int M) {
-    return off_gconst(g, M) + static_cast<size_t>(g.max_groups) * kSlab * 8;
-  }
   __host__ __device__ static size_t off_full(const TmaGeo& g, int M) {
-    return (off_sums(g, M) + static_cast<size_t>(g.max_groups) * M * 8 + 15) & ~static_cast<size_t>(15);
+    return off_gconst(g, M) + static_cast<size_t>(g.max_groups) * kSlab * 4;
   }
   // FULL staging: (scale bits | zero << 16) per group and column, then a group index per k
   __host__ __device__ static size_t full_bytes(const TmaGeo& g) {
@@ -171,6 +168,8 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
   using P = Pack<BITS>;
   using MP = MmaPairs<BITS>;
   using SM = TmaSmem<BITS>;
+  // the exact-difference unpack of the FOLD path (any valid instantiation where FOLD is off)
+  using DP = DiffPairs<typename std::conditional<FOLD, T, __half>::type, FOLD ? BITS : 4>;
   constexpr int PER = P::kPerUnit;
   constexpr int ROWS = P::kRowsPerUnit;
   constexpr int NP = MP::kPairs;
@@ -229,9 +228,7 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
   uint8_t* sbuf = smem;                                               // weight chunks
   uint32_t* sB = reinterpret_cast<uint32_t*>(smem + SM::off_stage(geo));
   float* recv = reinterpret_cast<float*>(smem + SM::off_recv(geo, Mtok));
-  float2* sK = reinterpret_cast<float2*>(smem + SM::off_gconst(geo, Mtok));   // [group][column]
-  float* sT = reinterpret_cast<float*>(smem + SM::off_sums(geo, Mtok));       // [group][M]
-  float* sQ = sT + geo.max_groups * Mtok;                                      // [group][M]
+  uint32_t* sK = reinterpret_cast<uint32_t*>(smem + SM::off_gconst(geo, Mtok));   // [group][word][column]
   uint32_t* sSZ = reinterpret_cast<uint32_t*>(smem + SM::off_full(geo, Mtok));  // [group][column]
   uint16_t* sG = reinterpret_cast<uint16_t*>(sSZ + geo.full_groups * kSlab);    // [k of the range]
   uint8_t* misc = smem + SM::off_misc(geo, Mtok);
@@ -245,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
 
   // Scales and zeros of the groups this range touches (FOLD): their loads go out first, ahead
   // of the weight stream (behind it they would wait for the whole slice), and land in shared
-  // memory as (scale, scale * zero) per group and column.
+  // memory per group and column as (scale bits | runtime zero << 16).
   const int g_lo = (cu0 * PER) / a.group;
   const int g_end = (ct1 * 4 * PER - 1) / a.group;
   const int ngrp = ntile > 0 ? (g_end < a.G - 1 ? g_end : a.G - 1) - g_lo + 1 : 0;
@@ -271,17 +268,13 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
     for (int j = 0; j < kGB; ++j) {
       const int i = base + j * kThreads + static_cast<int>(threadIdx.x);
       if (i < ngrp * 32) {
-        float2 v[4];
+        uint32_t w[4];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          const uint16_t h = c & 1 ? hi16(c < 2 ? gsv[j].x : gsv[j].y) : lo16(c < 2 ? gsv[j].x : gsv[j].y);
-          const float sc = __half2float(__ushort_as_half(h));
-          const int z = static_cast<int>((gzf[j] >> (BITS * c)) & P::kMask) + a.zero_offset;
-          v[c] = make_float2(sc, sc * static_cast<float>(z));
+          const uint32_t h = c & 1 ? hi16(c < 2 ? gsv[j].x : gsv[j].y) : lo16(c < 2 ? gsv[j].x : gsv[j].y);
+          w[c] = h | ((((gzf[j] >> (BITS * c)) & P::kMask) + a.zero_offset) << 16);
         }
-        float4* dst = reinterpret_cast<float4*>(sK + (i >> 5) * kSlab + 4 * (i & 31));
-        dst[0] = make_float4(v[0].x, v[0].y, v[1].x, v[1].y);
-        dst[1] = make_float4(v[2].x, v[2].y, v[3].x, v[3].y);
+        *reinterpret_cast<uint4*>(sK + (i >> 5) * kSlab + 4 * (i & 31)) = make_uint4(w[0], w[1], w[2], w[3]);
       }
     }
   };
@@ -382,65 +375,13 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
   }
   pdl_wait();
 
-  // Stage activations: sB[u][m][p] = (a[m][k0 + lo_k(p)], a[m][k0 + hi_k(p)]), zero past K or M
-  // (FOLD: times 2^-shift(p), matching the raw codes of CodePairs).
+  // Stage activations: sB[u][m][p] = (a[m][k0 + lo_k(p)], a[m][k0 + hi_k(p)]), zero past K or M.
   const uint16_t* A16 = static_cast<const uint16_t*>(a.A);
   const int nunits = ntile * 4;
   stage_pairs<PER, NP>(A16, a.perm, Mtok, a.K, cu0, nunits, a.units,
                        [](int p) { return MP::lo_k(p); }, [](int p) { return MP::hi_k(p); },
-                       [&](int uu, int m, int p, uint32_t v) {
-                         if constexpr (FOLD)
-                           v = scale_pow2_pair(v, CodePairs<T, BITS>::shift_lo(p), CodePairs<T, BITS>::shift_hi(p), T());
-                         sB[uu * UW + m * NP + p] = v;
-                       });
+                       [&](int uu, int m, int p, uint32_t v) { sB[uu * UW + m * NP + p] = v; });
   __syncthreads();
-  if constexpr (FOLD) {
-    // Per group and token: kMagic * T and Q, with T = sum_k b_k and Q = sum_k 2^shift b_k over
-    // the staged activations (the two corrections of the raw-code MMA).  One warp per group;
-    // the lanes of a token split its pairs and meet in a fixed shuffle order (deterministic).
-    using CP = CodePairs<T, BITS>;
-    const int upg = a.group / PER;
-    const int lps = Mtok <= 1 ? 5 : Mtok <= 2 ? 4 : Mtok <= 4 ? 3 : Mtok <= 8 ? 2 : Mtok <= 16 ? 1 : 0;
-    const int m = lane >> lps, sub = lane & ((1 << lps) - 1);
-    for (int gi = warp; gi < ngrp; gi += kWarps) {
-      int u_lo = (g_lo + gi) * upg - cu0, u_hi = u_lo + upg;
-      u_lo = u_lo < 0 ? 0 : u_lo;
-      u_hi = u_hi > nunits ? nunits : u_hi;
-      float t = 0.f, q = 0.f;
-      if (m < Mtok) {
-        for (int uu = u_lo + sub; uu < u_hi; uu += (1 << lps)) {
-          uint32_t v[NP];
-          const uint32_t* src = sB + uu * UW + m * NP;
-          if constexpr (NP % 4 == 0) {
-#pragma unroll
-            for (int i = 0; i < NP / 4; ++i) {
-              const uint4 x = reinterpret_cast<const uint4*>(src)[i];
-              v[4 * i] = x.x; v[4 * i + 1] = x.y; v[4 * i + 2] = x.z; v[4 * i + 3] = x.w;
-            }
-          } else {
-            const uint2 x = reinterpret_cast<const uint2*>(src)[0];
-            v[0] = x.x; v[1] = x.y;
-          }
-#pragma unroll
-          for (int pp = 0; pp < NP; ++pp) {
-            const float fl = F16Traits<T>::to_f32(F16Traits<T>::from_bits(lo16(v[pp])));
-            const float fh = F16Traits<T>::to_f32(F16Traits<T>::from_bits(hi16(v[pp])));
-            t += fl + fh;
-            q = fmaf(fl, static_cast<float>(1 << CP::shift_lo(pp)), fmaf(fh, static_cast<float>(1 << CP::shift_hi(pp)), q));
-          }
-        }
-      }
-      for (int o = (1 << lps) >> 1; o > 0; o >>= 1) {
-        t += __shfl_xor_sync(0xFFFFFFFFu, t, o);
-        q += __shfl_xor_sync(0xFFFFFFFFu, q, o);
-      }
-      if (sub == 0 && m < Mtok) {
-        sT[gi * Mtok + m] = CP::kMagic * t;
-        sQ[gi * Mtok + m] = q;
-      }
-    }
-    __syncthreads();
-  }
 
   float acc[2][NB][4];
 #pragma unroll
@@ -479,14 +420,24 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
   };
 
   if constexpr (FOLD) {
-    using CP = CodePairs<T, BITS>;
-    static_assert(CP::kPairs == NP, "pairing must match the activation staging");
-    // Raw-code MMAs into a per-group accumulator cg; at each group end
-    //   acc += scale * (cg - kMagic T) - scale * zero * Q.
+    static_assert(DP::kPairs == NP, "pairing must match the activation staging");
+    // MMAs of exact (q - zero) pairs into a per-group accumulator cg; at each group end
+    //   acc += scale * cg.
     // Tiles go in blocks of 4 where a block stays inside one chunk and one group (shared-memory
     // offsets then are immediates); absent tokens read token M-1's activations (their outputs
     // are never stored).
     float cg[2][NB][4];
+    float gs[4];                                       // the current group's scales (4 columns)
+    uint32_t gk[4][DP::kConsts];                       // and the unpack constants of its zeros
+    auto load_group = [&](int gi) {
+      const uint4 v = *reinterpret_cast<const uint4*>(sK + gi * kSlab + col0);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint32_t e = (&v.x)[c];
+        gs[c] = __half2float(__ushort_as_half(lo16(e)));
+        DP::consts(static_cast<int>(e >> 16), gk[c]);
+      }
+    };
     auto clear_cg = [&]() {
 #pragma unroll
       for (int t = 0; t < 2; ++t)
@@ -495,25 +446,13 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
 #pragma unroll
           for (int i = 0; i < 4; ++i) cg[t][nb][i] = 0.f;
     };
-    auto fold = [&](int gi) {
-      const float4 k01 = *reinterpret_cast<const float4*>(sK + gi * kSlab + col0);
-      const float4 k23 = *reinterpret_cast<const float4*>(sK + gi * kSlab + col0 + 2);
-      const float ks[4] = {k01.x, k01.z, k23.x, k23.z}, kz[4] = {k01.y, k01.w, k23.y, k23.w};
+    auto fold = [&]() {
 #pragma unroll
-      for (int nb = 0; nb < NB; ++nb)
+      for (int t = 0; t < 2; ++t)
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          int m = nb * 8 + 2 * tq + h;
-          m = m < Mtok ? m : Mtok - 1;
-          const float mt = sT[gi * Mtok + m], q = sQ[gi * Mtok + m];
+        for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
-          for (int t = 0; t < 2; ++t)
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-              const int i = 2 * r + h, c = 2 * t + r;
-              acc[t][nb][i] = fmaf(-kz[c], q, fmaf(ks[c], cg[t][nb][i] - mt, acc[t][nb][i]));
-            }
-        }
+          for (int i = 0; i < 4; ++i) acc[t][nb][i] = fmaf(gs[2 * t + (i >> 1)], cg[t][nb][i], acc[t][nb][i]);
     };
     int boff[NB];                                      // word offset of this thread's tokens
 #pragma unroll
@@ -540,8 +479,8 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
       for (int t = 0; t < 2; ++t) {
         uint32_t d0[NP], d1[NP];
         if constexpr (BITS == 3) {
-          CP::run3((&wv[0].x)[2 * t], (&wv[1].x)[2 * t], (&wv[2].x)[2 * t], d0);
-          CP::run3((&wv[0].x)[2 * t + 1], (&wv[1].x)[2 * t + 1], (&wv[2].x)[2 * t + 1], d1);
+          DP::run3((&wv[0].x)[2 * t], (&wv[1].x)[2 * t], (&wv[2].x)[2 * t], gk[2 * t], d0);
+          DP::run3((&wv[0].x)[2 * t + 1], (&wv[1].x)[2 * t + 1], (&wv[2].x)[2 * t + 1], gk[2 * t + 1], d1);
         }
 #pragma unroll
         for (int j = 0; j < NP / 2; ++j)
@@ -571,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
       uint32_t d[4][NP];
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
-        if constexpr (BITS != 3) CP::run((&wv.x)[cc], d[cc]);
+        if constexpr (BITS != 3) DP::run((&wv.x)[cc], gk[cc], d[cc]);
       }
 #pragma unroll
       for (int j = 0; j < NP / 2; ++j)
@@ -590,6 +529,7 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
     const uint8_t* wo = wslot;
     const uint8_t* cslot = wslot;                      // this warp's box slot of the chunk
     clear_cg();
+    if (ntile > 0) load_group(0);
     for (int kt = 0; kt < ntile;) {                    // control flow is uniform over the CTA
       if (kt == chunk_end) {
         if (c >= 0 && c + geo.nbuf < nchunk) refill(c + geo.nbuf);   // the buffer just consumed
@@ -621,14 +561,15 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
       }
       dirty = true;
       if (kt == g_end_kt) {
-        fold(gi);
+        fold();
         clear_cg();
         dirty = false;
         ++gi;
         g_end_kt += tpg;
+        if (kt < ntile) load_group(gi);
       }
     }
-    if (dirty) fold(gi);
+    if (dirty) fold();
   } else {
     for (int c = 0; c < nchunk; ++c) {
       const bool ok = __all_sync(0xFFFFFFFFu, tma_wait(bar(bw, c % geo.nbuf), (c / geo.nbuf) & 1, abort_flag, a.status));
@@ -820,8 +761,56 @@ TmaGeo make_geo(int units, int cs, int M, int group, int ctas, int sm_count, int
   return g;
 }
 
+// The launch geometry of one decode call: the cluster size (K split) and the shared-memory layout.
+// `regs` is the kernel's register count (it bounds the CTAs per SM), `E` the experts side by
+// side in the grid (1 for a single weight).  Host code only; the launcher and the host-side
+// geometry tests both call it.
+struct GeoChoice {
+  int cs;
+  TmaGeo geo;
+  bool fits;          // false: the layout fits no CTA even split 16 ways; nothing may launch
+};
+
+template <int BITS>
+GeoChoice select_geometry(const Problem& p, bool fold, int regs, int sms, int E) {
+  const int units = p.K / Pack<BITS>::kPerUnit;
+  const int slabs = (p.N + kSlab - 1) / kSlab;
+  const int by_regs = regs > 0 ? 65536 / (((regs + 7) & ~7) * kThreads) : 5;
+  const int max_per_sm = by_regs < 1 ? 1 : (by_regs > 5 ? 5 : by_regs);
+  // FOLD: one wave when it can be had -- the largest K split (at most the chosen one) whose grid
+  // is resident at once; halving stops where a CTA's shared memory would no longer fit (a
+  // smaller split stages more activations), and the chosen split stays when no split gives one
+  // wave.  FULL keeps the chosen split: it is latency-bound and gains from every extra CTA.
+  auto geo_for = [&](int c) {
+    return make_geo<BITS>(units, c, p.M, p.group, slabs * c * E, sms, max_per_sm, !fold, p.g_idx != nullptr,
+                          p.G);
+  };
+  // A 16-CTA cluster is used only when it gives one wave; otherwise (and for FULL) at most 8.
+  const int cs0 = choose_cluster(p, Pack<BITS>::kPerUnit);
+  int cs = cs0 < 8 ? cs0 : 8;
+  for (int c = cs0; fold && c >= 1; c /= 2) {
+    const size_t bytes = (TmaSmem<BITS>::bytes(geo_for(c), p.M) + 1023) & ~static_cast<size_t>(1023);
+    if (bytes > 227 * 1024) break;
+    int per_sm = static_cast<int>(233472 / (bytes + 1024));
+    per_sm = per_sm < max_per_sm ? per_sm : max_per_sm;
+    if (static_cast<long long>(slabs) * c * E <= static_cast<long long>(per_sm) * sms) {
+      cs = c;
+      break;
+    }
+  }
+  TmaGeo geo = geo_for(cs);
+  // A layout that does not fit one CTA (a long K range with many tokens stages many activations):
+  // widen the split while every warp of a CTA keeps a k-tile of its own; beyond 16 CTAs nothing is
+  // launched and the caller takes another path.
+  while (TmaSmem<BITS>::bytes(geo, p.M) > kMaxCtaSmem && cs < 16 && units >= 4 * (2 * cs) * kWarps) {
+    cs *= 2;
+    geo = geo_for(cs);
+  }
+  return GeoChoice{cs, geo, TmaSmem<BITS>::bytes(geo, p.M) <= kMaxCtaSmem};
+}
+
 template <int BITS, int MT, int MX, typename T, bool FOLD, bool GROUPED>
-cudaError_t launch_mma(const Problem& p, int cs, cudaStream_t stream) {
+cudaError_t launch_mma(const Problem& p, cudaStream_t stream) {
   Args a;
   a.A = p.A; a.M = p.M; a.K = p.K; a.N = p.N;
   a.qweight = p.qweight; a.qzeros = p.qzeros;
@@ -844,43 +833,15 @@ cudaError_t launch_mma(const Problem& p, int cs, cudaStream_t stream) {
     regs = cudaFuncGetAttributes(&fa, kern) == cudaSuccess ? fa.numRegs : 0;
     regs_cache.store(regs, std::memory_order_relaxed);
   }
-  const int by_regs = regs > 0 ? 65536 / (((regs + 7) & ~7) * kThreads) : 5;
-  const int max_per_sm = by_regs < 1 ? 1 : (by_regs > 5 ? 5 : by_regs);
-  // FOLD: one wave when it can be had -- the largest K split (at most the chosen one) whose grid
-  // is resident at once; halving stops where a CTA's shared memory would no longer fit (a
-  // smaller split stages more activations), and the chosen split stays when no split gives one
-  // wave.  FULL keeps the chosen split: it is latency-bound and gains from every extra CTA.
-  auto geo_for = [&](int c) {
-    return make_geo<BITS>(a.units, c, p.M, p.group, slabs * c * E, sms, max_per_sm, !FOLD, p.g_idx != nullptr,
-                          p.G);
-  };
-  // A 16-CTA cluster is used only when it gives one wave; otherwise (and for FULL) at most 8.
-  const int cs0 = cs;
-  cs = cs0 < 8 ? cs0 : 8;
-  for (int c = cs0; FOLD && c >= 1; c /= 2) {
-    const size_t bytes = (TmaSmem<BITS>::bytes(geo_for(c), p.M) + 1023) & ~static_cast<size_t>(1023);
-    if (bytes > 227 * 1024) break;
-    int per_sm = static_cast<int>(233472 / (bytes + 1024));
-    per_sm = per_sm < max_per_sm ? per_sm : max_per_sm;
-    if (static_cast<long long>(slabs) * c * E <= static_cast<long long>(per_sm) * sms) {
-      cs = c;
-      break;
-    }
-  }
-  TmaGeo geo = geo_for(cs);
-  // A layout that does not fit one CTA (a long K range with many tokens stages many activations):
-  // widen the split while every warp of a CTA keeps a k-tile of its own; beyond 16 CTAs nothing is
-  // launched and the caller takes another path.
-  while (TmaSmem<BITS>::bytes(geo, p.M) > kMaxCtaSmem && cs < 16 && a.units >= 4 * (2 * cs) * kWarps) {
-    cs *= 2;
-    geo = geo_for(cs);
-  }
-  if (TmaSmem<BITS>::bytes(geo, p.M) > kMaxCtaSmem) return cudaErrorInvalidConfiguration;
+  const GeoChoice choice = select_geometry<BITS>(p, FOLD, regs, sms, E);
+  if (!choice.fits) return cudaErrorInvalidConfiguration;
+  const int cs = choice.cs;
+  const TmaGeo geo = choice.geo;
   if constexpr (MT == 8 && MX > 0) {
     // refills ahead: the runtime-count instantiation, whose warps refill independently, is faster
     // there (measured); the exact one wins when the whole slice is in flight
     const int chunks = (geo.tiles_per_cta + geo.chunk_tiles - 1) / geo.chunk_tiles;
-    if (geo.nbuf < chunks) return launch_mma<BITS, MT, 0, T, FOLD, GROUPED>(p, cs0, stream);
+    if (geo.nbuf < chunks) return launch_mma<BITS, MT, 0, T, FOLD, GROUPED>(p, stream);
   }
   CUtensorMap tmW;
   {

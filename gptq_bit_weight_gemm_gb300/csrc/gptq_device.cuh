@@ -414,6 +414,36 @@ struct CodePairs<__half, 3> {
   }
 };
 
+// 3-bit, fp16, exact q - z in the pairing of CodePairs<__half, 3>: one fma per pair turns the
+// raw pair (1024 + 2^slo q_lo, 1024 + 2^shi q_hi) into (q_lo, q_hi) -- the product by
+// (2^-slo, 2^-shi) and the sum with -(1024 2^-slo, 1024 2^-shi) are exact, so one rounding of an
+// exact small integer -- and one sub takes the zero (consts(): z in both halves).
+template <>
+struct DiffPairs<__half, 3> {
+  static constexpr int kPairs = 16, kConsts = 1;
+  __host__ __device__ static constexpr int lo_k(int p) { return CodePairs<__half, 3>::lo_k(p); }
+  __host__ __device__ static constexpr int hi_k(int p) { return CodePairs<__half, 3>::hi_k(p); }
+  __device__ static __forceinline__ void consts(int z, uint32_t (&k)[kConsts]) {
+    const uint32_t h = __half_as_ushort(__int2half_rn(z));   // an integer in [0, 8]: exact
+    k[0] = h * 0x00010001u;
+  }
+  __device__ static __forceinline__ void run3(uint32_t w0, uint32_t w1, uint32_t w2,
+                                              const uint32_t (&k)[kConsts], uint32_t (&d)[kPairs]) {
+    CodePairs<__half, 3>::run3(w0, w1, w2, d);
+#pragma unroll
+    for (int p = 0; p < kPairs; ++p) {
+      constexpr int kExpBias = 15;
+      const int slo = CodePairs<__half, 3>::shift_lo(p), shi = CodePairs<__half, 3>::shift_hi(p);
+      // fp16 bit patterns of 2^-s and of -1024 * 2^-s (exponent fields 15 - s and 25 - s)
+      const uint32_t mult = static_cast<uint32_t>((kExpBias - slo) << 10) |
+                            (static_cast<uint32_t>((kExpBias - shi) << 10) << 16);
+      const uint32_t neg = (0x8000u | static_cast<uint32_t>((kExpBias + 10 - slo) << 10)) |
+                           ((0x8000u | static_cast<uint32_t>((kExpBias + 10 - shi) << 10)) << 16);
+      d[p] = sub2(fma2(d[p], mult, neg, __half()), k[0], __half());
+    }
+  }
+};
+
 // A 16-bit pair times (2^-slo, 2^-shi) (exact unless a result is subnormal, where it rounds).
 __device__ __forceinline__ uint32_t scale_pow2_pair(uint32_t v, int slo, int shi, __half) {
   if (slo == 0 && shi == 0) return v;
