@@ -170,14 +170,21 @@ def dequant(qweight, qzeros, scales, g_idx=None, *, K, bits, group, fmt=V2, dtyp
     return out
 
 
-def quantize_rtn(W, *, bits, group, g_idx=None, sym=False, fmt=V2, stream=None):
-    """Round-to-nearest checkpoint of fp32 weights W [K, N]: (qweight, qzeros, scales)."""
+def quantize_rtn(W, *, bits, group, g_idx=None, sym=False, fmt=V2, out=None, stream=None):
+    """Round-to-nearest checkpoint of fp32 weights W [K, N]: (qweight, qzeros, scales), written
+    into `out` = (qweight, qzeros, scales) when given."""
     torch = _torch()
     K, N = W.shape
     G = 1 if group == -1 else K // group
-    qweight = torch.empty((K * bits // 32, N), dtype=torch.int32, device=W.device)
-    qzeros = torch.empty((G, N * bits // 32), dtype=torch.int32, device=W.device)
-    scales = torch.empty((G, N), dtype=torch.float16, device=W.device)
+    if out is not None:
+        qweight, qzeros, scales = out
+    else:
+        qweight = torch.empty((K * bits // 32, N), dtype=torch.int32, device=W.device)
+        qzeros = torch.empty((G, N * bits // 32), dtype=torch.int32, device=W.device)
+        scales = torch.empty((G, N), dtype=torch.float16, device=W.device)
+    if (tuple(qweight.shape) != (K * bits // 32, N) or tuple(qzeros.shape) != (G, N * bits // 32)
+            or tuple(scales.shape) != (G, N)):
+        raise ValueError("quantize_rtn: output buffers of the wrong shape")
     rc = lib().gptq_quantize_rtn(_ptr(W, torch.float32, "W"), K, N, bits, group,
                                  _ptr(g_idx, torch.int32, "g_idx"), int(bool(sym)), fmt,
                                  _ptr(qweight), _ptr(qzeros), _ptr(scales), _stream(stream))

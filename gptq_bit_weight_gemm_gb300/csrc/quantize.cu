@@ -182,6 +182,13 @@ __global__ void __launch_bounds__(kThreads) k_zeros_to_v1(int32_t* qzeros, long 
   }
 }
 
+// Launched after the writer kernels, without programmatic dependent launch, so it starts only
+// when they have completed and their stores are visible.  The GEMM kernels read the checkpoint
+// before their own dependency wait (they may start while the kernel before them runs); with
+// this kernel in between, a GEMM issued right after gptq_quantize_rtn overlaps only this empty
+// kernel, never the writers.
+__global__ void k_writer_fence() {}
+
 int grid_for(long long work) {
   const long long need = (work + kThreads - 1) / kThreads;
   const long long cap = static_cast<long long>(device_info().sm_count) * 8;
@@ -203,8 +210,13 @@ cudaError_t launch_bits(const QuantProblem& q, cudaStream_t stream) {
   const long long cunits = static_cast<long long>(q.K / Pack<BITS>::kPerUnit) * (q.N / 4);
   k_quant_codes<BITS><<<grid_for(cunits), kThreads, 0, stream>>>(a);
   e = cudaGetLastError();
-  if (e != cudaSuccess || q.fmt != 1) return e;
-  k_zeros_to_v1<BITS><<<grid_for(zunits), kThreads, 0, stream>>>(q.qzeros, zunits);
+  if (e != cudaSuccess) return e;
+  if (q.fmt == 1) {
+    k_zeros_to_v1<BITS><<<grid_for(zunits), kThreads, 0, stream>>>(q.qzeros, zunits);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  k_writer_fence<<<1, 32, 0, stream>>>();
   return cudaGetLastError();
 }
 

@@ -38,6 +38,16 @@
  * only a per-device status word and per-device launch attributes; it never allocates device
  * memory in these calls.
  *
+ * Stream order: the GEMM entry points (gptq_gemm, gptq_gemm_perm, gptq_gemm_perm_noalloc) use
+ * programmatic dependent launch, so their kernels may start while the kernel issued just before
+ * them on `stream` is still running.  They read A (and perm) only after that kernel has
+ * completed, but they may read the checkpoint -- qweight, qzeros, scales, g_idx -- before, to
+ * start the weight stream early.  Hence the checkpoint must not be written by the kernel issued
+ * immediately before the call on the same stream (nor by a kernel still running when that one
+ * starts, which only a caller that itself uses programmatic dependent launch can arrange).  A
+ * checkpoint written by gptq_quantize_rtn may be used by the very next call: that entry point
+ * ends with an ordering step of its own.  gptq_gemm_grouped reads everything after the wait.
+ *
  * Errors: every entry point returns GPTQ_OK (0) or a negative gptq_status from host-side
  * validation or a failed launch; nothing is launched when validation fails.  Kernels never
  * trap: a bounded wait that runs out, or an act-order index outside [0, G), sets a bit in
