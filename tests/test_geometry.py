@@ -1,7 +1,8 @@
 """Host-side launch geometry of the decode kernels, checked without a GPU.
 
-tests/geometry_probe.cu is compiled against the library's headers (nvcc, host code only) and asked
-for the cluster split and shared-memory layout of a sweep of problems: every width, K up to 53248,
+tests/geometry_probe.cu is compiled against the library's headers (nvcc, host code only) and asks
+the launcher's own geometry selection (select_geometry in decode_mma.cuh) for the cluster split
+and shared-memory layout of a sweep of problems: every width, K up to 53248,
 N with ragged slabs, 1 to 32 tokens, groups from 32 rows to one per column, the scale-folding and
 the per-weight dequant paths, act-order, and grouped launches of 8 experts.  Every layout must:
   - fit one CTA's shared memory (227 KB),
@@ -54,7 +55,7 @@ def _problems():
                 for E in (1, 8):
                     if gidx and E > 1:
                         continue
-                    for regs in (64, 168):
+                    for regs in (64, 216):    # the decode kernels compile to 64 .. 214 registers
                         yield bits, K, N, M, group, int(fold), int(gidx), E, regs
 
 
