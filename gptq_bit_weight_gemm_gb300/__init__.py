@@ -139,17 +139,23 @@ def _stream(stream):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def gemm(A, qweight, qzeros, scales, g_idx=None, *, bits, group, fmt=V2, out=None, stream=None):
-    """C[M, N] = A[M, K] @ dequant(qweight, qzeros, scales, g_idx) on the current stream."""
+def gemm(A, qweight, qzeros, scales, g_idx=None, *, bits, group, fmt=V2, out=None, workspace=None,
+         stream=None):
+    """C[M, N] = A[M, K] @ dequant(qweight, qzeros, scales, g_idx) on the current stream.  bf16
+    activations take a workspace of workspace_size(...) bytes (allocated here when not given)."""
     torch = _torch()
     M, K = A.shape
     N = qweight.shape[1]
     if out is None:
         out = torch.empty((M, N), dtype=A.dtype, device=A.device)
+    if workspace is None and A.dtype == torch.bfloat16 and M > 0:
+        workspace = torch.empty(workspace_size(M, K, N, bits, group), dtype=torch.uint8, device=A.device)
+    ws_ptr = _ptr(workspace, name="workspace") if workspace is not None else None
+    ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
     rc = lib().gptq_gemm(_ptr(A, name="A"), M, K, _dtype_code(A),
                          _ptr(qweight, torch.int32, "qweight"), _ptr(qzeros, torch.int32, "qzeros"),
                          _ptr(scales, torch.float16, "scales"), _ptr(g_idx, torch.int32, "g_idx"),
-                         N, bits, group, fmt, _ptr(out, A.dtype, "out"), None, 0, _stream(stream))
+                         N, bits, group, fmt, _ptr(out, A.dtype, "out"), ws_ptr, ws_len, _stream(stream))
     _check(rc, "gptq_gemm")
     return out
 

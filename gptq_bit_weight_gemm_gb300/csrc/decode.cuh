@@ -105,10 +105,11 @@ __device__ __forceinline__ void cluster_wait() {
 // Stage activation pairs into shared memory.  Work item = (unit u, real token m < M): one
 // thread reads the unit's PER consecutive activations of row m with 16-byte loads (8-byte for
 // 8-bit units) and writes the NP pairs (lo_k(p), hi_k(p)) through `put(u, m, p, value)`.  A
-// thread's loads for up to kStageBatch items are all issued before any of them is used, so the
-// staging costs about one L2 round trip, not one per item.  Rows m >= M and units past the last
-// one are written as zero by the caller.
-constexpr int kStageBatch = 4;
+// thread's loads for up to stage_batch(PER) items (32 registers of activations) are all issued
+// before any of them is used, so the staging costs one L2 round trip per batch -- under a
+// saturated weight stream that round trip is over a microsecond.  Rows m >= M and units past
+// the last one are written as zero by the caller.
+__host__ __device__ constexpr int stage_batch(int per) { return per >= 32 ? 2 : 64 / per; }
 
 template <int PER>
 struct UnitVec {   // a unit's activations: PER 16-bit values
@@ -151,6 +152,7 @@ __device__ __forceinline__ void stage_pairs(const uint16_t* A, const int32_t* pe
                                             int ufirst, int nunits, int units, LoK lo_k, HiK hi_k,
                                             Put put) {
   const int items = nunits * M;
+  constexpr int kStageBatch = stage_batch(PER);
   for (int base = 0; base < items; base += kStageBatch * static_cast<int>(blockDim.x)) {
     UnitVec<PER> v[kStageBatch];
 #pragma unroll
@@ -201,13 +203,9 @@ cudaError_t launch_mma(const Problem& p, cudaStream_t stream);
 // one weight per expert (blockIdx.z), each with its own rows of A and C.
 template <int BITS, int MT, int MX, typename T, bool GROUPED = false>
 cudaError_t launch_mt(const Problem& p, cudaStream_t stream) {
-  constexpr bool kHas16 = (BITS == 2 || BITS == 4 ||
-                           ((BITS == 8 || BITS == 3) && std::is_same<T, __half>::value));
   // the scale folds per group when groups align with k-tiles (4 units)
-  const bool fold = kHas16 && p.g_idx == nullptr && (p.group % (4 * Pack<BITS>::kPerUnit)) == 0;
-  if constexpr (kHas16) {
-    if (fold) return launch_mma<BITS, MT, MX, T, true, GROUPED>(p, stream);
-  }
+  const bool fold = p.g_idx == nullptr && (p.group % (4 * Pack<BITS>::kPerUnit)) == 0;
+  if (fold) return launch_mma<BITS, MT, MX, T, true, GROUPED>(p, stream);
   return launch_mma<BITS, MT, MX, T, false, GROUPED>(p, stream);
 }
 

@@ -141,9 +141,11 @@ struct TmaSmem {
   __host__ __device__ static size_t off_misc(const TmaGeo& g, int M) {
     return off_full(g, M) + full_bytes(g);
   }
-  // bytes past the 1024-aligned base, plus the worst-case alignment pad
+  // bytes past the 1024-aligned base (mbarriers, the abort flag, the issued-chunk record, per
+  // token the largest staged magnitude and its power-of-two scale), plus the worst-case
+  // alignment pad
   __host__ __device__ static size_t bytes(const TmaGeo& g, int M) {
-    return off_misc(g, M) + 8 * kWarps * g.nbuf + 4 * (kWarps * g.nbuf + 1) + 1024;
+    return off_misc(g, M) + 8 * kWarps * g.nbuf + 4 * (kWarps * g.nbuf + 1) + 8 * static_cast<size_t>(M) + 1024;
   }
 };
 
@@ -168,8 +170,18 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
   using P = Pack<BITS>;
   using MP = MmaPairs<BITS>;
   using SM = TmaSmem<BITS>;
-  // the exact-difference unpack of the FOLD path (any valid instantiation where FOLD is off)
-  using DP = DiffPairs<typename std::conditional<FOLD, T, __half>::type, FOLD ? BITS : 4>;
+  // The multiply type TC.  The FOLD path with 2- and 4-bit codes multiplies exact (q - zero)
+  // integers and unrounded activations in T itself.  Everywhere else the multiply runs in fp16:
+  // the FULL path rounds each weight (a bf16 weight would carry up to 2^-8 relative error, more
+  // than the GEMM's 2e-3 bound; fp16 carries 2^-11), and bf16 cannot hold the 8-bit and 3-bit
+  // codes' magic-number forms exactly.  bf16 activations are then staged as fp16 times a power of
+  // two per token (exact), and the partial sums are scaled back in fp32 before the one rounding.
+  constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+  constexpr bool kNative = !kBf16 || (FOLD && (BITS == 2 || BITS == 4));
+  constexpr bool kConvert = !kNative;
+  using TC = typename std::conditional<kNative, T, __half>::type;
+  // the exact-difference unpack of the FOLD path
+  using DP = DiffPairs<TC, BITS>;
   constexpr int PER = P::kPerUnit;
   constexpr int ROWS = P::kRowsPerUnit;
   constexpr int NP = MP::kPairs;
@@ -234,6 +246,10 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
   uint8_t* misc = smem + SM::off_misc(geo, Mtok);
   const uint32_t bar0 = ptx::smem_addr(misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 8 * kWarps * geo.nbuf);
+  // bf16 activations: per token the largest staged |a| (bf16 bits) and the power of two 2^e the
+  // fp16 staging was divided by
+  uint32_t* tok_max = reinterpret_cast<uint32_t*>(misc + 8 * kWarps * geo.nbuf + 4 * (kWarps * geo.nbuf + 1));
+  float* tok_scale = reinterpret_cast<float*>(tok_max + Mtok);
   // With refills (more chunks than buffers) and 2 to 8 tokens, warp w's box slot of buffer b
   // arrives on its own mbarrier, so warps refill and stream independently; otherwise one mbarrier
   // per chunk, refilled by the whole CTA at once (all 512 bytes of each row together, which
@@ -246,20 +262,25 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
   const int g_lo = (cu0 * PER) / a.group;
   const int g_end = (ct1 * 4 * PER - 1) / a.group;
   const int ngrp = ntile > 0 ? (g_end < a.G - 1 ? g_end : a.G - 1) - g_lo + 1 : 0;
+  // The loads only fetch raw words: nothing consumes them before the weight copies are issued
+  // (a shift of a loaded word right away would hold thread 0 for a full memory latency first).
   constexpr int kGB = 4;                               // group items per thread in flight
   uint2 gsv[kGB];
-  uint32_t gzf[kGB];
+  uint2 gzw[kGB];                                      // the qzeros word(s) holding the 4 fields
   auto group_loads = [&](int base) {
 #pragma unroll
     for (int j = 0; j < kGB; ++j) {
       const int i = base + j * kThreads + static_cast<int>(threadIdx.x);
       gsv[j] = make_uint2(0u, 0u);
-      gzf[j] = 0u;
+      gzw[j] = make_uint2(0u, 0u);
       const int n = n_base + 4 * (i & 31);
       if (i < ngrp * 32 && n < a.N) {
         const int g = g_lo + (i >> 5);
         gsv[j] = __ldg(reinterpret_cast<const uint2*>(a.scales + static_cast<long long>(g) * a.N + n));
-        gzf[j] = zeros4<BITS>(a.qzeros + static_cast<long long>(g) * a.zwords, n);
+        const int32_t* zrow = a.qzeros + static_cast<long long>(g) * a.zwords;
+        const int bit = BITS * n;
+        gzw[j].x = static_cast<uint32_t>(__ldg(zrow + (bit >> 5)));
+        if (BITS == 3 && (bit & 31) + 12 > 32) gzw[j].y = static_cast<uint32_t>(__ldg(zrow + (bit >> 5) + 1));
       }
     }
   };
@@ -268,11 +289,13 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
     for (int j = 0; j < kGB; ++j) {
       const int i = base + j * kThreads + static_cast<int>(threadIdx.x);
       if (i < ngrp * 32) {
+        // the 4 zero fields of columns n .. n + 3, LSB-first (4 * BITS bits)
+        const uint32_t zf = __funnelshift_r(gzw[j].x, gzw[j].y, (BITS * (n_base + 4 * (i & 31))) & 31);
         uint32_t w[4];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const uint32_t h = c & 1 ? hi16(c < 2 ? gsv[j].x : gsv[j].y) : lo16(c < 2 ? gsv[j].x : gsv[j].y);
-          w[c] = h | ((((gzf[j] >> (BITS * c)) & P::kMask) + a.zero_offset) << 16);
+          w[c] = h | ((((zf >> (BITS * c)) & P::kMask) + a.zero_offset) << 16);
         }
         *reinterpret_cast<uint4*>(sK + (i >> 5) * kSlab + 4 * (i & 31)) = make_uint4(w[0], w[1], w[2], w[3]);
       }
@@ -292,6 +315,7 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
+  if (kConvert && static_cast<int>(threadIdx.x) < Mtok) tok_max[threadIdx.x] = 0u;
   __syncthreads();
   volatile int* last_issued = abort_flag + 1;          // [warp][nbuf] last chunk issued per buffer
   // the packed weights are read once: evict them first, so that activations and other reused
@@ -346,9 +370,10 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
       group_stores(base);
     }
   } else if (geo.full_groups > 0) {
-    // FULL: scales, runtime zeros and the group of every k of the range, read once into shared
-    // memory (with g_idx every group may occur, so all G are staged).  Checkpoint data, like the
-    // weights, so this too precedes griddepcontrol.wait.
+    // FULL: scales and runtime zeros (fp16 bits of each, scale in the low half) and the group of
+    // every k of the range, read once into shared memory (with g_idx every group may occur, so
+    // all G are staged).  Checkpoint data, like the weights, so this too precedes
+    // griddepcontrol.wait.
     const int g_base = a.g_idx ? 0 : g_lo;
     const int ng = a.g_idx ? a.G : ngrp;
     for (int i = threadIdx.x; i < ng * 32; i += kThreads) {
@@ -358,9 +383,10 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
         const int g = g_base + gi;
         const uint2 sv = __ldg(reinterpret_cast<const uint2*>(a.scales + static_cast<long long>(g) * a.N + n));
         const uint32_t zf = zeros4<BITS>(a.qzeros + static_cast<long long>(g) * a.zwords, n);
-        const uint32_t zz[4] = {((zf >> 0) & P::kMask) + a.zero_offset, ((zf >> BITS) & P::kMask) + a.zero_offset,
-                                ((zf >> (2 * BITS)) & P::kMask) + a.zero_offset,
-                                ((zf >> (3 * BITS)) & P::kMask) + a.zero_offset};
+        uint32_t zz[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c)   // an integer in [0, 256]: exact in fp16
+          zz[c] = __half_as_ushort(__int2half_rn(static_cast<int>(((zf >> (BITS * c)) & P::kMask) + a.zero_offset)));
         v = make_uint4(lo16(sv.x) | (zz[0] << 16), hi16(sv.x) | (zz[1] << 16), lo16(sv.y) | (zz[2] << 16),
                        hi16(sv.y) | (zz[3] << 16));
       }
@@ -382,6 +408,52 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
                        [](int p) { return MP::lo_k(p); }, [](int p) { return MP::hi_k(p); },
                        [&](int uu, int m, int p, uint32_t v) { sB[uu * UW + m * NP + p] = v; });
   __syncthreads();
+  if constexpr (kConvert) {
+    // bf16 -> fp16: per token, 2^e with max|a| * 2^-e in [2^15, 2^16) (below fp16's largest
+    // finite value for any bf16 significand); every staged value times 2^-e is exact and, in
+    // fp16's normal range, exactly representable; the partial sums are multiplied by 2^e before
+    // the reduction.
+    // per-thread maxima over the staged items (unit, token); where the token count divides the
+    // CTA, a thread's items all belong to one token and it flushes once
+    {
+      int cur_m = -1;
+      uint32_t mx = 0u;
+      for (int it = threadIdx.x; it < nunits * Mtok; it += kThreads) {
+        const int uu = it / Mtok, m = it - uu * Mtok;
+        if (m != cur_m) {
+          if (mx) atomicMax(tok_max + cur_m, mx);
+          cur_m = m;
+          mx = 0u;
+        }
+        const uint32_t* src = sB + uu * UW + m * NP;
+#pragma unroll
+        for (int p = 0; p < NP; ++p) {
+          const uint32_t v = src[p];
+          mx = max(mx, max(v & 0x7FFFu, (v >> 16) & 0x7FFFu));
+        }
+      }
+      if (mx) atomicMax(tok_max + cur_m, mx);
+    }
+    __syncthreads();
+    if (static_cast<int>(threadIdx.x) < Mtok) {
+      const uint32_t mx = tok_max[threadIdx.x];
+      int e = mx ? static_cast<int>(mx >> 7) - 127 - 15 : 0;   // exponent field of max|a|, minus 15
+      e = e < -126 ? -126 : (e > 126 ? 126 : e);               // 2^e and 2^-e stay normal floats
+      tok_scale[threadIdx.x] = __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
+    }
+    __syncthreads();
+    for (int it = threadIdx.x; it < nunits * Mtok; it += kThreads) {
+      const int uu = it / Mtok, m = it - uu * Mtok;
+      const float inv = __uint_as_float((254u << 23) - __float_as_uint(tok_scale[m]));   // 2^-e
+      uint32_t* w = sB + uu * UW + m * NP;
+#pragma unroll
+      for (int p = 0; p < NP; ++p) {
+        const uint32_t v = w[p];
+        w[p] = pack2(__uint_as_float(v << 16) * inv, __uint_as_float(v & 0xFFFF0000u) * inv, __half());
+      }
+    }
+    __syncthreads();
+  }
 
   float acc[2][NB][4];
 #pragma unroll
@@ -487,7 +559,7 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
 #pragma unroll
           for (int nb = 0; nb < NB; ++nb)
             mma16816(cg[t][nb], d0[2 * j], d1[2 * j], d0[2 * j + 1], d1[2 * j + 1], bf[nb][2 * j],
-                     bf[nb][2 * j + 1], T());
+                     bf[nb][2 * j + 1], TC());
       }
     };
     auto tile = [&](const uint8_t* wp, int kt) {
@@ -519,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
 #pragma unroll
           for (int nb = 0; nb < NB; ++nb)
             mma16816(cg[t][nb], d[2 * t][2 * j], d[2 * t + 1][2 * j], d[2 * t][2 * j + 1],
-                     d[2 * t + 1][2 * j + 1], bf[nb][2 * j], bf[nb][2 * j + 1], T());
+                     d[2 * t + 1][2 * j + 1], bf[nb][2 * j], bf[nb][2 * j + 1], TC());
     };
     const int tpg = a.group / (4 * PER);               // k-tiles per group (>= 1 here)
     int gi = 0, g_end_kt = tpg - (ct0 % tpg);          // local group, tile where it ends
@@ -588,41 +660,57 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
         const uint16_t* gk = sG + (kt * 4 + tq) * PER;   // staged groups of this unit's k
         // dequantize this unit for 4 columns: w[c][p] = RN((q - z) * s) pairs
         uint32_t w[4][NP];
-        float s[4], zf[4];
-        int cur_g = -1;
+        if (geo.full_groups > 0) {
+          // exact code pairs (q_lo, q_hi) of the 4 columns (the FOLD unpack with a zero of 0), then
+          // per pair the (scale, zero) words of its two k's groups for the 4 columns: (q - z) is
+          // exact in fp16 and one fp16 product rounds RN((q - z) s) once
+          using QP = DiffPairs<__half, BITS>;
+          uint32_t kz0[QP::kConsts];
+          QP::consts(0, kz0);
 #pragma unroll
-        for (int p = 0; p < NP; ++p) {
-          float v[4][2];
+          for (int cc = 0; cc < 4; ++cc) {
+            if constexpr (BITS == 3)
+              QP::run3((&wv[0].x)[cc], (&wv[1].x)[cc], (&wv[2].x)[cc], kz0, w[cc]);
+            else
+              QP::run((&wv[0].x)[cc], kz0, w[cc]);
+          }
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int j = h ? MP::hi_k(p) : MP::lo_k(p);
-            const int k = uk + j;
-            const int gg = geo.full_groups > 0 ? static_cast<int>(gk[j])
-                                               : (a.g_idx ? checked_group(a, k) : k / a.group);
-            if (gg != cur_g) {
-              if (geo.full_groups > 0) {
-                const uint4 sz = *reinterpret_cast<const uint4*>(sSZ + gg * kSlab + col0);
+          for (int p = 0; p < NP; ++p) {
+            const uint4 wl = *reinterpret_cast<const uint4*>(sSZ + gk[MP::lo_k(p)] * kSlab + col0);
+            const uint4 wh = *reinterpret_cast<const uint4*>(sSZ + gk[MP::hi_k(p)] * kSlab + col0);
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                  const uint32_t e = (&sz.x)[cc];
-                  s[cc] = __half2float(__ushort_as_half(lo16(e)));
-                  zf[cc] = __uint_as_float(0x4B000000u | (e >> 16));   // 2^23 + zero
-                }
-              } else {
+            for (int cc = 0; cc < 4; ++cc) {
+              const uint32_t el = (&wl.x)[cc], eh = (&wh.x)[cc];
+              w[cc][p] = hmul2(sub2(w[cc][p], __byte_perm(el, eh, 0x7632), __half()), __byte_perm(el, eh, 0x5410));
+            }
+          }
+        } else {
+          // groups, scales and zeros read through L1 (too many groups to stage)
+          float s[4], zf[4];
+          int cur_g = -1;
+#pragma unroll
+          for (int p = 0; p < NP; ++p) {
+            float v[4][2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int j = h ? MP::hi_k(p) : MP::lo_k(p);
+              const int k = uk + j;
+              const int gg = a.g_idx ? checked_group(a, k) : k / a.group;
+              if (gg != cur_g) {
                 int z[4];
                 load_sz<BITS>(a, gg, n0c, s, z);
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) zf[cc] = 8388608.0f + static_cast<float>(z[cc]);
+                cur_g = gg;
               }
-              cur_g = gg;
+              // q - z exactly (magic 2^23 has ulp 1), one fp32 product, rounded once below
+#pragma unroll
+              for (int cc = 0; cc < 4; ++cc)
+                v[cc][h] = (__uint_as_float(0x4B000000u | unit_code<BITS>(wv, cc, j)) - zf[cc]) * s[cc];
             }
-            // q - z exactly (magic 2^23 has ulp 1), one fp32 product, rounded once below
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc)
-              v[cc][h] = (__uint_as_float(0x4B000000u | unit_code<BITS>(wv, cc, j)) - zf[cc]) * s[cc];
+            for (int cc = 0; cc < 4; ++cc) w[cc][p] = pack2(v[cc][0], v[cc][1], TC());
           }
-#pragma unroll
-          for (int cc = 0; cc < 4; ++cc) w[cc][p] = pack2(v[cc][0], v[cc][1], T());
         }
 #pragma unroll
         for (int j = 0; j < NP / 2; ++j)
@@ -631,7 +719,7 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
 #pragma unroll
             for (int nb = 0; nb < NB; ++nb)
               mma16816(acc[t][nb], w[2 * t][2 * j], w[2 * t + 1][2 * j], w[2 * t][2 * j + 1],
-                       w[2 * t + 1][2 * j + 1], bf[nb][2 * j], bf[nb][2 * j + 1], T());
+                       w[2 * t + 1][2 * j + 1], bf[nb][2 * j], bf[nb][2 * j + 1], TC());
       }
       if (c + geo.nbuf < nchunk) refill(c + geo.nbuf);   // the buffer just consumed
     }
@@ -657,7 +745,7 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
           const int col = col0 + 2 * t + r;
           const int owner = col >> pr_shift;
           float* dst = cluster.map_shared_rank(recv, owner);
-          dst[rank * per_rank + (col - owner * per_rank)] = acc[t][0][2 * r];
+          dst[rank * per_rank + (col - owner * per_rank)] = kConvert ? acc[t][0][2 * r] * tok_scale[0] : acc[t][0][2 * r];
         }
   } else {
     // several tokens: through shared memory first, so that consecutive threads push consecutive
@@ -671,7 +759,7 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int col = col0 + 2 * t + (i >> 1), m = nb * 8 + 2 * tq + (i & 1);
-          if (m < Mr) part[m * kSlab + col] = acc[t][nb][i];
+          if (m < Mr) part[m * kSlab + col] = kConvert ? acc[t][nb][i] * tok_scale[m] : acc[t][nb][i];
         }
     __syncthreads();
     cluster_wait();

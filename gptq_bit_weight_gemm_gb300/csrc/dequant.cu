@@ -7,8 +7,9 @@
 // number 2^23), multiplied by the fp16 scale in fp32 (exact: at most 9 + 11 significant bits)
 // and rounded once to the output dtype, so the result is bit-exact.
 //
-// Memory-bound: each thread owns one packed unit of 4 adjacent columns (one 16-byte load per
-// qweight row) and writes 8 bytes per k, so a warp writes 256 contiguous bytes per output row.
+// Memory-bound (it writes four times the packed bytes at 4 bits): each thread owns one packed
+// unit of 8 adjacent columns (two 16-byte loads per qweight row) and writes 16 bytes per k, so a
+// warp writes 512 contiguous bytes of each output row.
 #include "gptq_device.cuh"
 #include "gptq_internal.h"
 
@@ -16,6 +17,7 @@ namespace gptq {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kCols = 8;             // columns per thread
 
 struct DqArgs {
   const int32_t* qweight;
@@ -32,20 +34,24 @@ __global__ void __launch_bounds__(kThreads) k_dequant(const DqArgs a) {
   using P = Pack<BITS>;
   constexpr int PER = P::kPerUnit;
   constexpr int ROWS = P::kRowsPerUnit;
-  const int n4_count = a.N / 4;
-  const long long total = static_cast<long long>(a.units) * n4_count;
+  const int n8_count = a.N / kCols;
+  const long long total = static_cast<long long>(a.units) * n8_count;
   T* W = static_cast<T*>(a.W);
   for (long long idx = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x; idx < total;
        idx += static_cast<long long>(gridDim.x) * kThreads) {
-    const int u = static_cast<int>(idx / n4_count);
-    const int n0 = static_cast<int>(idx - static_cast<long long>(u) * n4_count) * 4;
-    uint4 wv[ROWS];
+    const int u = static_cast<int>(idx / n8_count);
+    const int n0 = static_cast<int>(idx - static_cast<long long>(u) * n8_count) * kCols;
+    uint32_t wv[ROWS][kCols];
 #pragma unroll
-    for (int r = 0; r < ROWS; ++r)
-      wv[r] = ld_stream_v4(a.qweight + (static_cast<long long>(u) * ROWS + r) * a.N + n0);
+    for (int r = 0; r < ROWS; ++r) {
+      const int32_t* src = a.qweight + (static_cast<long long>(u) * ROWS + r) * a.N + n0;
+      const uint4 lo = ld_stream_v4(src), hi = ld_stream_v4(src + 4);
+      wv[r][0] = lo.x; wv[r][1] = lo.y; wv[r][2] = lo.z; wv[r][3] = lo.w;
+      wv[r][4] = hi.x; wv[r][5] = hi.y; wv[r][6] = hi.z; wv[r][7] = hi.w;
+    }
     int cur_g = -1;
-    float s[4];
-    int z[4];
+    float s[kCols];
+    int z[kCols];
 #pragma unroll 4
     for (int j = 0; j < PER; ++j) {
       const int k = u * PER + j;
@@ -60,33 +66,38 @@ __global__ void __launch_bounds__(kThreads) k_dequant(const DqArgs a) {
         g = k / a.group;
       }
       if (g != cur_g) {
-        const uint2 sv =
-            __ldg(reinterpret_cast<const uint2*>(a.scales + static_cast<long long>(g) * a.N + n0));
-        s[0] = __half2float(__ushort_as_half(static_cast<uint16_t>(sv.x & 0xFFFFu)));
-        s[1] = __half2float(__ushort_as_half(static_cast<uint16_t>(sv.x >> 16)));
-        s[2] = __half2float(__ushort_as_half(static_cast<uint16_t>(sv.y & 0xFFFFu)));
-        s[3] = __half2float(__ushort_as_half(static_cast<uint16_t>(sv.y >> 16)));
-        const uint32_t zf = zeros4<BITS>(a.qzeros + static_cast<long long>(g) * a.zwords, n0);
+        const uint4 sv = __ldg(reinterpret_cast<const uint4*>(a.scales + static_cast<long long>(g) * a.N + n0));
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-          z[c] = static_cast<int>((zf >> (BITS * c)) & P::kMask) + a.zero_offset;
+        for (int c = 0; c < kCols; ++c) {
+          const uint32_t word = (&sv.x)[c >> 1];
+          s[c] = __half2float(__ushort_as_half(static_cast<uint16_t>(c & 1 ? word >> 16 : word & 0xFFFFu)));
+        }
+        const int32_t* zrow = a.qzeros + static_cast<long long>(g) * a.zwords;
+        const uint32_t zlo = zeros4<BITS>(zrow, n0), zhi = zeros4<BITS>(zrow, n0 + 4);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          z[c] = static_cast<int>((zlo >> (BITS * c)) & P::kMask) + a.zero_offset;
+          z[c + 4] = static_cast<int>((zhi >> (BITS * c)) & P::kMask) + a.zero_offset;
+        }
         cur_g = g;
       }
-      float w[4];
+      float w[kCols];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < kCols; ++c) {
         uint32_t code;
         if constexpr (BITS == 3) {
-          code = code3((&wv[0].x)[c], (&wv[1].x)[c], (&wv[2].x)[c], j);
+          code = code3(wv[0][c], wv[1][c], wv[2][c], j);
         } else {
-          code = ((&wv[0].x)[c] >> (BITS * j)) & P::kMask;
+          code = (wv[0][c] >> (BITS * j)) & P::kMask;
         }
         w[c] = diff_f32(code, z[c]) * s[c];   // exact
       }
-      uint2 out;
+      uint4 out;
       out.x = pack2(w[0], w[1], T());
       out.y = pack2(w[2], w[3], T());
-      *reinterpret_cast<uint2*>(W + static_cast<long long>(k) * a.N + n0) = out;
+      out.z = pack2(w[4], w[5], T());
+      out.w = pack2(w[6], w[7], T());
+      *reinterpret_cast<uint4*>(W + static_cast<long long>(k) * a.N + n0) = out;
     }
   }
 }
@@ -100,7 +111,7 @@ cudaError_t launch_typed(const Problem& p, cudaStream_t stream) {
   a.zero_offset = p.zero_offset; a.zwords = p.N * BITS / 32;
   a.units = p.K / Pack<BITS>::kPerUnit;
   a.W = p.out; a.status = p.status;
-  const long long total = static_cast<long long>(a.units) * (p.N / 4);
+  const long long total = static_cast<long long>(a.units) * (p.N / kCols);
   const long long need = (total + kThreads - 1) / kThreads;
   const long long cap = static_cast<long long>(device_info().sm_count) * 8;
   const int grid = static_cast<int>(need < cap ? need : cap);

@@ -181,8 +181,8 @@ extern "C" int gptq_dequant(const int32_t* qweight, const int32_t* qzeros, const
 }
 
 extern "C" size_t gptq_gemm_workspace_size(int M, int K, int N, int bits, int group) {
-  (void)M; (void)K; (void)N; (void)bits; (void)group;
-  return 0;
+  (void)N; (void)bits; (void)group;
+  return gptq::prefill_workspace_bytes(M, K);
 }
 
 extern "C" int gptq_gemm(const void* A, int M, int K, int a_dtype, const int32_t* qweight,
@@ -195,11 +195,10 @@ extern "C" int gptq_gemm(const void* A, int M, int K, int a_dtype, const int32_t
   if (fmt != GPTQ_FMT_V1 && fmt != GPTQ_FMT_V2) return GPTQ_ERR_ARG;
   if (a_dtype != GPTQ_F16 && a_dtype != GPTQ_BF16) return GPTQ_ERR_ARG;
   if (M < 0) return GPTQ_ERR_SHAPE;
-  if (workspace_bytes < gptq_gemm_workspace_size(M, K, N, bits, group)) return GPTQ_ERR_WORKSPACE;
-  (void)workspace;
   if (M == 0) return GPTQ_OK;
   if (!A || !C) return GPTQ_ERR_ARG;
   if (!gptq::aligned(A, 16) || !gptq::aligned(C, 16)) return GPTQ_ERR_ALIGN;
+  if (workspace && !gptq::aligned(workspace, 16)) return GPTQ_ERR_ALIGN;
   rc = gptq::device_ready(&p);
   if (rc) return rc;
   p.A = A;
@@ -207,6 +206,8 @@ extern "C" int gptq_gemm(const void* A, int M, int K, int a_dtype, const int32_t
   p.dtype = a_dtype;
   p.zero_offset = fmt == GPTQ_FMT_V1 ? 1 : 0;
   p.out = C;
+  p.workspace = workspace;
+  p.workspace_bytes = workspace ? workspace_bytes : 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (M <= gptq::kDecodeMaxM) {
     const cudaError_t e = gptq::launch_decode(p, s);
@@ -214,6 +215,8 @@ extern "C" int gptq_gemm(const void* A, int M, int K, int a_dtype, const int32_t
     // this M even split 16 ways; the tensor-core kernel takes the problem (any M)
     if (e != cudaErrorInvalidConfiguration) return gptq::from_cuda(e);
   }
+  // the tensor-core kernel multiplies bf16 activations as an fp16 copy in the workspace
+  if (a_dtype == GPTQ_BF16 && p.workspace_bytes < gptq::prefill_workspace_bytes(M, K)) return GPTQ_ERR_WORKSPACE;
   return gptq::from_cuda(gptq::launch_prefill(p, s));
 }
 

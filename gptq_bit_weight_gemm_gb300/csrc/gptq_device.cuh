@@ -87,8 +87,6 @@ struct F16Traits;
 template <>
 struct F16Traits<__half> {
   using T2 = __half2;
-  static constexpr uint32_t kMagic2 = 0x64006400u;   // (1024, 1024): ulp 1 on [1024, 2048)
-  static constexpr float kMagic = 1024.0f;
   __device__ static __forceinline__ float to_f32(__half x) { return __half2float(x); }
   __device__ static __forceinline__ __half from_f32(float x) { return __float2half_rn(x); }
   __device__ static __forceinline__ uint16_t bits(__half x) { return __half_as_ushort(x); }
@@ -98,8 +96,6 @@ struct F16Traits<__half> {
 template <>
 struct F16Traits<__nv_bfloat16> {
   using T2 = __nv_bfloat162;
-  static constexpr uint32_t kMagic2 = 0x43004300u;   // (128, 128): ulp 1 on [128, 256)
-  static constexpr float kMagic = 128.0f;
   __device__ static __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
   __device__ static __forceinline__ __nv_bfloat16 from_f32(float x) {
     return __float2bfloat16_rn(x);
@@ -117,14 +113,25 @@ __device__ __forceinline__ uint32_t sub2(uint32_t a, uint32_t b, __half) {
   __half2 r = __hsub2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
   return *reinterpret_cast<uint32_t*>(&r);
 }
+__device__ __forceinline__ uint32_t fma2(uint32_t a, uint32_t b, uint32_t c, __half) {
+  __half2 r = __hfma2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b),
+                      *reinterpret_cast<__half2*>(&c));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
 __device__ __forceinline__ uint32_t sub2(uint32_t a, uint32_t b, __nv_bfloat16) {
   __nv_bfloat162 r =
       __hsub2(*reinterpret_cast<__nv_bfloat162*>(&a), *reinterpret_cast<__nv_bfloat162*>(&b));
   return *reinterpret_cast<uint32_t*>(&r);
 }
-__device__ __forceinline__ uint32_t fma2(uint32_t a, uint32_t b, uint32_t c, __half) {
-  __half2 r = __hfma2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b),
-                      *reinterpret_cast<__half2*>(&c));
+__device__ __forceinline__ uint32_t fma2(uint32_t a, uint32_t b, uint32_t c, __nv_bfloat16) {
+  __nv_bfloat162 r = __hfma2(*reinterpret_cast<__nv_bfloat162*>(&a),
+                             *reinterpret_cast<__nv_bfloat162*>(&b),
+                             *reinterpret_cast<__nv_bfloat162*>(&c));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  __half2 r = __hmul2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
   return *reinterpret_cast<uint32_t*>(&r);
 }
 
@@ -138,13 +145,6 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, __nv_bfloat16) {
   return *reinterpret_cast<uint32_t*>(&r);
 }
 
-// Replicate a 16-bit float value into both halves.
-template <typename T>
-__device__ __forceinline__ uint32_t splat2(float x) {
-  uint32_t h = F16Traits<T>::bits(F16Traits<T>::from_f32(x));
-  return h | (h << 16);
-}
-
 // Both halves set to the 16-bit float with bit pattern base + mult * z.  Above a power of two
 // 2^e the 16-bit formats step by 2^(e - 10) (fp16) or 2^(e - 7) (bf16), so 2^e + z (or its
 // negative) has the pattern bits(2^e) + z * 2^(10 - e) (fp16) while that stays below the next
@@ -156,22 +156,15 @@ __device__ __forceinline__ uint32_t splat_bits(uint32_t base, uint32_t mult, int
 // ------------------------------------------------------------------------------------------
 // Exact (q - zero) pairs from one packed word, as 16-bit floats.
 //
-// DiffPairs<T, BITS> turns one packed word into kPairs registers of two 16-bit values each;
-// pair p holds the codes of k = lo_k(p) (low half) and k = hi_k(p) (high half) of the word.
+// DiffPairs<T, BITS> turns one packed word (three for 3-bit) into kPairs registers of two
+// 16-bit values each; pair p holds the codes of k = lo_k(p) (low half) and k = hi_k(p) (high half).
 // The code is OR-ed into the mantissa of a magic number M with unit last place (1024 for fp16,
 // 128 for bf16); a code sitting `sh` bits up reads as M + 2^sh q, and one sub or fma with a
 // per-zero constant (consts(), computed once per group) gives q - zero exactly.  Valid for
-// __half with 2, 4 and 8 bits and for __nv_bfloat16 with 2 and 4 bits.
+// __half with 2, 3, 4 and 8 bits and for __nv_bfloat16 with 2 and 4 bits.
 // ------------------------------------------------------------------------------------------
 template <typename T, int BITS>
 struct DiffPairs;
-
-__device__ __forceinline__ uint32_t fma2(uint32_t a, uint32_t b, uint32_t c, __nv_bfloat16) {
-  __nv_bfloat162 r = __hfma2(*reinterpret_cast<__nv_bfloat162*>(&a),
-                             *reinterpret_cast<__nv_bfloat162*>(&b),
-                             *reinterpret_cast<__nv_bfloat162*>(&c));
-  return *reinterpret_cast<uint32_t*>(&r);
-}
 
 template <>
 struct DiffPairs<__half, 4> {
@@ -190,24 +183,6 @@ struct DiffPairs<__half, 4> {
     d[1] = fma2(lop3_and_or(w, 0x00F000F0u, M2), inv16, k[1], __half());
     d[2] = sub2(lop3_and_or(w8, 0x000F000Fu, M2), k[0], __half());
     d[3] = fma2(lop3_and_or(w8, 0x00F000F0u, M2), inv16, k[1], __half());
-  }
-};
-
-template <>
-struct DiffPairs<__nv_bfloat16, 4> {
-  static constexpr int kPairs = 4, kConsts = 1;
-  __device__ static __forceinline__ int lo_k(int p) { return p; }
-  __device__ static __forceinline__ int hi_k(int p) { return p + 4; }
-  __device__ static __forceinline__ void consts(int z, uint32_t (&k)[kConsts]) {
-    k[0] = splat_bits(0x4300u, 1u, z);     // 128 + z
-  }
-  __device__ static __forceinline__ void run(uint32_t w, const uint32_t (&k)[kConsts],
-                                             uint32_t (&d)[kPairs]) {
-    const uint32_t M2 = 0x43004300u;
-    d[0] = sub2(lop3_and_or(w, 0x000F000Fu, M2), k[0], __nv_bfloat16());
-    d[1] = sub2(lop3_and_or(w >> 4, 0x000F000Fu, M2), k[0], __nv_bfloat16());
-    d[2] = sub2(lop3_and_or(w >> 8, 0x000F000Fu, M2), k[0], __nv_bfloat16());
-    d[3] = sub2(lop3_and_or(w >> 12, 0x000F000Fu, M2), k[0], __nv_bfloat16());
   }
 };
 
@@ -238,6 +213,40 @@ struct DiffPairs<__half, 2> {
 };
 
 template <>
+struct DiffPairs<__half, 8> {
+  static constexpr int kPairs = 2, kConsts = 1;
+  __device__ static __forceinline__ int lo_k(int p) { return p; }
+  __device__ static __forceinline__ int hi_k(int p) { return p + 2; }
+  __device__ static __forceinline__ void consts(int z, uint32_t (&k)[kConsts]) {
+    k[0] = splat_bits(0x6400u, 1u, z);     // 1024 + z
+  }
+  __device__ static __forceinline__ void run(uint32_t w, const uint32_t (&k)[kConsts],
+                                             uint32_t (&d)[kPairs]) {
+    // bytes (0, 2) and (1, 3) under the 0x64 exponent byte
+    d[0] = sub2(__byte_perm(w, 0x64646464u, 0x4240u), k[0], __half());
+    d[1] = sub2(__byte_perm(w, 0x64646464u, 0x4341u), k[0], __half());
+  }
+};
+
+template <>
+struct DiffPairs<__nv_bfloat16, 4> {
+  static constexpr int kPairs = 4, kConsts = 1;
+  __device__ static __forceinline__ int lo_k(int p) { return p; }
+  __device__ static __forceinline__ int hi_k(int p) { return p + 4; }
+  __device__ static __forceinline__ void consts(int z, uint32_t (&k)[kConsts]) {
+    k[0] = splat_bits(0x4300u, 1u, z);     // 128 + z
+  }
+  __device__ static __forceinline__ void run(uint32_t w, const uint32_t (&k)[kConsts],
+                                             uint32_t (&d)[kPairs]) {
+    const uint32_t M2 = 0x43004300u;
+    d[0] = sub2(lop3_and_or(w, 0x000F000Fu, M2), k[0], __nv_bfloat16());
+    d[1] = sub2(lop3_and_or(w >> 4, 0x000F000Fu, M2), k[0], __nv_bfloat16());
+    d[2] = sub2(lop3_and_or(w >> 8, 0x000F000Fu, M2), k[0], __nv_bfloat16());
+    d[3] = sub2(lop3_and_or(w >> 12, 0x000F000Fu, M2), k[0], __nv_bfloat16());
+  }
+};
+
+template <>
 struct DiffPairs<__nv_bfloat16, 2> {
   static constexpr int kPairs = 8, kConsts = 3;
   __device__ static __forceinline__ int lo_k(int p) { return p; }
@@ -262,115 +271,16 @@ struct DiffPairs<__nv_bfloat16, 2> {
   }
 };
 
-template <>
-struct DiffPairs<__half, 8> {
-  static constexpr int kPairs = 2, kConsts = 1;
-  __device__ static __forceinline__ int lo_k(int p) { return p; }
-  __device__ static __forceinline__ int hi_k(int p) { return p + 2; }
-  __device__ static __forceinline__ void consts(int z, uint32_t (&k)[kConsts]) {
-    k[0] = splat_bits(0x6400u, 1u, z);     // 1024 + z
-  }
-  __device__ static __forceinline__ void run(uint32_t w, const uint32_t (&k)[kConsts],
-                                             uint32_t (&d)[kPairs]) {
-    // bytes (0, 2) and (1, 3) under the 0x64 exponent byte
-    d[0] = sub2(__byte_perm(w, 0x64646464u, 0x4240u), k[0], __half());
-    d[1] = sub2(__byte_perm(w, 0x64646464u, 0x4341u), k[0], __half());
-  }
-};
-
 // ------------------------------------------------------------------------------------------
-// Raw codes as 16-bit floats, zero not subtracted (decode kernels).
+// Raw codes as 16-bit floats, zero not subtracted: the 3-bit pairing.
 //
-// CodePairs<T, BITS> is DiffPairs without the per-pair sub/fma: pair p of a word holds
-// kMagic + 2^shift_lo(p) * q (low half) and kMagic + 2^shift_hi(p) * q (high half) for the codes
-// lo_k(p), hi_k(p) (2/4/8-bit: the DiffPairs pairing), i.e. only masks (plus shared shifts).
-// With the matching activation halves scaled by 2^-shift,
-//   sum_k b_k (kMagic + 2^shift q_k) = kMagic * sum_k b_k + sum_k (2^shift b_k) q_k,
-// so sum_k (2^shift b_k)(q_k - z) is the MMA result minus kMagic * sum_k b_k and minus
-// z * sum_k 2^shift b_k -- two sums per quantization group and token.
+// CodePairs<__half, 3>::run3 turns the 3 words of a 3-bit unit into 16 registers of two fp16
+// values each, 1024 + 2^shift_lo(p) * q (low half) and 1024 + 2^shift_hi(p) * q (high half) for
+// the codes lo_k(p), hi_k(p), with masks only; DiffPairs<__half, 3> then takes the zero out
+// exactly.
 // ------------------------------------------------------------------------------------------
 template <typename T, int BITS>
 struct CodePairs;
-
-template <>
-struct CodePairs<__half, 4> {
-  static constexpr int kPairs = 4;
-  static constexpr float kMagic = 1024.0f;
-  __host__ __device__ static constexpr int shift_lo(int p) { return (p & 1) ? 4 : 0; }
-  __host__ __device__ static constexpr int shift_hi(int p) { return shift_lo(p); }
-  __device__ static __forceinline__ void run(uint32_t w, uint32_t (&d)[kPairs]) {
-    const uint32_t M2 = 0x64006400u, w8 = w >> 8;
-    d[0] = lop3_and_or(w, 0x000F000Fu, M2);
-    d[1] = lop3_and_or(w, 0x00F000F0u, M2);
-    d[2] = lop3_and_or(w8, 0x000F000Fu, M2);
-    d[3] = lop3_and_or(w8, 0x00F000F0u, M2);
-  }
-};
-
-template <>
-struct CodePairs<__nv_bfloat16, 4> {
-  static constexpr int kPairs = 4;
-  static constexpr float kMagic = 128.0f;
-  __host__ __device__ static constexpr int shift_lo(int) { return 0; }
-  __host__ __device__ static constexpr int shift_hi(int) { return 0; }
-  __device__ static __forceinline__ void run(uint32_t w, uint32_t (&d)[kPairs]) {
-    const uint32_t M2 = 0x43004300u;
-    d[0] = lop3_and_or(w, 0x000F000Fu, M2);
-    d[1] = lop3_and_or(w >> 4, 0x000F000Fu, M2);
-    d[2] = lop3_and_or(w >> 8, 0x000F000Fu, M2);
-    d[3] = lop3_and_or(w >> 12, 0x000F000Fu, M2);
-  }
-};
-
-template <>
-struct CodePairs<__half, 2> {
-  static constexpr int kPairs = 8;
-  static constexpr float kMagic = 1024.0f;
-  __host__ __device__ static constexpr int shift_lo(int p) { return 2 * (p & 3); }
-  __host__ __device__ static constexpr int shift_hi(int p) { return shift_lo(p); }
-  __device__ static __forceinline__ void run(uint32_t w, uint32_t (&d)[kPairs]) {
-    const uint32_t M2 = 0x64006400u;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const uint32_t x = h ? (w >> 8) : w;
-      d[4 * h + 0] = lop3_and_or(x, 0x00030003u, M2);
-      d[4 * h + 1] = lop3_and_or(x, 0x000C000Cu, M2);
-      d[4 * h + 2] = lop3_and_or(x, 0x00300030u, M2);
-      d[4 * h + 3] = lop3_and_or(x, 0x00C000C0u, M2);
-    }
-  }
-};
-
-template <>
-struct CodePairs<__nv_bfloat16, 2> {
-  static constexpr int kPairs = 8;
-  static constexpr float kMagic = 128.0f;
-  __host__ __device__ static constexpr int shift_lo(int p) { return (p & 3) == 3 ? 0 : 2 * (p & 3); }
-  __host__ __device__ static constexpr int shift_hi(int p) { return shift_lo(p); }
-  __device__ static __forceinline__ void run(uint32_t w, uint32_t (&d)[kPairs]) {
-    const uint32_t M2 = 0x43004300u;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const uint32_t x = h ? (w >> 8) : w;
-      d[4 * h + 0] = lop3_and_or(x, 0x00030003u, M2);
-      d[4 * h + 1] = lop3_and_or(x, 0x000C000Cu, M2);
-      d[4 * h + 2] = lop3_and_or(x, 0x00300030u, M2);
-      d[4 * h + 3] = lop3_and_or(x >> 6, 0x00030003u, M2);
-    }
-  }
-};
-
-template <>
-struct CodePairs<__half, 8> {
-  static constexpr int kPairs = 2;
-  static constexpr float kMagic = 1024.0f;
-  __host__ __device__ static constexpr int shift_lo(int) { return 0; }
-  __host__ __device__ static constexpr int shift_hi(int) { return 0; }
-  __device__ static __forceinline__ void run(uint32_t w, uint32_t (&d)[kPairs]) {
-    d[0] = __byte_perm(w, 0x64646464u, 0x4240u);
-    d[1] = __byte_perm(w, 0x64646464u, 0x4341u);
-  }
-};
 
 // 3-bit, fp16: a unit is 32 codes in a 96-bit LSB-first stream of 3 words (code j at bit 3j).
 // A pair can be read by one mask when its two codes sit at bits [p, p+3) and [16+p', 16+p'+3)
@@ -443,31 +353,6 @@ struct DiffPairs<__half, 3> {
     }
   }
 };
-
-// A 16-bit pair times (2^-slo, 2^-shi) (exact unless a result is subnormal, where it rounds).
-__device__ __forceinline__ uint32_t scale_pow2_pair(uint32_t v, int slo, int shi, __half) {
-  if (slo == 0 && shi == 0) return v;
-  const __half2 f = __halves2half2(__ushort_as_half(static_cast<uint16_t>((15 - slo) << 10)),
-                                   __ushort_as_half(static_cast<uint16_t>((15 - shi) << 10)));
-  __half2 r = __hmul2(*reinterpret_cast<__half2*>(&v), f);
-  return *reinterpret_cast<uint32_t*>(&r);
-}
-__device__ __forceinline__ uint32_t scale_pow2_pair(uint32_t v, int slo, int shi, __nv_bfloat16) {
-  if (slo == 0 && shi == 0) return v;
-  const __nv_bfloat162 f = __halves2bfloat162(__ushort_as_bfloat16(static_cast<uint16_t>((127 - slo) << 7)),
-                                              __ushort_as_bfloat16(static_cast<uint16_t>((127 - shi) << 7)));
-  __nv_bfloat162 r = __hmul2(*reinterpret_cast<__nv_bfloat162*>(&v), f);
-  return *reinterpret_cast<uint32_t*>(&r);
-}
-
-// Sum of the two halves of a 16-bit pair, in fp32.
-__device__ __forceinline__ float sum2_f32(uint32_t x, __half) {
-  const float2 f = __half22float2(*reinterpret_cast<__half2*>(&x));
-  return f.x + f.y;
-}
-__device__ __forceinline__ float sum2_f32(uint32_t x, __nv_bfloat16) {
-  return __uint_as_float(x << 16) + __uint_as_float(x & 0xFFFF0000u);
-}
 
 // Exact q - z as an fp32 (any width): magic 2^23 has ulp 1.
 __device__ __forceinline__ float diff_f32(uint32_t code, int z) {

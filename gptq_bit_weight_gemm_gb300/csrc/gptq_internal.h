@@ -29,6 +29,10 @@ struct Problem {
   const int32_t* offsets;
   int E;
   int rows;
+  // caller workspace (the tensor-core kernel with bf16 activations: the fp16 copy of A and its
+  // row scales, prefill_workspace_bytes)
+  void* workspace;
+  size_t workspace_bytes;
 };
 
 struct DeviceInfo {
@@ -44,6 +48,8 @@ cudaError_t launch_dequant(const Problem& p, cudaStream_t stream);
 cudaError_t launch_decode(const Problem& p, cudaStream_t stream);
 cudaError_t launch_decode_grouped(const Problem& p, cudaStream_t stream);
 cudaError_t launch_prefill(const Problem& p, cudaStream_t stream);
+// Workspace the tensor-core kernel needs for bf16 activations of M x K (0 for fp16).
+size_t prefill_workspace_bytes(int M, int K);
 cudaError_t launch_gather_cols(const void* A, const int32_t* perm, int M, int K, void* out,
                                cudaStream_t stream);
 cudaError_t launch_wait_selftest(unsigned* status, uint64_t limit_ns, int* flag, cudaStream_t stream);

@@ -11,16 +11,21 @@
 //   warp 4      TMA producer: A tile [256 x 64] (128-byte swizzle) and the packed qweight tile
 //               [64 k x 256 n] for each k-step into a 3-stage ring;
 //   warps 6-21  dequantizers, two threads per tile column (4 chunks of 8 k each): exact
-//               q - zero as 16-bit floats (DiffPairs), then one rounding of (q - zero) * scale --
-//               fp16: HMUL2 (an exact product rounded once); bf16: fp32 products (f32x2) rounded
-//               once -- stored K-major with the 128-byte swizzle into a 3-stage B ring (2 for
-//               8-bit), then fence.proxy.async + mbarrier arrive.  The next group's scale and
-//               zero words are loaded one group ahead;
+//               q - zero as fp16 (DiffPairs), then one rounding of (q - zero) * scale to fp16
+//               (HMUL2: an exact product rounded once), stored K-major with the 128-byte swizzle
+//               into a 3-stage B ring (2 for 8-bit), then fence.proxy.async + mbarrier arrive.
+//               The next group's scale and zero words are loaded one group ahead;
 //   warp 5      TMEM owner and MMA issuer: per k-step 4 x 2 tcgen05.mma (M=128, N=256, K=16),
 //               one per 128-row half of A, both reading the same B tile; tcgen05.commit frees
 //               the ring slots and signals the accumulators;
 //   warps 0-3   epilogue: tcgen05.ld of the two 128 x 256 fp32 accumulators (512 TMEM
-//               columns), rounding to A's dtype, direct 64-byte row-segment stores.
+//               columns), times the row's power-of-two scale (bf16 input), rounding to A's dtype,
+//               direct 64-byte row-segment stores.
+// The multiply is fp16 x fp16 for both activation types.  bf16 activations are first rewritten
+// into the caller's workspace as fp16 times a power of two per row (k_rows_to_f16, exact), and
+// that power of two is multiplied back into the fp32 accumulators: a bf16 weight operand would
+// carry up to 2^-8 relative error per product, beyond the GEMM's 2e-3 bound, while the fp16
+// weight carries 2^-11.
 // Every mbarrier wait is bounded (2 s of %globaltimer): on expiry the kernel sets
 // GPTQ_DEV_TIMEOUT in the status word, every role stops, in-flight copies and MMAs are waited
 // for (bounded), TMEM is freed and the CTA exits.
@@ -71,6 +76,7 @@ struct Args {
   const int32_t* qzeros;
   const __half* scales;
   const int32_t* g_idx;
+  const float* row_scale;   // bf16 input: 2^e per row of A (the fp16 copy was divided by it)
   void* C;
   unsigned* status;
 };
@@ -158,113 +164,102 @@ __device__ __forceinline__ uint32_t local_code(const uint32_t (&w)[Geo<BITS>::kR
 }
 
 // ------------------------------------------------------------------------------ dequant
-// Per-group constants of one column: the exact-unpack constants of DiffPairs, the scale as a
-// 16-bit pair (fp16 output) or as fp32 (bf16 output), and the runtime zero.
-template <int BITS, typename T>
+// Per-group constants of one column: the exact-unpack constants of DiffPairs, the fp16 scale in
+// both halves of a word, the scale as fp32 and the runtime zero.
+template <int BITS>
 struct ColConsts {
-  using DPT = typename std::conditional<(BITS == 8 || !std::is_same<T, __nv_bfloat16>::value),
-                                        __half, T>::type;   // unpack type (bf16 8-bit: fp16)
-  uint32_t kz[BITS == 3 ? 1 : DiffPairs<DPT, BITS == 3 ? 4 : BITS>::kConsts];
-  uint32_t s2;   // fp16 scale in both halves
+  uint32_t kz[DiffPairs<__half, BITS>::kConsts];
+  uint32_t s2;
   float s;
   int z;
   __device__ __forceinline__ void set(float sc, uint16_t sbits, int zero) {
     s = sc;
     z = zero;
     s2 = static_cast<uint32_t>(sbits) | (static_cast<uint32_t>(sbits) << 16);
-    if constexpr (BITS != 3) DiffPairs<DPT, BITS>::consts(zero, kz);
+    if constexpr (BITS != 3) DiffPairs<__half, BITS>::consts(zero, kz);
   }
 };
 
-__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
-  __half2 r = __hmul2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
-  return *reinterpret_cast<uint32_t*>(&r);
-}
-__device__ __forceinline__ float bf_lo(uint32_t x) { return __uint_as_float(x << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
-__device__ __forceinline__ float h_lo(uint32_t x) { return __half2float(__ushort_as_half(static_cast<uint16_t>(x & 0xFFFFu))); }
-__device__ __forceinline__ float h_hi(uint32_t x) { return __half2float(__ushort_as_half(static_cast<uint16_t>(x >> 16))); }
-
-// Round (x0, x1) * s to bf16 and pack (x0 low half).
-__device__ __forceinline__ uint32_t scale_pack_bf16(float x0, float x1, float s) {
-  const float2 p = ptx::mul_f32x2(make_float2(x0, x1), make_float2(s, s));
-  return pack2(p.x, p.y, __nv_bfloat16());
-}
-
 // One 16-byte chunk (8 consecutive k of one column) for 4-bit: word w.
-template <typename T>
-__device__ __forceinline__ uint4 dq_chunk4(uint32_t w, const ColConsts<4, T>& cc) {
-  uint32_t d[4];
-  uint4 o;
-  if constexpr (std::is_same<T, __half>::value) {
-    DiffPairs<__half, 4>::run(w, cc.kz, d);              // d[p] = (k p, k p+4) - z, exact
-    uint32_t e[4];
+__device__ __forceinline__ uint4 dq_chunk4(uint32_t w, const ColConsts<4>& cc) {
+  uint32_t d[4], e[4];
+  DiffPairs<__half, 4>::run(w, cc.kz, d);                // d[p] = (k p, k p+4) - z, exact
 #pragma unroll
-    for (int p = 0; p < 4; ++p) e[p] = hmul2(d[p], cc.s2);   // one rounding: RN((q - z) s)
-    o.x = __byte_perm(e[0], e[1], 0x5410);
-    o.y = __byte_perm(e[2], e[3], 0x5410);
-    o.z = __byte_perm(e[0], e[1], 0x7632);
-    o.w = __byte_perm(e[2], e[3], 0x7632);
-  } else {
-    DiffPairs<__nv_bfloat16, 4>::run(w, cc.kz, d);
-    o.x = scale_pack_bf16(bf_lo(d[0]), bf_lo(d[1]), cc.s);
-    o.y = scale_pack_bf16(bf_lo(d[2]), bf_lo(d[3]), cc.s);
-    o.z = scale_pack_bf16(bf_hi(d[0]), bf_hi(d[1]), cc.s);
-    o.w = scale_pack_bf16(bf_hi(d[2]), bf_hi(d[3]), cc.s);
-  }
-  return o;
+  for (int p = 0; p < 4; ++p) e[p] = hmul2(d[p], cc.s2); // one rounding: RN((q - z) s)
+  return make_uint4(__byte_perm(e[0], e[1], 0x5410), __byte_perm(e[2], e[3], 0x5410),
+                    __byte_perm(e[0], e[1], 0x7632), __byte_perm(e[2], e[3], 0x7632));
 }
 
 // Two chunks (16 consecutive k of one column) for 2-bit: word w.
-template <typename T>
-__device__ __forceinline__ void dq_chunks2(uint32_t w, const ColConsts<2, T>& cc, uint4& lo, uint4& hi) {
-  uint32_t d[8];
-  if constexpr (std::is_same<T, __half>::value) {
-    DiffPairs<__half, 2>::run(w, cc.kz, d);              // d[p] = (k p, k p+8) - z
-    uint32_t e[8];
+__device__ __forceinline__ void dq_chunks2(uint32_t w, const ColConsts<2>& cc, uint4& lo, uint4& hi) {
+  uint32_t d[8], e[8];
+  DiffPairs<__half, 2>::run(w, cc.kz, d);                // d[p] = (k p, k p+8) - z
 #pragma unroll
-    for (int p = 0; p < 8; ++p) e[p] = hmul2(d[p], cc.s2);
-    lo = make_uint4(__byte_perm(e[0], e[1], 0x5410), __byte_perm(e[2], e[3], 0x5410),
-                    __byte_perm(e[4], e[5], 0x5410), __byte_perm(e[6], e[7], 0x5410));
-    hi = make_uint4(__byte_perm(e[0], e[1], 0x7632), __byte_perm(e[2], e[3], 0x7632),
-                    __byte_perm(e[4], e[5], 0x7632), __byte_perm(e[6], e[7], 0x7632));
-  } else {
-    DiffPairs<__nv_bfloat16, 2>::run(w, cc.kz, d);
-    lo = make_uint4(scale_pack_bf16(bf_lo(d[0]), bf_lo(d[1]), cc.s),
-                    scale_pack_bf16(bf_lo(d[2]), bf_lo(d[3]), cc.s),
-                    scale_pack_bf16(bf_lo(d[4]), bf_lo(d[5]), cc.s),
-                    scale_pack_bf16(bf_lo(d[6]), bf_lo(d[7]), cc.s));
-    hi = make_uint4(scale_pack_bf16(bf_hi(d[0]), bf_hi(d[1]), cc.s),
-                    scale_pack_bf16(bf_hi(d[2]), bf_hi(d[3]), cc.s),
-                    scale_pack_bf16(bf_hi(d[4]), bf_hi(d[5]), cc.s),
-                    scale_pack_bf16(bf_hi(d[6]), bf_hi(d[7]), cc.s));
-  }
+  for (int p = 0; p < 8; ++p) e[p] = hmul2(d[p], cc.s2);
+  lo = make_uint4(__byte_perm(e[0], e[1], 0x5410), __byte_perm(e[2], e[3], 0x5410),
+                  __byte_perm(e[4], e[5], 0x5410), __byte_perm(e[6], e[7], 0x5410));
+  hi = make_uint4(__byte_perm(e[0], e[1], 0x7632), __byte_perm(e[2], e[3], 0x7632),
+                  __byte_perm(e[4], e[5], 0x7632), __byte_perm(e[6], e[7], 0x7632));
 }
 
-// One chunk for 8-bit: words w0 (k 0..3) and w1 (k 4..7); the unpack is fp16 for both dtypes.
-template <typename T>
-__device__ __forceinline__ uint4 dq_chunk8(uint32_t w0, uint32_t w1, const ColConsts<8, T>& cc) {
+// One chunk for 8-bit: words w0 (k 0..3) and w1 (k 4..7).
+__device__ __forceinline__ uint4 dq_chunk8(uint32_t w0, uint32_t w1, const ColConsts<8>& cc) {
   uint32_t d0[2], d1[2];
   DiffPairs<__half, 8>::run(w0, cc.kz, d0);              // (k0, k2), (k1, k3) - z
   DiffPairs<__half, 8>::run(w1, cc.kz, d1);
-  uint4 o;
-  if constexpr (std::is_same<T, __half>::value) {
-    const uint32_t a0 = hmul2(d0[0], cc.s2), a1 = hmul2(d0[1], cc.s2);
-    const uint32_t b0 = hmul2(d1[0], cc.s2), b1 = hmul2(d1[1], cc.s2);
-    o.x = __byte_perm(a0, a1, 0x5410);
-    o.y = __byte_perm(a0, a1, 0x7632);
-    o.z = __byte_perm(b0, b1, 0x5410);
-    o.w = __byte_perm(b0, b1, 0x7632);
-  } else {
-    o.x = scale_pack_bf16(h_lo(d0[0]), h_lo(d0[1]), cc.s);
-    o.y = scale_pack_bf16(h_hi(d0[0]), h_hi(d0[1]), cc.s);
-    o.z = scale_pack_bf16(h_lo(d1[0]), h_lo(d1[1]), cc.s);
-    o.w = scale_pack_bf16(h_hi(d1[0]), h_hi(d1[1]), cc.s);
-  }
-  return o;
+  const uint32_t a0 = hmul2(d0[0], cc.s2), a1 = hmul2(d0[1], cc.s2);
+  const uint32_t b0 = hmul2(d1[0], cc.s2), b1 = hmul2(d1[1], cc.s2);
+  return make_uint4(__byte_perm(a0, a1, 0x5410), __byte_perm(a0, a1, 0x7632),
+                    __byte_perm(b0, b1, 0x5410), __byte_perm(b0, b1, 0x7632));
 }
 
-template <int BITS, typename T, bool PERK>
+// bf16 activations for the fp16 multiply: out[m][k] = fp16(A[m][k] * 2^-e_m), row_scale[m] = 2^e_m,
+// with max_k |A[m][k]| * 2^-e_m in [2^15, 2^16) -- below fp16's largest finite value for any bf16
+// significand.  Multiplying by a power of two is exact, and so is the conversion for every value in
+// fp16's normal range; values more than 2^29 below the row's largest round (their products are far
+// below the GEMM's absolute tolerance).  One CTA per row at a time, 16-byte loads and stores.
+__global__ void __launch_bounds__(256) k_rows_to_f16(const uint16_t* __restrict__ A, int M, int K,
+                                                     uint16_t* __restrict__ out, float* __restrict__ row_scale) {
+  __shared__ uint32_t warp_max[8];
+  for (int m = blockIdx.x; m < M; m += gridDim.x) {
+    const uint4* row = reinterpret_cast<const uint4*>(A + static_cast<long long>(m) * K);
+    uint4* orow = reinterpret_cast<uint4*>(out + static_cast<long long>(m) * K);
+    const int nv = K / 8;
+    uint32_t mx = 0u;
+    for (int i = threadIdx.x; i < nv; i += blockDim.x) {
+      const uint4 v = __ldg(row + i);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t x = (&v.x)[j];
+        mx = max(mx, max(x & 0x7FFFu, (x >> 16) & 0x7FFFu));
+      }
+    }
+    mx = __reduce_max_sync(0xFFFFFFFFu, mx);
+    if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = mx;
+    __syncthreads();
+    mx = 0u;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) mx = max(mx, warp_max[w]);
+    int e = mx ? static_cast<int>(mx >> 7) - 127 - 15 : 0;   // exponent field of max|a|, minus 15
+    e = e < -126 ? -126 : (e > 126 ? 126 : e);               // 2^e and 2^-e stay normal floats
+    const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+    for (int i = threadIdx.x; i < nv; i += blockDim.x) {
+      const uint4 v = __ldg(row + i);
+      uint4 o;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t x = (&v.x)[j];
+        (&o.x)[j] = pack2(__uint_as_float(x << 16) * inv, __uint_as_float(x & 0xFFFF0000u) * inv, __half());
+      }
+      orow[i] = o;
+    }
+    if (threadIdx.x == 0) row_scale[m] = __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
+    __syncthreads();                                       // warp_max is reused by the next row
+  }
+}
+
+// TOUT: the output (and activation) type; the multiply is fp16 x fp16 for both.
+template <int BITS, typename TOUT, bool PERK>
 __global__ void __launch_bounds__(kThreads, 1)
     k_prefill(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
               const Args a) {
@@ -353,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc =
-          ptx::umma_idesc_f16(std::is_same<T, __half>::value ? 0u : 1u, 128u, static_cast<uint32_t>(kBN));
+          ptx::umma_idesc_f16(0u, 128u, static_cast<uint32_t>(kBN));   // fp16 x fp16
       int s = 0, sb = 0;
       uint32_t ph = 0, phb = 0, aph = 0;
       bool ok = true;
@@ -409,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int pf_g = -1;                          // group whose scale/zero are prefetched
       uint16_t pf_s = 0;
       uint2 pf_z = make_uint2(0u, 0u);
-      ColConsts<BITS, T> cc;
+      ColConsts<BITS> cc;
       for (int ks = 0; ks < ksteps; ++ks) {
         if (!wait_bar(sy, full(s), ph)) { ok = false; break; }
         uint32_t wl[kHalfRows];
@@ -449,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               uint4 out = make_uint4(0u, 0u, 0u, 0u);
               if (k0 < a.K) {
                 group_at(k0);
-                if (n_ok) out = dq_chunk4<T>(wl[c], cc);
+                if (n_ok) out = dq_chunk4(wl[c], cc);
               }
               *reinterpret_cast<uint4*>(bt + swz(col, 4 * hf + c)) = out;
             }
@@ -460,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
               if (k0 < a.K) {
                 group_at(k0);
-                if (n_ok) dq_chunks2<T>(wl[i], cc, lo, hi);
+                if (n_ok) dq_chunks2(wl[i], cc, lo, hi);
               }
               *reinterpret_cast<uint4*>(bt + swz(col, 4 * hf + 2 * i)) = lo;
               *reinterpret_cast<uint4*>(bt + swz(col, 4 * hf + 2 * i + 1)) = hi;
@@ -472,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               uint4 out = make_uint4(0u, 0u, 0u, 0u);
               if (k0 < a.K) {
                 group_at(k0);
-                if (n_ok) out = dq_chunk8<T>(wl[2 * c], wl[2 * c + 1], cc);
+                if (n_ok) out = dq_chunk8(wl[2 * c], wl[2 * c + 1], cc);
               }
               *reinterpret_cast<uint4*>(bt + swz(col, 4 * hf + c)) = out;
             }
@@ -487,8 +482,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                   float v[8];
 #pragma unroll
                   for (int j = 0; j < 8; ++j) v[j] = diff_f32(local_code<BITS>(wl, c, j), cc.z) * cc.s;
-                  out = make_uint4(pack2(v[0], v[1], T()), pack2(v[2], v[3], T()),
-                                   pack2(v[4], v[5], T()), pack2(v[6], v[7], T()));
+                  out = make_uint4(pack2(v[0], v[1], __half()), pack2(v[2], v[3], __half()),
+                                   pack2(v[4], v[5], __half()), pack2(v[6], v[7], __half()));
                 }
               }
               *reinterpret_cast<uint4*>(bt + swz(col, 4 * hf + c)) = out;
@@ -507,8 +502,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float sj = __half2float(a.scales[static_cast<long long>(g) * a.N + n]);
                 v[j] = diff_f32(local_code<BITS>(wl, c, j), zero_of<BITS>(a, g, n)) * sj;
               }
-              out = make_uint4(pack2(v[0], v[1], T()), pack2(v[2], v[3], T()),
-                               pack2(v[4], v[5], T()), pack2(v[6], v[7], T()));
+              out = make_uint4(pack2(v[0], v[1], __half()), pack2(v[2], v[3], __half()),
+                               pack2(v[4], v[5], __half()), pack2(v[6], v[7], __half()));
             }
             *reinterpret_cast<uint4*>(bt + swz(col, 4 * hf + c)) = out;
           }
@@ -523,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------------- epilogue (warps 0-3)
     const int q = warp;   // TMEM lanes 32q .. 32q + 31
     uint32_t aph = 0;
-    T* C = static_cast<T*>(a.C);
+    TOUT* C = static_cast<TOUT*>(a.C);
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
       const int mt = t % num_m, nt = t / num_m;
       if (!wait_bar(sy, acc_full, aph)) break;
@@ -531,6 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
       for (int half = 0; half < 2; ++half) {
         const int m = mt * kBM + half * 128 + q * 32 + lane;
+        const float rs = (a.row_scale != nullptr && m < a.M) ? a.row_scale[m] : 1.0f;
 #pragma unroll 1
         for (int cc = 0; cc < kBN / 32; ++cc) {
           uint32_t r[32];
@@ -542,10 +538,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
               uint4 o;
-              o.x = pack2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]), T());
-              o.y = pack2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]), T());
-              o.z = pack2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]), T());
-              o.w = pack2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]), T());
+              o.x = pack2(__uint_as_float(r[8 * v + 0]) * rs, __uint_as_float(r[8 * v + 1]) * rs, TOUT());
+              o.y = pack2(__uint_as_float(r[8 * v + 2]) * rs, __uint_as_float(r[8 * v + 3]) * rs, TOUT());
+              o.z = pack2(__uint_as_float(r[8 * v + 4]) * rs, __uint_as_float(r[8 * v + 5]) * rs, TOUT());
+              o.w = pack2(__uint_as_float(r[8 * v + 6]) * rs, __uint_as_float(r[8 * v + 7]) * rs, TOUT());
               dst[v] = o;
             }
           }
@@ -599,8 +595,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-template <int BITS, typename T, bool PERK>
-cudaError_t launch_typed(const Problem& p, cudaStream_t stream) {
+template <int BITS, typename TOUT, bool PERK>
+cudaError_t launch_typed(const Problem& p, const void* A16, const float* row_scale, cudaStream_t stream) {
   using Gm = Geo<BITS>;
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
@@ -610,9 +606,7 @@ cudaError_t launch_typed(const Problem& p, cudaStream_t stream) {
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.K) * 2};
     const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(kBM)};
     const cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(&tmA, std::is_same<T, __half>::value ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
-                                                          : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                     2, const_cast<void*>(p.A), dims, strides, box, estr,
+    CUresult r = enc(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(A16), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
@@ -634,9 +628,10 @@ cudaError_t launch_typed(const Problem& p, cudaStream_t stream) {
   a.qzeros = p.qzeros;
   a.scales = static_cast<const __half*>(p.scales);
   a.g_idx = p.g_idx;
+  a.row_scale = row_scale;
   a.C = p.out;
   a.status = p.status;
-  auto kern = k_prefill<BITS, T, PERK>;
+  auto kern = k_prefill<BITS, TOUT, PERK>;
   static bool attr_set = false;   // per instantiation; the attribute is per function
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -650,16 +645,27 @@ cudaError_t launch_typed(const Problem& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-template <int BITS, typename T>
-cudaError_t launch_t(const Problem& p, cudaStream_t stream) {
+template <int BITS, typename TOUT>
+cudaError_t launch_t(const Problem& p, const void* A16, const float* row_scale, cudaStream_t stream) {
   // fast path: one group per unpacked word (2-bit words hold 16 k) and per 8-k chunk
   const bool perk = p.g_idx != nullptr || (p.group % (BITS == 2 ? 16 : 8)) != 0;
-  return perk ? launch_typed<BITS, T, true>(p, stream) : launch_typed<BITS, T, false>(p, stream);
+  return perk ? launch_typed<BITS, TOUT, true>(p, A16, row_scale, stream)
+              : launch_typed<BITS, TOUT, false>(p, A16, row_scale, stream);
 }
 
 template <int BITS>
 cudaError_t launch_bits(const Problem& p, cudaStream_t stream) {
-  return p.dtype == 0 ? launch_t<BITS, __half>(p, stream) : launch_t<BITS, __nv_bfloat16>(p, stream);
+  if (p.dtype == 0) return launch_t<BITS, __half>(p, p.A, nullptr, stream);
+  // bf16: the fp16 copy of A and the row scales in the caller's workspace
+  const size_t a_bytes = (static_cast<size_t>(p.M) * p.K * 2 + 255) & ~static_cast<size_t>(255);
+  if (p.workspace == nullptr || p.workspace_bytes < prefill_workspace_bytes(p.M, p.K)) return cudaErrorInvalidValue;
+  uint16_t* A16 = static_cast<uint16_t*>(p.workspace);
+  float* row_scale = reinterpret_cast<float*>(static_cast<unsigned char*>(p.workspace) + a_bytes);
+  const int blocks = p.M < device_info().sm_count * 8 ? p.M : device_info().sm_count * 8;
+  k_rows_to_f16<<<blocks, 256, 0, stream>>>(static_cast<const uint16_t*>(p.A), p.M, p.K, A16, row_scale);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_t<BITS, __nv_bfloat16>(p, A16, row_scale, stream);
 }
 
 }  // namespace prefill
@@ -667,6 +673,12 @@ cudaError_t launch_bits(const Problem& p, cudaStream_t stream) {
 cudaError_t launch_wait_selftest(unsigned* status, uint64_t limit_ns, int* flag, cudaStream_t stream) {
   prefill::k_wait_selftest<<<1, 32, 0, stream>>>(status, limit_ns, flag);
   return cudaGetLastError();
+}
+
+size_t prefill_workspace_bytes(int M, int K) {
+  if (M <= 0 || K <= 0) return 0;
+  return ((static_cast<size_t>(M) * K * 2 + 255) & ~static_cast<size_t>(255)) +
+         ((static_cast<size_t>(M) * 4 + 255) & ~static_cast<size_t>(255));
 }
 
 cudaError_t launch_prefill(const Problem& p, cudaStream_t stream) {

@@ -109,9 +109,19 @@ int gptq_dequant(const int32_t* qweight, const int32_t* qzeros, const void* scal
  * distributed shared memory); larger M runs the tcgen05 tensor-core kernel, and so does M <= 32
  * when K is so long that the decode kernel's staged activations fit no CTA even split 16 ways
  * (K beyond 28672 with many tokens).
- * Device pointers: A, qweight, qzeros, scales, g_idx (nullable), C.  `workspace` may be NULL
- * when gptq_gemm_workspace_size() returns 0 (every current path); otherwise it must be a
- * device buffer of at least that many bytes, owned by the caller.
+ * The multiply is fp16 x fp16 with fp32 accumulation for both activation types: weights are
+ * rounded once to fp16 (the exact product (q - zero) * scale, as gptq_dequant gives it), and
+ * bf16 activations are multiplied as fp16 times a power of two per row (exact for every value
+ * in fp16's normal range; values more than 2^29 below the row's largest may round), the power
+ * of two multiplied back into the fp32 result.  A weight rounded to bf16 would carry up to 2^-8
+ * relative error, more than the 2e-3 accuracy bound; fp16 carries 2^-11.  Consequently a
+ * dequantized weight beyond fp16's range (|(q - zero) * scale| > 65504, i.e. scale > 256 for
+ * 8-bit codes) is outside what the per-weight and tensor-core paths handle, for either dtype.
+ * Device pointers: A, qweight, qzeros, scales, g_idx (nullable), C, workspace.  `workspace`
+ * (16-byte aligned, owned by the caller) is used only when A is bf16 and the tensor-core kernel
+ * runs: it then holds the fp16 copy of A and its row scales and must be at least
+ * gptq_gemm_workspace_size() bytes (GPTQ_ERR_WORKSPACE otherwise, nothing launched).  With fp16
+ * activations, or M <= 32 and K within the decode kernel's reach, it may be NULL.
  * Returns GPTQ_OK or a negative gptq_status.
  */
 int gptq_gemm(const void* A, int M, int K, int a_dtype, const int32_t* qweight,
@@ -202,7 +212,9 @@ int gptq_gemm_perm_noalloc(const void* A, int M, int K, int a_dtype, const int32
                            const int32_t* qweight, const int32_t* qzeros, const void* scales,
                            int N, int bits, int group, int fmt, void* C, void* stream);
 
-/* Bytes of device workspace gptq_gemm needs for this problem (0 for every current path). */
+/* Bytes of device workspace gptq_gemm may need for this problem: the fp16 copy of bf16
+ * activations and their row scales, (M * K * 2 rounded up to 256) + (M * 4 rounded up to 256);
+ * 0 for M <= 0.  Enough for every activation dtype and path. */
 size_t gptq_gemm_workspace_size(int M, int K, int N, int bits, int group);
 
 /*

@@ -152,12 +152,22 @@ def test_raw_checkpoint_gemm_with_outliers_and_degenerate_columns(bits, dt, fmt,
 @pytest.mark.parametrize("bits,dt,fmt,act", RAW)
 def test_raw_checkpoint_dequant_and_one_hot_rows_bit_exact(bits, dt, fmt, act):
     """gptq_dequant equals the oracle bit for bit, and one-hot rows of A through every GEMM path
-    (M = 1, 16, 32 decode; 130 tensor-core) reproduce those rows of the dequantized weight."""
+    (M = 1, 16, 32 decode; 130 tensor-core) reproduce those rows of the dequantized weight.
+
+    The GEMMs multiply in fp16 for both activation types.  The per-weight and tensor-core paths
+    (act-order, M > 32) multiply the weight rounded to fp16, so with bf16 outputs a one-hot row
+    gives that fp16 weight rounded again to bf16; the folded decode path keeps the exact product
+    (q - zero) * scale in fp32 and rounds it once."""
     ck = _raw(bits, dt, fmt, act)
     qw, qz, sc, gi = dev(ck)
     K, N = ck["K"], ck["N"]
     ref = oracle.dequant(ck["qweight"], ck["qzeros"], ck["scales"], ck["g_idx"], K, N, bits, 128,
                          ck["fmt"], ODT[dt])
+    ref_via_f16 = ref
+    if dt == "bf16":
+        w16 = oracle.dequant(ck["qweight"], ck["qzeros"], ck["scales"], ck["g_idx"], K, N, bits, 128,
+                             ck["fmt"], oracle.F16)
+        ref_via_f16 = oracle.round_to(oracle.to_double(w16, oracle.F16).astype(np.float32), oracle.BF16)
     W = g.dequant(qw, qz, sc, gi, K=K, bits=bits, group=128, fmt=ck["fmt"], dtype=TDT[dt])
     got = bits16(W)
     assert np.array_equal(got, ref), "dequant: %d mismatches" % int((got != ref).sum())
@@ -170,7 +180,7 @@ def test_raw_checkpoint_dequant_and_one_hot_rows_bit_exact(bits, dt, fmt, act):
         torch.cuda.synchronize()
         c = bits16(C)
         # -0 and +0 both represent an exact zero
-        exp = ref[rows]
+        exp = (ref_via_f16 if (act or M > 32) else ref)[rows]
         same = (c == exp) | (((c & 0x7FFF) == 0) & ((exp & 0x7FFF) == 0))
         assert same.all(), "M=%d: %d of %d outputs differ from dequant" % (M, int((~same).sum()), same.size)
 

@@ -37,7 +37,9 @@ def test_exports_every_declared_symbol(lib):
 def test_strerror_and_workspace(lib):
     for code in range(0, -9, -1):
         assert g.strerror(code).startswith(g._STATUS[code])
-    assert g.workspace_size(1, 4096, 11008, 4, 128) == 0
+    assert g.workspace_size(1, 4096, 11008, 4, 128) == 8192 + 256        # fp16 copy of A + row scale
+    assert g.workspace_size(4096, 4096, 14336, 4, 128) == 4096 * 4096 * 2 + 4096 * 4
+    assert g.workspace_size(0, 4096, 11008, 4, 128) == 0
 
 
 P = ctypes.c_void_p
@@ -221,7 +223,7 @@ int main(void) {
                 NULL) != GPTQ_ERR_ARG) return 2;
   if (gptq_gemm_grouped(NULL, 0, 256, GPTQ_F16, NULL, 1, 8, NULL, NULL, NULL, 256, 4, 128,
                         GPTQ_FMT_V2, NULL, NULL) != GPTQ_ERR_ARG) return 3;
-  if (gptq_gemm_workspace_size(1, 4096, 11008, 4, 128) != 0) return 4;
+  if (gptq_gemm_workspace_size(1, 4096, 11008, 4, 128) != 8448) return 4;
   if (strlen(gptq_strerror(GPTQ_ERR_SHAPE)) == 0) return 5;
   printf("c consumer ok\n");
   return 0;
