@@ -5,7 +5,11 @@ group 128, GPTQv2 -- metric "M=1 decode weight GB/s" with algorithmic bytes = qw
 qzeros + A.  One step = one gptq_gemm launch on one batch (M = 1 token).  Steps run as CUDA-graph
 replays over S rotating copies of the weights whose total size is more than 3x the L2 cache, so
 every step reads its weights from HBM.  The same line carries the secondary figure of the
-metric: M = 4096 prefill TFLOP/s (A bf16 [4096, 4096] x W [4096, 14336] 4-bit g128).
+metric (M = 4096 prefill TFLOP/s, A bf16 [4096, 4096] x W [4096, 14336] 4-bit g128) and a
+per-configuration section: every one of the five workload configurations at its exact shape
+(decode at each of its token counts, act-order through gptq_gemm and prepacked, the three
+prefill variants), the standalone dequant and the mixture-of-experts layer, each timed as the
+median of 10 graph replays (a first replay discarded) with its roofline fraction.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -139,6 +143,31 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(sel), "window": window}
 
 
+# ------------------------------------------------------------------------------------ host
+def host_info():
+    """Core count and CPU model of the host the CPU legs run on."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if model is None:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for line in f:
+                    if line.lower().startswith("model name"):
+                        model = line.split(":", 1)[1].strip()
+                        break
+        except Exception:
+            pass
+    import platform
+    return {"nproc": os.cpu_count(), "cpu_model": model, "machine": platform.machine()}
+
+
 # ------------------------------------------------------------------------------------ ranks
 def max_over_ranks(x, dist, device):
     """The largest value of x over all ranks (x itself on one rank)."""
@@ -156,6 +185,41 @@ def whole_job_gbs(world, bytes_per_step, steps, seconds):
     return world * bytes_per_step * steps / seconds / 1e9
 
 
+# ------------------------------------------------------------------------------------ timing
+def replay_median(torch, stream, graph, launches, replays=11):
+    """Per-launch time of a captured graph of `launches` launches: `replays` replays, each timed
+    with CUDA events on the launching stream; the first is discarded and the median of the rest
+    is returned (ms per launch), with the spread (min, max) of those replays."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(replays)]
+    with torch.cuda.stream(stream):
+        for st, en in evs:
+            st.record(stream)
+            graph.replay()
+            en.record(stream)
+    stream.synchronize()
+    ms = [st.elapsed_time(en) / launches for st, en in evs[1:]]
+    return float(np.median(ms)), float(min(ms)), float(max(ms))
+
+
+def capture(torch, stream, launch, n):
+    """Run `launch(i)` for i < n once (kernel attributes are set outside capture), then capture n
+    launches in one CUDA graph."""
+    with torch.cuda.stream(stream):
+        for i in range(n):
+            launch(i)
+    stream.synchronize()
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr, stream=stream):
+        for i in range(n):
+            launch(i)
+    return gr
+
+
+def roofline(achieved, peak, unit, bound, source, traffic=None):
+    return {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+            "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": source}
+
+
 # ------------------------------------------------------------------------------------ our arm
 def run_ours(args, rank, world, local_rank):
     import torch
@@ -168,7 +232,8 @@ def run_ours(args, rank, world, local_rank):
     stream = torch.cuda.Stream(device=dev)
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 0) or L2_BYTES_FALLBACK
-    hbm_peak, bf16_peak, bf16_sust, peak_src = load_peaks()
+    peaks = load_peaks()
+    hbm_peak, bf16_peak, bf16_sust, peak_src = peaks
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -176,6 +241,9 @@ def run_ours(args, rank, world, local_rank):
     def barrier():
         if dist is not None:
             dist.barrier()
+
+    uuid = "GPU-" + str(props.uuid) if hasattr(props, "uuid") else str(local_rank)
+    sampler = ClockSampler(uuid)
 
     # ---- inputs: seeded draws -> device -> GPU round-to-nearest checkpoint writer
     wl, M = DECODE, 1
@@ -196,24 +264,11 @@ def run_ours(args, rank, world, local_rank):
 
     # ---- CUDA graphs of R launches (and one of the remainder) replayed for exact step counts
     R = S * max(1, 256 // S)
-    with torch.cuda.stream(stream):
-        for i in range(2 * S):
-            launch(i)   # sets kernel attributes before capture
-    stream.synchronize()
-
-    def capture(n):
-        gr = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gr, stream=stream):
-            for i in range(n):
-                launch(i)
-        return gr
-
-    main_graph = capture(R)
+    main_graph = capture(torch, stream, launch, R)
     rem_graphs = {}
-
     for n in (args.warmup, args.steps):   # every graph is captured before anything is timed
         if n % R and n % R not in rem_graphs:
-            rem_graphs[n % R] = capture(n % R)
+            rem_graphs[n % R] = capture(torch, stream, launch, n % R)
 
     def run_steps(n):
         for _ in range(n // R):
@@ -221,16 +276,38 @@ def run_ours(args, rank, world, local_rank):
         if n % R:
             rem_graphs[n % R].replay()
 
-    uuid = "GPU-" + str(props.uuid) if hasattr(props, "uuid") else str(local_rank)
-    sampler = ClockSampler(uuid)
+    # kernel figure the replay way: median of 10 replays of R launches (first replay discarded),
+    # and one launch on its own
+    med_ms, min_ms, max_ms = replay_median(torch, stream, main_graph, R)
+    single = []
+    with torch.cuda.stream(stream):
+        for i in range(12):
+            st, en = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            st.record(stream)
+            launch(i)
+            en.record(stream)
+            stream.synchronize()
+            single.append(st.elapsed_time(en))
+    single_ms = float(np.median(single[2:]))
+
     with torch.cuda.stream(stream):
         run_steps(args.warmup)
     stream.synchronize()
+    # clock window: the timed region of a short run lasts well under the sampler's 100 ms period,
+    # so the same graph keeps the GPU busy for about a second right before it
+    tc0 = time.time()
+    with torch.cuda.stream(stream):
+        while time.time() - tc0 < 1.2:
+            main_graph.replay()
+            stream.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
     t0 = time.time()
     with torch.cuda.stream(stream):
+        # a short GPU sleep queued ahead of the start event: the graph launches are enqueued while
+        # it runs, so the timed region holds the K steps back to back and no host launch latency
+        torch.cuda._sleep(200000)
         start.record(stream)
         run_steps(args.steps)
         end.record(stream)
@@ -242,6 +319,8 @@ def run_ours(args, rank, world, local_rank):
     ms_per_step = ms_total / args.steps
     value = whole_job_gbs(world, set_bytes, args.steps, ms_total * 1e-3)   # GB/s over all ranks
     kernel_gbs = set_bytes / (ms_per_step * 1e-3) / 1e9                 # per launch, this GPU
+    clocks = sampler.summary(tc0, t1)
+    clocks["window"] = "timed region and the 1.2 s of the same graph replays before it"
 
     # ---- end to end through the public API: A from pinned host memory, C read back
     a_host = A.cpu().pin_memory()
@@ -265,13 +344,16 @@ def run_ours(args, rank, world, local_rank):
         te1 = time.perf_counter()
     e2e_s = max_over_ranks(te1 - te0, dist, dev)
     e2e_value = whole_job_gbs(world, set_bytes, n_e2e, e2e_s)
-    sampler.stop()
-    clocks = sampler.summary(t0, t1)
+    del sets, main_graph, rem_graphs
+    torch.cuda.synchronize()
 
-    # ---- secondary figure: M = 4096 prefill TFLOP/s
-    prefill = run_prefill(g, torch, dev, stream, bf16_peak, peak_src, l2) if not args.skip_prefill else None
+    # ---- the secondary figure (M = 4096 prefill) and the per-configuration section
+    configs = None if args.skip_configs else run_configs(g, torch, dev, stream, peaks, l2, args.config_filter)
+    sampler.stop()
+    prefill = None
+    if configs is not None:
+        prefill = next((r for r in configs if r["workload"] == PREFILL.name and r["path"] == "gptq_gemm"), None)
     sweep = run_sweep(g, torch, dev, stream, hbm_peak, bf16_peak, l2, args.sweep_filter) if args.all else None
-    del sets
     torch.cuda.synchronize()
     assert g.device_status(stream) == 0, "device status word reported an error"
 
@@ -294,11 +376,18 @@ def run_ours(args, rank, world, local_rank):
                    "accumulate": "fp32", "bytes_per_step": set_bytes,
                    "l2": "inputs rotate over %d weight sets = %.0f MB > 3x L2 (%.0f MB)" % (
                        S, S * set_bytes / 1e6, l2 / 1e6),
-                   "timing": "CUDA events on the launching stream around CUDA-graph replays",
+                   "timing": "CUDA events on the launching stream around CUDA-graph replays of the K "
+                             "steps, queued behind a short GPU sleep so that no host launch latency "
+                             "falls inside the timed region",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
-        "roofline": {"bound": "hbm", "achieved": round(kernel_gbs, 1), "peak": hbm_peak,
-                     "unit": "GB/s", "frac": round(kernel_gbs / hbm_peak, 4),
-                     "traffic": traffic, "peak_source": peak_src + " (hbm_gbs)"},
+        "roofline": roofline(kernel_gbs, hbm_peak, "GB/s", "hbm", peak_src + " (hbm_gbs)", traffic),
+        "kernel_replays": {"us_median": round(med_ms * 1e3, 3), "us_min": round(min_ms * 1e3, 3),
+                           "us_max": round(max_ms * 1e3, 3), "launches_per_replay": R, "replays": 10,
+                           "GB/s": round(set_bytes / (med_ms * 1e-3) / 1e9, 1),
+                           "frac": round(set_bytes / (med_ms * 1e-3) / 1e9 / hbm_peak, 4),
+                           "single_launch_us": round(single_ms * 1e3, 3),
+                           "note": "median of 10 replays of one graph (a first replay discarded); "
+                                   "single launch: event pair around one launch, synchronized"},
         "e2e": {"value": round(e2e_value, 3), "unit": "GB/s", "h2d_bytes_per_step": M * wl.K * 2,
                 "d2h_bytes_per_step": M * wl.N * 2,
                 "note": "weights resident on the device (the model); per step: A host->device, "
@@ -308,100 +397,136 @@ def run_ours(args, rank, world, local_rank):
     }
     if prefill is not None:
         line["prefill"] = prefill
+    if configs is not None:
+        line["configs"] = configs
     if sweep is not None:
         line["all_workloads"] = sweep
     return line
 
 
-def run_prefill(g, torch, dev, stream, bf16_peak, peak_src, l2):
-    wl = PREFILL
-    M = wl.Ms[0]
-    draw = gptq_inputs.draw_weights(wl)
-    W = torch.from_numpy(draw.W).to(dev)
-    qw, qz, sc = g.quantize_rtn(W, bits=wl.bits, group=wl.group, fmt=g.V2)
-    del W
-    A = gptq_inputs.draw_activations(wl, M).to(dev)
-    C = torch.empty((M, wl.N), dtype=A.dtype, device=dev)
-    flop = 2.0 * M * wl.N * wl.K
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            g.gemm(A, qw, qz, sc, bits=wl.bits, group=wl.group, out=C, stream=stream)
-        stream.synchronize()
-        n = 10
-        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s.record(stream)
-        for _ in range(n):
-            g.gemm(A, qw, qz, sc, bits=wl.bits, group=wl.group, out=C, stream=stream)
-        e.record(stream)
-    stream.synchronize()
-    ms = s.elapsed_time(e) / n
-    tflops = flop / (ms * 1e-3) / 1e12
-    return {"workload": "prefill_4bit_g128", "M": M, "K": wl.K, "N": wl.N, "value": round(tflops, 2),
-            "unit": "TFLOP/s", "ms_per_launch": ms,
-            "roofline": {"bound": "tensor", "achieved": round(tflops, 2), "peak": bf16_peak,
-                         "unit": "TFLOP/s", "frac": round(tflops / bf16_peak, 4),
-                         "traffic": load_traffic("prefill_4bit"),
-                         "peak_source": peak_src + " (bf16_tflops, burst)"},
-            "note": "A (33.5 MB) and W (29 MB) fit in L2 but are re-read per tile; timed back to back"}
-
-
-# ------------------------------------------------------------------------------------ sweep
-def time_workload(g, torch, dev, stream, wl, M, fmt, l2, reps=200, prepacked=False):
-    """Per-launch time of gptq_gemm on one workload: CUDA graph of `reps` launches over weight
-    copies whose total exceeds 3x L2 (or the whole problem when one copy is larger).
-    prepacked: an act-order checkpoint with its rows sorted by group (gptq_prepack_act_order),
-    multiplied by gptq_gemm_perm."""
+# ------------------------------------------------------------------------------------ configs
+def _checkpoint(g, torch, dev, wl, fmt=None):
     draw = gptq_inputs.draw_weights(wl)
     W = torch.from_numpy(draw.W).to(dev)
     gi = None if draw.g_idx is None else torch.from_numpy(draw.g_idx).to(dev)
-    f = g.V2 if fmt == "v2" else g.V1
+    f = fmt if fmt is not None else g.V2
     qw, qz, sc = g.quantize_rtn(W, bits=wl.bits, group=wl.group, g_idx=gi, sym=wl.sym, fmt=f)
     del W
-    perm = None
-    if prepacked:
+    return draw, qw, qz, sc, gi
+
+
+def time_gemm(g, torch, dev, stream, wl, M, l2, path="gemm", fmt=None, reps=200):
+    """Median per-launch time of one GEMM call on one workload: a CUDA graph of launches over S
+    rotating copies of every input (S x bytes > 3x L2 where one copy is smaller), replayed 11
+    times, the first replay discarded.  path: "gemm" (gptq_gemm, with g_idx for act-order),
+    "perm" (act-order rows sorted on the host, gptq_gemm_perm) or "dequant" (gptq_dequant)."""
+    f = fmt if fmt is not None else g.V2
+    draw, qw, qz, sc, gi = _checkpoint(g, torch, dev, wl, f)
+    perm = ws = None
+    if path == "perm":
         qw2, p = g.prepack_act_order(qw.cpu().numpy(), draw.g_idx, K=wl.K, N=wl.N, bits=wl.bits,
                                      group=wl.group)
-        qw, perm = torch.from_numpy(qw2).to(dev), torch.from_numpy(p).to(dev)
+        qw, perm, gi = torch.from_numpy(qw2).to(dev), torch.from_numpy(p).to(dev), None
         ws = torch.empty(max(1, g.gemm_perm_workspace_size(M, wl.K)), dtype=torch.uint8, device=dev)
-    A = gptq_inputs.draw_activations(wl, M).to(dev)
-    nbytes = algorithmic_bytes(wl, M)
-    S = max(1, min(256, int(np.ceil(3 * l2 / nbytes))))   # > 3x L2 of weights (the tiny case: L2)
-    sets = [(qw.clone(), qz.clone(), sc.clone(), A.clone(),
-             torch.empty((M, wl.N), dtype=A.dtype, device=dev)) for _ in range(S)]
-    n = max(S, (reps // S) * S) if M <= 64 else S * max(1, 8 // S)
+    A = gptq_inputs.draw_activations(wl, M).to(dev) if path != "dequant" else None
+    if path == "dequant":
+        out_shape, out_dt = (wl.K, wl.N), torch.float16 if wl.act_dtype == "f16" else torch.bfloat16
+        nbytes = algorithmic_bytes(wl, 0) - (wl.K * 4 if wl.act_order else 0) + wl.K * wl.N * 2
+    else:
+        out_shape, out_dt = (M, wl.N), A.dtype
+        nbytes = algorithmic_bytes(wl, M)
+    per_set = nbytes + (0 if path == "dequant" else M * wl.N * 2)
+    # bf16 activations through the tensor-core kernel: the caller's workspace (fp16 copy of A)
+    gws = None
+    if path == "gemm" and A is not None and A.dtype == torch.bfloat16:
+        gws = torch.empty(g.workspace_size(M, wl.K, wl.N, wl.bits, wl.group), dtype=torch.uint8, device=dev)
+    S = max(1, min(256, int(np.ceil(3 * l2 / per_set))))
+    sets = [(qw.clone(), qz.clone(), sc.clone(), None if A is None else A.clone(),
+             torch.empty(out_shape, dtype=out_dt, device=dev)) for _ in range(S)]
+    n = S * max(1, reps // S) if (M <= 64 and path != "dequant") else S * max(1, 8 // S)
 
     def launch(i):
         q, z, s_, a, c = sets[i % S]
-        if prepacked:
+        if path == "perm":
             g.gemm_perm(a, perm, q, z, s_, bits=wl.bits, group=wl.group, fmt=f, out=c, workspace=ws,
                         stream=stream)
+        elif path == "dequant":
+            g.dequant(q, z, s_, gi, K=wl.K, bits=wl.bits, group=wl.group, fmt=f, dtype=out_dt, out=c,
+                      stream=stream)
         else:
-            g.gemm(a, q, z, s_, gi, bits=wl.bits, group=wl.group, fmt=f, out=c, stream=stream)
+            g.gemm(a, q, z, s_, gi, bits=wl.bits, group=wl.group, fmt=f, out=c, workspace=gws, stream=stream)
 
-    with torch.cuda.stream(stream):
-        for i in range(2 * S):
-            launch(i)
-    stream.synchronize()
-    gr = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(gr, stream=stream):
-        for i in range(n):
-            launch(i)
-    with torch.cuda.stream(stream):
-        gr.replay()
-        st, en = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        st.record(stream)
-        for _ in range(3):
-            gr.replay()
-        en.record(stream)
-    stream.synchronize()
-    ms = st.elapsed_time(en) / (3 * n)
+    gr = capture(torch, stream, launch, n)
+    ms, ms_min, ms_max = replay_median(torch, stream, gr, n)
     del sets, gr
-    return ms, nbytes
+    return ms, nbytes, S
 
 
+def run_configs(g, torch, dev, stream, peaks, l2, only=""):
+    """Every workload configuration at its exact shape, with its roofline fraction."""
+    hbm_peak, bf16_peak, _, src = peaks
+    W = gptq_inputs.WORKLOADS
+    plan = [
+        # (config, workload, M, path, label)
+        ("1", "tiny_4bit_g64", 4, "gemm", "correctness case"),
+        ("2", "llama7b_decode_4bit_g128", 1, "gemm", ""),
+        ("2", "llama7b_decode_4bit_g128", 8, "gemm", ""),
+        ("2", "llama7b_decode_4bit_g128", 16, "gemm", ""),
+        ("3", "lowbit_2bit_g64", 1, "gemm", ""),
+        ("3", "lowbit_2bit_g64", 8, "gemm", ""),
+        ("3", "lowbit_2bit_g64", 32, "gemm", ""),
+        ("4", "act_order_3bit_g128", 16, "gemm", "g_idx through gptq_gemm"),
+        ("4", "act_order_3bit_g128", 16, "perm", "rows sorted on the host, gptq_gemm_perm"),
+        ("5", "prefill_4bit_g128", 4096, "gemm", ""),
+        ("5", "prefill_8bit_sym_g128", 4096, "gemm", ""),
+        ("5", "prefill_4bit_gall", 4096, "gemm", ""),
+        ("5", "prefill_4bit_g128", 0, "dequant", "gptq_dequant to bf16"),
+        ("2", "llama7b_decode_4bit_g128", 0, "dequant", "gptq_dequant to fp16"),
+    ]
+    rows = []
+    for cfg, name, M, path, label in plan:
+        if only and only not in name:
+            continue
+        wl = W[name]
+        ms, nbytes, S = time_gemm(g, torch, dev, stream, wl, M, l2, path=path)
+        row = {"config": cfg, "workload": name, "M": M, "path": {"gemm": "gptq_gemm", "perm": "gptq_gemm_perm",
+                                                                 "dequant": "gptq_dequant"}[path],
+               "us": round(ms * 1e3, 3)}
+        if label:
+            row["note"] = label
+        if path != "dequant" and M > g.DECODE_MAX_M:
+            tflops = 2.0 * M * wl.N * wl.K / (ms * 1e-3) / 1e12
+            key = {"prefill_4bit_g128": "prefill_4bit"}.get(name)
+            row.update(value=round(tflops, 2), unit="TFLOP/s",
+                       roofline=roofline(tflops, bf16_peak, "TFLOP/s", "tensor", src + " (bf16_tflops, burst)",
+                                         load_traffic(key) if key else None))
+        else:
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            key = {("llama7b_decode_4bit_g128", 1): "decode_m1_4bit"}.get((name, M)) if path == "gemm" else None
+            row.update(value=round(gbs, 1), unit="GB/s", bytes=nbytes,
+                       roofline=roofline(gbs, hbm_peak, "GB/s", "hbm", src + " (hbm_gbs)",
+                                         load_traffic(key) if key else None))
+        row["inputs"] = "%d rotating copies (%.0f MB)" % (S, S * nbytes / 1e6)
+        rows.append(row)
+        print(json.dumps(row), file=sys.stderr, flush=True)
+    for name, mw in gptq_inputs.MOE_WORKLOADS.items():
+        if only and only not in name:
+            continue
+        for T in mw.Ts:
+            ms, nbytes, active, nrows, max_m = time_grouped(g, torch, dev, stream, mw, T, l2)
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            row = {"config": "moe", "workload": name, "M": T, "path": "gptq_gemm_grouped", "rows": nrows,
+                   "experts_active": active, "us": round(ms * 1e3, 3), "value": round(gbs, 1), "unit": "GB/s",
+                   "bytes": nbytes, "roofline": roofline(gbs, hbm_peak, "GB/s", "hbm", src + " (hbm_gbs)")}
+            rows.append(row)
+            print(json.dumps(row), file=sys.stderr, flush=True)
+    return rows
+
+
+# ------------------------------------------------------------------------------------ sweep
 def time_grouped(g, torch, dev, stream, mw, T, l2, reps=200):
-    """Per-launch time of gptq_gemm_grouped on a mixture-of-experts layer: T tokens routed to
-    top-k experts (rows grouped by expert), CUDA graph of launches over expert-weight copies
+    """Median per-launch time of gptq_gemm_grouped on a mixture-of-experts layer: T tokens routed
+    to top-k experts (rows grouped by expert), CUDA graph of launches over expert-weight copies
     whose total exceeds 3x L2."""
     r = gptq_inputs.draw_routing(mw, T)
     toks = gptq_inputs.draw_token_activations(mw, T)
@@ -429,28 +554,15 @@ def time_grouped(g, torch, dev, stream, mw, T, l2, reps=200):
         g.gemm_grouped(A, offsets, q, z, s_, bits=mw.bits, group=mw.group, max_m=max_m, fmt=g.V2, out=c,
                        stream=stream)
 
-    with torch.cuda.stream(stream):
-        for i in range(2 * S):
-            launch(i)
-    stream.synchronize()
-    gr = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(gr, stream=stream):
-        for i in range(n):
-            launch(i)
-    with torch.cuda.stream(stream):
-        gr.replay()
-        st, en = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        st.record(stream)
-        for _ in range(3):
-            gr.replay()
-        en.record(stream)
-    stream.synchronize()
-    ms = st.elapsed_time(en) / (3 * n)
+    gr = capture(torch, stream, launch, n)
+    ms, _, _ = replay_median(torch, stream, gr, n)
     del sets, gr
     return ms, nbytes, active, int(r.offsets[-1]), max_m
 
 
 def run_sweep(g, torch, dev, stream, hbm_peak, bf16_peak, l2, only=""):
+    """--all: every workload x token count x checkpoint format (v1 and v2), gptq_gemm and, for
+    act-order, the prepacked call."""
     rows = []
     for name, wl in gptq_inputs.WORKLOADS.items():
         if only not in name:
@@ -462,8 +574,8 @@ def run_sweep(g, torch, dev, stream, hbm_peak, bf16_peak, l2, only=""):
             for fmt, pre in variants:
                 if pre and M > g.DECODE_MAX_M:
                     continue
-                ms, nbytes = time_workload(g, torch, dev, stream, wl, M, fmt.split("+")[0], l2,
-                                           prepacked=pre)
+                f = g.V2 if fmt.startswith("v2") else g.V1
+                ms, nbytes, _ = time_gemm(g, torch, dev, stream, wl, M, l2, path="perm" if pre else "gemm", fmt=f)
                 gbs = nbytes / (ms * 1e-3) / 1e9
                 tflops = 2.0 * M * wl.N * wl.K / (ms * 1e-3) / 1e12
                 row = {"workload": name, "M": M, "fmt": fmt, "us": round(ms * 1e3, 3),
@@ -471,18 +583,6 @@ def run_sweep(g, torch, dev, stream, hbm_peak, bf16_peak, l2, only=""):
                        "TFLOP/s": round(tflops, 2), "tensor_frac": round(tflops / bf16_peak, 4)}
                 rows.append(row)
                 print(json.dumps(row), file=sys.stderr, flush=True)
-    for name, mw in gptq_inputs.MOE_WORKLOADS.items():
-        if only not in name:
-            continue
-        for T in mw.Ts:
-            ms, nbytes, active, nrows, max_m = time_grouped(g, torch, dev, stream, mw, T, l2)
-            gbs = nbytes / (ms * 1e-3) / 1e9
-            row = {"workload": name, "M": T, "fmt": "v2 grouped", "rows": nrows, "experts_active": active,
-                   "max_m": max_m, "us": round(ms * 1e3, 3), "GB/s": round(gbs, 1),
-                   "hbm_frac": round(gbs / hbm_peak, 4),
-                   "TFLOP/s": round(2.0 * nrows * mw.N * mw.K / (ms * 1e-3) / 1e12, 2), "tensor_frac": None}
-            rows.append(row)
-            print(json.dumps(row), file=sys.stderr, flush=True)
     return rows
 
 
@@ -500,11 +600,12 @@ def oracle_sample(ck, wl, ncols):
             np.ascontiguousarray(ck["scales"][:, :ncols]))
 
 
-def time_oracle_step(ck, wl, A16, ncols):
+def time_oracle_step(ck, wl, A16, ncols, dtype_code=None):
     import oracle
     qw, qz, sc = oracle_sample(ck, wl, ncols)
     t = time.perf_counter()
-    oracle.gemm(A16, oracle.F16, qw, qz, sc, ck["g_idx"], ncols, wl.bits, wl.group, oracle.V2)
+    oracle.gemm(A16, oracle.F16 if dtype_code is None else dtype_code, qw, qz, sc, ck["g_idx"], ncols,
+                wl.bits, wl.group, oracle.V2)
     return time.perf_counter() - t
 
 
@@ -513,22 +614,42 @@ def sample_bytes(wl, M, ncols):
     return algorithmic_bytes(sub, M)
 
 
-def cpu_baseline(budget_s=12.0):
-    """The oracle as it stands (one thread) on a bounded column sample of the decode workload."""
+def cpu_baseline(budget_s=8.0):
+    """The oracle as it stands (one thread) on a bounded column sample of the decode workload,
+    and on 64 rows of the M = 4096 prefill workload (extrapolated to all 4096 rows)."""
+    import oracle
     wl, M = DECODE, 1
     ck = oracle_checkpoint(wl)
     A16 = gptq_inputs.bits16(gptq_inputs.draw_activations(wl, M))
     t32 = time_oracle_step(ck, wl, A16, 32 * 8)
     ncols = int(min(wl.N, max(256, (budget_s / 4) / max(t32, 1e-6) * 256)) // 32 * 32)
+    time_oracle_step(ck, wl, A16, ncols)                 # discarded first run (cold caches)
     reps, total, t_end = 0, 0.0, time.perf_counter() + budget_s
     while time.perf_counter() < t_end or reps == 0:
         total += time_oracle_step(ck, wl, A16, ncols)
         reps += 1
     per = total / reps
     gbs = sample_bytes(wl, M, ncols) / per / 1e9
-    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": "decode M=1, K=4096, first %d of 11008 columns (4-bit g128 v2), %d runs, "
-                      "%.2f s each (unpack + fp32 dequant + fp32 GEMM, single thread)" % (ncols, reps, per)}
+    host = host_info()
+    out = {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "host": host,
+           "sample": "decode M=1, K=4096, first %d of 11008 columns (4-bit g128 v2), %d runs after one "
+                     "discarded, %.2f s each (unpack + fp32 dequant + fp32 GEMM, single thread)" % (ncols, reps, per)}
+    # prefill leg: 64 seeded rows of the M = 4096 problem, all N; time x 64 for the whole problem
+    pw = PREFILL
+    pck = oracle_checkpoint(pw)
+    A = gptq_inputs.draw_activations(pw, pw.Ms[0])
+    rows = np.sort(np.random.default_rng(64).choice(pw.Ms[0], size=64, replace=False)).astype(np.int32)
+    A64 = gptq_inputs.bits16(A)[rows]
+    t = time.perf_counter()
+    oracle.gemm(A64, oracle.BF16, pck["qweight"], pck["qzeros"], pck["scales"], None, pw.N, pw.bits, pw.group,
+                oracle.V2)
+    dt = time.perf_counter() - t
+    tflops = 2.0 * 64 * pw.N * pw.K / dt / 1e12
+    out["prefill"] = {"value": round(tflops, 6), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                      "seconds_64_rows": round(dt, 3), "seconds_extrapolated_4096_rows": round(dt * 64, 1),
+                      "sample": "prefill_4bit_g128: 64 seeded rows of A [4096, 4096] x W [4096, 14336] "
+                                "(4-bit g128 v2, bf16), all columns; the full problem is 64x this time"}
+    return out
 
 
 def run_reference(args):
@@ -555,9 +676,43 @@ def run_reference(args):
         "config": {"workload": "llama7b_decode_4bit_g128", "M": M, "K": wl.K, "N": wl.N,
                    "bits": wl.bits, "group": wl.group, "fmt": "v2", "sample_columns": ncols},
         "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, "host": host_info()},
         "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
+
+
+def run_profile_target(args):
+    """--profile WORKLOAD:M[:PATH]: just `warmup + steps` eager launches of one call on one
+    workload (PATH gemm, perm or dequant), for a profiler to capture; prints one short line."""
+    import torch
+    import gptq_bit_weight_gemm_gb300 as g
+    from gptq_bit_weight_gemm_gb300 import build as lib_build
+    lib_build.build()
+    parts = args.profile.split(":")
+    wl, M = gptq_inputs.WORKLOADS[parts[0]], int(parts[1])
+    path = parts[2] if len(parts) > 2 else "gemm"
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.Stream()
+    draw, qw, qz, sc, gi = _checkpoint(g, torch, dev, wl)
+    perm = ws = None
+    if path == "perm":
+        qw2, p = g.prepack_act_order(qw.cpu().numpy(), draw.g_idx, K=wl.K, N=wl.N, bits=wl.bits, group=wl.group)
+        qw, perm, gi = torch.from_numpy(qw2).to(dev), torch.from_numpy(p).to(dev), None
+        ws = torch.empty(max(1, g.gemm_perm_workspace_size(M, wl.K)), dtype=torch.uint8, device=dev)
+    A = gptq_inputs.draw_activations(wl, max(M, 1)).to(dev)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup + args.steps):
+            if path == "perm":
+                g.gemm_perm(A, perm, qw, qz, sc, bits=wl.bits, group=wl.group, workspace=ws, stream=stream)
+            elif path == "dequant":
+                g.dequant(qw, qz, sc, gi, K=wl.K, bits=wl.bits, group=wl.group, stream=stream,
+                          dtype=torch.float16 if wl.act_dtype == "f16" else torch.bfloat16)
+            else:
+                g.gemm(A, qw, qz, sc, gi, bits=wl.bits, group=wl.group, stream=stream)
+    stream.synchronize()
+    assert g.device_status(stream) == 0
+    print(json.dumps({"profile": args.profile, "launches": args.warmup + args.steps}))
 
 
 def main():
@@ -566,14 +721,23 @@ def main():
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=2000)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--skip-prefill", action="store_true")
+    ap.add_argument("--skip-configs", action="store_true",
+                    help="leave out the per-configuration section (and with it the prefill figure)")
+    ap.add_argument("--config-filter", default="",
+                    help="only the configurations whose workload name contains this string")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--all", action="store_true",
-                    help="also time every workload and M (per-launch us, GB/s, TFLOP/s)")
+                    help="also time every workload, token count and format (per-launch us, GB/s, TFLOP/s)")
     ap.add_argument("--sweep-filter", default="",
                     help="with --all: only the workloads whose name contains this string")
+    ap.add_argument("--profile", default="",
+                    help="WORKLOAD:M[:gemm|perm|dequant]: only launch that call warmup+steps times "
+                         "(for a profiler), no timing")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
+    if args.profile:
+        run_profile_target(args)
+        return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
