@@ -419,15 +419,19 @@ def time_gemm(g, torch, dev, stream, wl, M, l2, path="gemm", fmt=None, reps=200)
     """Median per-launch time of one GEMM call on one workload: a CUDA graph of launches over S
     rotating copies of every input (S x bytes > 3x L2 where one copy is smaller), replayed 11
     times, the first replay discarded.  path: "gemm" (gptq_gemm, with g_idx for act-order),
-    "perm" (act-order rows sorted on the host, gptq_gemm_perm) or "dequant" (gptq_dequant)."""
+    "perm" (act-order rows sorted on the host, gptq_gemm_perm), "il" (qweight in the interleaved
+    layout, gptq_gemm_interleaved; act-order checkpoints sorted first, through perm) or "dequant"
+    (gptq_dequant)."""
     f = fmt if fmt is not None else g.V2
     draw, qw, qz, sc, gi = _checkpoint(g, torch, dev, wl, f)
     perm = ws = None
-    if path == "perm":
+    if path in ("perm", "il") and draw.g_idx is not None:
         qw2, p = g.prepack_act_order(qw.cpu().numpy(), draw.g_idx, K=wl.K, N=wl.N, bits=wl.bits,
                                      group=wl.group)
         qw, perm, gi = torch.from_numpy(qw2).to(dev), torch.from_numpy(p).to(dev), None
         ws = torch.empty(max(1, g.gemm_perm_workspace_size(M, wl.K)), dtype=torch.uint8, device=dev)
+    if path == "il":
+        qw = torch.from_numpy(g.prepack_interleave(qw.cpu().numpy(), K=wl.K, N=wl.N, bits=wl.bits)).to(dev)
     A = gptq_inputs.draw_activations(wl, M).to(dev) if path != "dequant" else None
     if path == "dequant":
         out_shape, out_dt = (wl.K, wl.N), torch.float16 if wl.act_dtype == "f16" else torch.bfloat16
@@ -450,6 +454,9 @@ def time_gemm(g, torch, dev, stream, wl, M, l2, path="gemm", fmt=None, reps=200)
         if path == "perm":
             g.gemm_perm(a, perm, q, z, s_, bits=wl.bits, group=wl.group, fmt=f, out=c, workspace=ws,
                         stream=stream)
+        elif path == "il":
+            g.gemm_interleaved(a, q, z, s_, perm, N=wl.N, bits=wl.bits, group=wl.group, fmt=f, out=c,
+                               workspace=ws, stream=stream)
         elif path == "dequant":
             g.dequant(q, z, s_, gi, K=wl.K, bits=wl.bits, group=wl.group, fmt=f, dtype=out_dt, out=c,
                       stream=stream)
@@ -472,11 +479,14 @@ def run_configs(g, torch, dev, stream, peaks, l2, only=""):
         ("2", "llama7b_decode_4bit_g128", 1, "gemm", ""),
         ("2", "llama7b_decode_4bit_g128", 8, "gemm", ""),
         ("2", "llama7b_decode_4bit_g128", 16, "gemm", ""),
+        ("2", "llama7b_decode_4bit_g128", 1, "il", "interleaved layout, gptq_gemm_interleaved"),
+        ("2", "llama7b_decode_4bit_g128", 16, "il", "interleaved layout, gptq_gemm_interleaved"),
         ("3", "lowbit_2bit_g64", 1, "gemm", ""),
         ("3", "lowbit_2bit_g64", 8, "gemm", ""),
         ("3", "lowbit_2bit_g64", 32, "gemm", ""),
         ("4", "act_order_3bit_g128", 16, "gemm", "g_idx through gptq_gemm"),
         ("4", "act_order_3bit_g128", 16, "perm", "rows sorted on the host, gptq_gemm_perm"),
+        ("4", "act_order_3bit_g128", 16, "il", "rows sorted, then interleaved, gptq_gemm_interleaved"),
         ("5", "prefill_4bit_g128", 4096, "gemm", ""),
         ("5", "prefill_8bit_sym_g128", 4096, "gemm", ""),
         ("5", "prefill_4bit_gall", 4096, "gemm", ""),
@@ -490,6 +500,7 @@ def run_configs(g, torch, dev, stream, peaks, l2, only=""):
         wl = W[name]
         ms, nbytes, S = time_gemm(g, torch, dev, stream, wl, M, l2, path=path)
         row = {"config": cfg, "workload": name, "M": M, "path": {"gemm": "gptq_gemm", "perm": "gptq_gemm_perm",
+                                                                 "il": "gptq_gemm_interleaved",
                                                                  "dequant": "gptq_dequant"}[path],
                "us": round(ms * 1e3, 3)}
         if label:
@@ -695,16 +706,21 @@ def run_profile_target(args):
     stream = torch.cuda.Stream()
     draw, qw, qz, sc, gi = _checkpoint(g, torch, dev, wl)
     perm = ws = None
-    if path == "perm":
+    if path in ("perm", "il") and draw.g_idx is not None:
         qw2, p = g.prepack_act_order(qw.cpu().numpy(), draw.g_idx, K=wl.K, N=wl.N, bits=wl.bits, group=wl.group)
         qw, perm, gi = torch.from_numpy(qw2).to(dev), torch.from_numpy(p).to(dev), None
         ws = torch.empty(max(1, g.gemm_perm_workspace_size(M, wl.K)), dtype=torch.uint8, device=dev)
+    if path == "il":
+        qw = torch.from_numpy(g.prepack_interleave(qw.cpu().numpy(), K=wl.K, N=wl.N, bits=wl.bits)).to(dev)
     A = gptq_inputs.draw_activations(wl, max(M, 1)).to(dev)
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         for _ in range(args.warmup + args.steps):
             if path == "perm":
                 g.gemm_perm(A, perm, qw, qz, sc, bits=wl.bits, group=wl.group, workspace=ws, stream=stream)
+            elif path == "il":
+                g.gemm_interleaved(A, qw, qz, sc, perm, N=wl.N, bits=wl.bits, group=wl.group, workspace=ws,
+                                   stream=stream)
             elif path == "dequant":
                 g.dequant(qw, qz, sc, gi, K=wl.K, bits=wl.bits, group=wl.group, stream=stream,
                           dtype=torch.float16 if wl.act_dtype == "f16" else torch.bfloat16)
@@ -731,7 +747,7 @@ def main():
     ap.add_argument("--sweep-filter", default="",
                     help="with --all: only the workloads whose name contains this string")
     ap.add_argument("--profile", default="",
-                    help="WORKLOAD:M[:gemm|perm|dequant]: only launch that call warmup+steps times "
+                    help="WORKLOAD:M[:gemm|perm|il|dequant]: only launch that call warmup+steps times "
                          "(for a profiler), no timing")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"

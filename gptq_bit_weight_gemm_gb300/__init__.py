@@ -14,6 +14,9 @@ Operations (page "增强 vLLM 对 GPTQv2 格式的支持：分析与实现", sec
   repack_zeros_v1_to_v2(qzeros_v1, N, bits)                  (host memory)
   prepack_act_order(qweight, g_idx, K, N, bits, group)      (host memory) -> (qweight', perm)
   gemm_perm(A, perm, qweight', qzeros, scales, bits, group) -> A[:, perm] @ dequant(W'), M <= 32
+  prepack_interleave(qweight, K, N, bits)                    (host memory) -> qweight in the decode
+                                                             kernel's interleaved layout
+  gemm_interleaved(A, qweight_il, qzeros, scales, perm, N, bits, group) -> the decode GEMM on it
   gemm_grouped(A, offsets, qweight[E], qzeros[E], scales[E], bits, group, max_m)
                                                              -> rows of expert e times W_e
   device_status(stream)                                      -> GPTQ_DEV_* bits
@@ -66,6 +69,8 @@ _SIGNATURES = {
     "gptq_gemm_perm_workspace_size": (_SZ, [_I, _I]),
     "gptq_gemm_perm_noalloc": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "gptq_gemm_grouped": (_I, [_P, _I, _I, _I, _P, _I, _I, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
+    "gptq_prepack_interleave": (_I, [_P, _I, _I, _I, _P]),
+    "gptq_gemm_interleaved": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P]),
 }
 
 
@@ -244,6 +249,35 @@ def gemm_perm(A, perm, qweight, qzeros, scales, *, bits, group, fmt=V2, out=None
                               _ptr(scales, torch.float16, "scales"), N, bits, group, fmt,
                               _ptr(out, A.dtype, "out"), ws_ptr, ws_len, _stream(stream))
     _check(rc, "gptq_gemm_perm")
+    return out
+
+
+def prepack_interleave(qweight, *, K, N, bits):
+    """Host: qweight (numpy int32 [K*bits/32, N]) in the decode kernel's interleaved layout."""
+    qw = np.ascontiguousarray(qweight, dtype=np.int32)
+    out = np.empty(qw.size, dtype=np.int32)
+    rc = lib().gptq_prepack_interleave(qw.ctypes.data_as(_P), K, N, bits, out.ctypes.data_as(_P))
+    _check(rc, "gptq_prepack_interleave")
+    return out
+
+
+def gemm_interleaved(A, qweight_il, qzeros, scales, perm=None, *, N, bits, group, fmt=V2, out=None,
+                     workspace=None, stream=None):
+    """C[M, N] = A @ dequant(W) (A[:, perm] @ ... with perm) for an interleaved qweight, M <= 32."""
+    torch = _torch()
+    M, K = A.shape
+    if out is None:
+        out = torch.empty((M, N), dtype=A.dtype, device=A.device)
+    ws_bytes = gemm_perm_workspace_size(M, K) if perm is not None else 0
+    if ws_bytes and workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=A.device)
+    ws_ptr = _ptr(workspace, name="workspace") if ws_bytes else None
+    ws_len = workspace.numel() * workspace.element_size() if ws_bytes else 0
+    rc = lib().gptq_gemm_interleaved(_ptr(A, name="A"), M, K, _dtype_code(A), _ptr(perm, torch.int32, "perm"),
+                                     _ptr(qweight_il, torch.int32, "qweight_il"), _ptr(qzeros, torch.int32, "qzeros"),
+                                     _ptr(scales, torch.float16, "scales"), N, bits, group, fmt,
+                                     _ptr(out, A.dtype, "out"), ws_ptr, ws_len, _stream(stream))
+    _check(rc, "gptq_gemm_interleaved")
     return out
 
 

@@ -43,6 +43,9 @@ struct Args {
   // expert e (blockIdx.z); `rows` bounds them.  nullptr for a single weight.
   const int32_t* offsets;
   int rows;
+  // interleaved weights (gptq_prepack_interleave): k-tiles per 32-column block, else 0 (the
+  // checkpoint's own row-major layout, read through the tensor map)
+  int il_tiles;
 };
 
 __device__ __forceinline__ void split(int total, int parts, int idx, int& b, int& e) {
@@ -105,11 +108,11 @@ __device__ __forceinline__ void cluster_wait() {
 // Stage activation pairs into shared memory.  Work item = (unit u, real token m < M): one
 // thread reads the unit's PER consecutive activations of row m with 16-byte loads (8-byte for
 // 8-bit units) and writes the NP pairs (lo_k(p), hi_k(p)) through `put(u, m, p, value)`.  A
-// thread's loads for up to stage_batch(PER) items (32 registers of activations) are all issued
-// before any of them is used, so the staging costs one L2 round trip per batch -- under a
-// saturated weight stream that round trip is over a microsecond.  Rows m >= M and units past
-// the last one are written as zero by the caller.
-__host__ __device__ constexpr int stage_batch(int per) { return per >= 32 ? 2 : 64 / per; }
+// thread's loads for up to stage_batch(PER) items are all issued before any of them is used, so
+// the staging costs one L2 round trip per batch.  (Batches of 8 units measured slower at 1 to 8
+// tokens -- 8.3 -> 8.5 us at one token on llama-7B -- and no faster at 16.)  Rows m >= M and units
+// past the last one are written as zero by the caller.
+__host__ __device__ constexpr int stage_batch(int per) { return per >= 32 ? 2 : 4; }
 
 template <int PER>
 struct UnitVec {   // a unit's activations: PER 16-bit values
@@ -147,17 +150,18 @@ struct UnitVec {   // a unit's activations: PER 16-bit values
   }
 };
 
+// tid / nthr: this thread's index among the nthr threads that stage.
 template <int PER, int NP, class LoK, class HiK, class Put>
 __device__ __forceinline__ void stage_pairs(const uint16_t* A, const int32_t* perm, int M, int K,
                                             int ufirst, int nunits, int units, LoK lo_k, HiK hi_k,
-                                            Put put) {
+                                            Put put, int tid, int nthr) {
   const int items = nunits * M;
   constexpr int kStageBatch = stage_batch(PER);
-  for (int base = 0; base < items; base += kStageBatch * static_cast<int>(blockDim.x)) {
+  for (int base = 0; base < items; base += kStageBatch * nthr) {
     UnitVec<PER> v[kStageBatch];
 #pragma unroll
     for (int j = 0; j < kStageBatch; ++j) {
-      const int it = base + j * static_cast<int>(blockDim.x) + static_cast<int>(threadIdx.x);
+      const int it = base + j * nthr + tid;
       const int uu = M == 1 ? it : it / M, m = it - uu * M;
       if (it < items && ufirst + uu < units) {
         if (perm)
@@ -168,7 +172,7 @@ __device__ __forceinline__ void stage_pairs(const uint16_t* A, const int32_t* pe
     }
 #pragma unroll
     for (int j = 0; j < kStageBatch; ++j) {
-      const int it = base + j * static_cast<int>(blockDim.x) + static_cast<int>(threadIdx.x);
+      const int it = base + j * nthr + tid;
       const int uu = M == 1 ? it : it / M, m = it - uu * M;
       if (it < items) {
         const bool live = ufirst + uu < units;

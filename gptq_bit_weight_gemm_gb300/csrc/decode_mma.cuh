@@ -321,12 +321,34 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
   // the packed weights are read once: evict them first, so that activations and other reused
   // data keep their place in L2
   const uint64_t stream_policy = ptx::policy_evict_first();
+  // Interleaved weights (gptq_prepack_interleave): warp w's 32-column block is contiguous along
+  // K, 512 * ROWS bytes per k-tile in lane order, so one 1D bulk copy moves its part of a chunk;
+  // its byte count stops at the CTA's last k-tile (nothing past the block is read) and a block
+  // past N copies nothing.
+  constexpr uint32_t kIlTile = 512u * ROWS;
+  auto il_bytes = [&](int w, int c) -> uint32_t {
+    if ((n_base >> 5) + w >= (a.N >> 5)) return 0u;
+    const int nt = ntile - c * geo.chunk_tiles;
+    return static_cast<uint32_t>(nt < geo.chunk_tiles ? nt : geo.chunk_tiles) * kIlTile;
+  };
+  auto il_copy = [&](int w, int c, uint32_t dst, uint32_t barw, uint32_t bytes) {
+    if (bytes == 0u) return;
+    const size_t tile0 = static_cast<size_t>((n_base >> 5) + w) * a.il_tiles + ct0 + c * geo.chunk_tiles;
+    ptx::bulk_load_hint(dst, reinterpret_cast<const uint8_t*>(a.qweight) + tile0 * kIlTile, bytes, barw,
+                        stream_policy);
+  };
   // copy warp w's 32 columns of chunk c into buffer c % nbuf (its own slot and mbarrier)
   auto issue_for = [&](int w, int c) {
     const int b = c % geo.nbuf;
     last_issued[w * geo.nbuf + b] = c;
     const uint32_t dst = ptx::smem_addr(sbuf + static_cast<size_t>(b) * geo.chunk_bytes +
                                         static_cast<size_t>(w) * geo.slot_bytes);
+    if (a.il_tiles) {
+      const uint32_t bytes = il_bytes(w, c);
+      ptx::mbar_arrive_expect_tx(bar(w, b), bytes);
+      il_copy(w, c, dst, bar(w, b), bytes);
+      return;
+    }
     const int row0 = w_row0 + (cu0 + c * geo.chunk_tiles * 4) * ROWS;
     ptx::mbar_arrive_expect_tx(bar(w, b), static_cast<uint32_t>(geo.chunk_rows * kBoxRowBytes));
     ptx::tma_load_2d_hint(dst, &tmW, n_base + w * kBoxCols, row0, bar(w, b), stream_policy);
@@ -335,12 +357,20 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
   auto issue_chunk = [&](int c) {
     const int b = c % geo.nbuf;
     last_issued[b] = c;
+    auto slot_addr = [&](int w) {
+      return ptx::smem_addr(sbuf + static_cast<size_t>(b) * geo.chunk_bytes + static_cast<size_t>(w) * geo.slot_bytes);
+    };
+    if (a.il_tiles) {
+      uint32_t total = 0u;
+      for (int w = 0; w < kWarps; ++w) total += il_bytes(w, c);
+      ptx::mbar_arrive_expect_tx(bar(0, b), total);
+      for (int w = 0; w < kWarps; ++w) il_copy(w, c, slot_addr(w), bar(0, b), il_bytes(w, c));
+      return;
+    }
     const int row0 = w_row0 + (cu0 + c * geo.chunk_tiles * 4) * ROWS;
     ptx::mbar_arrive_expect_tx(bar(0, b), static_cast<uint32_t>(kWarps * geo.chunk_rows * kBoxRowBytes));
     for (int w = 0; w < kWarps; ++w)
-      ptx::tma_load_2d_hint(ptx::smem_addr(sbuf + static_cast<size_t>(b) * geo.chunk_bytes +
-                                           static_cast<size_t>(w) * geo.slot_bytes),
-                            &tmW, n_base + w * kBoxCols, row0, bar(0, b), stream_policy);
+      ptx::tma_load_2d_hint(slot_addr(w), &tmW, n_base + w * kBoxCols, row0, bar(0, b), stream_policy);
   };
   // refill after chunk c_next - nbuf was consumed: per warp (its slot) or by the whole CTA
   // (per_warp is uniform over the CTA, and so is the loop's chunk sequence)
@@ -406,7 +436,8 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
   const int nunits = ntile * 4;
   stage_pairs<PER, NP>(A16, a.perm, Mtok, a.K, cu0, nunits, a.units,
                        [](int p) { return MP::lo_k(p); }, [](int p) { return MP::hi_k(p); },
-                       [&](int uu, int m, int p, uint32_t v) { sB[uu * UW + m * NP + p] = v; });
+                       [&](int uu, int m, int p, uint32_t v) { sB[uu * UW + m * NP + p] = v; },
+                       static_cast<int>(threadIdx.x), kThreads);
   __syncthreads();
   if constexpr (kConvert) {
     // bf16 -> fp16: per token, 2^e with max|a| * 2^-e in [2^15, 2^16) (below fp16's largest
@@ -485,10 +516,14 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
       }
     }
   };
-  // this thread's 16 bytes of packed row r of a chunk buffer
+  // this thread's 16 bytes of row r (0 .. ROWS - 1) of its unit in local k-tile l of a chunk slot:
+  // the tensor-map layout holds 128-byte rows with the 128-byte swizzle, the interleaved one
+  // 512-byte k-tile rows in lane order
   const uint8_t* wslot = sbuf + warp * geo.slot_bytes;
-  auto wrow = [&](const uint8_t* cb, int r) {
-    return *reinterpret_cast<const uint4*>(cb + r * kBoxRowBytes + ((quad ^ (r & 7)) << 4));
+  auto wfrag = [&](const uint8_t* slot, int l, int r) {
+    if (a.il_tiles) return *reinterpret_cast<const uint4*>(slot + (l * ROWS + r) * 512 + lane * 16);
+    const int row = (l * 4 + tq) * ROWS + r;
+    return *reinterpret_cast<const uint4*>(slot + row * kBoxRowBytes + ((quad ^ (row & 7)) << 4));
   };
 
   if constexpr (FOLD) {
@@ -536,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
     auto tile3 = [&](const uint8_t* cslot, int l, int kt) {
       uint4 wv[3];
 #pragma unroll
-      for (int r = 0; r < 3; ++r) wv[r] = wrow(cslot, (l * 4 + tq) * 3 + r);
+      for (int r = 0; r < 3; ++r) wv[r] = wfrag(cslot, l, r);
       uint32_t bf[NB][NP];
 #pragma unroll
       for (int nb = 0; nb < NB; ++nb) {
@@ -608,9 +643,13 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
         ++c;
         ok = __all_sync(0xFFFFFFFFu, tma_wait(bar(bw, c % geo.nbuf), (c / geo.nbuf) & 1, abort_flag, a.status));
         cslot = wslot + static_cast<size_t>(c % geo.nbuf) * geo.chunk_bytes;
-        const uint8_t* cb = cslot + tq * kBoxRowBytes;
-        we = cb + ((quad ^ tq) << 4);
-        wo = cb + ((quad ^ tq ^ 4) << 4);
+        if (a.il_tiles) {
+          we = wo = cslot + lane * 16;
+        } else {
+          const uint8_t* cb = cslot + tq * kBoxRowBytes;
+          we = cb + ((quad ^ tq) << 4);
+          wo = cb + ((quad ^ tq ^ 4) << 4);
+        }
         chunk_kt = c * geo.chunk_tiles;
         chunk_end = chunk_kt + geo.chunk_tiles < ntile ? chunk_kt + geo.chunk_tiles : ntile;
       }
@@ -649,10 +688,9 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
       const int kt0 = c * geo.chunk_tiles;
       const int kt_end = kt0 + geo.chunk_tiles < ntile ? kt0 + geo.chunk_tiles : ntile;
       for (int kt = kt0; ok && kt < kt_end; ++kt) {
-        const int rl = ((kt - kt0) * 4 + tq) * ROWS;   // first row of the unit
         uint4 wv[ROWS];
 #pragma unroll
-        for (int r = 0; r < ROWS; ++r) wv[r] = wrow(cb, rl + r);
+        for (int r = 0; r < ROWS; ++r) wv[r] = wfrag(cb, kt - kt0, r);
         uint32_t bf[NB][NP];
         load_b(kt, bf);
         const int u = cu0 + kt * 4 + tq;
@@ -909,6 +947,7 @@ cudaError_t launch_mma(const Problem& p, cudaStream_t stream) {
   a.C = p.out; a.status = p.status;
   a.offsets = GROUPED ? p.offsets : nullptr;
   a.rows = p.rows;
+  a.il_tiles = p.interleaved ? a.units / 4 : 0;
   const int E = GROUPED ? p.E : 1;                     // weights side by side (grid z)
   const int slabs = (p.N + kSlab - 1) / kSlab;
   const int sms = device_info().sm_count;
@@ -931,8 +970,8 @@ cudaError_t launch_mma(const Problem& p, cudaStream_t stream) {
     const int chunks = (geo.tiles_per_cta + geo.chunk_tiles - 1) / geo.chunk_tiles;
     if (geo.nbuf < chunks) return launch_mma<BITS, MT, 0, T, FOLD, GROUPED>(p, stream);
   }
-  CUtensorMap tmW;
-  {
+  CUtensorMap tmW = {};
+  if (!p.interleaved) {
     constexpr int ROWS = Pack<BITS>::kRowsPerUnit;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.N), static_cast<cuuint64_t>(a.units) * ROWS * E};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.N) * 4};

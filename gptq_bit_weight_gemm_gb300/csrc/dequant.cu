@@ -3,15 +3,21 @@
 // The capability of the reconstruct kernel on the page "增强 vLLM 对 GPTQv2 格式的支持：分析
 // 与实现" (section "调整细节：根据格式选择处理方式": reconstruct_exllama_2bit_kernel calls
 // dequant_2bit_16 on each 32-bit lane of a 128-bit load with zeros[i] + zero_offset), for every
-// width, both checkpoint formats and act-order.  q - zero is formed exactly in fp32 (magic
-// number 2^23), multiplied by the fp16 scale in fp32 (exact: at most 9 + 11 significant bits)
-// and rounded once to the output dtype, so the result is bit-exact.
+// width, both checkpoint formats and act-order.  The result is bit-exact: q - zero is exact and
+// the product is rounded once to the output dtype.
 //
-// Memory-bound (it writes four times the packed bytes at 4 bits): each thread owns one packed
-// unit of 8 adjacent columns (two 16-byte loads per qweight row) and writes 16 bytes per k, so a
-// warp writes 512 contiguous bytes of each output row.
+// Memory-bound in principle (it writes four times the packed bytes at 4 bits), so the unpack must
+// cost few instructions per weight.  Each thread owns one packed unit of 8 adjacent columns (two
+// 16-byte loads per qweight row) and writes 16 bytes per k, so a warp writes 512 contiguous bytes
+// of each output row.  With one group per unit (no act-order, groups of at least a unit) the codes
+// become exact fp16 (q - zero) pairs (DiffPairs: a mask into a magic mantissa and one fp16 op per
+// pair), then fp16 output: one HMUL2 per pair (an exact product rounded once); bf16 output: the
+// pair widened to fp32, one fp32x2 product (exact) and one conversion that rounds once.  Otherwise
+// (act-order, or groups smaller than a unit) each weight is formed in fp32: magic-number q - zero,
+// one product, one rounding.
 #include "gptq_device.cuh"
 #include "gptq_internal.h"
+#include "sm100_ptx.cuh"
 
 namespace gptq {
 namespace {
@@ -29,7 +35,78 @@ struct DqArgs {
   unsigned* status;
 };
 
-template <int BITS, typename T, bool ACT>
+// Scales and runtime zeros of columns n0 .. n0 + 7 for group g.
+template <int BITS>
+__device__ __forceinline__ void load_group8(const DqArgs& a, int g, int n0, uint32_t (&sbits)[kCols / 2],
+                                            int (&z)[kCols]) {
+  const uint4 sv = __ldg(reinterpret_cast<const uint4*>(a.scales + static_cast<long long>(g) * a.N + n0));
+  sbits[0] = sv.x; sbits[1] = sv.y; sbits[2] = sv.z; sbits[3] = sv.w;
+  const int32_t* zrow = a.qzeros + static_cast<long long>(g) * a.zwords;
+  const uint32_t zlo = zeros4<BITS>(zrow, n0), zhi = zeros4<BITS>(zrow, n0 + 4);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    z[c] = static_cast<int>((zlo >> (BITS * c)) & Pack<BITS>::kMask) + a.zero_offset;
+    z[c + 4] = static_cast<int>((zhi >> (BITS * c)) & Pack<BITS>::kMask) + a.zero_offset;
+  }
+}
+
+__device__ __forceinline__ float h_lo(uint32_t x) { return __half2float(__ushort_as_half(lo16(x))); }
+__device__ __forceinline__ float h_hi(uint32_t x) { return __half2float(__ushort_as_half(hi16(x))); }
+
+// (q - z) * s for the two halves of an exact fp16 pair, as a T pair, rounded once.
+template <typename T>
+__device__ __forceinline__ uint32_t scale_pair(uint32_t d, uint32_t s2, float s) {
+  if constexpr (std::is_same<T, __half>::value) {
+    return hmul2(d, s2);
+  } else {
+    const float2 p = ptx::mul_f32x2(make_float2(h_lo(d), h_hi(d)), make_float2(s, s));
+    return pack2(p.x, p.y, __nv_bfloat16());
+  }
+}
+
+// One unit, one group: exact pairs, then 16-byte row stores.
+template <int BITS, typename T>
+__device__ __forceinline__ void unit_pairs(const DqArgs& a, const uint32_t (&wv)[Pack<BITS>::kRowsPerUnit][kCols],
+                                           int u, int n0, T* W) {
+  using DP = DiffPairs<__half, BITS>;
+  constexpr int PER = Pack<BITS>::kPerUnit;
+  constexpr int NP = DP::kPairs;
+  const int g = (u * PER) / a.group;
+  uint32_t sbits[kCols / 2];
+  int z[kCols];
+  load_group8<BITS>(a, g, n0, sbits, z);
+  // e[c][p]: column c's pair p, (q - z) * s rounded to T
+  uint32_t e[kCols][NP];
+#pragma unroll
+  for (int c = 0; c < kCols; ++c) {
+    uint32_t kz[DP::kConsts];
+    DP::consts(z[c], kz);
+    if constexpr (BITS == 3)
+      DP::run3(wv[0][c], wv[1][c], wv[2][c], kz, e[c]);
+    else
+      DP::run(wv[0][c], kz, e[c]);
+    const uint32_t sb = c & 1 ? (sbits[c >> 1] >> 16) : (sbits[c >> 1] & 0xFFFFu);
+    const float s = __half2float(__ushort_as_half(static_cast<uint16_t>(sb)));
+#pragma unroll
+    for (int p = 0; p < NP; ++p) e[c][p] = scale_pair<T>(e[c][p], sb * 0x00010001u, s);
+  }
+  // row k = lo_k(p) gathers the low halves of pair p over the 8 columns, row hi_k(p) the high
+#pragma unroll
+  for (int p = 0; p < NP; ++p) {
+    uint4 lo, hi;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      (&lo.x)[i] = __byte_perm(e[2 * i][p], e[2 * i + 1][p], 0x5410);
+      (&hi.x)[i] = __byte_perm(e[2 * i][p], e[2 * i + 1][p], 0x7632);
+    }
+    const long long k_lo = static_cast<long long>(u) * PER + DP::lo_k(p);
+    const long long k_hi = static_cast<long long>(u) * PER + DP::hi_k(p);
+    *reinterpret_cast<uint4*>(W + k_lo * a.N + n0) = lo;
+    *reinterpret_cast<uint4*>(W + k_hi * a.N + n0) = hi;
+  }
+}
+
+template <int BITS, typename T, bool ACT, bool PAIRS>
 __global__ void __launch_bounds__(kThreads) k_dequant(const DqArgs a) {
   using P = Pack<BITS>;
   constexpr int PER = P::kPerUnit;
@@ -49,6 +126,10 @@ __global__ void __launch_bounds__(kThreads) k_dequant(const DqArgs a) {
       wv[r][0] = lo.x; wv[r][1] = lo.y; wv[r][2] = lo.z; wv[r][3] = lo.w;
       wv[r][4] = hi.x; wv[r][5] = hi.y; wv[r][6] = hi.z; wv[r][7] = hi.w;
     }
+    if constexpr (PAIRS) {
+      unit_pairs<BITS, T>(a, wv, u, n0, W);
+      continue;
+    }
     int cur_g = -1;
     float s[kCols];
     int z[kCols];
@@ -66,19 +147,11 @@ __global__ void __launch_bounds__(kThreads) k_dequant(const DqArgs a) {
         g = k / a.group;
       }
       if (g != cur_g) {
-        const uint4 sv = __ldg(reinterpret_cast<const uint4*>(a.scales + static_cast<long long>(g) * a.N + n0));
+        uint32_t sbits[kCols / 2];
+        load_group8<BITS>(a, g, n0, sbits, z);
 #pragma unroll
-        for (int c = 0; c < kCols; ++c) {
-          const uint32_t word = (&sv.x)[c >> 1];
-          s[c] = __half2float(__ushort_as_half(static_cast<uint16_t>(c & 1 ? word >> 16 : word & 0xFFFFu)));
-        }
-        const int32_t* zrow = a.qzeros + static_cast<long long>(g) * a.zwords;
-        const uint32_t zlo = zeros4<BITS>(zrow, n0), zhi = zeros4<BITS>(zrow, n0 + 4);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          z[c] = static_cast<int>((zlo >> (BITS * c)) & P::kMask) + a.zero_offset;
-          z[c + 4] = static_cast<int>((zhi >> (BITS * c)) & P::kMask) + a.zero_offset;
-        }
+        for (int c = 0; c < kCols; ++c)
+          s[c] = __half2float(__ushort_as_half(static_cast<uint16_t>(c & 1 ? sbits[c >> 1] >> 16 : sbits[c >> 1] & 0xFFFFu)));
         cur_g = g;
       }
       float w[kCols];
@@ -115,10 +188,14 @@ cudaError_t launch_typed(const Problem& p, cudaStream_t stream) {
   const long long need = (total + kThreads - 1) / kThreads;
   const long long cap = static_cast<long long>(device_info().sm_count) * 8;
   const int grid = static_cast<int>(need < cap ? need : cap);
+  // one group per unit: the pair path
+  const bool pairs = p.g_idx == nullptr && p.group % Pack<BITS>::kPerUnit == 0;
   if (p.g_idx)
-    k_dequant<BITS, T, true><<<grid, kThreads, 0, stream>>>(a);
+    k_dequant<BITS, T, true, false><<<grid, kThreads, 0, stream>>>(a);
+  else if (pairs)
+    k_dequant<BITS, T, false, true><<<grid, kThreads, 0, stream>>>(a);
   else
-    k_dequant<BITS, T, false><<<grid, kThreads, 0, stream>>>(a);
+    k_dequant<BITS, T, false, false><<<grid, kThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

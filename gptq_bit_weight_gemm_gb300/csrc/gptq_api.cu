@@ -359,6 +359,67 @@ extern "C" int gptq_gemm_perm_noalloc(const void* A, int M, int K, int a_dtype, 
   return gptq::from_decode(gptq::launch_decode(p, s));
 }
 
+extern "C" int gptq_prepack_interleave(const int32_t* qweight, int K, int N, int bits, int32_t* qweight_il) {
+  if (!gptq::bits_ok(bits) || !qweight || !qweight_il) return GPTQ_ERR_ARG;
+  const int per = bits == 3 ? 32 : 32 / bits, rows = bits == 3 ? 3 : 1;
+  if (K <= 0 || N <= 0 || N % 32 || K % (4 * per)) return GPTQ_ERR_SHAPE;
+  const int tiles = K / per / 4, blocks = N / 32;
+  // word ((((cb * tiles + kt) * rows + r) * 32 + lane) * 4 + c) holds row (4 kt + t) * rows + r and
+  // column 32 cb + 4 quad(g) + c of the checkpoint, for lane = 4 g + t: the 16 bytes that lane of
+  // the decode kernel's warp loads for unit t of k-tile kt, columns quad(g) of its 32-column block
+  std::vector<int32_t> out(static_cast<size_t>(K / per) * rows * N);
+  size_t i = 0;
+  for (int cb = 0; cb < blocks; ++cb)
+    for (int kt = 0; kt < tiles; ++kt)
+      for (int r = 0; r < rows; ++r)
+        for (int lane = 0; lane < 32; ++lane) {
+          const int g = lane >> 2, t = lane & 3;
+          const int quad = ((g & 1) << 2) | (g >> 1);
+          const size_t src = (static_cast<size_t>(kt * 4 + t) * rows + r) * N + cb * 32 + quad * 4;
+          for (int c = 0; c < 4; ++c) out[i++] = qweight[src + c];
+        }
+  for (size_t j = 0; j < out.size(); ++j) qweight_il[j] = out[j];
+  return GPTQ_OK;
+}
+
+extern "C" int gptq_gemm_interleaved(const void* A, int M, int K, int a_dtype, const int32_t* perm,
+                                     const int32_t* qweight_il, const int32_t* qzeros, const void* scales, int N,
+                                     int bits, int group, int fmt, void* C, void* workspace,
+                                     size_t workspace_bytes, void* stream) {
+  Problem p = {};
+  int rc = gptq::check_common(qweight_il, qzeros, scales, nullptr, K, N, bits, group, &p);
+  if (rc) return rc;
+  if (fmt != GPTQ_FMT_V1 && fmt != GPTQ_FMT_V2) return GPTQ_ERR_ARG;
+  if (a_dtype != GPTQ_F16 && a_dtype != GPTQ_BF16) return GPTQ_ERR_ARG;
+  const int per = bits == 3 ? 32 : 32 / bits;
+  // whole k-tiles of 4 units, and groups made of whole k-tiles (the scale folds per group)
+  if (K % (4 * per) || p.group % (4 * per)) return GPTQ_ERR_SHAPE;
+  if (M < 0 || M > gptq::kDecodeMaxM) return GPTQ_ERR_SHAPE;
+  const size_t ws = perm ? gptq_gemm_perm_workspace_size(M, K) : 0;
+  if (workspace_bytes < ws) return GPTQ_ERR_WORKSPACE;
+  if (M == 0) return GPTQ_OK;
+  if (!A || !C || (ws && !workspace)) return GPTQ_ERR_ARG;
+  if (!gptq::aligned(A, 16) || !gptq::aligned(C, 16) || (perm && !gptq::aligned(perm, 16))) return GPTQ_ERR_ALIGN;
+  if (ws && !gptq::aligned(workspace, 16)) return GPTQ_ERR_ALIGN;
+  rc = gptq::device_ready(&p);
+  if (rc) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  p.M = M;
+  p.dtype = a_dtype;
+  p.zero_offset = fmt == GPTQ_FMT_V1 ? 1 : 0;
+  p.out = C;
+  p.interleaved = true;
+  p.A = A;
+  p.perm = perm;
+  if (ws) {
+    cudaError_t e = gptq::launch_gather_cols(A, perm, M, K, workspace, s);
+    if (e != cudaSuccess) return gptq::from_cuda(e);
+    p.A = workspace;
+    p.perm = nullptr;
+  }
+  return gptq::from_decode(gptq::launch_decode(p, s));
+}
+
 extern "C" int gptq_prepack_act_order(const int32_t* qweight, const int32_t* g_idx, int K, int N,
                                       int bits, int group, int32_t* qweight_out, int32_t* perm) {
   if (!gptq::bits_ok(bits) || !qweight || !g_idx || !qweight_out || !perm) return GPTQ_ERR_ARG;

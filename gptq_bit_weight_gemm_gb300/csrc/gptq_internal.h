@@ -33,6 +33,8 @@ struct Problem {
   // row scales, prefill_workspace_bytes)
   void* workspace;
   size_t workspace_bytes;
+  // qweight is in the interleaved layout of gptq_prepack_interleave (decode kernels only)
+  bool interleaved;
 };
 
 struct DeviceInfo {

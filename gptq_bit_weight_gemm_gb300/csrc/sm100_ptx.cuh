@@ -91,6 +91,16 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const void* tmap,
       : "memory");
 }
 
+// 1D bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned) with an L2 policy.
+__device__ __forceinline__ void bulk_load_hint(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                               uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
 // L2 policy for data read once (streamed weights): evicted first, so reused data stays in L2.
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;

@@ -212,6 +212,39 @@ int gptq_gemm_perm_noalloc(const void* A, int M, int K, int a_dtype, const int32
                            const int32_t* qweight, const int32_t* qzeros, const void* scales,
                            int N, int bits, int group, int fmt, void* C, void* stream);
 
+/*
+ * gptq_prepack_interleave -- HOST function: rewrite qweight into the decode kernel's own layout,
+ * the offline reordering the page "4.3 Weight-only INT4 量化：GPTQ、AWQ 与 Marlin Kernel" (section
+ * 6.1) describes for Marlin: packed words arranged so that what one lane of the kernel loads is
+ * contiguous.  The codes, their packing inside a word and qzeros / scales are unchanged; only
+ * whole words move.  Every 32-column block becomes one contiguous run along K; inside it each
+ * k-tile (4 units: 32/bits * 4 consecutive k, 128 for 3-bit) is 512 bytes per qweight row of a
+ * unit, in lane order: word (((cb * T + kt) * R + r) * 32 + lane) * 4 + c holds checkpoint row
+ * (4 kt + t) * R + r and column 32 cb + 4 q + c, where lane = 4 g + t, q = (g & 1) * 4 + g / 2,
+ * T = K * bits / 128 (K / 128 for 3-bit) k-tiles and R = 3 rows per unit for 3-bit, else 1.
+ * A warp's 16-byte fragment loads then read 512 contiguous bytes (no swizzle), and the kernel
+ * copies each warp's part of a chunk with one 1D bulk copy (no tensor map).
+ * qweight, qweight_il: host arrays of K * bits / 32 * N int32 (they may not overlap).
+ * Shapes: N a multiple of 32, K a multiple of 4 * 32 / bits (128 for 3-bit).
+ * Returns GPTQ_OK, GPTQ_ERR_ARG or GPTQ_ERR_SHAPE.
+ */
+int gptq_prepack_interleave(const int32_t* qweight, int K, int N, int bits, int32_t* qweight_il);
+
+/*
+ * gptq_gemm_interleaved -- gptq_gemm (M <= 32, the decode kernel) on a checkpoint whose qweight
+ * went through gptq_prepack_interleave; qzeros and scales are the checkpoint's own.  `perm`
+ * (nullable) is the act-order permutation of gptq_prepack_act_order, for a checkpoint sorted by
+ * group before it was interleaved; then C = A[:, perm] @ W and, for M > 1, `workspace` takes
+ * gptq_gemm_perm_workspace_size(M, K) bytes (otherwise it may be NULL).  The groups must be whole
+ * k-tiles (group a multiple of 4 * 32 / bits, 128 for 3-bit; -1 allowed): the scale folds per
+ * group.  Same arithmetic, results and stream-order rules as gptq_gemm.
+ * Returns GPTQ_OK or a negative gptq_status (GPTQ_ERR_SHAPE for M > 32 or misaligned K/group).
+ */
+int gptq_gemm_interleaved(const void* A, int M, int K, int a_dtype, const int32_t* perm,
+                          const int32_t* qweight_il, const int32_t* qzeros, const void* scales, int N,
+                          int bits, int group, int fmt, void* C, void* workspace, size_t workspace_bytes,
+                          void* stream);
+
 /* Bytes of device workspace gptq_gemm may need for this problem: the fp16 copy of bf16
  * activations and their row scales, (M * K * 2 rounded up to 256) + (M * 4 rounded up to 256);
  * 0 for M <= 0.  Enough for every activation dtype and path. */

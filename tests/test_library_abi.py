@@ -29,7 +29,8 @@ def test_exports_every_declared_symbol(lib):
                                "gptq_get_device_status", "gptq_strerror",
                                "gptq_selftest_wait_timeout", "gptq_prepack_act_order",
                                "gptq_gemm_perm", "gptq_gemm_perm_workspace_size",
-                               "gptq_gemm_perm_noalloc", "gptq_gemm_grouped"])
+                               "gptq_gemm_perm_noalloc", "gptq_gemm_grouped",
+                               "gptq_prepack_interleave", "gptq_gemm_interleaved"])
     for name in declared:
         assert hasattr(lib, name), name
 
