@@ -44,7 +44,6 @@ namespace prefill {
 constexpr int kBM = 256;            // rows of A per tile (two UMMA M=128 halves)
 constexpr int kBN = 256;            // columns per tile (UMMA N=256)
 constexpr int kBK = 64;             // k per stage: one 128-byte swizzle row of 16-bit values
-constexpr int kStages = 3;          // A + packed-W ring
 constexpr int kEpiWarps = 4;
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
@@ -60,6 +59,7 @@ template <int BITS>
 struct Geo {
   static constexpr int kRows = kBK * BITS / 32;                // qweight rows per k-step
   static constexpr uint32_t kWBytes = kBN * kRows * 4;         // packed tile bytes
+  static constexpr int kStages = 3;                            // A + packed-W ring depth
   static constexpr int kBStages = BITS == 8 ? 2 : 3;           // dequantized-B ring depth
   static constexpr uint32_t kOffW = kStages * kATileBytes;
   static constexpr uint32_t kOffB = kOffW + kStages * kWBytes;
@@ -264,6 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     k_prefill(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
               const Args a) {
   using Gm = Geo<BITS>;
+  constexpr int kStages = Gm::kStages;
   constexpr int kBStages = Gm::kBStages;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -321,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int s = 0;
       uint32_t ph = 0;
-      uint32_t issued = 0, last_par[kStages] = {0, 0, 0};
+      uint32_t issued = 0, last_par[kStages] = {};
       bool ok = true;
       for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
         const int mt = t % num_m, nt = t / num_m;
