@@ -418,7 +418,9 @@ def _checkpoint(g, torch, dev, wl, fmt=None):
 def time_gemm(g, torch, dev, stream, wl, M, l2, path="gemm", fmt=None, reps=200):
     """Median per-launch time of one GEMM call on one workload: a CUDA graph of launches over S
     rotating copies of every input (S x bytes > 3x L2 where one copy is smaller), replayed 11
-    times, the first replay discarded.  path: "gemm" (gptq_gemm, with g_idx for act-order),
+    times, the first replay discarded.  path: "gemm" (gptq_gemm; act-order: g_idx with the
+    workspace in which the rows are sorted by group on the device), "rows" (gptq_gemm with g_idx
+    and the per-row-group kernels),
     "perm" (act-order rows sorted on the host, gptq_gemm_perm), "il" (qweight in the interleaved
     layout, gptq_gemm_interleaved; act-order checkpoints sorted first, through perm) or "dequant"
     (gptq_dequant)."""
@@ -440,10 +442,16 @@ def time_gemm(g, torch, dev, stream, wl, M, l2, path="gemm", fmt=None, reps=200)
         out_shape, out_dt = (M, wl.N), A.dtype
         nbytes = algorithmic_bytes(wl, M)
     per_set = nbytes + (0 if path == "dequant" else M * wl.N * 2)
-    # bf16 activations through the tensor-core kernel: the caller's workspace (fp16 copy of A)
+    # the caller's workspace: act-order rows sorted on the device, or bf16 activations through the
+    # tensor-core kernel (fp16 copy of A)
     gws = None
-    if path == "gemm" and A is not None and A.dtype == torch.bfloat16:
-        gws = torch.empty(g.workspace_size(M, wl.K, wl.N, wl.bits, wl.group), dtype=torch.uint8, device=dev)
+    if path in ("gemm", "rows") and A is not None:
+        size = g.act_order_workspace_size(M, wl.K, wl.N, wl.bits, wl.group) if (
+            path == "gemm" and draw.g_idx is not None) else 0
+        if size == 0 and A.dtype == torch.bfloat16:
+            size = g.workspace_size(M, wl.K, wl.N, wl.bits, wl.group)
+        if size:
+            gws = torch.empty(size, dtype=torch.uint8, device=dev)
     S = max(1, min(256, int(np.ceil(3 * l2 / per_set))))
     sets = [(qw.clone(), qz.clone(), sc.clone(), None if A is None else A.clone(),
              torch.empty(out_shape, dtype=out_dt, device=dev)) for _ in range(S)]
@@ -461,7 +469,8 @@ def time_gemm(g, torch, dev, stream, wl, M, l2, path="gemm", fmt=None, reps=200)
             g.dequant(q, z, s_, gi, K=wl.K, bits=wl.bits, group=wl.group, fmt=f, dtype=out_dt, out=c,
                       stream=stream)
         else:
-            g.gemm(a, q, z, s_, gi, bits=wl.bits, group=wl.group, fmt=f, out=c, workspace=gws, stream=stream)
+            g.gemm(a, q, z, s_, gi, bits=wl.bits, group=wl.group, fmt=f, out=c, workspace=gws,
+                   sort_rows=(path == "gemm"), stream=stream)
 
     gr = capture(torch, stream, launch, n)
     ms, ms_min, ms_max = replay_median(torch, stream, gr, n)
@@ -484,7 +493,11 @@ def run_configs(g, torch, dev, stream, peaks, l2, only=""):
         ("3", "lowbit_2bit_g64", 1, "gemm", ""),
         ("3", "lowbit_2bit_g64", 8, "gemm", ""),
         ("3", "lowbit_2bit_g64", 32, "gemm", ""),
-        ("4", "act_order_3bit_g128", 16, "gemm", "g_idx through gptq_gemm"),
+        ("4", "act_order_3bit_g128", 16, "gemm", "g_idx through gptq_gemm, rows sorted by group on the device"),
+        ("4", "act_order_3bit_g128", 16, "rows", "g_idx through gptq_gemm, per-row groups"),
+        ("4", "act_order_3bit_g128", 1, "gemm", "one token, rows sorted by group on the device"),
+        ("4", "act_order_3bit_g128", 1, "rows", "one token, per-row groups"),
+        ("4", "act_order_3bit_g128", 4096, "gemm", "4096 tokens, rows sorted by group on the device"),
         ("4", "act_order_3bit_g128", 16, "perm", "rows sorted on the host, gptq_gemm_perm"),
         ("4", "act_order_3bit_g128", 16, "il", "rows sorted, then interleaved, gptq_gemm_interleaved"),
         ("5", "prefill_4bit_g128", 4096, "gemm", ""),
@@ -500,6 +513,7 @@ def run_configs(g, torch, dev, stream, peaks, l2, only=""):
         wl = W[name]
         ms, nbytes, S = time_gemm(g, torch, dev, stream, wl, M, l2, path=path)
         row = {"config": cfg, "workload": name, "M": M, "path": {"gemm": "gptq_gemm", "perm": "gptq_gemm_perm",
+                                                                 "rows": "gptq_gemm (per-row groups)",
                                                                  "il": "gptq_gemm_interleaved",
                                                                  "dequant": "gptq_dequant"}[path],
                "us": round(ms * 1e3, 3)}
@@ -694,7 +708,8 @@ def run_reference(args):
 
 def run_profile_target(args):
     """--profile WORKLOAD:M[:PATH]: just `warmup + steps` eager launches of one call on one
-    workload (PATH gemm, perm or dequant), for a profiler to capture; prints one short line."""
+    workload (PATH gemm, rows, perm, il or dequant), for a profiler to capture; prints one short
+    line."""
     import torch
     import gptq_bit_weight_gemm_gb300 as g
     from gptq_bit_weight_gemm_gb300 import build as lib_build
@@ -725,7 +740,7 @@ def run_profile_target(args):
                 g.dequant(qw, qz, sc, gi, K=wl.K, bits=wl.bits, group=wl.group, stream=stream,
                           dtype=torch.float16 if wl.act_dtype == "f16" else torch.bfloat16)
             else:
-                g.gemm(A, qw, qz, sc, gi, bits=wl.bits, group=wl.group, stream=stream)
+                g.gemm(A, qw, qz, sc, gi, bits=wl.bits, group=wl.group, sort_rows=(path != "rows"), stream=stream)
     stream.synchronize()
     assert g.device_status(stream) == 0
     print(json.dumps({"profile": args.profile, "launches": args.warmup + args.steps}))

@@ -59,6 +59,7 @@ _SIGNATURES = {
     "gptq_dequant": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
     "gptq_gemm": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P]),
     "gptq_gemm_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
+    "gptq_gemm_act_order_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "gptq_repack_zeros_v1_to_v2": (_I, [_P, _P, _I, _I, _I]),
     "gptq_quantize_rtn": (_I, [_P, _I, _I, _I, _I, _P, _I, _I, _P, _P, _P, _P]),
     "gptq_get_device_status": (_I, [_P, ctypes.POINTER(ctypes.c_uint)]),
@@ -145,16 +146,22 @@ def _stream(stream):
 
 
 def gemm(A, qweight, qzeros, scales, g_idx=None, *, bits, group, fmt=V2, out=None, workspace=None,
-         stream=None):
-    """C[M, N] = A[M, K] @ dequant(qweight, qzeros, scales, g_idx) on the current stream.  bf16
-    activations take a workspace of workspace_size(...) bytes (allocated here when not given)."""
+         sort_rows=True, stream=None):
+    """C[M, N] = A[M, K] @ dequant(qweight, qzeros, scales, g_idx) on the current stream.  When no
+    workspace is given one is allocated here: act-order (g_idx) with sort_rows, where the shape
+    qualifies, takes act_order_workspace_size(...) bytes (rows sorted by group on the device);
+    otherwise bf16 activations take workspace_size(...) bytes."""
     torch = _torch()
     M, K = A.shape
     N = qweight.shape[1]
     if out is None:
         out = torch.empty((M, N), dtype=A.dtype, device=A.device)
-    if workspace is None and A.dtype == torch.bfloat16 and M > 0:
-        workspace = torch.empty(workspace_size(M, K, N, bits, group), dtype=torch.uint8, device=A.device)
+    if workspace is None and M > 0:
+        size = act_order_workspace_size(M, K, N, bits, group) if (g_idx is not None and sort_rows) else 0
+        if size == 0 and A.dtype == torch.bfloat16:
+            size = workspace_size(M, K, N, bits, group)
+        if size:
+            workspace = torch.empty(size, dtype=torch.uint8, device=A.device)
     ws_ptr = _ptr(workspace, name="workspace") if workspace is not None else None
     ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
     rc = lib().gptq_gemm(_ptr(A, name="A"), M, K, _dtype_code(A),
@@ -303,6 +310,10 @@ def gemm_grouped(A, offsets, qweight, qzeros, scales, *, bits, group, max_m, fmt
 
 def workspace_size(M, K, N, bits, group):
     return int(lib().gptq_gemm_workspace_size(M, K, N, bits, group))
+
+
+def act_order_workspace_size(M, K, N, bits, group):
+    return int(lib().gptq_gemm_act_order_workspace_size(M, K, N, bits, group))
 
 
 def device_status(stream=None):

@@ -46,6 +46,10 @@ struct Args {
   // interleaved weights (gptq_prepack_interleave): k-tiles per 32-column block, else 0 (the
   // checkpoint's own row-major layout, read through the tensor map)
   int il_tiles;
+  // nullable: the kernel does nothing unless *run_flag == run_when (set by an earlier kernel in
+  // the stream; such launches are never programmatic-dependent, so the flag is final at entry)
+  const int* run_flag;
+  int run_when;
 };
 
 __device__ __forceinline__ void split(int total, int parts, int idx, int& b, int& e) {

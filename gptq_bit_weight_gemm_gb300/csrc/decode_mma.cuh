@@ -188,6 +188,8 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
   constexpr int NB = (MT + 7) / 8;                    // token blocks of 8
   extern __shared__ __align__(128) unsigned char smem_raw[];
 
+  // a flag-gated launch whose flag says no: every CTA leaves before any barrier or copy
+  if (args.run_flag != nullptr && *args.run_flag != args.run_when) return;
   pdl_launch_dependents();
   // Grouped: expert e = blockIdx.z multiplies rows [offsets[e], offsets[e + 1]) of A into the
   // same rows of C, with its own scales, zeros and packed rows (e * K * bits / 32 onward in the
@@ -948,6 +950,8 @@ cudaError_t launch_mma(const Problem& p, cudaStream_t stream) {
   a.offsets = GROUPED ? p.offsets : nullptr;
   a.rows = p.rows;
   a.il_tiles = p.interleaved ? a.units / 4 : 0;
+  a.run_flag = p.run_flag;
+  a.run_when = p.run_when;
   const int E = GROUPED ? p.E : 1;                     // weights side by side (grid z)
   const int slabs = (p.N + kSlab - 1) / kSlab;
   const int sms = device_info().sm_count;
@@ -1019,7 +1023,7 @@ cudaError_t launch_mma(const Problem& p, cudaStream_t stream) {
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
+  cfg.numAttrs = p.no_pdl ? 1 : 2;   // no_pdl: start only after the previous kernel completed
   return cudaLaunchKernelEx(&cfg, kern, tmW, a, geo);
 }
 

@@ -185,6 +185,103 @@ extern "C" size_t gptq_gemm_workspace_size(int M, int K, int N, int bits, int gr
   return gptq::prefill_workspace_bytes(M, K);
 }
 
+namespace gptq {
+namespace {
+
+// Workspace of the act-order path of gptq_gemm: [flag | perm (K) | code sources (K) | sorted
+// qweight | the tensor-core kernel's workspace for M x K (also the decode kernels' gathered
+// activations)], each part starting on a 256-byte boundary.
+struct ActOrderLayout {
+  size_t perm, src, qweight, rest, total;
+};
+
+ActOrderLayout act_order_layout(int M, int K, int N, int bits) {
+  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  ActOrderLayout l;
+  l.perm = 256;
+  l.src = l.perm + up(static_cast<size_t>(K) * 4);
+  l.qweight = l.src + up(static_cast<size_t>(K) * 4);
+  l.rest = l.qweight + up(static_cast<size_t>(K) * bits / 32 * N * 4);
+  l.total = l.rest + prefill_workspace_bytes(M > 0 ? M : 1, K);
+  return l;
+}
+
+// Shapes whose rows the device sorts: the sort and repack fit their shared memory, and the sorted
+// groups suit the group-wise (exact-difference) kernels: groups of whole k-tiles.
+bool act_order_shape_ok(int K, int G, int group, int bits) {
+  const int per = bits == 3 ? 32 : 32 / bits;
+  return sort_groups_fits(K, G, group) && repack_strip_width(K, bits) > 0 && group % (4 * per) == 0;
+}
+
+// gptq_gemm with g_idx through sorted rows.  Launches, in stream order: the sort (perm, flag), the
+// repack (flag 1 only), the group-wise GEMM on the sorted weight with A gathered through perm
+// (flag 1 only), and the per-row-group GEMM on the original checkpoint (flag 0 only: g_idx with an
+// entry out of range, or groups of unequal size).  The flag-gated kernels start only after their
+// predecessor has completed (no programmatic dependent launch): they read what it wrote.
+int gemm_act_order(const Problem& p, cudaStream_t s) {
+  const ActOrderLayout l = act_order_layout(p.M, p.K, p.N, p.bits);
+  unsigned char* ws = static_cast<unsigned char*>(p.workspace);
+  int* flag = reinterpret_cast<int*>(ws);
+  int32_t* perm = reinterpret_cast<int32_t*>(ws + l.perm);
+  uint32_t* src = reinterpret_cast<uint32_t*>(ws + l.src);
+  int32_t* qw_sorted = reinterpret_cast<int32_t*>(ws + l.qweight);
+  void* rest = ws + l.rest;
+  const size_t rest_bytes = l.total - l.rest;
+  cudaError_t e = launch_sort_groups(p.g_idx, p.K, p.G, p.group, p.bits, perm, src, flag, s);
+  if (e != cudaSuccess) return from_cuda(e);
+  e = launch_repack_rows(p.qweight, src, flag, p.K, p.N, p.bits, qw_sorted, s);
+  if (e != cudaSuccess) return from_cuda(e);
+
+  Problem q = p;
+  q.g_idx = nullptr;
+  q.qweight = qw_sorted;
+  q.run_flag = flag;
+  q.run_when = 1;
+  q.no_pdl = true;
+  q.workspace = rest;
+  q.workspace_bytes = rest_bytes;
+  bool fast_done = false;
+  if (p.M <= kDecodeMaxM) {
+    Problem d = q;
+    if (p.M > 1) {
+      e = launch_gather_cols(p.A, perm, p.M, p.K, rest, s);
+      if (e != cudaSuccess) return from_cuda(e);
+      d.A = rest;
+    } else {
+      d.perm = perm;                            // one token: gathered while staging
+    }
+    e = launch_decode(d, s);
+    if (e == cudaSuccess) fast_done = true;
+    else if (e != cudaErrorInvalidConfiguration) return from_cuda(e);
+  }
+  if (!fast_done) {
+    q.perm = perm;                              // the tensor-core kernel gathers A into `rest`
+    e = launch_prefill(q, s);
+    if (e != cudaSuccess) return from_cuda(e);
+  }
+
+  Problem f = p;
+  f.run_flag = flag;
+  f.run_when = 0;
+  f.no_pdl = true;
+  f.workspace = rest;
+  f.workspace_bytes = rest_bytes;
+  if (p.M <= kDecodeMaxM) {
+    e = launch_decode(f, s);
+    if (e != cudaErrorInvalidConfiguration) return from_cuda(e);
+  }
+  return from_cuda(launch_prefill(f, s));
+}
+
+}  // namespace
+}  // namespace gptq
+
+extern "C" size_t gptq_gemm_act_order_workspace_size(int M, int K, int N, int bits, int group) {
+  if (M <= 0 || K <= 0 || N <= 0 || group <= 0 || K % group || !gptq::bits_ok(bits)) return 0;
+  if (!gptq::act_order_shape_ok(K, K / group, group, bits)) return 0;
+  return gptq::act_order_layout(M, K, N, bits).total;
+}
+
 extern "C" int gptq_gemm(const void* A, int M, int K, int a_dtype, const int32_t* qweight,
                          const int32_t* qzeros, const void* scales, const int32_t* g_idx, int N,
                          int bits, int group, int fmt, void* C, void* workspace,
@@ -209,6 +306,12 @@ extern "C" int gptq_gemm(const void* A, int M, int K, int a_dtype, const int32_t
   p.workspace = workspace;
   p.workspace_bytes = workspace ? workspace_bytes : 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // act-order with room for the sorted copy: sort the rows on the device, then the group-wise
+  // kernels (gptq_gemm_act_order_workspace_size is 0 for shapes that do not qualify)
+  if (g_idx) {
+    const size_t need = gptq_gemm_act_order_workspace_size(M, K, N, bits, group);
+    if (need && p.workspace_bytes >= need) return gptq::gemm_act_order(p, s);
+  }
   if (M <= gptq::kDecodeMaxM) {
     const cudaError_t e = gptq::launch_decode(p, s);
     // cudaErrorInvalidConfiguration: nothing launched, the decode layout does not fit this K at

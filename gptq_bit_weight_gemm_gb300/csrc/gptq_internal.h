@@ -35,6 +35,13 @@ struct Problem {
   size_t workspace_bytes;
   // qweight is in the interleaved layout of gptq_prepack_interleave (decode kernels only)
   bool interleaved;
+  // nullable: the kernels do nothing unless *run_flag == run_when (a device flag written by an
+  // earlier kernel of the same stream)
+  const int* run_flag;
+  int run_when;
+  // launch without programmatic dependent launch: the kernel starts once the previous kernel has
+  // completed (needed when it reads weights that the previous kernels wrote)
+  bool no_pdl;
 };
 
 struct DeviceInfo {
@@ -54,6 +61,18 @@ cudaError_t launch_prefill(const Problem& p, cudaStream_t stream);
 size_t prefill_workspace_bytes(int M, int K);
 cudaError_t launch_gather_cols(const void* A, const int32_t* perm, int M, int K, void* out,
                                cudaStream_t stream);
+// Act-order on the device: the stable sort of the rows by g_idx (perm; src, the packed word and
+// bit offset of each sorted row's code; flag = 1 when every group holds exactly `group` rows,
+// else 0) and the packed weight rewritten in that order (only when the flag is 1).  Shared
+// memory per CTA is at most kMaxActOrderSmem; sort_groups_fits and repack_strip_width (0: no
+// strip fits) say whether a shape qualifies.
+constexpr size_t kMaxActOrderSmem = 200 * 1024;
+bool sort_groups_fits(int K, int G, int group);
+int repack_strip_width(int K, int bits);
+cudaError_t launch_sort_groups(const int32_t* g_idx, int K, int G, int group, int bits, int32_t* perm,
+                               uint32_t* src, int* flag, cudaStream_t stream);
+cudaError_t launch_repack_rows(const int32_t* qweight, const uint32_t* src, const int* flag, int K, int N,
+                               int bits, int32_t* out, cudaStream_t stream);
 cudaError_t launch_wait_selftest(unsigned* status, uint64_t limit_ns, int* flag, cudaStream_t stream);
 
 struct QuantProblem {

@@ -79,6 +79,8 @@ struct Args {
   const float* row_scale;   // bf16 input: 2^e per row of A (the fp16 copy was divided by it)
   void* C;
   unsigned* status;
+  const int* run_flag;      // nullable: run only if *run_flag == run_when
+  int run_when;
 };
 
 struct Sync {
@@ -217,9 +219,14 @@ __device__ __forceinline__ uint4 dq_chunk8(uint32_t w0, uint32_t w1, const ColCo
 // with max_k |A[m][k]| * 2^-e_m in [2^15, 2^16) -- below fp16's largest finite value for any bf16
 // significand.  Multiplying by a power of two is exact, and so is the conversion for every value in
 // fp16's normal range; values more than 2^29 below the row's largest round (their products are far
-// below the GEMM's absolute tolerance).  One CTA per row at a time, 16-byte loads and stores.
+// below the GEMM's absolute tolerance).  One CTA per row at a time, 16-byte loads and stores.  With
+// perm (act-order rows sorted by group) the output column k takes A[m][perm[k]] (the row maximum
+// does not depend on the order).  run_flag as in Args.
 __global__ void __launch_bounds__(256) k_rows_to_f16(const uint16_t* __restrict__ A, int M, int K,
+                                                     const int32_t* __restrict__ perm,
+                                                     const int* run_flag, int run_when,
                                                      uint16_t* __restrict__ out, float* __restrict__ row_scale) {
+  if (run_flag != nullptr && *run_flag != run_when) return;
   __shared__ uint32_t warp_max[8];
   for (int m = blockIdx.x; m < M; m += gridDim.x) {
     const uint4* row = reinterpret_cast<const uint4*>(A + static_cast<long long>(m) * K);
@@ -244,7 +251,20 @@ __global__ void __launch_bounds__(256) k_rows_to_f16(const uint16_t* __restrict_
     e = e < -126 ? -126 : (e > 126 ? 126 : e);               // 2^e and 2^-e stay normal floats
     const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
     for (int i = threadIdx.x; i < nv; i += blockDim.x) {
-      const uint4 v = __ldg(row + i);
+      uint4 v;
+      if (perm == nullptr) {
+        v = __ldg(row + i);
+      } else {
+        const uint16_t* r16 = A + static_cast<long long>(m) * K;
+        uint32_t h[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          int src = __ldg(perm + 8 * i + j);
+          src = src < 0 ? 0 : (src >= K ? K - 1 : src);   // a bad entry never reads outside the row
+          h[j] = __ldg(r16 + src);
+        }
+        v = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
+      }
       uint4 o;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -267,6 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kStages = Gm::kStages;
   constexpr int kBStages = Gm::kBStages;
   extern __shared__ unsigned char smem_raw[];
+  if (a.run_flag != nullptr && *a.run_flag != a.run_when) return;   // flag-gated launch: not this one
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = ptx::smem_addr(smem);
@@ -632,6 +653,8 @@ cudaError_t launch_typed(const Problem& p, const void* A16, const float* row_sca
   a.row_scale = row_scale;
   a.C = p.out;
   a.status = p.status;
+  a.run_flag = p.run_flag;
+  a.run_when = p.run_when;
   auto kern = k_prefill<BITS, TOUT, PERK>;
   static bool attr_set = false;   // per instantiation; the attribute is per function
   if (!attr_set) {
@@ -656,15 +679,23 @@ cudaError_t launch_t(const Problem& p, const void* A16, const float* row_scale, 
 
 template <int BITS>
 cudaError_t launch_bits(const Problem& p, cudaStream_t stream) {
-  if (p.dtype == 0) return launch_t<BITS, __half>(p, p.A, nullptr, stream);
-  // bf16: the fp16 copy of A and the row scales in the caller's workspace
+  if (p.dtype == 0 && p.perm == nullptr) return launch_t<BITS, __half>(p, p.A, nullptr, stream);
+  // bf16, or columns gathered through perm: the fp16 copy of A (and for bf16 the row scales) in
+  // the caller's workspace
   const size_t a_bytes = (static_cast<size_t>(p.M) * p.K * 2 + 255) & ~static_cast<size_t>(255);
   if (p.workspace == nullptr || p.workspace_bytes < prefill_workspace_bytes(p.M, p.K)) return cudaErrorInvalidValue;
   uint16_t* A16 = static_cast<uint16_t*>(p.workspace);
+  cudaError_t e;
+  if (p.dtype == 0) {
+    e = launch_gather_cols(p.A, p.perm, p.M, p.K, A16, stream);
+    if (e != cudaSuccess) return e;
+    return launch_t<BITS, __half>(p, A16, nullptr, stream);
+  }
   float* row_scale = reinterpret_cast<float*>(static_cast<unsigned char*>(p.workspace) + a_bytes);
   const int blocks = p.M < device_info().sm_count * 8 ? p.M : device_info().sm_count * 8;
-  k_rows_to_f16<<<blocks, 256, 0, stream>>>(static_cast<const uint16_t*>(p.A), p.M, p.K, A16, row_scale);
-  cudaError_t e = cudaGetLastError();
+  k_rows_to_f16<<<blocks, 256, 0, stream>>>(static_cast<const uint16_t*>(p.A), p.M, p.K, p.perm,
+                                             p.run_flag, p.run_when, A16, row_scale);
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_t<BITS, __nv_bfloat16>(p, A16, row_scale, stream);
 }

@@ -122,6 +122,15 @@ int gptq_dequant(const int32_t* qweight, const int32_t* qzeros, const void* scal
  * runs: it then holds the fp16 copy of A and its row scales and must be at least
  * gptq_gemm_workspace_size() bytes (GPTQ_ERR_WORKSPACE otherwise, nothing launched).  With fp16
  * activations, or M <= 32 and K within the decode kernel's reach, it may be NULL.
+ * Act-order (g_idx given): with a workspace of at least
+ * gptq_gemm_act_order_workspace_size(M, K, N, bits, group) bytes (nonzero), the call sorts the
+ * rows by group on the device (the stable sort of gptq_prepack_act_order), writes the sorted
+ * packed weight into the workspace and runs the group-wise kernels on it with A's columns taken
+ * through the sort -- the same result as gptq_prepack_act_order + gptq_gemm_perm, computed per
+ * call.  When g_idx does not describe groups of exactly `group` rows (or holds an entry outside
+ * [0, G)), a device flag routes the call to the per-row-group kernels instead, inside the same
+ * launches' stream order, with no host synchronisation.  A smaller workspace selects those
+ * per-row-group kernels directly.
  * Returns GPTQ_OK or a negative gptq_status.
  */
 int gptq_gemm(const void* A, int M, int K, int a_dtype, const int32_t* qweight,
@@ -249,6 +258,16 @@ int gptq_gemm_interleaved(const void* A, int M, int K, int a_dtype, const int32_
  * activations and their row scales, (M * K * 2 rounded up to 256) + (M * 4 rounded up to 256);
  * 0 for M <= 0.  Enough for every activation dtype and path. */
 size_t gptq_gemm_workspace_size(int M, int K, int N, int bits, int group);
+
+/* Bytes of device workspace with which gptq_gemm runs an act-order problem (g_idx given) on
+ * rows sorted by group on the device: a flag (256 bytes), the sorted row order and each sorted
+ * row's code position (K * 4 bytes each, rounded up to 256), the sorted packed weight
+ * (K * bits / 32 * N * 4, rounded up to 256) and gptq_gemm_workspace_size(max(M, 1), K, ...).
+ * 0 when the shape does not qualify: K % group, G * 128 + K * 2 above 200 KB (the sort's shared
+ * memory), a group of more than 65535 rows, a packed column of more than 200 KB in 4-column
+ * strips, or a group size that is not a multiple of 4 * (32 / bits) rows (128 rows for 3-bit);
+ * gptq_gemm then always uses the per-row-group kernels. */
+size_t gptq_gemm_act_order_workspace_size(int M, int K, int N, int bits, int group);
 
 /*
  * gptq_repack_zeros_v1_to_v2 -- HOST function: rewrite a v1 qzeros array ([G, N*bits/32],

@@ -117,12 +117,16 @@ def dev(ck):
 
 
 def check_gemm(ck, A, dtype, what):
+    """The GEMM against the oracle; act-order checkpoints both on rows sorted by group on the device
+    and with per-row groups."""
     qw, qz, sc, gi = dev(ck)
-    C = g.gemm(A.to(DEV), qw, qz, sc, gi, bits=ck["bits"], group=ck["group"], fmt=ck["fmt"])
-    torch.cuda.synchronize()
     Cref, B = oracle.gemm(bits16(A), ODT[dtype], ck["qweight"], ck["qzeros"], ck["scales"], ck["g_idx"],
                           ck["N"], ck["bits"], ck["group"], ck["fmt"])
-    assert_gemm_close(C, Cref, B, what)
+    for sort_rows in ((True, False) if gi is not None else (True,)):
+        C = g.gemm(A.to(DEV), qw, qz, sc, gi, bits=ck["bits"], group=ck["group"], fmt=ck["fmt"],
+                   sort_rows=sort_rows)
+        torch.cuda.synchronize()
+        assert_gemm_close(C, Cref, B, "%s sort_rows=%s" % (what, sort_rows))
     return C, Cref, B
 
 
@@ -155,9 +159,10 @@ def test_raw_checkpoint_dequant_and_one_hot_rows_bit_exact(bits, dt, fmt, act):
     (M = 1, 16, 32 decode; 130 tensor-core) reproduce those rows of the dequantized weight.
 
     The GEMMs multiply in fp16 for both activation types.  The per-weight and tensor-core paths
-    (act-order, M > 32) multiply the weight rounded to fp16, so with bf16 outputs a one-hot row
-    gives that fp16 weight rounded again to bf16; the folded decode path keeps the exact product
-    (q - zero) * scale in fp32 and rounds it once."""
+    (act-order with per-row groups, M > 32) multiply the weight rounded to fp16, so with bf16
+    outputs a one-hot row gives that fp16 weight rounded again to bf16; the folded decode path
+    (also act-order on rows sorted by group on the device) keeps the exact product
+    (q - zero) * scale in fp32 and rounds it once.  Act-order runs both ways."""
     ck = _raw(bits, dt, fmt, act)
     qw, qz, sc, gi = dev(ck)
     K, N = ck["K"], ck["N"]
@@ -176,13 +181,16 @@ def test_raw_checkpoint_dequant_and_one_hot_rows_bit_exact(bits, dt, fmt, act):
         rows = np.sort(rng.choice(K, size=M, replace=False))
         A = torch.zeros((M, K), dtype=TDT[dt])
         A[np.arange(M), rows] = 1.0
-        C = g.gemm(A.to(DEV), qw, qz, sc, gi, bits=bits, group=128, fmt=ck["fmt"])
-        torch.cuda.synchronize()
-        c = bits16(C)
-        # -0 and +0 both represent an exact zero
-        exp = (ref_via_f16 if (act or M > 32) else ref)[rows]
-        same = (c == exp) | (((c & 0x7FFF) == 0) & ((exp & 0x7FFF) == 0))
-        assert same.all(), "M=%d: %d of %d outputs differ from dequant" % (M, int((~same).sum()), same.size)
+        for sort_rows in ((True, False) if act else (True,)):
+            C = g.gemm(A.to(DEV), qw, qz, sc, gi, bits=bits, group=128, fmt=ck["fmt"], sort_rows=sort_rows)
+            torch.cuda.synchronize()
+            c = bits16(C)
+            # -0 and +0 both represent an exact zero
+            per_weight = (act and not sort_rows) or M > 32
+            exp = (ref_via_f16 if per_weight else ref)[rows]
+            same = (c == exp) | (((c & 0x7FFF) == 0) & ((exp & 0x7FFF) == 0))
+            assert same.all(), "M=%d sort_rows=%s: %d of %d outputs differ from dequant" % (
+                M, sort_rows, int((~same).sum()), same.size)
 
 
 # ------------------------------------------------------------------------------ quantizer-made degenerate groups

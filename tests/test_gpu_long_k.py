@@ -58,9 +58,11 @@ def test_gemm_long_k_many_tokens(K, bits, group):
     assert_gemm_close(C, Cref, B, "K=%d bits=%d group=%d" % (K, bits, group))
 
 
-def test_gemm_long_k_act_order_on_the_tensor_core_fallback():
+@pytest.mark.parametrize("sort_rows", [True, False], ids=["sorted", "per_row"])
+def test_gemm_long_k_act_order_on_the_tensor_core_fallback(sort_rows):
     """K = 53248 at 32 tokens fits no decode layout, so gptq_gemm runs the tensor-core kernel; with
-    act-order its per-k group lookup (g_idx) must match the oracle too."""
+    act-order it must match the oracle both on rows sorted by group on the device (4-column repack
+    strips) and with its per-k group lookup (g_idx)."""
     K, N, M, bits, group = 53248, 256, 32, 4, 128
     import dataclasses
     wl = dataclasses.replace(BASE.resized(K, N, (M,), name="long_k_act"), bits=bits, group=group,
@@ -69,8 +71,9 @@ def test_gemm_long_k_act_order_on_the_tensor_core_fallback():
     ck = oracle.make_checkpoint(draw.W, bits, group, draw.g_idx, False, oracle.V2)
     A = gptq_inputs.draw_activations(wl, M)
     qw, qz, sc = _dev(ck)
+    assert g.act_order_workspace_size(M, K, N, bits, group) > 0
     C = g.gemm(A.to(DEV), qw, qz, sc, torch.from_numpy(ck["g_idx"]).to(DEV), bits=bits, group=group,
-               fmt=g.V2)
+               fmt=g.V2, sort_rows=sort_rows)
     torch.cuda.synchronize()
     Cref, B = oracle.gemm(bits16(A), oracle.F16, ck["qweight"], ck["qzeros"], ck["scales"], ck["g_idx"], N,
                           bits, group, oracle.V2)

@@ -30,7 +30,8 @@ def test_exports_every_declared_symbol(lib):
                                "gptq_selftest_wait_timeout", "gptq_prepack_act_order",
                                "gptq_gemm_perm", "gptq_gemm_perm_workspace_size",
                                "gptq_gemm_perm_noalloc", "gptq_gemm_grouped",
-                               "gptq_prepack_interleave", "gptq_gemm_interleaved"])
+                               "gptq_prepack_interleave", "gptq_gemm_interleaved",
+                               "gptq_gemm_act_order_workspace_size"])
     for name in declared:
         assert hasattr(lib, name), name
 
@@ -186,6 +187,22 @@ def test_gemm_grouped_validation_without_gpu(lib, kw, code):
                                a["qweight"], a["qzeros"], a["scales"], a["N"], a["bits"], a["group"],
                                a["fmt"], a["C"], None)
     assert rc == code
+
+
+def test_act_order_workspace_size(lib):
+    # flag (256) + row order and code positions (K * 4 each) + sorted packed weight + the
+    # tensor-core workspace for M x K
+    assert g.act_order_workspace_size(16, 5120, 13824, 3, 128) == (256 + 2 * 20480 + 5120 * 3 // 32 * 13824 * 4
+                                                                   + 16 * 5120 * 2 + 256)
+    assert g.act_order_workspace_size(1, 4096, 11008, 4, 128) == (256 + 2 * 16384 + 4096 // 8 * 11008 * 4
+                                                                  + 8192 + 256)
+    assert g.act_order_workspace_size(3, 96, 32, 8, 32) == 256 + 2 * 512 + 24 * 32 * 4 + 768 + 256
+    assert g.act_order_workspace_size(4, 512, 128, 2, 16) == 0      # groups of 16 rows at 2 bits (not whole k-tiles)
+    assert g.act_order_workspace_size(4, 1024, 128, 3, 64) == 0     # 3-bit groups must be multiples of 128
+    assert g.act_order_workspace_size(4, 4096, 128, 4, 1) == 0      # 4096 groups: the sort's 520 KB
+    assert g.act_order_workspace_size(4, 131072, 128, 4, 128) == 0  # a 4-column strip of 256 KB
+    assert g.act_order_workspace_size(0, 512, 128, 4, 64) == 0
+    assert g.act_order_workspace_size(4, 500, 128, 4, 64) == 0      # group does not divide K
 
 
 def test_gemm_perm_workspace_size(lib):
