@@ -708,13 +708,38 @@ def run_reference(args):
 
 def run_profile_target(args):
     """--profile WORKLOAD:M[:PATH]: just `warmup + steps` eager launches of one call on one
-    workload (PATH gemm, rows, perm, il or dequant), for a profiler to capture; prints one short
-    line."""
+    workload (PATH gemm, rows, perm, il or dequant; a mixture-of-experts workload with M tokens
+    runs gptq_gemm_grouped), for a profiler to capture; prints one short line."""
     import torch
     import gptq_bit_weight_gemm_gb300 as g
     from gptq_bit_weight_gemm_gb300 import build as lib_build
     lib_build.build()
     parts = args.profile.split(":")
+    if parts[0] in gptq_inputs.MOE_WORKLOADS:
+        mw, T = gptq_inputs.MOE_WORKLOADS[parts[0]], int(parts[1])
+        dev = torch.device("cuda", 0)
+        stream = torch.cuda.Stream()
+        r = gptq_inputs.draw_routing(mw, T)
+        toks = gptq_inputs.draw_token_activations(mw, T)
+        A = toks[torch.from_numpy(r.row_token).long()].contiguous().to(dev)
+        offsets = torch.from_numpy(r.offsets).to(dev)
+        max_m = int(np.diff(r.offsets).max())
+        qws, qzs, scs = [], [], []
+        for e in range(mw.E):
+            W = torch.from_numpy(gptq_inputs.draw_expert_weights(mw, e)).to(dev)
+            qw, qz, sc = g.quantize_rtn(W, bits=mw.bits, group=mw.group, fmt=g.V2)
+            qws.append(qw); qzs.append(qz); scs.append(sc)
+            del W
+        qw, qz, sc = torch.stack(qws), torch.stack(qzs), torch.stack(scs)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup + args.steps):
+                g.gemm_grouped(A, offsets, qw, qz, sc, bits=mw.bits, group=mw.group, max_m=max_m, fmt=g.V2,
+                               stream=stream)
+        stream.synchronize()
+        assert g.device_status(stream) == 0
+        print(json.dumps({"profile": args.profile, "launches": args.warmup + args.steps}))
+        return
     wl, M = gptq_inputs.WORKLOADS[parts[0]], int(parts[1])
     path = parts[2] if len(parts) > 2 else "gemm"
     dev = torch.device("cuda", 0)
