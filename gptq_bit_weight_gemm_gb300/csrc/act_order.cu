@@ -42,7 +42,8 @@ __device__ __forceinline__ uint32_t code_source(int k) {
 // warp (hist[w][g], shared-memory atomics), pass 2 turns the counts into each warp's first slot
 // inside each group (one warp per group, a shuffle scan over the 32 warps' counts) and checks that
 // every group holds `group` rows, pass 3 walks the warp's rows in order, 32 at a time: equal keys
-// among the 32 are matched (their order is the lane order), and the lowest lane of each key takes
+// among the 32 are found with one warp ballot per key bit (their order is the lane order; a
+// ballot per bit measured faster than match.any here), and the lowest lane of each key takes
 // the key's next slots with one atomic add that returns the slot before it.  A warp's atomics
 // execute in its program order, so slots follow the row order; batches of eight such steps issue
 // their atomics back to back.  Ties keep their row order, so the result is the one ordering the
@@ -54,9 +55,13 @@ __device__ __forceinline__ uint32_t code_source(int k) {
 template <int BITS>
 __global__ void __launch_bounds__(kSortThreads) k_sort_groups(const int32_t* __restrict__ g_idx, int K, int G,
                                                               int group, int32_t* __restrict__ perm,
-                                                              uint32_t* __restrict__ src, int* __restrict__ flag) {
-  extern __shared__ uint32_t hist[];   // [32][G], then the keys [K] (16-bit)
-  uint16_t* keys = reinterpret_cast<uint16_t*>(hist + 32 * G);
+                                                              uint32_t* __restrict__ src, int* __restrict__ flag,
+                                                              int staged) {
+  // [32][G] counts; then, when `staged`, perm and src of all K rows; then the keys [K] (16-bit)
+  extern __shared__ uint32_t hist[];
+  int32_t* sperm = reinterpret_cast<int32_t*>(hist + 32 * G);
+  uint32_t* ssrc = hist + 32 * G + (staged ? K : 0);
+  uint16_t* keys = reinterpret_cast<uint16_t*>(hist + 32 * G + (staged ? 2 * K : 0));
   __shared__ int bad;
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -108,6 +113,7 @@ __global__ void __launch_bounds__(kSortThreads) k_sort_groups(const int32_t* __r
     return;
   }
   constexpr int kSteps = 8;
+  const int nbits = 32 - __clz(G + 31);        // keys below G + 32
   for (int k0 = k_lo; k0 < k_hi; k0 += 32 * kSteps) {
     int g[kSteps];
     unsigned peers[kSteps];
@@ -115,27 +121,49 @@ __global__ void __launch_bounds__(kSortThreads) k_sort_groups(const int32_t* __r
 #pragma unroll
     for (int i = 0; i < kSteps; ++i) {
       const int k = k0 + 32 * i + lane;
-      g[i] = k < k_hi ? static_cast<int>(keys[k]) : -1 - lane;
+      g[i] = k < k_hi ? static_cast<int>(keys[k]) : G + lane;   // lanes past the chunk: unique keys
+      peers[i] = 0xFFFFFFFFu;
     }
+    // lanes with equal keys: one ballot per key bit (eight independent steps side by side)
+    for (int b = 0; b < nbits; ++b) {
 #pragma unroll
-    for (int i = 0; i < kSteps; ++i) peers[i] = __match_any_sync(0xFFFFFFFFu, g[i]);
+      for (int i = 0; i < kSteps; ++i) {
+        const bool v = (g[i] >> b) & 1;
+        const unsigned bal = __ballot_sync(0xFFFFFFFFu, v);
+        peers[i] &= v ? bal : ~bal;
+      }
+    }
 #pragma unroll
     for (int i = 0; i < kSteps; ++i) {
       old[i] = 0u;
-      if (g[i] >= 0 && lane == __ffs(peers[i]) - 1) old[i] = atomicAdd(&h[g[i]], static_cast<uint32_t>(__popc(peers[i])));
+      if (g[i] < G && lane == __ffs(peers[i]) - 1) old[i] = atomicAdd(&h[g[i]], static_cast<uint32_t>(__popc(peers[i])));
     }
 #pragma unroll
     for (int i = 0; i < kSteps; ++i) {
       const uint32_t slot = __shfl_sync(0xFFFFFFFFu, old[i], __ffs(peers[i]) - 1);
-      if (g[i] >= 0) {
+      if (g[i] < G) {
         const int k = k0 + 32 * i + lane;
         const int dst = g[i] * group + static_cast<int>(slot) + __popc(peers[i] & ((1u << lane) - 1u));
-        perm[dst] = k;
-        src[dst] = code_source<BITS>(k);
+        if (staged) {
+          sperm[dst] = k;
+          ssrc[dst] = code_source<BITS>(k);
+        } else {
+          perm[dst] = k;
+          src[dst] = code_source<BITS>(k);
+        }
       }
     }
   }
   __syncthreads();
+  if (staged) {
+    // scattered stores stay in shared memory; global memory gets 16-byte coalesced ones (one SM
+    // issuing K scattered 4-byte global stores took most of the kernel's time)
+    for (int i = threadIdx.x; i < K / 4; i += kSortThreads) {
+      reinterpret_cast<int4*>(perm)[i] = reinterpret_cast<const int4*>(sperm)[i];
+      reinterpret_cast<uint4*>(src)[i] = reinterpret_cast<const uint4*>(ssrc)[i];
+    }
+    __syncthreads();
+  }
   if (threadIdx.x == 0) *flag = 1;
 }
 
@@ -250,16 +278,20 @@ cudaError_t allow_smem(F kern, std::atomic<unsigned long long>& done) {
 
 size_t sort_groups_smem(int K, int G) { return static_cast<size_t>(G) * 32 * 4 + static_cast<size_t>(K) * 2; }
 
+// With room for the whole row order and code table as well, the sort places rows in shared memory.
+bool sort_groups_staged(int K, int G) { return sort_groups_smem(K, G) + static_cast<size_t>(K) * 8 <= kMaxActOrderSmem; }
+
 size_t repack_smem(int K, int bits, int sw) { return (static_cast<size_t>(K) * bits / 32 + 1) * sw * 4; }
 
 template <int BITS>
 cudaError_t launch_sort_bits(const int32_t* g_idx, int K, int G, int group, int32_t* perm, uint32_t* src,
                              int* flag, cudaStream_t stream) {
   static std::atomic<unsigned long long> smem_set{0};
-  const size_t smem = sort_groups_smem(K, G);
+  const int staged = sort_groups_staged(K, G) ? 1 : 0;
+  const size_t smem = sort_groups_smem(K, G) + (staged ? static_cast<size_t>(K) * 8 : 0);
   cudaError_t e = allow_smem(k_sort_groups<BITS>, smem_set);
   if (e != cudaSuccess) return e;
-  k_sort_groups<BITS><<<1, kSortThreads, smem, stream>>>(g_idx, K, G, group, perm, src, flag);
+  k_sort_groups<BITS><<<1, kSortThreads, smem, stream>>>(g_idx, K, G, group, perm, src, flag, staged);
   return cudaGetLastError();
 }
 
