@@ -67,7 +67,9 @@ struct Geo {
   // barriers: full[S], empty[S], bfull[BS], bempty[BS], acc_full, acc_empty, drain
   static constexpr uint32_t kNumBars = 2 * kStages + 2 * Geo::kBStages + 3;
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag
-  static constexpr uint32_t kBytes = kOffMisc + 16;
+  // epilogue staging: per epilogue warp 32 rows x 64 bytes (one 32-column chunk of its rows)
+  static constexpr uint32_t kOffEpi = (kOffMisc + 16 + 127) & ~127u;
+  static constexpr uint32_t kBytes = kOffEpi + kEpiWarps * 32 * 64;
   static constexpr size_t kDynSmem = kBytes + 1024;             // slack to align the base
 };
 
@@ -538,9 +540,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ---------------------------------------------------------------- epilogue (warps 0-3)
+    // Each chunk (32 rows x 32 columns) goes TMEM -> registers (lane = row) -> shared memory ->
+    // global: the staging turns 32 rows' 16-byte pieces per store instruction into 8 rows' 64-byte
+    // segments.  Chunk v of row r sits at slot v ^ ((r >> 1) & 3), so that both the row-wise
+    // writes and the segment-wise reads are free of bank conflicts.
     const int q = warp;   // TMEM lanes 32q .. 32q + 31
     uint32_t aph = 0;
     TOUT* C = static_cast<TOUT*>(a.C);
+    uint4* stage = reinterpret_cast<uint4*>(smem + Gm::kOffEpi) + q * 128;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
       const int mt = t % num_m, nt = t / num_m;
       if (!wait_bar(sy, acc_full, aph)) break;
@@ -555,18 +562,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + half * 256 + cc * 32, r);
           ptx::tmem_ld_wait();
           const int n0 = nt * kBN + cc * 32;
-          if (m < a.M && n0 < a.N) {
-            uint4* dst = reinterpret_cast<uint4*>(C + static_cast<long long>(m) * a.N + n0);
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              uint4 o;
-              o.x = pack2(__uint_as_float(r[8 * v + 0]) * rs, __uint_as_float(r[8 * v + 1]) * rs, TOUT());
-              o.y = pack2(__uint_as_float(r[8 * v + 2]) * rs, __uint_as_float(r[8 * v + 3]) * rs, TOUT());
-              o.z = pack2(__uint_as_float(r[8 * v + 4]) * rs, __uint_as_float(r[8 * v + 5]) * rs, TOUT());
-              o.w = pack2(__uint_as_float(r[8 * v + 6]) * rs, __uint_as_float(r[8 * v + 7]) * rs, TOUT());
-              dst[v] = o;
+          for (int v = 0; v < 4; ++v) {
+            uint4 o;
+            o.x = pack2(__uint_as_float(r[8 * v + 0]) * rs, __uint_as_float(r[8 * v + 1]) * rs, TOUT());
+            o.y = pack2(__uint_as_float(r[8 * v + 2]) * rs, __uint_as_float(r[8 * v + 3]) * rs, TOUT());
+            o.z = pack2(__uint_as_float(r[8 * v + 4]) * rs, __uint_as_float(r[8 * v + 5]) * rs, TOUT());
+            o.w = pack2(__uint_as_float(r[8 * v + 6]) * rs, __uint_as_float(r[8 * v + 7]) * rs, TOUT());
+            stage[lane * 4 + (v ^ ((lane >> 1) & 3))] = o;
+          }
+          __syncwarp();
+          if (n0 < a.N) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int row = 8 * j + (lane >> 2), sg = lane & 3;
+              const int mr = mt * kBM + half * 128 + q * 32 + row;
+              const uint4 val = stage[row * 4 + (sg ^ ((row >> 1) & 3))];
+              if (mr < a.M) *reinterpret_cast<uint4*>(C + static_cast<long long>(mr) * a.N + n0 + 8 * sg) = val;
             }
           }
+          __syncwarp();
         }
       }
       ptx::tc_fence_before();
@@ -620,6 +635,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 template <int BITS, typename TOUT, bool PERK>
 cudaError_t launch_typed(const Problem& p, const void* A16, const float* row_scale, cudaStream_t stream) {
   using Gm = Geo<BITS>;
+  static_assert(Gm::kDynSmem <= 232448, "the layout must fit one CTA's shared memory (227 KB)");
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   CUtensorMap tmA, tmW;
