@@ -180,9 +180,41 @@ struct ColConsts {
     s = sc;
     z = zero;
     s2 = static_cast<uint32_t>(sbits) | (static_cast<uint32_t>(sbits) << 16);
-    if constexpr (BITS != 3) DiffPairs<__half, BITS>::consts(zero, kz);
+    DiffPairs<__half, BITS>::consts(zero, kz);
   }
 };
+
+// 3-bit: the pair (of DiffPairs<__half, 3>) holding code k of a unit, and which half of it.
+__host__ __device__ constexpr int pair_of_k3(int k) {
+  for (int p = 0; p < 16; ++p)
+    if (code3_pair(p, 0) == k || code3_pair(p, 1) == k) return p;
+  return 0;
+}
+__host__ __device__ constexpr int half_of_k3(int k) {
+  for (int p = 0; p < 16; ++p)
+    if (code3_pair(p, 1) == k) return 1;
+  return 0;
+}
+
+// One 3-bit unit (32 consecutive k of one column, words w0..w2) as four 16-byte chunks of
+// RN((q - z) s): the exact (q - z) pairs of DiffPairs (its own pairing of the 32 codes), one HMUL2
+// per pair, then each output word (k = 2i, 2i + 1) gathered from its two pairs' halves by one
+// byte permute.
+__device__ __forceinline__ void dq_unit3(uint32_t w0, uint32_t w1, uint32_t w2, const ColConsts<3>& cc,
+                                         uint4 (&out)[4]) {
+  uint32_t d[16];
+  DiffPairs<__half, 3>::run3(w0, w1, w2, cc.kz, d);
+#pragma unroll
+  for (int p = 0; p < 16; ++p) d[p] = hmul2(d[p], cc.s2);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int ka = 2 * i, kb = 2 * i + 1;
+    const uint32_t sel = static_cast<uint32_t>(2 * half_of_k3(ka)) | static_cast<uint32_t>(2 * half_of_k3(ka) + 1) << 4 |
+                         static_cast<uint32_t>(4 + 2 * half_of_k3(kb)) << 8 |
+                         static_cast<uint32_t>(5 + 2 * half_of_k3(kb)) << 12;
+    (&out[i >> 2].x)[i & 3] = __byte_perm(d[pair_of_k3(ka)], d[pair_of_k3(kb)], sel);
+  }
+}
 
 // One 16-byte chunk (8 consecutive k of one column) for 4-bit: word w.
 __device__ __forceinline__ uint4 dq_chunk4(uint32_t w, const ColConsts<4>& cc) {
@@ -416,6 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int dq = threadIdx.x - kDqWarp0 * 32;
     const int col = dq % kBN;
     const int hf = dq / kBN;
+    const bool group32 = a.group % 32 == 0;   // one group over each thread's 32 k of a k-step
     int s = 0, sb = 0;
     uint32_t ph = 0, phb = 0;
     bool ok = true;
@@ -495,6 +528,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
               *reinterpret_cast<uint4*>(bt + swz(col, 4 * hf + c)) = out;
             }
+          } else if (group32 && kst + 32 <= a.K) {
+            // 3-bit, the thread's unit inside one group: exact pairs, one rounding each
+            uint4 out[4] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u),
+                            make_uint4(0u, 0u, 0u, 0u)};
+            group_at(kst);
+            if (n_ok) dq_unit3(wl[0], wl[1], wl[2], cc, out);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4*>(bt + swz(col, 4 * hf + c)) = out[c];
           } else {
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
