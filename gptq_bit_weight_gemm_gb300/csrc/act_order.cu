@@ -244,22 +244,34 @@ __global__ void __launch_bounds__(256) k_repack_rows(const uint32_t* __restrict_
   }
 }
 
-// One element per thread-iteration, consecutive threads on consecutive k' of a row: the writes
-// and the perm reads coalesce; the reads of A are a gather (A is small and stays in L2).  The
-// kernel lets the dependent GEMM launch at once (its CTAs stream weights meanwhile) and waits
-// for its own predecessor before reading A.
+// Consecutive threads on consecutive 8-column pieces of a row: the writes and the perm reads
+// coalesce; the reads of A are a gather within the row (the row stays in L1/L2).  The kernel lets
+// the dependent GEMM launch at once (its CTAs stream weights meanwhile) and waits for its own
+// predecessor before reading A.
 __global__ void __launch_bounds__(256) k_gather_cols(const uint16_t* __restrict__ A,
                                                      const int32_t* __restrict__ perm, int M, int K,
                                                      uint16_t* __restrict__ out) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const long long total = static_cast<long long>(M) * K;
+  // eight consecutive k' per thread-iteration: two 16-byte reads of perm, eight 2-byte gathers
+  // from the row, one 16-byte store (K is a multiple of 32; perm and out are 16-byte aligned)
+  const int k8 = K / 8;
+  const long long total = static_cast<long long>(M) * k8;
   const long long step = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += step) {
-    const int m = static_cast<int>(i / K), k = static_cast<int>(i - static_cast<long long>(m) * K);
-    int src = __ldg(perm + k);
-    src = src < 0 ? 0 : (src >= K ? K - 1 : src);        // a bad entry never reads outside the row
-    out[i] = __ldg(A + static_cast<long long>(m) * K + src);
+    const int m = static_cast<int>(i / k8), k0 = static_cast<int>(i - static_cast<long long>(m) * k8) * 8;
+    const int4 p0 = __ldg(reinterpret_cast<const int4*>(perm + k0));
+    const int4 p1 = __ldg(reinterpret_cast<const int4*>(perm + k0 + 4));
+    const int src[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+    const uint16_t* row = A + static_cast<long long>(m) * K;
+    uint32_t h[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int sk = src[j] < 0 ? 0 : (src[j] >= K ? K - 1 : src[j]);   // a bad entry never reads outside the row
+      h[j] = __ldg(row + sk);
+    }
+    reinterpret_cast<uint4*>(out)[i] = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16),
+                                                  h[6] | (h[7] << 16));
   }
 }
 
@@ -356,7 +368,7 @@ cudaError_t launch_repack_rows(const int32_t* qweight, const uint32_t* src, cons
 
 cudaError_t launch_gather_cols(const void* A, const int32_t* perm, int M, int K, void* out,
                                cudaStream_t stream) {
-  const long long total = static_cast<long long>(M) * K;
+  const long long total = static_cast<long long>(M) * (K / 8);   // 8-column pieces
   long long blocks = (total + 255) / 256;
   const long long cap = static_cast<long long>(device_info().sm_count) * 8;
   if (blocks > cap) blocks = cap;
