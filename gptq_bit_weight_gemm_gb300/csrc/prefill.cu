@@ -200,12 +200,18 @@ __host__ __device__ constexpr int half_of_k3(int k) {
 // RN((q - z) s): the exact (q - z) pairs of DiffPairs (its own pairing of the 32 codes), one HMUL2
 // per pair, then each output word (k = 2i, 2i + 1) gathered from its two pairs' halves by one
 // byte permute.
+template <bool PERMA>
 __device__ __forceinline__ void dq_unit3(uint32_t w0, uint32_t w1, uint32_t w2, const ColConsts<3>& cc,
                                          uint4 (&out)[4]) {
   uint32_t d[16];
   DiffPairs<__half, 3>::run3(w0, w1, w2, cc.kz, d);
 #pragma unroll
   for (int p = 0; p < 16; ++p) d[p] = hmul2(d[p], cc.s2);
+  if constexpr (PERMA) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) out[c] = make_uint4(d[4 * c], d[4 * c + 1], d[4 * c + 2], d[4 * c + 3]);
+    return;
+  }
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const int ka = 2 * i, kb = 2 * i + 1;
@@ -216,22 +222,53 @@ __device__ __forceinline__ void dq_unit3(uint32_t w0, uint32_t w1, uint32_t w2, 
   }
 }
 
+// The k order of the dequantized pairs.  Each width's exact-pair unpack yields (q - z) pairs whose
+// two k are not adjacent; writing them to the B tile in natural k order costs one byte permute per
+// word.  With bf16 activations the fp16 copy of A is written anyway (k_rows_to_f16), so it can take
+// the pairs' order instead: inside each block of `span` k, position j of the tile (and of the copy
+// of A) holds k = a_src<BITS>(j).  The contraction does not depend on the order of k, only on A
+// and B agreeing.  BITS 0: natural order.
+template <int BITS>
+__host__ __device__ constexpr int a_span() { return BITS == 3 ? 32 : BITS == 2 ? 16 : 8; }
+template <int BITS>
+__host__ __device__ constexpr int a_src(int j) {
+  if constexpr (BITS == 4) {
+    return (j & ~7) + ((j & 7) >> 1) + 4 * (j & 1);      // pairs (p, p + 4)
+  } else if constexpr (BITS == 2) {
+    return (j & ~15) + ((j & 15) >> 1) + 8 * (j & 1);    // pairs (p, p + 8)
+  } else if constexpr (BITS == 8) {
+    return (j & ~3) + ((j & 3) == 1 ? 2 : (j & 3) == 2 ? 1 : (j & 3));   // pairs (0, 2), (1, 3)
+  } else if constexpr (BITS == 3) {
+    return (j & 1) ? code3_pair(j >> 1, 1) : code3_pair(j >> 1, 0);
+  } else {
+    return j;
+  }
+}
+
 // One 16-byte chunk (8 consecutive k of one column) for 4-bit: word w.
+template <bool PERMA>
 __device__ __forceinline__ uint4 dq_chunk4(uint32_t w, const ColConsts<4>& cc) {
   uint32_t d[4], e[4];
   DiffPairs<__half, 4>::run(w, cc.kz, d);                // d[p] = (k p, k p+4) - z, exact
 #pragma unroll
   for (int p = 0; p < 4; ++p) e[p] = hmul2(d[p], cc.s2); // one rounding: RN((q - z) s)
+  if constexpr (PERMA) return make_uint4(e[0], e[1], e[2], e[3]);
   return make_uint4(__byte_perm(e[0], e[1], 0x5410), __byte_perm(e[2], e[3], 0x5410),
                     __byte_perm(e[0], e[1], 0x7632), __byte_perm(e[2], e[3], 0x7632));
 }
 
 // Two chunks (16 consecutive k of one column) for 2-bit: word w.
+template <bool PERMA>
 __device__ __forceinline__ void dq_chunks2(uint32_t w, const ColConsts<2>& cc, uint4& lo, uint4& hi) {
   uint32_t d[8], e[8];
   DiffPairs<__half, 2>::run(w, cc.kz, d);                // d[p] = (k p, k p+8) - z
 #pragma unroll
   for (int p = 0; p < 8; ++p) e[p] = hmul2(d[p], cc.s2);
+  if constexpr (PERMA) {
+    lo = make_uint4(e[0], e[1], e[2], e[3]);
+    hi = make_uint4(e[4], e[5], e[6], e[7]);
+    return;
+  }
   lo = make_uint4(__byte_perm(e[0], e[1], 0x5410), __byte_perm(e[2], e[3], 0x5410),
                   __byte_perm(e[4], e[5], 0x5410), __byte_perm(e[6], e[7], 0x5410));
   hi = make_uint4(__byte_perm(e[0], e[1], 0x7632), __byte_perm(e[2], e[3], 0x7632),
@@ -239,12 +276,14 @@ __device__ __forceinline__ void dq_chunks2(uint32_t w, const ColConsts<2>& cc, u
 }
 
 // One chunk for 8-bit: words w0 (k 0..3) and w1 (k 4..7).
+template <bool PERMA>
 __device__ __forceinline__ uint4 dq_chunk8(uint32_t w0, uint32_t w1, const ColConsts<8>& cc) {
   uint32_t d0[2], d1[2];
   DiffPairs<__half, 8>::run(w0, cc.kz, d0);              // (k0, k2), (k1, k3) - z
   DiffPairs<__half, 8>::run(w1, cc.kz, d1);
   const uint32_t a0 = hmul2(d0[0], cc.s2), a1 = hmul2(d0[1], cc.s2);
   const uint32_t b0 = hmul2(d1[0], cc.s2), b1 = hmul2(d1[1], cc.s2);
+  if constexpr (PERMA) return make_uint4(a0, a1, b0, b1);
   return make_uint4(__byte_perm(a0, a1, 0x5410), __byte_perm(a0, a1, 0x7632),
                     __byte_perm(b0, b1, 0x5410), __byte_perm(b0, b1, 0x7632));
 }
@@ -255,7 +294,9 @@ __device__ __forceinline__ uint4 dq_chunk8(uint32_t w0, uint32_t w1, const ColCo
 // fp16's normal range; values more than 2^29 below the row's largest round (their products are far
 // below the GEMM's absolute tolerance).  One CTA per row at a time, 16-byte loads and stores.  With
 // perm (act-order rows sorted by group) the output column k takes A[m][perm[k]] (the row maximum
-// does not depend on the order).  run_flag as in Args.
+// does not depend on the order); with PB (a width) the columns of each block of a_span<PB>() are
+// written in the order a_src<PB> of that width's dequantized pairs.  run_flag as in Args.
+template <int PB>
 __global__ void __launch_bounds__(256) k_rows_to_f16(const uint16_t* __restrict__ A, int M, int K,
                                                      const int32_t* __restrict__ perm,
                                                      const int* run_flag, int run_when,
@@ -284,36 +325,49 @@ __global__ void __launch_bounds__(256) k_rows_to_f16(const uint16_t* __restrict_
     int e = mx ? static_cast<int>(mx >> 7) - 127 - 15 : 0;   // exponent field of max|a|, minus 15
     e = e < -126 ? -126 : (e > 126 ? 126 : e);               // 2^e and 2^-e stay normal floats
     const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
-    for (int i = threadIdx.x; i < nv; i += blockDim.x) {
-      uint4 v;
+    constexpr int kSpan = PB == 0 ? 8 : a_span<PB>();      // columns per block
+    constexpr int kV = kSpan / 8;                           // 16-byte pieces per block
+    for (int b = threadIdx.x; b < K / kSpan; b += blockDim.x) {
+      uint32_t h[kSpan];                                    // the block's bf16 values, in k order
       if (perm == nullptr) {
-        v = __ldg(row + i);
+#pragma unroll
+        for (int v = 0; v < kV; ++v) {
+          const uint4 x = __ldg(row + b * kV + v);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            h[8 * v + 2 * j] = (&x.x)[j] & 0xFFFFu;
+            h[8 * v + 2 * j + 1] = (&x.x)[j] >> 16;
+          }
+        }
       } else {
         const uint16_t* r16 = A + static_cast<long long>(m) * K;
-        uint32_t h[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          int src = __ldg(perm + 8 * i + j);
+        for (int j = 0; j < kSpan; ++j) {
+          int src = __ldg(perm + b * kSpan + j);
           src = src < 0 ? 0 : (src >= K ? K - 1 : src);   // a bad entry never reads outside the row
           h[j] = __ldg(r16 + src);
         }
-        v = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
       }
-      uint4 o;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint32_t x = (&v.x)[j];
-        (&o.x)[j] = pack2(__uint_as_float(x << 16) * inv, __uint_as_float(x & 0xFFFF0000u) * inv, __half());
+      for (int v = 0; v < kV; ++v) {
+        uint4 o;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int j0 = 8 * v + 2 * j;
+          const uint32_t lo = h[PB == 0 ? j0 : a_src<PB>(j0)], hi = h[PB == 0 ? j0 + 1 : a_src<PB>(j0 + 1)];
+          (&o.x)[j] = pack2(__uint_as_float(lo << 16) * inv, __uint_as_float(hi << 16) * inv, __half());
+        }
+        orow[b * kV + v] = o;
       }
-      orow[i] = o;
     }
     if (threadIdx.x == 0) row_scale[m] = __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
     __syncthreads();                                       // warp_max is reused by the next row
   }
 }
 
-// TOUT: the output (and activation) type; the multiply is fp16 x fp16 for both.
-template <int BITS, typename TOUT, bool PERK>
+// TOUT: the output (and activation) type; the multiply is fp16 x fp16 for both.  PERMA: the fp16
+// copy of A is in the pairs' k order (a_src), and so are the B tiles.
+template <int BITS, typename TOUT, bool PERK, bool PERMA>
 __global__ void __launch_bounds__(kThreads, 1)
     k_prefill(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
               const Args a) {
@@ -501,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               uint4 out = make_uint4(0u, 0u, 0u, 0u);
               if (k0 < a.K) {
                 group_at(k0);
-                if (n_ok) out = dq_chunk4(wl[c], cc);
+                if (n_ok) out = dq_chunk4<PERMA>(wl[c], cc);
               }
               *reinterpret_cast<uint4*>(bt + swz(col, 4 * hf + c)) = out;
             }
@@ -512,7 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
               if (k0 < a.K) {
                 group_at(k0);
-                if (n_ok) dq_chunks2(wl[i], cc, lo, hi);
+                if (n_ok) dq_chunks2<PERMA>(wl[i], cc, lo, hi);
               }
               *reinterpret_cast<uint4*>(bt + swz(col, 4 * hf + 2 * i)) = lo;
               *reinterpret_cast<uint4*>(bt + swz(col, 4 * hf + 2 * i + 1)) = hi;
@@ -524,7 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               uint4 out = make_uint4(0u, 0u, 0u, 0u);
               if (k0 < a.K) {
                 group_at(k0);
-                if (n_ok) out = dq_chunk8(wl[2 * c], wl[2 * c + 1], cc);
+                if (n_ok) out = dq_chunk8<PERMA>(wl[2 * c], wl[2 * c + 1], cc);
               }
               *reinterpret_cast<uint4*>(bt + swz(col, 4 * hf + c)) = out;
             }
@@ -533,7 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint4 out[4] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u),
                             make_uint4(0u, 0u, 0u, 0u)};
             group_at(kst);
-            if (n_ok) dq_unit3(wl[0], wl[1], wl[2], cc, out);
+            if (n_ok) dq_unit3<PERMA>(wl[0], wl[1], wl[2], cc, out);
 #pragma unroll
             for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4*>(bt + swz(col, 4 * hf + c)) = out[c];
           } else {
@@ -544,9 +598,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (k0 < a.K) {
                 group_at(k0);
                 if (n_ok) {
+                  // (with PERMA the launcher takes this path only for halves past K: a 3-bit
+                  // PERMA launch has groups of whole 32-k units)
                   float v[8];
 #pragma unroll
-                  for (int j = 0; j < 8; ++j) v[j] = diff_f32(local_code<BITS>(wl, c, j), cc.z) * cc.s;
+                  for (int j = 0; j < 8; ++j) {
+                    const int sk = PERMA ? a_src<BITS>(8 * c + j) : 8 * c + j;
+                    v[j] = diff_f32(local_code<BITS>(wl, sk >> 3, sk & 7), cc.z) * cc.s;
+                  }
                   out = make_uint4(pack2(v[0], v[1], __half()), pack2(v[2], v[3], __half()),
                                    pack2(v[4], v[5], __half()), pack2(v[6], v[7], __half()));
                 }
@@ -563,9 +622,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               float v[8];
 #pragma unroll
               for (int j = 0; j < 8; ++j) {
-                const int g = clamp_group<BITS>(a, k0 + j);
+                const int sk = PERMA ? a_src<BITS>(8 * c + j) : 8 * c + j;   // k - kst
+                const int g = clamp_group<BITS>(a, kst + sk);
                 const float sj = __half2float(a.scales[static_cast<long long>(g) * a.N + n]);
-                v[j] = diff_f32(local_code<BITS>(wl, c, j), zero_of<BITS>(a, g, n)) * sj;
+                v[j] = diff_f32(local_code<BITS>(wl, sk >> 3, sk & 7), zero_of<BITS>(a, g, n)) * sj;
               }
               out = make_uint4(pack2(v[0], v[1], __half()), pack2(v[2], v[3], __half()),
                                pack2(v[4], v[5], __half()), pack2(v[6], v[7], __half()));
@@ -673,7 +733,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-template <int BITS, typename TOUT, bool PERK>
+template <int BITS, typename TOUT, bool PERK, bool PERMA>
 cudaError_t launch_typed(const Problem& p, const void* A16, const float* row_scale, cudaStream_t stream) {
   using Gm = Geo<BITS>;
   static_assert(Gm::kDynSmem <= 232448, "the layout must fit one CTA's shared memory (227 KB)");
@@ -712,7 +772,7 @@ cudaError_t launch_typed(const Problem& p, const void* A16, const float* row_sca
   a.status = p.status;
   a.run_flag = p.run_flag;
   a.run_when = p.run_when;
-  auto kern = k_prefill<BITS, TOUT, PERK>;
+  auto kern = k_prefill<BITS, TOUT, PERK, PERMA>;
   static bool attr_set = false;   // per instantiation; the attribute is per function
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -726,17 +786,28 @@ cudaError_t launch_typed(const Problem& p, const void* A16, const float* row_sca
   return cudaGetLastError();
 }
 
-template <int BITS, typename TOUT>
+// fast path: one group per unpacked word (2-bit words hold 16 k) and per 8-k chunk
+template <int BITS>
+bool per_k_groups(const Problem& p) {
+  return p.g_idx != nullptr || (p.group % (BITS == 2 ? 16 : 8)) != 0;
+}
+
+// A in the pairs' k order: possible when the copy of A is written here (bf16), and for 3-bit (whose
+// order spans a 32-k unit) when each unit lies in one group or the groups are looked up per k.
+template <int BITS>
+bool pairs_order(const Problem& p) {
+  return p.dtype == 1 && (BITS != 3 || per_k_groups<BITS>(p) || p.group % 32 == 0);
+}
+
+template <int BITS, typename TOUT, bool PERMA>
 cudaError_t launch_t(const Problem& p, const void* A16, const float* row_scale, cudaStream_t stream) {
-  // fast path: one group per unpacked word (2-bit words hold 16 k) and per 8-k chunk
-  const bool perk = p.g_idx != nullptr || (p.group % (BITS == 2 ? 16 : 8)) != 0;
-  return perk ? launch_typed<BITS, TOUT, true>(p, A16, row_scale, stream)
-              : launch_typed<BITS, TOUT, false>(p, A16, row_scale, stream);
+  return per_k_groups<BITS>(p) ? launch_typed<BITS, TOUT, true, PERMA>(p, A16, row_scale, stream)
+                               : launch_typed<BITS, TOUT, false, PERMA>(p, A16, row_scale, stream);
 }
 
 template <int BITS>
 cudaError_t launch_bits(const Problem& p, cudaStream_t stream) {
-  if (p.dtype == 0 && p.perm == nullptr) return launch_t<BITS, __half>(p, p.A, nullptr, stream);
+  if (p.dtype == 0 && p.perm == nullptr) return launch_t<BITS, __half, false>(p, p.A, nullptr, stream);
   // bf16, or columns gathered through perm: the fp16 copy of A (and for bf16 the row scales) in
   // the caller's workspace
   const size_t a_bytes = (static_cast<size_t>(p.M) * p.K * 2 + 255) & ~static_cast<size_t>(255);
@@ -746,15 +817,21 @@ cudaError_t launch_bits(const Problem& p, cudaStream_t stream) {
   if (p.dtype == 0) {
     e = launch_gather_cols(p.A, p.perm, p.M, p.K, A16, stream);
     if (e != cudaSuccess) return e;
-    return launch_t<BITS, __half>(p, A16, nullptr, stream);
+    return launch_t<BITS, __half, false>(p, A16, nullptr, stream);
   }
   float* row_scale = reinterpret_cast<float*>(static_cast<unsigned char*>(p.workspace) + a_bytes);
   const int blocks = p.M < device_info().sm_count * 8 ? p.M : device_info().sm_count * 8;
-  k_rows_to_f16<<<blocks, 256, 0, stream>>>(static_cast<const uint16_t*>(p.A), p.M, p.K, p.perm,
-                                             p.run_flag, p.run_when, A16, row_scale);
+  const bool perma = pairs_order<BITS>(p);
+  if (perma)
+    k_rows_to_f16<BITS><<<blocks, 256, 0, stream>>>(static_cast<const uint16_t*>(p.A), p.M, p.K, p.perm,
+                                                     p.run_flag, p.run_when, A16, row_scale);
+  else
+    k_rows_to_f16<0><<<blocks, 256, 0, stream>>>(static_cast<const uint16_t*>(p.A), p.M, p.K, p.perm,
+                                                  p.run_flag, p.run_when, A16, row_scale);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  return launch_t<BITS, __nv_bfloat16>(p, A16, row_scale, stream);
+  return perma ? launch_t<BITS, __nv_bfloat16, true>(p, A16, row_scale, stream)
+               : launch_t<BITS, __nv_bfloat16, false>(p, A16, row_scale, stream);
 }
 
 }  // namespace prefill
