@@ -217,21 +217,39 @@ cudaError_t launch_mt(const Problem& p, cudaStream_t stream) {
   return launch_mma<BITS, MT, MX, T, false, GROUPED>(p, stream);
 }
 
+// Whether 17..32 tokens run as two 16-token blocks side by side (each CTA with the 16-token
+// kernel's registers and staging, the weights read twice) rather than one 32-token block.
+// Measured (CUDA-graph replay): faster on small matrices (2-bit [4096, 4096]: M=32 17.3 -> 14.5 us,
+// M=24 15.3 -> 14.4) and for 3-bit at exactly 32 tokens (act-order [5120, 13824] prepacked: 74.8 ->
+// 55.6 us); slower on large 4-bit ones (llama-7B [4096, 11008] M=32: 30.2 -> 34.5 us) and for
+// 3-bit at 20 tokens (44.3 -> 49.3 us).  Where the 32-token layout fits no CTA, the split is
+// tried before giving up.
+inline bool token_split_pays(const Problem& p) {
+  return static_cast<long long>(p.K) * p.N <= (1ll << 24) || (p.bits == 3 && p.M == 32);
+}
+
 // Every M <= 32 runs the tensor-core decode kernel (token blocks of 8; one token has an
 // instantiation of its own, where the token count is a compile-time constant): even at one token,
 // handing the multiply-accumulate to the tensor core leaves the SM with only the unpack to issue.
 template <int BITS, typename T>
 cudaError_t launch_tokens(const Problem& p, cudaStream_t stream) {
+  // 17..32 tokens as two 16-token blocks side by side (grid z), both reading the same weights
+  auto split = [&]() {
+    Problem q = p;
+    q.tok_split = 2;
+    return p.M == 32 ? launch_mt<BITS, 16, 16, T>(q, stream) : launch_mt<BITS, 16, 0, T>(q, stream);
+  };
+  if (p.M > 16 && token_split_pays(p)) return split();
   switch (p.M) {
     case 1: return launch_mt<BITS, 1, 1, T>(p, stream);
     case 8: return launch_mt<BITS, 8, 8, T>(p, stream);
     case 16: return launch_mt<BITS, 16, 16, T>(p, stream);
-    case 32: return launch_mt<BITS, 32, 32, T>(p, stream);
     default: break;
   }
   if (p.M <= 8) return launch_mt<BITS, 8, 0, T>(p, stream);
   if (p.M <= 16) return launch_mt<BITS, 16, 0, T>(p, stream);
-  return launch_mt<BITS, 32, 0, T>(p, stream);
+  const cudaError_t e = p.M == 32 ? launch_mt<BITS, 32, 32, T>(p, stream) : launch_mt<BITS, 32, 0, T>(p, stream);
+  return e == cudaErrorInvalidConfiguration ? split() : e;
 }
 
 template <int BITS>

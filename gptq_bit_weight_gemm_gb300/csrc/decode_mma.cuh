@@ -215,7 +215,9 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
     w_row0 = e * ga.units * ROWS;
   }
   const Args& a = GROUPED ? ga : args;
-  const int Mtok = MX > 0 ? MX : a.M;                 // tokens (compile-time when MX > 0)
+  // token split (one weight, grid z = token blocks of MT): this CTA's block of rows of A and C
+  const int tz = GROUPED ? 0 : static_cast<int>(blockIdx.z);
+  const int Mtok = MX > 0 ? MX : (GROUPED ? a.M : min(MT, a.M - tz * MT));   // tokens (compile-time when MX > 0)
   const int UW = unit_words(Mtok, NP);
   cluster_arrive_relaxed();
   cg::cluster_group cluster = cg::this_cluster();
@@ -434,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
   pdl_wait();
 
   // Stage activations: sB[u][m][p] = (a[m][k0 + lo_k(p)], a[m][k0 + hi_k(p)]), zero past K or M.
-  const uint16_t* A16 = static_cast<const uint16_t*>(a.A);
+  const uint16_t* A16 = static_cast<const uint16_t*>(a.A) + static_cast<long long>(tz) * MT * a.K;
   const int nunits = ntile * 4;
   stage_pairs<PER, NP>(A16, a.perm, Mtok, a.K, cu0, nunits, a.units,
                        [](int p) { return MP::lo_k(p); }, [](int p) { return MP::hi_k(p); },
@@ -811,7 +813,7 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
     }
   }
   cluster.sync();
-  T* C = static_cast<T*>(a.C);
+  T* C = static_cast<T*>(a.C) + static_cast<long long>(tz) * MT * a.N;
   for (int i = threadIdx.x; i < Mr * per_rank; i += kThreads) {
     const int m = i >> pr_shift, c = i - (m << pr_shift);
     const int n = n_base + rank * per_rank + c;
@@ -952,7 +954,10 @@ cudaError_t launch_mma(const Problem& p, cudaStream_t stream) {
   a.il_tiles = p.interleaved ? a.units / 4 : 0;
   a.run_flag = p.run_flag;
   a.run_when = p.run_when;
-  const int E = GROUPED ? p.E : 1;                     // weights side by side (grid z)
+  const int E = GROUPED ? p.E : 1;                     // weights side by side
+  const int Z = GROUPED ? p.E : (p.tok_split > 1 ? p.tok_split : 1);   // grid z: experts or token blocks
+  Problem pz = p;                                      // the geometry of one token block
+  if (!GROUPED && Z > 1) pz.M = MT;
   const int slabs = (p.N + kSlab - 1) / kSlab;
   const int sms = device_info().sm_count;
   auto kern = k_decode_mma<BITS, MT, MX, T, FOLD, GROUPED>;
@@ -964,7 +969,7 @@ cudaError_t launch_mma(const Problem& p, cudaStream_t stream) {
     regs = cudaFuncGetAttributes(&fa, kern) == cudaSuccess ? fa.numRegs : 0;
     regs_cache.store(regs, std::memory_order_relaxed);
   }
-  const GeoChoice choice = select_geometry<BITS>(p, FOLD, regs, sms, E);
+  const GeoChoice choice = select_geometry<BITS>(pz, FOLD, regs, sms, Z);
   if (!choice.fits) return cudaErrorInvalidConfiguration;
   const int cs = choice.cs;
   const TmaGeo geo = choice.geo;
@@ -985,7 +990,7 @@ cudaError_t launch_mma(const Problem& p, cudaStream_t stream) {
                            strides, box, estr, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
-  const size_t smem = TmaSmem<BITS>::bytes(geo, p.M);
+  const size_t smem = TmaSmem<BITS>::bytes(geo, pz.M);
   // once per device, FOLD only: the full shared-memory carveout (left to the driver, it may pick
   // a smaller one and fit fewer CTAs per SM than the one-wave budget above assumes).  The FULL
   // path keeps the driver's choice: it re-reads scales through L1, which the carveout would shrink.
@@ -1011,7 +1016,7 @@ cudaError_t launch_mma(const Problem& p, cudaStream_t stream) {
     }
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(cs, slabs, E);
+  cfg.gridDim = dim3(cs, slabs, Z);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;

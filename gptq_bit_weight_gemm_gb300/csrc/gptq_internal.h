@@ -42,6 +42,9 @@ struct Problem {
   // launch without programmatic dependent launch: the kernel starts once the previous kernel has
   // completed (needed when it reads weights that the previous kernels wrote)
   bool no_pdl;
+  // decode kernels: the tokens in blocks of the kernel's token tile, one block per grid z (0/1:
+  // one block), all reading the same weights
+  int tok_split;
 };
 
 struct DeviceInfo {

@@ -1,8 +1,10 @@
 """GPU parity for long K at many tokens, where the decode kernels' staged activations outgrow one
 CTA's shared memory at the usual K split: the launcher widens the split (up to 16-CTA clusters),
-and where even that does not fit, gptq_gemm runs the tensor-core kernel while the decode-only
-calls (gptq_gemm_perm, gptq_gemm_grouped) refuse the shape with GPTQ_ERR_SHAPE.  Shapes follow the
-down projections of 70B- and 405B-class models (K = 28672, 53248) on a narrow column slice."""
+runs 17..32 tokens as two 16-token blocks when one 32-token block fits no CTA, and where even that
+does not fit, gptq_gemm runs the tensor-core kernel while the decode-only calls (gptq_gemm_perm,
+gptq_gemm_grouped) refuse the shape with GPTQ_ERR_SHAPE.  Shapes follow the down projections of
+70B- and 405B-class models (K = 28672, 53248) on a narrow column slice, and K = 98304 for the
+refusal."""
 import numpy as np
 import pytest
 import torch
@@ -44,7 +46,7 @@ def _dev(ck):
     (16384, 4, 32),      # the usual 8-way split would need 248 KB per CTA: widened to 16
     (28672, 4, 128),     # 70B-class down projection
     (28672, 8, 128),
-    (53248, 2, 128),     # 405B-class: no split fits, the tensor-core kernel runs
+    (53248, 2, 128),     # 405B-class: two 16-token blocks at a 16-way split
 ])
 def test_gemm_long_k_many_tokens(K, bits, group):
     N, M = 256, 32
@@ -60,9 +62,10 @@ def test_gemm_long_k_many_tokens(K, bits, group):
 
 @pytest.mark.parametrize("sort_rows", [True, False], ids=["sorted", "per_row"])
 def test_gemm_long_k_act_order_on_the_tensor_core_fallback(sort_rows):
-    """K = 53248 at 32 tokens fits no decode layout, so gptq_gemm runs the tensor-core kernel; with
-    act-order it must match the oracle both on rows sorted by group on the device (4-column repack
-    strips) and with its per-k group lookup (g_idx)."""
+    """K = 53248 at 32 tokens fits no 32-token decode layout; the call runs two 16-token blocks or,
+    where those do not fit either, the tensor-core kernel.  With act-order it must match the oracle
+    both on rows sorted by group on the device (4-column repack strips) and with the per-row-group
+    kernels (g_idx)."""
     K, N, M, bits, group = 53248, 256, 32, 4, 128
     import dataclasses
     wl = dataclasses.replace(BASE.resized(K, N, (M,), name="long_k_act"), bits=bits, group=group,
@@ -80,8 +83,23 @@ def test_gemm_long_k_act_order_on_the_tensor_core_fallback(sort_rows):
     assert_gemm_close(C, Cref, B, "K=%d act-order" % K)
 
 
-def test_decode_only_calls_refuse_what_fits_no_cta():
+def test_gemm_perm_long_k_runs_as_two_token_blocks():
+    """K = 53248 at 32 tokens: one 32-token block fits no CTA, two 16-token blocks do; the
+    decode-only call runs them and matches the oracle."""
     K, N, M, bits, group = 53248, 256, 32, 2, 128
+    wl, ck = _checkpoint(K, N, bits, group)
+    A = gptq_inputs.draw_activations(wl, M)
+    qw, qz, sc = _dev(ck)
+    perm = torch.arange(K, dtype=torch.int32, device=DEV)
+    C = g.gemm_perm(A.to(DEV), perm, qw, qz, sc, bits=bits, group=group, fmt=g.V2)
+    torch.cuda.synchronize()
+    Cref, B = oracle.gemm(bits16(A), oracle.F16, ck["qweight"], ck["qzeros"], ck["scales"], None, N, bits,
+                          group, oracle.V2)
+    assert_gemm_close(C, Cref, B, "gemm_perm K=%d M=%d" % (K, M))
+
+
+def test_decode_only_calls_refuse_what_fits_no_cta():
+    K, N, M, bits, group = 98304, 256, 32, 2, 128
     wl, ck = _checkpoint(K, N, bits, group)
     A = gptq_inputs.draw_activations(wl, M).to(DEV)
     qw, qz, sc = _dev(ck)
