@@ -915,9 +915,13 @@ GeoChoice select_geometry(const Problem& p, bool fold, int regs, int sms, int E)
     return make_geo<BITS>(units, c, p.M, p.group, slabs * c * E, sms, max_per_sm, !fold, p.g_idx != nullptr,
                           p.G);
   };
-  // A 16-CTA cluster is used only when it gives one wave; otherwise (and for FULL) at most 8.
+  // A 16-CTA cluster is used only when it gives one wave; otherwise (and for FULL) at most 8, and
+  // at most 4 for several weights side by side (grouped experts), whose grids run many waves:
+  // fewer, larger CTAs measured faster there (8 experts x [4096, 14336] 4-bit: T=8 106 -> 82 us,
+  // T=1 26 -> 22 us).
   const int cs0 = choose_cluster(p, Pack<BITS>::kPerUnit);
-  int cs = cs0 < 8 ? cs0 : 8;
+  const int cs_cap = E > 1 ? 4 : 8;
+  int cs = cs0 < cs_cap ? cs0 : cs_cap;
   for (int c = cs0; fold && c >= 1; c /= 2) {
     const size_t bytes = (TmaSmem<BITS>::bytes(geo_for(c), p.M) + 1023) & ~static_cast<size_t>(1023);
     if (bytes > 227 * 1024) break;
