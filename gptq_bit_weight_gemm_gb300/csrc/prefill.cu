@@ -122,24 +122,6 @@ __device__ __forceinline__ int zero_of(const Args& a, int g, int n) {
   return static_cast<int>(v & Pack<BITS>::kMask) + a.zero_offset;
 }
 
-// The qzeros word(s) holding column n's field in row g (loads only; decoded by zero_from).
-template <int BITS>
-__device__ __forceinline__ uint2 zero_words(const Args& a, int g, int n) {
-  const int32_t* row = a.qzeros + static_cast<long long>(g) * a.zwords;
-  const int bit = BITS * n;
-  uint2 w;
-  w.x = static_cast<uint32_t>(__ldg(row + (bit >> 5)));
-  w.y = ((bit & 31) + BITS > 32) ? static_cast<uint32_t>(__ldg(row + (bit >> 5) + 1)) : 0u;
-  return w;
-}
-template <int BITS>
-__device__ __forceinline__ int zero_from(const Args& a, uint2 w, int n) {
-  const int bit = BITS * n;
-  uint32_t v = w.x >> (bit & 31);
-  if ((bit & 31) + BITS > 32) v |= w.y << (32 - (bit & 31));
-  return static_cast<int>(v & Pack<BITS>::kMask) + a.zero_offset;
-}
-
 template <int BITS>
 __device__ __forceinline__ int clamp_group(const Args& a, int k) {
   if (a.g_idx == nullptr) return k / a.group;
@@ -512,10 +494,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool n_ok = n < a.N;
       const int nc = n_ok ? n : a.N - 1;      // clamped column for scale/zero reads
       int gnext = 0;                          // first k of the next group (fast path)
-      int pf_g = -1;                          // group whose scale/zero are prefetched
+      int pf_g = -1;                          // group whose scale/zero are prefetched (starts at gnext)
       uint16_t pf_s = 0;
       uint2 pf_z = make_uint2(0u, 0u);
       ColConsts<BITS> cc;
+      // the column's scale and zero field in group 0; group g is g rows further
+      const __half* s_col = a.scales + nc;
+      const int zbit = BITS * nc;
+      const int32_t* z_col = a.qzeros + (zbit >> 5);
+      const int zsh = zbit & 31;
       for (int ks = 0; ks < ksteps; ++ks) {
         if (!wait_bar(sy, full(s), ph)) { ok = false; break; }
         uint32_t wl[kHalfRows];
@@ -531,21 +518,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           // One group per 16 k at least (fast-path condition), tracked without division.  The
           // next group's scale and zero word are prefetched into registers one group ahead so
           // that no global load sits on the dequant critical path.
+          auto load_group = [&](int g) {
+            pf_s = __half_as_ushort(__ldg(s_col + static_cast<long long>(g) * a.N));
+            const int32_t* zp = z_col + static_cast<long long>(g) * a.zwords;
+            pf_z.x = static_cast<uint32_t>(__ldg(zp));
+            if constexpr (BITS == 3) pf_z.y = zsh + 3 > 32 ? static_cast<uint32_t>(__ldg(zp + 1)) : 0u;
+          };
           auto group_at = [&](int k) {
             if (k >= gnext) {
-              if (pf_g < 0 || k >= (pf_g + 1) * a.group || k < pf_g * a.group) {
-                pf_g = k / a.group;                      // first group of the tile: load now
-                pf_s = __half_as_ushort(__ldg(a.scales + static_cast<long long>(pf_g) * a.N + nc));
-                pf_z = zero_words<BITS>(a, pf_g, nc);
+              int g = pf_g;                              // the prefetched group starts at gnext
+              if (g < 0 || k >= gnext + a.group) {       // first group of the tile: load now
+                g = k / a.group;
+                load_group(g);
               }
-              const int g = pf_g;
               gnext = (g + 1) * a.group;
-              cc.set(__half2float(__ushort_as_half(pf_s)), pf_s, zero_from<BITS>(a, pf_z, nc));
-              if (gnext < a.K) {                          // prefetch group g + 1
-                pf_g = g + 1;
-                pf_s = __half_as_ushort(__ldg(a.scales + static_cast<long long>(pf_g) * a.N + nc));
-                pf_z = zero_words<BITS>(a, pf_g, nc);
-              }
+              uint32_t zf = pf_z.x >> zsh;
+              if constexpr (BITS == 3) zf |= zsh + 3 > 32 ? pf_z.y << (32 - zsh) : 0u;
+              cc.set(__half2float(__ushort_as_half(pf_s)), pf_s,
+                     static_cast<int>(zf & Pack<BITS>::kMask) + a.zero_offset);
+              pf_g = gnext < a.K ? g + 1 : -1;           // prefetch group g + 1
+              if (pf_g >= 0) load_group(pf_g);
             }
           };
           if constexpr (BITS == 4) {
