@@ -4,7 +4,8 @@ tests/geometry_probe.cu is compiled against the library's headers (nvcc, host co
 the launcher's own geometry selection (select_geometry in decode_mma.cuh) for the cluster split
 and shared-memory layout of a sweep of problems: every width, K up to 53248,
 N with ragged slabs, 1 to 32 tokens, groups from 32 rows to one per column, the scale-folding and
-the per-weight dequant paths, act-order, and grouped launches of 8 experts.  Every layout must:
+the per-weight dequant paths, act-order, grouped launches of 8 experts, and two token blocks side
+by side (17..32 tokens as two 16-token blocks).  Every layout must:
   - fit one CTA's shared memory (227 KB),
   - keep TMA boxes within the hardware's 256 rows, in 1024-byte aligned slots of 32 columns,
   - cover the whole K range with its CTAs and every chunk of a CTA with buffers,
@@ -52,7 +53,7 @@ def _problems():
             for fold, gidx in ((True, False), (False, False), (False, True)):
                 if fold and not foldable:
                     continue
-                for E in (1, 8):
+                for E in (1, 2, 8):    # 2: two 16-token blocks side by side (the token split)
                     if gidx and E > 1:
                         continue
                     for regs in (64, 216):    # the decode kernels compile to 64 .. 214 registers
