@@ -231,10 +231,16 @@ __global__ void __launch_bounds__(256) k_repack_rows(const uint32_t* __restrict_
       const int ob = BITS * j;                             // a constant once unrolled
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
-        const uint32_t code = (BITS == 3 ? __funnelshift_r((&lo.x)[cc], (&hi.x)[cc], sh) : (&lo.x)[cc] >> sh) &
-                              P::kMask;
-        acc[cc][ob >> 5] |= code << (ob & 31);
-        if ((ob & 31) + BITS > 32) acc[cc][(ob >> 5) + 1] |= code >> (32 - (ob & 31));
+        if constexpr (BITS == 3) {
+          const uint32_t code = __funnelshift_r((&lo.x)[cc], (&hi.x)[cc], sh) & 7u;
+          acc[cc][ob >> 5] |= code << (ob & 31);
+          if ((ob & 31) + BITS > 32) acc[cc][(ob >> 5) + 1] |= code >> (32 - (ob & 31));
+        } else {
+          // a rotation by (sh - ob) mod 32 moves the code from bit sh to bit ob (2/4/8-bit codes
+          // never straddle a word), and one and-or places it: two instructions per code
+          const uint32_t w = (&lo.x)[cc];
+          acc[cc][0] |= __funnelshift_r(w, w, e - static_cast<uint32_t>(ob)) & (P::kMask << ob);
+        }
       }
     }
 #pragma unroll
