@@ -322,29 +322,30 @@ def run_ours(args, rank, world, local_rank):
     clocks = sampler.summary(tc0, t1)
     clocks["window"] = "timed region and the 1.2 s of the same graph replays before it"
 
-    # ---- end to end through the public API: A from pinned host memory, C read back
+    # ---- end to end through the public API: gptq_gemm_host with A in pinned host memory and C
+    # returned to pinned host memory (the copies, the GEMM and the wait inside the call)
     a_host = A.cpu().pin_memory()
     c_host = torch.empty((M, wl.N), dtype=A.dtype).pin_memory()
     n_e2e = max(1, min(args.steps, 2000))
+
+    # the arguments of each weight set's call marshalled once (g.HostGemm): a step is the C call
+    host_calls = [g.HostGemm(a_host, a, q, z, s, bits=wl.bits, group=wl.group, fmt=g.V2, C_dev=c,
+                             C_host=c_host, stream=stream) for (q, z, s, a, c) in sets]
+
+    def host_step(i):
+        host_calls[i % S]()
+
     with torch.cuda.stream(stream):
         for i in range(min(50, n_e2e)):
-            q, z, s, a, c = sets[i % S]
-            a.copy_(a_host, non_blocking=True)
-            launch(i)
-            c_host.copy_(c, non_blocking=True)
-            stream.synchronize()
+            host_step(i)
         barrier()
         te0 = time.perf_counter()
         for i in range(n_e2e):
-            q, z, s, a, c = sets[i % S]
-            a.copy_(a_host, non_blocking=True)
-            launch(i)
-            c_host.copy_(c, non_blocking=True)
-            stream.synchronize()
+            host_step(i)
         te1 = time.perf_counter()
     e2e_s = max_over_ranks(te1 - te0, dist, dev)
     e2e_value = whole_job_gbs(world, set_bytes, n_e2e, e2e_s)
-    del sets, main_graph, rem_graphs
+    del sets, host_calls, main_graph, rem_graphs
     torch.cuda.synchronize()
 
     # ---- the secondary figure (M = 4096 prefill) and the per-configuration section
@@ -390,8 +391,9 @@ def run_ours(args, rank, world, local_rank):
                                    "single launch: event pair around one launch, synchronized"},
         "e2e": {"value": round(e2e_value, 3), "unit": "GB/s", "h2d_bytes_per_step": M * wl.K * 2,
                 "d2h_bytes_per_step": M * wl.N * 2,
-                "note": "weights resident on the device (the model); per step: A host->device, "
-                        "gptq_gemm, C device->host, stream synchronize"},
+                "note": "weights resident on the device (the model); per step one gptq_gemm_host call "
+                        "(arguments marshalled once per weight set): "
+                        "A host->device, gptq_gemm, C device->host, stream synchronize"},
         "gpu_launches": args.steps,
         "clocks": clocks,
     }

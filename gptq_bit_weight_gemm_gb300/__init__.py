@@ -58,6 +58,7 @@ _P, _I, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
 _SIGNATURES = {
     "gptq_dequant": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
     "gptq_gemm": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P]),
+    "gptq_gemm_host": (_I, [_P, _P, _I, _I, _I, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _SZ, _P]),
     "gptq_gemm_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "gptq_gemm_act_order_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "gptq_repack_zeros_v1_to_v2": (_I, [_P, _P, _I, _I, _I]),
@@ -170,6 +171,50 @@ def gemm(A, qweight, qzeros, scales, g_idx=None, *, bits, group, fmt=V2, out=Non
                          N, bits, group, fmt, _ptr(out, A.dtype, "out"), ws_ptr, ws_len, _stream(stream))
     _check(rc, "gptq_gemm")
     return out
+
+
+class HostGemm:
+    """gptq_gemm_host with its arguments marshalled once, for a loop that reruns one problem on
+    the same host and device buffers (only the host buffers' contents change between calls):
+    calling the object copies A_host [M, K] (a CPU tensor, page-locked for asynchronous copies)
+    into A_dev, computes C = A @ dequant(W) into C_dev, copies it into C_host (a CPU tensor) and
+    returns C_host once it holds the result.  The staging buffers and the workspace belong to the
+    caller (as for gemm, a bf16 prefill needs workspace_size(...) bytes)."""
+
+    def __init__(self, A_host, A_dev, qweight, qzeros, scales, g_idx=None, *, bits, group, C_dev, C_host,
+                 fmt=V2, workspace=None, stream=None):
+        torch = _torch()
+        M, K = A_host.shape
+        N = qweight.shape[1]
+        for t, name in ((A_host, "A_host"), (C_host, "C_host")):
+            if t.is_cuda or not t.is_contiguous():
+                raise ValueError("%s must be a contiguous CPU tensor" % name)
+        if A_dev.dtype != A_host.dtype or C_dev.dtype != A_host.dtype or C_host.dtype != A_host.dtype:
+            raise TypeError("A_host, A_dev, C_dev and C_host must share A's dtype")
+        if A_dev.numel() < M * K or C_dev.numel() < M * N or C_host.numel() < M * N:
+            raise ValueError("staging buffers smaller than the problem")
+        ws_ptr = _ptr(workspace, name="workspace") if workspace is not None else None
+        ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
+        # the tensors stay referenced for as long as the object can be called
+        self._keep = (A_host, A_dev, qweight, qzeros, scales, g_idx, C_dev, C_host, workspace)
+        self._args = (ctypes.c_void_p(A_host.data_ptr()), _ptr(A_dev, name="A_dev"), M, K, _dtype_code(A_host),
+                      _ptr(qweight, torch.int32, "qweight"), _ptr(qzeros, torch.int32, "qzeros"),
+                      _ptr(scales, torch.float16, "scales"), _ptr(g_idx, torch.int32, "g_idx"), N, bits, group,
+                      fmt, _ptr(C_dev, name="C_dev"), ctypes.c_void_p(C_host.data_ptr()), ws_ptr, ws_len,
+                      _stream(stream))
+        self._fn = lib().gptq_gemm_host
+        self.C_host = C_host
+
+    def __call__(self):
+        _check(self._fn(*self._args), "gptq_gemm_host")
+        return self.C_host
+
+
+def gemm_host(A_host, A_dev, qweight, qzeros, scales, g_idx=None, *, bits, group, C_dev, C_host, fmt=V2,
+              workspace=None, stream=None):
+    """One gptq_gemm_host call (see HostGemm): returns C_host holding C = A @ dequant(W)."""
+    return HostGemm(A_host, A_dev, qweight, qzeros, scales, g_idx, bits=bits, group=group, C_dev=C_dev,
+                    C_host=C_host, fmt=fmt, workspace=workspace, stream=stream)()
 
 
 def dequant(qweight, qzeros, scales, g_idx=None, *, K, bits, group, fmt=V2, dtype=None, out=None,

@@ -323,6 +323,27 @@ extern "C" int gptq_gemm(const void* A, int M, int K, int a_dtype, const int32_t
   return gptq::from_cuda(gptq::launch_prefill(p, s));
 }
 
+extern "C" int gptq_gemm_host(const void* A_host, void* A_dev, int M, int K, int a_dtype,
+                              const int32_t* qweight, const int32_t* qzeros, const void* scales,
+                              const int32_t* g_idx, int N, int bits, int group, int fmt, void* C_dev,
+                              void* C_host, void* workspace, size_t workspace_bytes, void* stream) {
+  if (M < 0 || K <= 0 || N <= 0) return GPTQ_ERR_SHAPE;
+  if (M == 0) return GPTQ_OK;
+  if (!A_host || !A_dev || !C_dev || !C_host) return GPTQ_ERR_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(A_dev, A_host, static_cast<size_t>(M) * K * 2, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return GPTQ_ERR_CUDA;
+  const int rc = gptq_gemm(A_dev, M, K, a_dtype, qweight, qzeros, scales, g_idx, N, bits, group, fmt, C_dev,
+                           workspace, workspace_bytes, stream);
+  if (rc != GPTQ_OK) {
+    cudaStreamSynchronize(s);                  // the copy of A has finished before the caller reuses it
+    return rc;
+  }
+  if (cudaMemcpyAsync(C_host, C_dev, static_cast<size_t>(M) * N * 2, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return GPTQ_ERR_CUDA;
+  return cudaStreamSynchronize(s) == cudaSuccess ? GPTQ_OK : GPTQ_ERR_CUDA;
+}
+
 extern "C" int gptq_gemm_grouped(const void* A, int rows, int K, int a_dtype, const int32_t* offsets,
                                  int E, int max_m, const int32_t* qweight, const int32_t* qzeros,
                                  const void* scales, int N, int bits, int group, int fmt, void* C,

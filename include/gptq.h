@@ -139,6 +139,24 @@ int gptq_gemm(const void* A, int M, int K, int a_dtype, const int32_t* qweight,
               void* stream);
 
 /*
+ * gptq_gemm_host -- gptq_gemm with the activations and the result in host memory: copies
+ * A_host [M, K] (16-bit, a_dtype) into the device buffer A_dev, runs gptq_gemm on `stream` with
+ * C in the device buffer C_dev, copies C_dev [M, N] into C_host and waits for the stream, so
+ * that C_host holds the result when the call returns.  The operation is gptq_gemm's (page
+ * section "调整细节：根据格式选择处理方式"); every other argument means what it means there.
+ * Host pointers: A_host, C_host (page-locked memory makes the copies asynchronous DMA; pageable
+ * memory works, more slowly).  Device pointers: A_dev (M*K*2 bytes), C_dev (M*N*2 bytes),
+ * qweight, qzeros, scales, g_idx (nullable), workspace; all owned by the caller.
+ * Returns GPTQ_OK, GPTQ_ERR_ARG for a NULL host or staging pointer, any gptq_gemm status (the
+ * stream is drained first, C_host is then not written), or GPTQ_ERR_CUDA if a copy or the
+ * synchronisation failed.  M == 0 returns GPTQ_OK with nothing copied.
+ */
+int gptq_gemm_host(const void* A_host, void* A_dev, int M, int K, int a_dtype,
+                   const int32_t* qweight, const int32_t* qzeros, const void* scales,
+                   const int32_t* g_idx, int N, int bits, int group, int fmt, void* C_dev,
+                   void* C_host, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * gptq_prepack_act_order -- HOST function: rewrite an act-order checkpoint (page section
  * "LLM 的权重量化": the quantization groups are the row sets {k : g_idx[k] == g}) so that the
  * groups are contiguous row ranges.  perm[k'] (the stable sort of the rows by g_idx) is the

@@ -31,7 +31,7 @@ def test_exports_every_declared_symbol(lib):
                                "gptq_gemm_perm", "gptq_gemm_perm_workspace_size",
                                "gptq_gemm_perm_noalloc", "gptq_gemm_grouped",
                                "gptq_prepack_interleave", "gptq_gemm_interleaved",
-                               "gptq_gemm_act_order_workspace_size"])
+                               "gptq_gemm_act_order_workspace_size", "gptq_gemm_host"])
     for name in declared:
         assert hasattr(lib, name), name
 
@@ -242,6 +242,13 @@ int main(void) {
   if (gptq_gemm_grouped(NULL, 0, 256, GPTQ_F16, NULL, 1, 8, NULL, NULL, NULL, 256, 4, 128,
                         GPTQ_FMT_V2, NULL, NULL) != GPTQ_ERR_ARG) return 3;
   if (gptq_gemm_workspace_size(1, 4096, 11008, 4, 128) != 8448) return 4;
+  /* the host-buffer call: a NULL host or staging pointer, and the empty problem */
+  if (gptq_gemm_host(NULL, NULL, 1, 256, GPTQ_F16, NULL, NULL, NULL, NULL, 256, 4, 128, GPTQ_FMT_V2,
+                     NULL, NULL, NULL, 0, NULL) != GPTQ_ERR_ARG) return 6;
+  if (gptq_gemm_host(NULL, NULL, 0, 256, GPTQ_F16, NULL, NULL, NULL, NULL, 256, 4, 128, GPTQ_FMT_V2,
+                     NULL, NULL, NULL, 0, NULL) != GPTQ_OK) return 7;
+  if (gptq_gemm_host(NULL, NULL, 1, 0, GPTQ_F16, NULL, NULL, NULL, NULL, 256, 4, 128, GPTQ_FMT_V2,
+                     NULL, NULL, NULL, 0, NULL) != GPTQ_ERR_SHAPE) return 8;
   if (strlen(gptq_strerror(GPTQ_ERR_SHAPE)) == 0) return 5;
   printf("c consumer ok\n");
   return 0;
