@@ -282,21 +282,26 @@ extern "C" size_t gptq_gemm_act_order_workspace_size(int M, int K, int N, int bi
   return gptq::act_order_layout(M, K, N, bits).total;
 }
 
-extern "C" int gptq_gemm(const void* A, int M, int K, int a_dtype, const int32_t* qweight,
-                         const int32_t* qzeros, const void* scales, const int32_t* g_idx, int N,
-                         int bits, int group, int fmt, void* C, void* workspace,
-                         size_t workspace_bytes, void* stream) {
+namespace gptq {
+namespace {
+
+// gptq_gemm's validation and routing.  decode_only: run only when the decode kernels take the
+// problem (M <= 32, no g_idx, K within their reach); *declined is then set, with nothing
+// launched, for a problem they do not take.
+int gemm_entry(const void* A, int M, int K, int a_dtype, const int32_t* qweight, const int32_t* qzeros,
+               const void* scales, const int32_t* g_idx, int N, int bits, int group, int fmt, void* C,
+               void* workspace, size_t workspace_bytes, void* stream, bool decode_only, bool* declined) {
   Problem p = {};
-  int rc = gptq::check_common(qweight, qzeros, scales, g_idx, K, N, bits, group, &p);
+  int rc = check_common(qweight, qzeros, scales, g_idx, K, N, bits, group, &p);
   if (rc) return rc;
   if (fmt != GPTQ_FMT_V1 && fmt != GPTQ_FMT_V2) return GPTQ_ERR_ARG;
   if (a_dtype != GPTQ_F16 && a_dtype != GPTQ_BF16) return GPTQ_ERR_ARG;
   if (M < 0) return GPTQ_ERR_SHAPE;
   if (M == 0) return GPTQ_OK;
   if (!A || !C) return GPTQ_ERR_ARG;
-  if (!gptq::aligned(A, 16) || !gptq::aligned(C, 16)) return GPTQ_ERR_ALIGN;
-  if (workspace && !gptq::aligned(workspace, 16)) return GPTQ_ERR_ALIGN;
-  rc = gptq::device_ready(&p);
+  if (!aligned(A, 16) || !aligned(C, 16)) return GPTQ_ERR_ALIGN;
+  if (workspace && !aligned(workspace, 16)) return GPTQ_ERR_ALIGN;
+  rc = device_ready(&p);
   if (rc) return rc;
   p.A = A;
   p.M = M;
@@ -306,21 +311,51 @@ extern "C" int gptq_gemm(const void* A, int M, int K, int a_dtype, const int32_t
   p.workspace = workspace;
   p.workspace_bytes = workspace ? workspace_bytes : 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (decode_only) {
+    cudaError_t e = cudaErrorInvalidConfiguration;
+    if (M <= kDecodeMaxM && g_idx == nullptr) e = launch_decode(p, s);
+    if (e == cudaErrorInvalidConfiguration) {
+      *declined = true;
+      return GPTQ_OK;
+    }
+    return from_cuda(e);
+  }
   // act-order with room for the sorted copy: sort the rows on the device, then the group-wise
   // kernels (gptq_gemm_act_order_workspace_size is 0 for shapes that do not qualify)
   if (g_idx) {
     const size_t need = gptq_gemm_act_order_workspace_size(M, K, N, bits, group);
-    if (need && p.workspace_bytes >= need) return gptq::gemm_act_order(p, s);
+    if (need && p.workspace_bytes >= need) return gemm_act_order(p, s);
   }
-  if (M <= gptq::kDecodeMaxM) {
-    const cudaError_t e = gptq::launch_decode(p, s);
+  if (M <= kDecodeMaxM) {
+    const cudaError_t e = launch_decode(p, s);
     // cudaErrorInvalidConfiguration: nothing launched, the decode layout does not fit this K at
     // this M even split 16 ways; the tensor-core kernel takes the problem (any M)
-    if (e != cudaErrorInvalidConfiguration) return gptq::from_cuda(e);
+    if (e != cudaErrorInvalidConfiguration) return from_cuda(e);
   }
   // the tensor-core kernel multiplies bf16 activations as an fp16 copy in the workspace
-  if (a_dtype == GPTQ_BF16 && p.workspace_bytes < gptq::prefill_workspace_bytes(M, K)) return GPTQ_ERR_WORKSPACE;
-  return gptq::from_cuda(gptq::launch_prefill(p, s));
+  if (a_dtype == GPTQ_BF16 && p.workspace_bytes < prefill_workspace_bytes(M, K)) return GPTQ_ERR_WORKSPACE;
+  return from_cuda(launch_prefill(p, s));
+}
+
+// Page-locked host memory the device reaches at the same address (unified addressing).
+bool device_mapped_host(const void* ptr) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, ptr) != cudaSuccess) {
+    cudaGetLastError();                        // an unknown pointer is not an error here
+    return false;
+  }
+  return at.type == cudaMemoryTypeHost && at.devicePointer == ptr;
+}
+
+}  // namespace
+}  // namespace gptq
+
+extern "C" int gptq_gemm(const void* A, int M, int K, int a_dtype, const int32_t* qweight,
+                         const int32_t* qzeros, const void* scales, const int32_t* g_idx, int N,
+                         int bits, int group, int fmt, void* C, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  return gptq::gemm_entry(A, M, K, a_dtype, qweight, qzeros, scales, g_idx, N, bits, group, fmt, C, workspace,
+                          workspace_bytes, stream, false, nullptr);
 }
 
 extern "C" int gptq_gemm_host(const void* A_host, void* A_dev, int M, int K, int a_dtype,
@@ -333,6 +368,18 @@ extern "C" int gptq_gemm_host(const void* A_host, void* A_dev, int M, int K, int
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemcpyAsync(A_dev, A_host, static_cast<size_t>(M) * K * 2, cudaMemcpyHostToDevice, s) != cudaSuccess)
     return GPTQ_ERR_CUDA;
+  // The decode kernels write C with plain stores: into page-locked host memory that the device
+  // reaches directly, they write the result in place of a device buffer and a copy back.
+  if (gptq::device_mapped_host(C_host)) {
+    bool declined = false;
+    const int rc = gptq::gemm_entry(A_dev, M, K, a_dtype, qweight, qzeros, scales, g_idx, N, bits, group, fmt,
+                                    C_host, workspace, workspace_bytes, stream, true, &declined);
+    if (rc != GPTQ_OK) {
+      cudaStreamSynchronize(s);
+      return rc;
+    }
+    if (!declined) return cudaStreamSynchronize(s) == cudaSuccess ? GPTQ_OK : GPTQ_ERR_CUDA;
+  }
   const int rc = gptq_gemm(A_dev, M, K, a_dtype, qweight, qzeros, scales, g_idx, N, bits, group, fmt, C_dev,
                            workspace, workspace_bytes, stream);
   if (rc != GPTQ_OK) {
