@@ -285,14 +285,12 @@ extern "C" size_t gptq_gemm_act_order_workspace_size(int M, int K, int N, int bi
 namespace gptq {
 namespace {
 
-// gptq_gemm's validation and routing.  decode_only: run only when the decode kernels take the
-// problem (M <= 32, no g_idx, K within their reach); *declined is then set, with nothing
-// launched, for a problem they do not take.
-int gemm_entry(const void* A, int M, int K, int a_dtype, const int32_t* qweight, const int32_t* qzeros,
-               const void* scales, const int32_t* g_idx, int N, int bits, int group, int fmt, void* C,
-               void* workspace, size_t workspace_bytes, void* stream, bool decode_only, bool* declined) {
-  Problem p = {};
-  int rc = check_common(qweight, qzeros, scales, g_idx, K, N, bits, group, &p);
+// gptq_gemm's argument validation: fills *p on success (p->M == 0: nothing to do).
+int gemm_prepare(const void* A, int M, int K, int a_dtype, const int32_t* qweight, const int32_t* qzeros,
+                 const void* scales, const int32_t* g_idx, int N, int bits, int group, int fmt, void* C,
+                 void* workspace, size_t workspace_bytes, Problem* p) {
+  *p = Problem{};
+  int rc = check_common(qweight, qzeros, scales, g_idx, K, N, bits, group, p);
   if (rc) return rc;
   if (fmt != GPTQ_FMT_V1 && fmt != GPTQ_FMT_V2) return GPTQ_ERR_ARG;
   if (a_dtype != GPTQ_F16 && a_dtype != GPTQ_BF16) return GPTQ_ERR_ARG;
@@ -301,19 +299,25 @@ int gemm_entry(const void* A, int M, int K, int a_dtype, const int32_t* qweight,
   if (!A || !C) return GPTQ_ERR_ARG;
   if (!aligned(A, 16) || !aligned(C, 16)) return GPTQ_ERR_ALIGN;
   if (workspace && !aligned(workspace, 16)) return GPTQ_ERR_ALIGN;
-  rc = device_ready(&p);
+  rc = device_ready(p);
   if (rc) return rc;
-  p.A = A;
-  p.M = M;
-  p.dtype = a_dtype;
-  p.zero_offset = fmt == GPTQ_FMT_V1 ? 1 : 0;
-  p.out = C;
-  p.workspace = workspace;
-  p.workspace_bytes = workspace ? workspace_bytes : 0;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  p->A = A;
+  p->M = M;
+  p->dtype = a_dtype;
+  p->zero_offset = fmt == GPTQ_FMT_V1 ? 1 : 0;
+  p->out = C;
+  p->workspace = workspace;
+  p->workspace_bytes = workspace ? workspace_bytes : 0;
+  return GPTQ_OK;
+}
+
+// gptq_gemm's routing of a validated problem.  decode_only: run only when the decode kernels take
+// the problem (M <= 32, no g_idx, K within their reach); *declined is then set, with nothing
+// launched, for a problem they do not take.
+int gemm_run(const Problem& p, cudaStream_t s, bool decode_only, bool* declined) {
   if (decode_only) {
     cudaError_t e = cudaErrorInvalidConfiguration;
-    if (M <= kDecodeMaxM && g_idx == nullptr) e = launch_decode(p, s);
+    if (p.M <= kDecodeMaxM && p.g_idx == nullptr) e = launch_decode(p, s);
     if (e == cudaErrorInvalidConfiguration) {
       *declined = true;
       return GPTQ_OK;
@@ -322,18 +326,18 @@ int gemm_entry(const void* A, int M, int K, int a_dtype, const int32_t* qweight,
   }
   // act-order with room for the sorted copy: sort the rows on the device, then the group-wise
   // kernels (gptq_gemm_act_order_workspace_size is 0 for shapes that do not qualify)
-  if (g_idx) {
-    const size_t need = gptq_gemm_act_order_workspace_size(M, K, N, bits, group);
+  if (p.g_idx) {
+    const size_t need = gptq_gemm_act_order_workspace_size(p.M, p.K, p.N, p.bits, p.group);
     if (need && p.workspace_bytes >= need) return gemm_act_order(p, s);
   }
-  if (M <= kDecodeMaxM) {
+  if (p.M <= kDecodeMaxM) {
     const cudaError_t e = launch_decode(p, s);
     // cudaErrorInvalidConfiguration: nothing launched, the decode layout does not fit this K at
     // this M even split 16 ways; the tensor-core kernel takes the problem (any M)
     if (e != cudaErrorInvalidConfiguration) return from_cuda(e);
   }
   // the tensor-core kernel multiplies bf16 activations as an fp16 copy in the workspace
-  if (a_dtype == GPTQ_BF16 && p.workspace_bytes < prefill_workspace_bytes(M, K)) return GPTQ_ERR_WORKSPACE;
+  if (p.dtype == GPTQ_BF16 && p.workspace_bytes < prefill_workspace_bytes(p.M, p.K)) return GPTQ_ERR_WORKSPACE;
   return from_cuda(launch_prefill(p, s));
 }
 
@@ -354,8 +358,11 @@ extern "C" int gptq_gemm(const void* A, int M, int K, int a_dtype, const int32_t
                          const int32_t* qzeros, const void* scales, const int32_t* g_idx, int N,
                          int bits, int group, int fmt, void* C, void* workspace,
                          size_t workspace_bytes, void* stream) {
-  return gptq::gemm_entry(A, M, K, a_dtype, qweight, qzeros, scales, g_idx, N, bits, group, fmt, C, workspace,
-                          workspace_bytes, stream, false, nullptr);
+  gptq::Problem p;
+  const int rc = gptq::gemm_prepare(A, M, K, a_dtype, qweight, qzeros, scales, g_idx, N, bits, group, fmt, C,
+                                    workspace, workspace_bytes, &p);
+  if (rc != GPTQ_OK || p.M == 0) return rc;
+  return gptq::gemm_run(p, static_cast<cudaStream_t>(stream), false, nullptr);
 }
 
 extern "C" int gptq_gemm_host(const void* A_host, void* A_dev, int M, int K, int a_dtype,
@@ -365,23 +372,27 @@ extern "C" int gptq_gemm_host(const void* A_host, void* A_dev, int M, int K, int
   if (M < 0 || K <= 0 || N <= 0) return GPTQ_ERR_SHAPE;
   if (M == 0) return GPTQ_OK;
   if (!A_host || !A_dev || !C_dev || !C_host) return GPTQ_ERR_ARG;
+  gptq::Problem p;
+  int rc = gptq::gemm_prepare(A_dev, M, K, a_dtype, qweight, qzeros, scales, g_idx, N, bits, group, fmt, C_dev,
+                              workspace, workspace_bytes, &p);
+  if (rc != GPTQ_OK) return rc;                // arguments are checked before anything is copied
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemcpyAsync(A_dev, A_host, static_cast<size_t>(M) * K * 2, cudaMemcpyHostToDevice, s) != cudaSuccess)
     return GPTQ_ERR_CUDA;
   // The decode kernels write C with plain stores: into page-locked host memory that the device
   // reaches directly, they write the result in place of a device buffer and a copy back.
-  if (gptq::device_mapped_host(C_host)) {
+  if (gptq::aligned(C_host, 16) && gptq::device_mapped_host(C_host)) {
+    gptq::Problem d = p;
+    d.out = C_host;
     bool declined = false;
-    const int rc = gptq::gemm_entry(A_dev, M, K, a_dtype, qweight, qzeros, scales, g_idx, N, bits, group, fmt,
-                                    C_host, workspace, workspace_bytes, stream, true, &declined);
+    rc = gptq::gemm_run(d, s, true, &declined);
     if (rc != GPTQ_OK) {
       cudaStreamSynchronize(s);
       return rc;
     }
     if (!declined) return cudaStreamSynchronize(s) == cudaSuccess ? GPTQ_OK : GPTQ_ERR_CUDA;
   }
-  const int rc = gptq_gemm(A_dev, M, K, a_dtype, qweight, qzeros, scales, g_idx, N, bits, group, fmt, C_dev,
-                           workspace, workspace_bytes, stream);
+  rc = gptq::gemm_run(p, s, false, nullptr);
   if (rc != GPTQ_OK) {
     cudaStreamSynchronize(s);                  // the copy of A has finished before the caller reuses it
     return rc;

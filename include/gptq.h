@@ -36,7 +36,8 @@
  * pointers, must be 16-byte aligned (g_idx: 4-byte), and run asynchronously on `stream`
  * (a cudaStream_t; NULL = legacy default stream) on the current device.  The library keeps
  * only a per-device status word and per-device launch attributes; it never allocates device
- * memory in these calls.
+ * memory in these calls.  gptq_gemm_host is the exception: it takes A and C in host memory and
+ * returns only once the stream has drained.
  *
  * Stream order: the GEMM entry points (gptq_gemm, gptq_gemm_perm, gptq_gemm_perm_noalloc) use
  * programmatic dependent launch, so their kernels may start while the kernel issued just before
@@ -149,9 +150,11 @@ int gptq_gemm(const void* A, int M, int K, int a_dtype, const int32_t* qweight,
  * address and the decode kernels take the problem (M <= 32, no g_idx), they write C straight
  * into C_host and C_dev is left untouched.  Device pointers: A_dev (M*K*2 bytes), C_dev (M*N*2
  * bytes), qweight, qzeros, scales, g_idx (nullable), workspace; all owned by the caller.
- * Returns GPTQ_OK, GPTQ_ERR_ARG for a NULL host or staging pointer, any gptq_gemm status (the
- * stream is drained first, C_host is then not written), or GPTQ_ERR_CUDA if a copy or the
- * synchronisation failed.  M == 0 returns GPTQ_OK with nothing copied.
+ * Returns GPTQ_OK, GPTQ_ERR_ARG for a NULL host or staging pointer, any gptq_gemm status, or
+ * GPTQ_ERR_CUDA if a copy or the synchronisation failed.  gptq_gemm's argument checks run
+ * before anything is copied; a status found when the kernels are chosen (GPTQ_ERR_WORKSPACE for
+ * a bf16 problem that the tensor-core kernel takes) comes after the copy of A, with the stream
+ * drained and C_host not written.  M == 0 returns GPTQ_OK with nothing copied.
  */
 int gptq_gemm_host(const void* A_host, void* A_dev, int M, int K, int a_dtype,
                    const int32_t* qweight, const int32_t* qzeros, const void* scales,

@@ -78,9 +78,13 @@ def test_empty_problem_and_validation_errors():
                       C_dev=C_dev, C_host=torch.empty((0, N), dtype=torch.float16))
     assert out.numel() == 0
     # a group size that does not divide K: gptq_gemm's own check, reported through the host call
+    # before anything is copied (the staging buffer keeps its contents)
+    A_dev.fill_(-3.0)
     with pytest.raises(g.GPTQError):
         g.gemm_host(torch.ones((1, K), dtype=torch.float16), A_dev, qw, qz, sc, bits=bits, group=96,
                     C_dev=C_dev, C_host=torch.empty((1, N), dtype=torch.float16))
+    torch.cuda.synchronize()
+    assert bool((A_dev == -3.0).all())
     # staging buffers of the wrong dtype or size are refused before the call
     with pytest.raises(TypeError):
         g.gemm_host(torch.ones((1, K), dtype=torch.float16), A_dev.to(torch.bfloat16), qw, qz, sc, bits=bits,
