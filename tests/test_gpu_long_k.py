@@ -111,3 +111,22 @@ def test_decode_only_calls_refuse_what_fits_no_cta():
     with pytest.raises(g.GPTQError) as e:
         g.gemm_grouped(A, offsets, qw[None], qz[None], sc[None], bits=bits, group=group, max_m=M)
     assert e.value.code == -2
+
+
+def test_host_buffer_call_where_the_decode_kernels_decline():
+    """gptq_gemm_host with page-locked C: the decode kernels would write C in place, but at K =
+    98304 and 32 tokens they take no layout; the call then copies C back from the tensor-core
+    kernel's result in C_dev."""
+    K, N, M, bits, group = 98304, 256, 32, 2, 128
+    wl, ck = _checkpoint(K, N, bits, group)
+    A = gptq_inputs.draw_activations(wl, M)
+    qw, qz, sc = _dev(ck)
+    A_host = A.contiguous().pin_memory()
+    C_host = torch.empty((M, N), dtype=A.dtype).pin_memory()
+    A_dev = torch.empty((M, K), dtype=A.dtype, device=DEV)
+    C_dev = torch.empty((M, N), dtype=A.dtype, device=DEV)
+    g.gemm_host(A_host, A_dev, qw, qz, sc, bits=bits, group=group, C_dev=C_dev, C_host=C_host)
+    Cref, B = oracle.gemm(bits16(A), oracle.F16, ck["qweight"], ck["qzeros"], ck["scales"], None, N, bits,
+                          group, oracle.V2)
+    assert_gemm_close(C_host, Cref, B, "host buffers, K=%d" % K)
+    assert torch.equal(C_host.view(torch.int16), C_dev.cpu().view(torch.int16))
