@@ -341,6 +341,18 @@ int gemm_run(const Problem& p, cudaStream_t s, bool decode_only, bool* declined)
   return from_cuda(launch_prefill(p, s));
 }
 
+// The activations copied in by a kernel that reads page-locked host memory directly: it lets its
+// dependents launch at once, so a decode kernel that follows with programmatic dependent launch
+// streams its weights while A is still arriving, and reads A after its dependency wait.  n16:
+// 16-byte pieces (M * K * 2 is a multiple of 64).
+__global__ void __launch_bounds__(256) k_copy_in(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                                 long long n16) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const long long step = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16; i += step)
+    dst[i] = src[i];
+}
+
 // Page-locked host memory the device reaches at the same address (unified addressing).
 bool device_mapped_host(const void* ptr) {
   cudaPointerAttributes at;
@@ -377,8 +389,17 @@ extern "C" int gptq_gemm_host(const void* A_host, void* A_dev, int M, int K, int
                               workspace, workspace_bytes, &p);
   if (rc != GPTQ_OK) return rc;                // arguments are checked before anything is copied
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemcpyAsync(A_dev, A_host, static_cast<size_t>(M) * K * 2, cudaMemcpyHostToDevice, s) != cudaSuccess)
+  const size_t a_bytes = static_cast<size_t>(M) * K * 2;
+  if (gptq::aligned(A_host, 16) && gptq::device_mapped_host(A_host)) {
+    const long long n16 = static_cast<long long>(a_bytes / 16);
+    long long blocks = (n16 + 255) / 256;
+    if (blocks > 64) blocks = 64;
+    gptq::k_copy_in<<<static_cast<unsigned>(blocks), 256, 0, s>>>(static_cast<const uint4*>(A_host),
+                                                                   static_cast<uint4*>(A_dev), n16);
+    if (cudaGetLastError() != cudaSuccess) return GPTQ_ERR_CUDA;
+  } else if (cudaMemcpyAsync(A_dev, A_host, a_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) {
     return GPTQ_ERR_CUDA;
+  }
   // The decode kernels write C with plain stores: into page-locked host memory that the device
   // reaches directly, they write the result in place of a device buffer and a copy back.
   if (gptq::aligned(C_host, 16) && gptq::device_mapped_host(C_host)) {
