@@ -145,11 +145,11 @@ int gptq_gemm(const void* A, int M, int K, int a_dtype, const int32_t* qweight,
  * C in the device buffer C_dev, copies C_dev [M, N] into C_host and waits for the stream, so
  * that C_host holds the result when the call returns.  The operation is gptq_gemm's (page
  * section "调整细节：根据格式选择处理方式"); every other argument means what it means there.
- * Host pointers: A_host, C_host.  Page-locked memory the device reaches at the same address is
- * read and written by kernels over the chip-to-chip link (A copied into A_dev by a kernel that
- * the GEMM overlaps; C as described next); pageable memory works, through DMA copies.  When C_host is page-locked memory the device reaches at the same
- * address and the decode kernels take the problem (M <= 32, no g_idx), they write C straight
- * into C_host and C_dev is left untouched.  Device pointers: A_dev (M*K*2 bytes), C_dev (M*N*2
+ * Host pointers: A_host, C_host.  Page-locked memory that the device reaches at the same
+ * address is read and written by kernels over the chip-to-chip link: A is copied into A_dev by a
+ * kernel that the GEMM overlaps, and when the decode kernels take the problem (M <= 32, no
+ * g_idx) they write C straight into C_host, leaving C_dev untouched.  Pageable memory works,
+ * through DMA copies.  Device pointers: A_dev (M*K*2 bytes), C_dev (M*N*2
  * bytes), qweight, qzeros, scales, g_idx (nullable), workspace; all owned by the caller.
  * Returns GPTQ_OK, GPTQ_ERR_ARG for a NULL host or staging pointer, any gptq_gemm status, or
  * GPTQ_ERR_CUDA if a copy or the synchronisation failed.  gptq_gemm's argument checks run
