@@ -328,7 +328,8 @@ def run_ours(args, rank, world, local_rank):
     c_host = torch.empty((M, wl.N), dtype=A.dtype).pin_memory()
     n_e2e = max(1, min(args.steps, 2000))
 
-    # the arguments of each weight set's call marshalled once (g.HostGemm): a step is the C call
+    # each weight set's call prepared once (g.HostGemm on a named stream: gptq_gemm_host captured
+    # into a graph); a step is one gptq_host_plan_run call
     host_calls = [g.HostGemm(a_host, a, q, z, s, bits=wl.bits, group=wl.group, fmt=g.V2, C_dev=c,
                              C_host=c_host, stream=stream) for (q, z, s, a, c) in sets]
 
@@ -391,9 +392,9 @@ def run_ours(args, rank, world, local_rank):
                                    "single launch: event pair around one launch, synchronized"},
         "e2e": {"value": round(e2e_value, 3), "unit": "GB/s", "h2d_bytes_per_step": M * wl.K * 2,
                 "d2h_bytes_per_step": M * wl.N * 2,
-                "note": "weights resident on the device (the model); per step one gptq_gemm_host call "
-                        "(arguments marshalled once per weight set): "
-                        "A host->device, gptq_gemm, C device->host, stream synchronize"},
+                "note": "weights resident on the device (the model); per step one gptq_host_plan_run "
+                        "call (gptq_gemm_host captured once per weight set): A host->device, gptq_gemm, "
+                        "C device->host, stream synchronize"},
         "gpu_launches": args.steps,
         "clocks": clocks,
     }

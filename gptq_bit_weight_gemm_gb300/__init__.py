@@ -59,6 +59,10 @@ _SIGNATURES = {
     "gptq_dequant": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
     "gptq_gemm": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P]),
     "gptq_gemm_host": (_I, [_P, _P, _I, _I, _I, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _SZ, _P]),
+    "gptq_host_plan_create": (_I, [ctypes.POINTER(ctypes.c_void_p), _P, _P, _I, _I, _I, _P, _P, _P, _P, _I, _I, _I,
+                                   _I, _P, _P, _P, _SZ, _P]),
+    "gptq_host_plan_run": (_I, [_P]),
+    "gptq_host_plan_destroy": (_I, [_P]),
     "gptq_gemm_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "gptq_gemm_act_order_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "gptq_repack_zeros_v1_to_v2": (_I, [_P, _P, _I, _I, _I]),
@@ -174,12 +178,14 @@ def gemm(A, qweight, qzeros, scales, g_idx=None, *, bits, group, fmt=V2, out=Non
 
 
 class HostGemm:
-    """gptq_gemm_host with its arguments marshalled once, for a loop that reruns one problem on
-    the same host and device buffers (only the host buffers' contents change between calls):
-    calling the object copies A_host [M, K] (a CPU tensor, page-locked for asynchronous copies)
-    into A_dev, computes C = A @ dequant(W) into C_dev, copies it into C_host (a CPU tensor) and
-    returns C_host once it holds the result.  The staging buffers and the workspace belong to the
-    caller (as for gemm, a bf16 prefill needs workspace_size(...) bytes)."""
+    """gptq_gemm_host prepared once, for a loop that reruns one problem on the same host and device
+    buffers (only the contents of A_host change between calls): calling the object takes A_host
+    [M, K] (a CPU tensor, page-locked for the direct path) into A_dev, computes C = A @ dequant(W)
+    and returns C_host (a CPU tensor) once it holds the result.  On a named stream the call is
+    captured into a CUDA graph (gptq_host_plan_create, which runs it once) and each call replays
+    the graph; on the default stream each call is one gptq_gemm_host call with the arguments
+    marshalled here.  The staging buffers and the workspace belong to the caller and must outlive
+    the object (as for gemm, a bf16 prefill needs workspace_size(...) bytes)."""
 
     def __init__(self, A_host, A_dev, qweight, qzeros, scales, g_idx=None, *, bits, group, C_dev, C_host,
                  fmt=V2, workspace=None, stream=None):
@@ -202,19 +208,61 @@ class HostGemm:
                       _ptr(scales, torch.float16, "scales"), _ptr(g_idx, torch.int32, "g_idx"), N, bits, group,
                       fmt, _ptr(C_dev, name="C_dev"), ctypes.c_void_p(C_host.data_ptr()), ws_ptr, ws_len,
                       _stream(stream))
-        self._fn = lib().gptq_gemm_host
         self.C_host = C_host
+        self._plan = None
+        if self._args[-1].value:
+            # a named stream: the call is captured once (gptq_host_plan_create, which also runs it
+            # once) and each call replays the capture
+            h = ctypes.c_void_p()
+            _check(lib().gptq_host_plan_create(ctypes.byref(h), *self._args), "gptq_host_plan_create")
+            self._plan = h
+            self._run = lib().gptq_host_plan_run
+        else:
+            self._fn = lib().gptq_gemm_host
 
     def __call__(self):
-        _check(self._fn(*self._args), "gptq_gemm_host")
+        if self._plan is not None:
+            _check(self._run(self._plan), "gptq_host_plan_run")
+        else:
+            _check(self._fn(*self._args), "gptq_gemm_host")
         return self.C_host
+
+    def close(self):
+        """Release the captured plan (also done when the object is collected)."""
+        if getattr(self, "_plan", None) is not None and _lib is not None:
+            lib().gptq_host_plan_destroy(self._plan)
+        self._plan = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def gemm_host(A_host, A_dev, qweight, qzeros, scales, g_idx=None, *, bits, group, C_dev, C_host, fmt=V2,
               workspace=None, stream=None):
-    """One gptq_gemm_host call (see HostGemm): returns C_host holding C = A @ dequant(W)."""
-    return HostGemm(A_host, A_dev, qweight, qzeros, scales, g_idx, bits=bits, group=group, C_dev=C_dev,
-                    C_host=C_host, fmt=fmt, workspace=workspace, stream=stream)()
+    """One gptq_gemm_host call: returns C_host holding C = A @ dequant(W) (HostGemm prepares the
+    call for a loop over the same buffers)."""
+    torch = _torch()
+    M, K = A_host.shape
+    N = qweight.shape[1]
+    for t, name in ((A_host, "A_host"), (C_host, "C_host")):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous CPU tensor" % name)
+    if A_dev.dtype != A_host.dtype or C_dev.dtype != A_host.dtype or C_host.dtype != A_host.dtype:
+        raise TypeError("A_host, A_dev, C_dev and C_host must share A's dtype")
+    if A_dev.numel() < M * K or C_dev.numel() < M * N or C_host.numel() < M * N:
+        raise ValueError("staging buffers smaller than the problem")
+    ws_ptr = _ptr(workspace, name="workspace") if workspace is not None else None
+    ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = lib().gptq_gemm_host(ctypes.c_void_p(A_host.data_ptr()), _ptr(A_dev, name="A_dev"), M, K,
+                              _dtype_code(A_host), _ptr(qweight, torch.int32, "qweight"),
+                              _ptr(qzeros, torch.int32, "qzeros"), _ptr(scales, torch.float16, "scales"),
+                              _ptr(g_idx, torch.int32, "g_idx"), N, bits, group, fmt, _ptr(C_dev, name="C_dev"),
+                              ctypes.c_void_p(C_host.data_ptr()), ws_ptr, ws_len, _stream(stream))
+    _check(rc, "gptq_gemm_host")
+    return C_host
 
 
 def dequant(qweight, qzeros, scales, g_idx=None, *, K, bits, group, fmt=V2, dtype=None, out=None,

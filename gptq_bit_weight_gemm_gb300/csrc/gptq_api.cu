@@ -377,6 +377,60 @@ extern "C" int gptq_gemm(const void* A, int M, int K, int a_dtype, const int32_t
   return gptq::gemm_run(p, static_cast<cudaStream_t>(stream), false, nullptr);
 }
 
+namespace gptq {
+namespace {
+
+// Where gptq_gemm_host moves A and C: page-locked host memory that the device reaches at the
+// same address is read and written by kernels, anything else goes through DMA copies.  A takes
+// the copy kernel only up to 32 KB: measured on llama-7B's [4096, 11008] (µs per call, direct
+// call / captured plan), the kernel gave 20.8 / 16.9 at M = 1 and 24.0 / 20.3 at M = 4, but
+// 31.8 / 41.5 at M = 16, where a DMA copy gives 32.5 / 30.5.
+struct HostRoute {
+  bool a_kernel;   // A copied in by k_copy_in
+  bool c_direct;   // the decode kernels may write C straight into C_host
+};
+
+constexpr size_t kCopyKernelMaxBytes = 32 * 1024;
+
+HostRoute host_route(const void* A_host, size_t a_bytes, const void* C_host) {
+  return HostRoute{a_bytes <= kCopyKernelMaxBytes && aligned(A_host, 16) && device_mapped_host(A_host),
+                   aligned(C_host, 16) && device_mapped_host(C_host)};
+}
+
+// gptq_gemm_host's stream work for a validated problem, without the final wait: A in, the GEMM,
+// C out.  On an error the caller drains the stream before returning it.
+int host_enqueue(const Problem& p, const HostRoute& r, const void* A_host, void* A_dev, void* C_dev, void* C_host,
+                 cudaStream_t s) {
+  const size_t a_bytes = static_cast<size_t>(p.M) * p.K * 2;
+  if (r.a_kernel) {
+    const long long n16 = static_cast<long long>(a_bytes / 16);
+    long long blocks = (n16 + 255) / 256;
+    if (blocks > 64) blocks = 64;
+    k_copy_in<<<static_cast<unsigned>(blocks), 256, 0, s>>>(static_cast<const uint4*>(A_host),
+                                                            static_cast<uint4*>(A_dev), n16);
+    if (cudaGetLastError() != cudaSuccess) return GPTQ_ERR_CUDA;
+  } else if (cudaMemcpyAsync(A_dev, A_host, a_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+    return GPTQ_ERR_CUDA;
+  }
+  // The decode kernels write C with plain stores: into page-locked host memory that the device
+  // reaches directly, they write the result in place of a device buffer and a copy back.
+  if (r.c_direct) {
+    Problem d = p;
+    d.out = C_host;
+    bool declined = false;
+    const int rc = gemm_run(d, s, true, &declined);
+    if (rc != GPTQ_OK || !declined) return rc;
+  }
+  const int rc = gemm_run(p, s, false, nullptr);
+  if (rc != GPTQ_OK) return rc;
+  if (cudaMemcpyAsync(C_host, C_dev, static_cast<size_t>(p.M) * p.N * 2, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return GPTQ_ERR_CUDA;
+  return GPTQ_OK;
+}
+
+}  // namespace
+}  // namespace gptq
+
 extern "C" int gptq_gemm_host(const void* A_host, void* A_dev, int M, int K, int a_dtype,
                               const int32_t* qweight, const int32_t* qzeros, const void* scales,
                               const int32_t* g_idx, int N, int bits, int group, int fmt, void* C_dev,
@@ -389,38 +443,72 @@ extern "C" int gptq_gemm_host(const void* A_host, void* A_dev, int M, int K, int
                               workspace, workspace_bytes, &p);
   if (rc != GPTQ_OK) return rc;                // arguments are checked before anything is copied
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const size_t a_bytes = static_cast<size_t>(M) * K * 2;
-  if (gptq::aligned(A_host, 16) && gptq::device_mapped_host(A_host)) {
-    const long long n16 = static_cast<long long>(a_bytes / 16);
-    long long blocks = (n16 + 255) / 256;
-    if (blocks > 64) blocks = 64;
-    gptq::k_copy_in<<<static_cast<unsigned>(blocks), 256, 0, s>>>(static_cast<const uint4*>(A_host),
-                                                                   static_cast<uint4*>(A_dev), n16);
-    if (cudaGetLastError() != cudaSuccess) return GPTQ_ERR_CUDA;
-  } else if (cudaMemcpyAsync(A_dev, A_host, a_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) {
-    return GPTQ_ERR_CUDA;
-  }
-  // The decode kernels write C with plain stores: into page-locked host memory that the device
-  // reaches directly, they write the result in place of a device buffer and a copy back.
-  if (gptq::aligned(C_host, 16) && gptq::device_mapped_host(C_host)) {
-    gptq::Problem d = p;
-    d.out = C_host;
-    bool declined = false;
-    rc = gptq::gemm_run(d, s, true, &declined);
-    if (rc != GPTQ_OK) {
-      cudaStreamSynchronize(s);
-      return rc;
-    }
-    if (!declined) return cudaStreamSynchronize(s) == cudaSuccess ? GPTQ_OK : GPTQ_ERR_CUDA;
-  }
-  rc = gptq::gemm_run(p, s, false, nullptr);
+  rc = gptq::host_enqueue(p, gptq::host_route(A_host, static_cast<size_t>(M) * K * 2, C_host), A_host, A_dev, C_dev, C_host, s);
   if (rc != GPTQ_OK) {
     cudaStreamSynchronize(s);                  // the copy of A has finished before the caller reuses it
     return rc;
   }
-  if (cudaMemcpyAsync(C_host, C_dev, static_cast<size_t>(M) * N * 2, cudaMemcpyDeviceToHost, s) != cudaSuccess)
-    return GPTQ_ERR_CUDA;
   return cudaStreamSynchronize(s) == cudaSuccess ? GPTQ_OK : GPTQ_ERR_CUDA;
+}
+
+// A prepared gptq_gemm_host: the stream work of one call captured into a CUDA graph.
+struct gptq_host_plan {
+  cudaGraphExec_t exec;
+  cudaStream_t stream;
+};
+
+extern "C" int gptq_host_plan_create(gptq_host_plan** plan, const void* A_host, void* A_dev, int M, int K,
+                                     int a_dtype, const int32_t* qweight, const int32_t* qzeros,
+                                     const void* scales, const int32_t* g_idx, int N, int bits, int group,
+                                     int fmt, void* C_dev, void* C_host, void* workspace,
+                                     size_t workspace_bytes, void* stream) {
+  if (!plan) return GPTQ_ERR_ARG;
+  *plan = nullptr;
+  if (!stream) return GPTQ_ERR_ARG;            // the legacy default stream cannot be captured
+  // one call first: it checks the problem end to end and does every one-time setup (launch
+  // attributes, occupancy queries) outside the capture
+  int rc = gptq_gemm_host(A_host, A_dev, M, K, a_dtype, qweight, qzeros, scales, g_idx, N, bits, group, fmt, C_dev,
+                          C_host, workspace, workspace_bytes, stream);
+  if (rc != GPTQ_OK) return rc;
+  gptq_host_plan* h = new gptq_host_plan{nullptr, static_cast<cudaStream_t>(stream)};
+  if (M == 0) {
+    *plan = h;
+    return GPTQ_OK;
+  }
+  gptq::Problem p;
+  rc = gptq::gemm_prepare(A_dev, M, K, a_dtype, qweight, qzeros, scales, g_idx, N, bits, group, fmt, C_dev,
+                          workspace, workspace_bytes, &p);
+  const gptq::HostRoute route = gptq::host_route(A_host, static_cast<size_t>(M) * K * 2, C_host);
+  cudaGraph_t graph = nullptr;
+  if (rc == GPTQ_OK && cudaStreamBeginCapture(h->stream, cudaStreamCaptureModeThreadLocal) != cudaSuccess)
+    rc = GPTQ_ERR_CUDA;
+  if (rc == GPTQ_OK) {
+    rc = gptq::host_enqueue(p, route, A_host, A_dev, C_dev, C_host, h->stream);
+    if (cudaStreamEndCapture(h->stream, &graph) != cudaSuccess && rc == GPTQ_OK) rc = GPTQ_ERR_CUDA;
+  }
+  if (rc == GPTQ_OK && cudaGraphInstantiate(&h->exec, graph, 0) != cudaSuccess) rc = GPTQ_ERR_CUDA;
+  if (graph) cudaGraphDestroy(graph);
+  if (rc != GPTQ_OK) {
+    cudaGetLastError();
+    delete h;
+    return rc;
+  }
+  *plan = h;
+  return GPTQ_OK;
+}
+
+extern "C" int gptq_host_plan_run(gptq_host_plan* plan) {
+  if (!plan) return GPTQ_ERR_ARG;
+  if (!plan->exec) return GPTQ_OK;             // M == 0
+  if (cudaGraphLaunch(plan->exec, plan->stream) != cudaSuccess) return GPTQ_ERR_CUDA;
+  return cudaStreamSynchronize(plan->stream) == cudaSuccess ? GPTQ_OK : GPTQ_ERR_CUDA;
+}
+
+extern "C" int gptq_host_plan_destroy(gptq_host_plan* plan) {
+  if (!plan) return GPTQ_OK;
+  if (plan->exec) cudaGraphExecDestroy(plan->exec);
+  delete plan;
+  return GPTQ_OK;
 }
 
 extern "C" int gptq_gemm_grouped(const void* A, int rows, int K, int a_dtype, const int32_t* offsets,

@@ -163,6 +163,26 @@ int gptq_gemm_host(const void* A_host, void* A_dev, int M, int K, int a_dtype,
                    void* C_host, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * gptq_host_plan_create / _run / _destroy -- gptq_gemm_host prepared once for a loop that reruns
+ * one problem on the same buffers (only the contents of A_host change between runs): create
+ * makes one gptq_gemm_host call (which checks everything and returns its status) and then
+ * captures the stream work of such a call into a CUDA graph; each run replays it on `stream` --
+ * A_host's current contents in, the GEMM, the result in C_host -- and returns once the stream
+ * has drained.  Arguments as for gptq_gemm_host; `stream` must not be NULL (the legacy default
+ * stream cannot be captured: GPTQ_ERR_ARG).  The buffers must outlive the plan.  create returns
+ * GPTQ_OK with *plan set, or an error status with *plan NULL; run returns GPTQ_OK, GPTQ_ERR_ARG
+ * for a NULL plan, or GPTQ_ERR_CUDA; destroy (NULL allowed) returns GPTQ_OK.
+ */
+typedef struct gptq_host_plan gptq_host_plan;
+int gptq_host_plan_create(gptq_host_plan** plan, const void* A_host, void* A_dev, int M, int K,
+                          int a_dtype, const int32_t* qweight, const int32_t* qzeros,
+                          const void* scales, const int32_t* g_idx, int N, int bits, int group,
+                          int fmt, void* C_dev, void* C_host, void* workspace, size_t workspace_bytes,
+                          void* stream);
+int gptq_host_plan_run(gptq_host_plan* plan);
+int gptq_host_plan_destroy(gptq_host_plan* plan);
+
+/*
  * gptq_prepack_act_order -- HOST function: rewrite an act-order checkpoint (page section
  * "LLM 的权重量化": the quantization groups are the row sets {k : g_idx[k] == g}) so that the
  * groups are contiguous row ranges.  perm[k'] (the stable sort of the rows by g_idx) is the

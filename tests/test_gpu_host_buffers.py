@@ -95,9 +95,12 @@ def test_empty_problem_and_validation_errors():
     assert g.device_status() == 0
 
 
-def test_prepared_call_reruns_on_new_host_contents():
-    """HostGemm marshals the arguments once; each call copies the host buffer's current contents."""
+@pytest.mark.parametrize("named_stream", [False, True], ids=["default_stream", "captured_plan"])
+def test_prepared_call_reruns_on_new_host_contents(named_stream):
+    """HostGemm prepares the call once (on a named stream: a captured graph); each call takes the
+    host buffer's current contents."""
     K, N, bits, group = 1024, 544, 4, 128
+    stream = torch.cuda.Stream() if named_stream else None
     wl = gptq_inputs.Workload("host", K, N, bits, group, "f16", (3,), ("v2",), seed=11)
     _, ck = checkpoint(wl, "v2")
     qw, qz, sc, _ = to_device(ck)
@@ -105,7 +108,9 @@ def test_prepared_call_reruns_on_new_host_contents():
     C_host = torch.empty((3, N), dtype=torch.float16).pin_memory()
     A_dev = torch.empty((3, K), dtype=torch.float16, device=DEV)
     C_dev = torch.empty((3, N), dtype=torch.float16, device=DEV)
-    call = g.HostGemm(A_host, A_dev, qw, qz, sc, bits=bits, group=group, C_dev=C_dev, C_host=C_host)
+    call = g.HostGemm(A_host, A_dev, qw, qz, sc, bits=bits, group=group, C_dev=C_dev, C_host=C_host,
+                      stream=stream)
+    assert (call._plan is not None) == named_stream
     for seed in (1, 2, 3):
         wl_s = gptq_inputs.Workload("host", K, N, bits, group, "f16", (3,), ("v2",), seed=seed)
         A = gptq_inputs.draw_activations(wl_s, 3)
@@ -115,3 +120,35 @@ def test_prepared_call_reruns_on_new_host_contents():
         Cref, B = oracle.gemm(bits16(A), dtype_code(wl), ck["qweight"], ck["qzeros"], ck["scales"], None,
                               N, bits, group, ck["fmt"])
         assert_gemm_close(C_host, Cref, B, "prepared call, activations %d" % seed)
+
+
+@pytest.mark.parametrize("case", [(4, 128, "f16", 16, 1024, 544), (8, 128, "bf16", 48, 384, 160),
+                                  (2, 64, "bf16", 5, 512, 288)], ids=lambda c: "b%d_g%d_%s_M%d_K%d_N%d" % c)
+def test_captured_plan_matches_the_direct_call(case):
+    """The captured plan replays exactly gptq_gemm_host's work: the same bits, for the decode and
+    the tensor-core kernels (bf16 prefill with its workspace), run after run."""
+    bits, group, dt, M, K, N = case
+    wl = gptq_inputs.Workload("host", K, N, bits, group, dt, (M,), ("v2",), seed=M + bits)
+    _, ck = checkpoint(wl, "v2")
+    qw, qz, sc, _ = to_device(ck)
+    A = gptq_inputs.draw_activations(wl, M)
+    A_host = A.contiguous().pin_memory()
+    C_host = torch.empty((M, N), dtype=A.dtype).pin_memory()
+    A_dev = torch.empty((M, K), dtype=A.dtype, device=DEV)
+    C_dev = torch.empty((M, N), dtype=A.dtype, device=DEV)
+    size = g.workspace_size(M, K, N, bits, group) if A.dtype == torch.bfloat16 else 0
+    ws = torch.empty(size, dtype=torch.uint8, device=DEV) if size else None
+    stream = torch.cuda.Stream()
+    direct = g.gemm_host(A_host, A_dev, qw, qz, sc, bits=bits, group=group, C_dev=C_dev,
+                         C_host=torch.empty((M, N), dtype=A.dtype).pin_memory(), workspace=ws, stream=stream).clone()
+    call = g.HostGemm(A_host, A_dev, qw, qz, sc, bits=bits, group=group, C_dev=C_dev, C_host=C_host, workspace=ws,
+                      stream=stream)
+    assert call._plan is not None
+    for _ in range(3):
+        C_host.zero_()
+        call()
+        assert torch.equal(C_host.view(torch.int16), direct.view(torch.int16))
+    Cref, B = oracle.gemm(bits16(A), dtype_code(wl), ck["qweight"], ck["qzeros"], ck["scales"], None, N, bits,
+                          group, ck["fmt"])
+    assert_gemm_close(C_host, Cref, B, "captured plan %s" % (case,))
+    call.close()

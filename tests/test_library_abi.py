@@ -31,7 +31,8 @@ def test_exports_every_declared_symbol(lib):
                                "gptq_gemm_perm", "gptq_gemm_perm_workspace_size",
                                "gptq_gemm_perm_noalloc", "gptq_gemm_grouped",
                                "gptq_prepack_interleave", "gptq_gemm_interleaved",
-                               "gptq_gemm_act_order_workspace_size", "gptq_gemm_host"])
+                               "gptq_gemm_act_order_workspace_size", "gptq_gemm_host",
+                               "gptq_host_plan_create", "gptq_host_plan_run", "gptq_host_plan_destroy"])
     for name in declared:
         assert hasattr(lib, name), name
 
@@ -249,6 +250,16 @@ int main(void) {
                      NULL, NULL, NULL, 0, NULL) != GPTQ_OK) return 7;
   if (gptq_gemm_host(NULL, NULL, 1, 0, GPTQ_F16, NULL, NULL, NULL, NULL, 256, 4, 128, GPTQ_FMT_V2,
                      NULL, NULL, NULL, 0, NULL) != GPTQ_ERR_SHAPE) return 8;
+  /* the prepared call: a NULL plan slot or the legacy default stream is refused first */
+  {
+    gptq_host_plan* plan = (gptq_host_plan*)1;
+    if (gptq_host_plan_create(NULL, NULL, NULL, 1, 256, GPTQ_F16, NULL, NULL, NULL, NULL, 256, 4, 128,
+                              GPTQ_FMT_V2, NULL, NULL, NULL, 0, NULL) != GPTQ_ERR_ARG) return 9;
+    if (gptq_host_plan_create(&plan, NULL, NULL, 1, 256, GPTQ_F16, NULL, NULL, NULL, NULL, 256, 4, 128,
+                              GPTQ_FMT_V2, NULL, NULL, NULL, 0, NULL) != GPTQ_ERR_ARG || plan != NULL) return 10;
+    if (gptq_host_plan_run(NULL) != GPTQ_ERR_ARG) return 11;
+    if (gptq_host_plan_destroy(NULL) != GPTQ_OK) return 12;
+  }
   if (strlen(gptq_strerror(GPTQ_ERR_SHAPE)) == 0) return 5;
   printf("c consumer ok\n");
   return 0;
