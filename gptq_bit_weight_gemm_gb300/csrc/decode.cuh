@@ -40,9 +40,11 @@ struct Args {
   void* C;
   unsigned* status;
   // grouped (one weight per expert): rows [offsets[e], offsets[e + 1]) of A and C belong to
-  // expert e (blockIdx.z); `rows` bounds them.  nullptr for a single weight.
+  // expert e of `experts`; `rows` bounds them.  The grid has min(experts, rows) expert slots
+  // (blockIdx.z): slot z takes the z-th expert that holds rows.  nullptr for a single weight.
   const int32_t* offsets;
   int rows;
+  int experts;
   // interleaved weights (gptq_prepack_interleave): k-tiles per 32-column block, else 0 (the
   // checkpoint's own row-major layout, read through the tensor map)
   int il_tiles;

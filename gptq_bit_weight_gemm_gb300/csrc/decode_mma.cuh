@@ -164,6 +164,37 @@ __device__ __forceinline__ bool tma_wait(uint32_t bar, uint32_t parity, volatile
   }
 }
 
+// Grouped launches: the expert of grid slot `slot` -- the slot-th expert (in order) whose rows
+// [offsets[e], offsets[e + 1]) are non-empty and valid (within [0, rows], at most max_m) -- found
+// by each warp on its own, 32 experts per step (a ballot, then the rank-th set bit).  Returns
+// {e or -1, offsets[e], offsets[e + 1], 1 if any expert's range is malformed}.  Kept out of line
+// so that it does not shape the register allocation of the kernel's main loop.
+static __device__ __noinline__ int4 find_expert(const int32_t* offsets, int experts, int rows, int max_m, int slot) {
+  const int lane = threadIdx.x & 31;
+  int e = -1, o0 = 0, o1 = 0, seen = 0;
+  bool bad_any = false;
+  for (int base = 0; base < experts; base += 32) {
+    const int x = base + lane;
+    int b0 = 0, b1 = 0;
+    if (x < experts) {
+      b0 = offsets[x];
+      b1 = offsets[x + 1];
+    }
+    const bool bad = x < experts && (b0 < 0 || b1 < b0 || b1 > rows || b1 - b0 > max_m);
+    const unsigned held = __ballot_sync(0xFFFFFFFFu, x < experts && !bad && b1 > b0);
+    bad_any |= __ballot_sync(0xFFFFFFFFu, bad) != 0u;
+    const int cnt = __popc(held);
+    if (e < 0 && slot < seen + cnt) {
+      const int src = static_cast<int>(__fns(held, 0u, slot - seen + 1));
+      e = base + src;
+      o0 = __shfl_sync(0xFFFFFFFFu, b0, src);
+      o1 = __shfl_sync(0xFFFFFFFFu, b1, src);
+    }
+    seen += cnt;
+  }
+  return make_int4(e, o0, o1, bad_any ? 1 : 0);
+}
+
 template <int BITS, int MT, int MX, typename T, bool FOLD, bool GROUPED = false>
 __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
     k_decode_mma(const __grid_constant__ CUtensorMap tmW, const Args args, const TmaGeo geo) {
@@ -191,21 +222,37 @@ __global__ void __launch_bounds__(kThreads, (MT <= 16 && BITS != 3 ? 5 : 1))
   // a flag-gated launch whose flag says no: every CTA leaves before any barrier or copy
   if (args.run_flag != nullptr && *args.run_flag != args.run_when) return;
   pdl_launch_dependents();
-  // Grouped: expert e = blockIdx.z multiplies rows [offsets[e], offsets[e + 1]) of A into the
-  // same rows of C, with its own scales, zeros and packed rows (e * K * bits / 32 onward in the
-  // stacked weight).  The offsets come from the kernel before this one, so they are read after
-  // griddepcontrol.wait; an expert without rows, the same for every CTA of its cluster, leaves
-  // before any cluster barrier or copy.
+  // Grouped: the expert e of slot blockIdx.z multiplies rows [offsets[e], offsets[e + 1]) of A
+  // into the same rows of C, with its own scales, zeros and packed rows (e * K * bits / 32 onward
+  // in the stacked weight).  The offsets come from the kernel before this one, so they are read
+  // after griddepcontrol.wait; a slot without an expert, the same for every CTA of its cluster,
+  // leaves before any cluster barrier or copy.
   Args ga = args;                                     // the expert's view (grouped only)
   int w_row0 = 0;
   if constexpr (GROUPED) {
     pdl_wait();
-    const int e = static_cast<int>(blockIdx.z);
-    const int o0 = ga.offsets[e], o1 = ga.offsets[e + 1];
-    if (o0 == o1) return;
-    if (o0 < 0 || o1 < o0 || o1 > ga.rows || o1 - o0 > ga.M) {   // ga.M: the caller's max_m (<= MT)
-      if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) atomicOr(ga.status, kStatusExpertRows);
-      return;
+    // With a slot per expert, slot z is expert z (two offsets read; a malformed range is flagged
+    // by its own slot).  With fewer slots than experts (fewer rows than experts), slot z takes the
+    // z-th expert that holds rows: every expert's range is read, and a malformed one (ga.M: the
+    // caller's max_m, <= MT) holds none and is flagged by the grid's first CTA.
+    int e, o0, o1;
+    if (static_cast<int>(gridDim.z) == ga.experts) {
+      e = static_cast<int>(blockIdx.z);
+      o0 = ga.offsets[e];
+      o1 = ga.offsets[e + 1];
+      if (o0 == o1) return;
+      if (o0 < 0 || o1 < o0 || o1 > ga.rows || o1 - o0 > ga.M) {
+        if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) atomicOr(ga.status, kStatusExpertRows);
+        return;
+      }
+    } else {
+      const int4 f = find_expert(ga.offsets, ga.experts, ga.rows, ga.M, static_cast<int>(blockIdx.z));
+      if (f.w && threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0)
+        atomicOr(ga.status, kStatusExpertRows);
+      e = f.x;
+      o0 = f.y;
+      o1 = f.z;
+      if (e < 0) return;                               // fewer experts hold rows than slots
     }
     ga.M = o1 - o0;
     ga.A = static_cast<const uint16_t*>(ga.A) + static_cast<long long>(o0) * ga.K;
@@ -955,11 +1002,14 @@ cudaError_t launch_mma(const Problem& p, cudaStream_t stream) {
   a.C = p.out; a.status = p.status;
   a.offsets = GROUPED ? p.offsets : nullptr;
   a.rows = p.rows;
+  a.experts = GROUPED ? p.E : 0;
   a.il_tiles = p.interleaved ? a.units / 4 : 0;
   a.run_flag = p.run_flag;
   a.run_when = p.run_when;
   const int E = GROUPED ? p.E : 1;                     // weights side by side
-  const int Z = GROUPED ? p.E : (p.tok_split > 1 ? p.tok_split : 1);   // grid z: experts or token blocks
+  // grid z: expert slots (no more than the rows, each of which belongs to one expert) or token blocks
+  const int Z = GROUPED ? (p.E < p.rows ? p.E : p.rows) : (p.tok_split > 1 ? p.tok_split : 1);
+  if (Z <= 0) return cudaSuccess;
   Problem pz = p;                                      // the geometry of one token block
   if (!GROUPED && Z > 1) pz.M = MT;
   const int slabs = (p.N + kSlab - 1) / kSlab;

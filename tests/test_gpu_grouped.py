@@ -149,6 +149,22 @@ def test_grouped_flags_bad_ranges(offsets, rows, bad):
         assert np.all(bits16(C)[lo:min(hi, rows)] == SENTINEL[torch.float16])
 
 
+def test_grouped_flags_bad_ranges_with_fewer_rows_than_experts():
+    """Fewer rows than experts: the grid then holds one slot per row, and slot z takes the z-th
+    expert that holds rows.  Malformed ranges (expert 2 ends past the rows, expert 3 decreases)
+    are skipped and flagged; the one valid expert is computed and the other rows keep the
+    sentinel."""
+    E, rows = 6, 3
+    mw = _case(E, 512, 256, 4, 128, "f16")
+    offsets = np.array([0, 1, 1, 5, 3, 3, 3], np.int32)
+    A = gptq_inputs.draw_token_activations(mw, rows)
+    ck = _experts(mw, "v2")
+    assert g.device_status() == 0
+    C = _gpu(mw, "v2", A, offsets, 2, ck)
+    assert g.device_status() & g.DEV_EXPERT_ROWS
+    _compare(mw, "v2", A, np.array([0, 1, 1, 1, 1, 1, 1], np.int32), C, ck)
+
+
 @pytest.mark.parametrize("T", MOE.Ts)
 def test_grouped_full_size(T):
     """The Mixtral-shaped expert layer at full size: 8 experts x [4096, 14336], 4-bit g128,
