@@ -227,7 +227,9 @@ size_t gptq_gemm_perm_workspace_size(int M, int K);
  * MoE models quantize every expert's weights, and vLLM runs them through a fused MoE path.  The
  * pages fix no layout; the one here is the plainest: the rows of A are already grouped by expert
  * (the caller gathers and orders them), and every expert has the same K, N, bits and group.
- * One launch covers all experts (one decode kernel, the expert as the third grid dimension).
+ * One launch covers all experts (one decode kernel with min(E, rows) expert slots as its third
+ * grid dimension: no more experts than rows can hold rows, and each slot takes the next expert
+ * that does).
  * Device pointers:
  *   A        [rows, K] fp16/bf16 (a_dtype), 16-byte aligned;
  *   offsets  [E + 1] int32, nondecreasing, offsets[0] = 0, offsets[E] <= rows, 4-byte aligned;
