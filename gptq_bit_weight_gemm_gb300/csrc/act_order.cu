@@ -113,21 +113,25 @@ __global__ void __launch_bounds__(kSortThreads) k_sort_groups(const int32_t* __r
     return;
   }
   constexpr int kSteps = 8;
-  const int nbits = 32 - __clz(G + 31);        // keys below G + 32
+  const int nbits = 32 - __clz(G - 1);         // keys below G (no bit at all when G == 1)
   for (int k0 = k_lo; k0 < k_hi; k0 += 32 * kSteps) {
     int g[kSteps];
     unsigned peers[kSteps];
     uint32_t old[kSteps];
+    bool in[kSteps];
 #pragma unroll
     for (int i = 0; i < kSteps; ++i) {
       const int k = k0 + 32 * i + lane;
-      g[i] = k < k_hi ? static_cast<int>(keys[k]) : G + lane;   // lanes past the chunk: unique keys
-      peers[i] = 0xFFFFFFFFu;
+      in[i] = k < k_hi;
+      g[i] = in[i] ? static_cast<int>(keys[k]) : 0;
+      peers[i] = __ballot_sync(0xFFFFFFFFu, in[i]);   // lanes past the chunk match no lane
     }
-    // lanes with equal keys: one ballot per key bit (eight independent steps side by side)
+    // lanes with equal keys: one ballot per key bit (up to eight independent steps side by side;
+    // a step past the chunk, the same for the whole warp, takes no ballot)
     for (int b = 0; b < nbits; ++b) {
 #pragma unroll
       for (int i = 0; i < kSteps; ++i) {
+        if (k0 + 32 * i >= k_hi) continue;
         const bool v = (g[i] >> b) & 1;
         const unsigned bal = __ballot_sync(0xFFFFFFFFu, v);
         peers[i] &= v ? bal : ~bal;
@@ -136,12 +140,12 @@ __global__ void __launch_bounds__(kSortThreads) k_sort_groups(const int32_t* __r
 #pragma unroll
     for (int i = 0; i < kSteps; ++i) {
       old[i] = 0u;
-      if (g[i] < G && lane == __ffs(peers[i]) - 1) old[i] = atomicAdd(&h[g[i]], static_cast<uint32_t>(__popc(peers[i])));
+      if (in[i] && lane == __ffs(peers[i]) - 1) old[i] = atomicAdd(&h[g[i]], static_cast<uint32_t>(__popc(peers[i])));
     }
 #pragma unroll
     for (int i = 0; i < kSteps; ++i) {
-      const uint32_t slot = __shfl_sync(0xFFFFFFFFu, old[i], __ffs(peers[i]) - 1);
-      if (g[i] < G) {
+      const uint32_t slot = __shfl_sync(0xFFFFFFFFu, old[i], in[i] ? __ffs(peers[i]) - 1 : lane);
+      if (in[i]) {
         const int k = k0 + 32 * i + lane;
         const int dst = g[i] * group + static_cast<int>(slot) + __popc(peers[i] & ((1u << lane) - 1u));
         if (staged) {
@@ -173,8 +177,9 @@ __global__ void __launch_bounds__(kSortThreads) k_sort_groups(const int32_t* __r
 // packed column in shared memory (asynchronous 16-byte copies of each row segment, all in flight
 // at once, plus one zero row so that a 3-bit code's two-word read never leaves the strip).  Each
 // thread then assembles one output unit for four adjacent columns: per code one table entry (the
-// same for every column: src from the sort), one 16-byte shared-memory read (two for 3-bit) and
-// per column a shift (a funnel shift for 3-bit) and an or.  Eight threads cover a 32-column row
+// same for every column: src from the sort), one 16-byte shared-memory read and per column a
+// rotation and an and-or (a 3-bit code at bit 30 or 31 also reads the next word: a funnel shift
+// takes it out and a rotation places it).  Eight threads cover a 32-column row
 // segment, so each warp's 16-byte writes form 128-byte segments.  The copies are issued before
 // griddepcontrol.wait (they read the checkpoint, not the sort's output); the rest runs only when
 // the sort accepted g_idx (flag 1).
@@ -226,18 +231,34 @@ __global__ void __launch_bounds__(256) k_repack_rows(const uint32_t* __restrict_
       const uint32_t sh = e & 31u;
       const uint32_t* wp = strip + (e >> 5) * sw + c4;
       const uint4 lo = *reinterpret_cast<const uint4*>(wp);
-      uint4 hi = lo;
-      if constexpr (BITS == 3) hi = *reinterpret_cast<const uint4*>(wp + sw);
       const int ob = BITS * j;                             // a constant once unrolled
+      if constexpr (BITS == 3) {
+        // rot: the code at bit ow of its output word, its bits past bit 31 wrapped to bits 0..
+        // Only a code at bit 30 or 31 runs into the next word (2 of a unit's 32): that word is
+        // read just then, so the strip is read about once per code instead of twice.
+        const uint32_t ow = static_cast<uint32_t>(ob & 31);
+        uint32_t rot[4];
+        if (sh <= 29u) {
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        if constexpr (BITS == 3) {
-          const uint32_t code = __funnelshift_r((&lo.x)[cc], (&hi.x)[cc], sh) & 7u;
-          acc[cc][ob >> 5] |= code << (ob & 31);
-          if ((ob & 31) + BITS > 32) acc[cc][(ob >> 5) + 1] |= code >> (32 - (ob & 31));
+          for (int cc = 0; cc < 4; ++cc) rot[cc] = __funnelshift_r((&lo.x)[cc], (&lo.x)[cc], sh - ow);
         } else {
-          // a rotation by (sh - ob) mod 32 moves the code from bit sh to bit ob (2/4/8-bit codes
-          // never straddle a word), and one and-or places it: two instructions per code
+          const uint4 hi = *reinterpret_cast<const uint4*>(wp + sw);
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            const uint32_t code = __funnelshift_r((&lo.x)[cc], (&hi.x)[cc], sh) & 7u;
+            rot[cc] = __funnelshift_l(code, code, ow);
+          }
+        }
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          acc[cc][ob >> 5] |= rot[cc] & (7u << ow);
+          if (ow + BITS > 32) acc[cc][(ob >> 5) + 1] |= rot[cc] & (7u >> (32 - ow));
+        }
+      } else {
+        // a rotation by (sh - ob) mod 32 moves the code from bit sh to bit ob (2/4/8-bit codes
+        // never straddle a word), and one and-or places it: two instructions per code
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
           const uint32_t w = (&lo.x)[cc];
           acc[cc][0] |= __funnelshift_r(w, w, e - static_cast<uint32_t>(ob)) & (P::kMask << ob);
         }

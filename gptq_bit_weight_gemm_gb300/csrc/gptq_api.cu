@@ -216,8 +216,12 @@ bool act_order_shape_ok(int K, int G, int group, int bits) {
 // gptq_gemm with g_idx through sorted rows.  Launches, in stream order: the sort (perm, flag), the
 // repack (flag 1 only), the group-wise GEMM on the sorted weight with A gathered through perm
 // (flag 1 only), and the per-row-group GEMM on the original checkpoint (flag 0 only: g_idx with an
-// entry out of range, or groups of unequal size).  The flag-gated kernels start only after their
-// predecessor has completed (no programmatic dependent launch): they read what it wrote.
+// entry out of range, or groups of unequal size).  The repack and the group-wise GEMM start only
+// after their predecessor has completed (no programmatic dependent launch): they read what it
+// wrote.  The per-row decode reads nothing the group-wise GEMM writes, and the flag is final once
+// that GEMM has started (the sort had completed before the repack finished), so it is a
+// programmatic dependent: with flag 1 its CTAs leave as slots free at the group-wise GEMM's tail
+// instead of costing a launch after it.
 int gemm_act_order(const Problem& p, cudaStream_t s) {
   const ActOrderLayout l = act_order_layout(p.M, p.K, p.N, p.bits);
   unsigned char* ws = static_cast<unsigned char*>(p.workspace);
@@ -267,7 +271,9 @@ int gemm_act_order(const Problem& p, cudaStream_t s) {
   f.workspace = rest;
   f.workspace_bytes = rest_bytes;
   if (p.M <= kDecodeMaxM) {
-    e = launch_decode(f, s);
+    Problem fd = f;
+    fd.no_pdl = false;
+    e = launch_decode(fd, s);
     if (e != cudaErrorInvalidConfiguration) return from_cuda(e);
   }
   return from_cuda(launch_prefill(f, s));
