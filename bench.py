@@ -458,6 +458,9 @@ def time_gemm(g, torch, dev, stream, wl, M, l2, path="gemm", fmt=None, reps=200)
     S = max(1, min(256, int(np.ceil(3 * l2 / per_set))))
     sets = [(qw.clone(), qz.clone(), sc.clone(), None if A is None else A.clone(),
              torch.empty(out_shape, dtype=out_dt, device=dev)) for _ in range(S)]
+    # the copies ran on the current stream; the launches go to `stream`, which (a PyTorch pool
+    # stream) does not wait for it
+    torch.cuda.synchronize()
     n = S * max(1, reps // S) if (M <= 64 and path != "dequant") else S * max(1, 8 // S)
 
     def launch(i):
@@ -477,6 +480,33 @@ def time_gemm(g, torch, dev, stream, wl, M, l2, path="gemm", fmt=None, reps=200)
 
     gr = capture(torch, stream, launch, n)
     ms, ms_min, ms_max = replay_median(torch, stream, gr, n)
+    del sets, gr
+    return ms, nbytes, S
+
+
+def time_device_prepack(g, torch, dev, stream, wl, l2, reps=64):
+    """Median per-call time of gptq_prepack_act_order_device (sort, repack, ordering kernel) on an
+    act-order workload, a CUDA graph of calls over rotating copies of qweight and g_idx.  Bytes:
+    qweight and g_idx read, the sorted qweight and perm written."""
+    import ctypes
+    draw, qw, qz, sc, gi = _checkpoint(g, torch, dev, wl)
+    nbytes = 2 * qw.numel() * 4 + 2 * wl.K * 4
+    S = max(1, min(256, int(np.ceil(3 * l2 / nbytes))))
+    wsb = g.prepack_act_order_device_workspace_size(wl.K, wl.bits, wl.group)
+    sets = [(qw.clone(), gi.clone(), torch.empty_like(qw), torch.empty(wl.K, dtype=torch.int32, device=dev),
+             torch.empty(wsb, dtype=torch.uint8, device=dev)) for _ in range(S)]
+    torch.cuda.synchronize()                   # the copies ran on another stream than the calls
+    n = S * max(1, reps // S)
+    p = lambda t: ctypes.c_void_p(t.data_ptr())
+
+    def launch(i):
+        q, gix, out, perm, ws = sets[i % S]
+        rc = g.lib().gptq_prepack_act_order_device(p(q), p(gix), wl.K, wl.N, wl.bits, wl.group, p(out), p(perm),
+                                                   p(ws), wsb, ctypes.c_void_p(stream.cuda_stream))
+        assert rc == 0, g.strerror(rc)
+
+    gr = capture(torch, stream, launch, n)
+    ms, _, _ = replay_median(torch, stream, gr, n)
     del sets, gr
     return ms, nbytes, S
 
@@ -503,6 +533,8 @@ def run_configs(g, torch, dev, stream, peaks, l2, only=""):
         ("4", "act_order_3bit_g128", 4096, "gemm", "4096 tokens, rows sorted by group on the device"),
         ("4", "act_order_3bit_g128", 16, "perm", "rows sorted on the host, gptq_gemm_perm"),
         ("4", "act_order_3bit_g128", 16, "il", "rows sorted, then interleaved, gptq_gemm_interleaved"),
+        ("4", "act_order_3bit_g128", 0, "devprep", "gptq_prepack_act_order_device: rows sorted on the device "
+                                                   "once per weight (qweight and g_idx read, sorted copy and perm written)"),
         ("5", "prefill_4bit_g128", 4096, "gemm", ""),
         ("5", "prefill_8bit_sym_g128", 4096, "gemm", ""),
         ("5", "prefill_4bit_gall", 4096, "gemm", ""),
@@ -514,15 +546,19 @@ def run_configs(g, torch, dev, stream, peaks, l2, only=""):
         if only and only not in name:
             continue
         wl = W[name]
-        ms, nbytes, S = time_gemm(g, torch, dev, stream, wl, M, l2, path=path)
+        if path == "devprep":
+            ms, nbytes, S = time_device_prepack(g, torch, dev, stream, wl, l2)
+        else:
+            ms, nbytes, S = time_gemm(g, torch, dev, stream, wl, M, l2, path=path)
         row = {"config": cfg, "workload": name, "M": M, "path": {"gemm": "gptq_gemm", "perm": "gptq_gemm_perm",
                                                                  "rows": "gptq_gemm (per-row groups)",
                                                                  "il": "gptq_gemm_interleaved",
-                                                                 "dequant": "gptq_dequant"}[path],
+                                                                 "dequant": "gptq_dequant",
+                                                                 "devprep": "gptq_prepack_act_order_device"}[path],
                "us": round(ms * 1e3, 3)}
         if label:
             row["note"] = label
-        if path != "dequant" and M > g.DECODE_MAX_M:
+        if path not in ("dequant", "devprep") and M > g.DECODE_MAX_M:
             tflops = 2.0 * M * wl.N * wl.K / (ms * 1e-3) / 1e12
             key = {"prefill_4bit_g128": "prefill_4bit"}.get(name)
             row.update(value=round(tflops, 2), unit="TFLOP/s",
@@ -575,6 +611,7 @@ def time_grouped(g, torch, dev, stream, mw, T, l2, reps=200):
     sets = [(qw.clone(), qz.clone(), sc.clone(), torch.empty((A.shape[0], mw.N), dtype=A.dtype, device=dev))
             for _ in range(S)]
     del qw, qz, sc
+    torch.cuda.synchronize()                   # the copies ran on another stream than the calls
     n = max(S, (reps // S) * S)
 
     def launch(i):

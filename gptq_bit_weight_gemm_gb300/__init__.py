@@ -13,6 +13,7 @@ Operations (page "增强 vLLM 对 GPTQv2 格式的支持：分析与实现", sec
   quantize_rtn(W, bits, group, g_idx, sym, fmt)              -> (qweight, qzeros, scales)
   repack_zeros_v1_to_v2(qzeros_v1, N, bits)                  (host memory)
   prepack_act_order(qweight, g_idx, K, N, bits, group)      (host memory) -> (qweight', perm)
+  prepack_act_order_device(qweight, g_idx, K, N, bits, group) (device memory) -> (qweight', perm)
   gemm_perm(A, perm, qweight', qzeros, scales, bits, group) -> A[:, perm] @ dequant(W'), M <= 32
   prepack_interleave(qweight, K, N, bits)                    (host memory) -> qweight in the decode
                                                              kernel's interleaved layout
@@ -33,7 +34,7 @@ HEADER = os.path.join(os.path.dirname(HERE), "include", "gptq.h")
 
 F16, BF16 = 0, 1
 V1, V2 = 1, 2
-DEV_TIMEOUT, DEV_GIDX_RANGE, DEV_SCALE_OVERFLOW, DEV_EXPERT_ROWS = 0x1, 0x2, 0x4, 0x8
+DEV_TIMEOUT, DEV_GIDX_RANGE, DEV_SCALE_OVERFLOW, DEV_EXPERT_ROWS, DEV_GIDX_GROUPS = 0x1, 0x2, 0x4, 0x8, 0x10
 DECODE_MAX_M = 32
 
 _STATUS = {0: "GPTQ_OK", -1: "GPTQ_ERR_ARG", -2: "GPTQ_ERR_SHAPE", -3: "GPTQ_ERR_ALIGN",
@@ -71,6 +72,8 @@ _SIGNATURES = {
     "gptq_strerror": (ctypes.c_char_p, [_I]),
     "gptq_selftest_wait_timeout": (_I, [ctypes.c_ulonglong, _P, _P]),
     "gptq_prepack_act_order": (_I, [_P, _P, _I, _I, _I, _I, _P, _P]),
+    "gptq_prepack_act_order_device": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _SZ, _P]),
+    "gptq_prepack_act_order_device_workspace_size": (_SZ, [_I, _I, _I]),
     "gptq_gemm_perm": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P]),
     "gptq_gemm_perm_workspace_size": (_SZ, [_I, _I]),
     "gptq_gemm_perm_noalloc": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
@@ -323,6 +326,31 @@ def prepack_act_order(qweight, g_idx, *, K, N, bits, group):
     rc = lib().gptq_prepack_act_order(qw.ctypes.data_as(_P), gi.ctypes.data_as(_P), K, N, bits, group,
                                       out.ctypes.data_as(_P), perm.ctypes.data_as(_P))
     _check(rc, "gptq_prepack_act_order")
+    return out, perm
+
+
+def prepack_act_order_device_workspace_size(K, bits, group):
+    return int(lib().gptq_prepack_act_order_device_workspace_size(K, bits, group))
+
+
+def prepack_act_order_device(qweight, g_idx, *, K, N, bits, group, workspace=None, stream=None):
+    """Device: sort an act-order checkpoint's rows by group on `stream` (asynchronous).  qweight
+    (int32 [K*bits/32, N]) and g_idx (int32 [K]) on the device -> (qweight_out, perm) on the
+    device, bit-identical to prepack_act_order.  A g_idx whose groups are not all of `group` rows
+    leaves both unwritten and sets DEV_GIDX_GROUPS in the device status word."""
+    torch = _torch()
+    ws_bytes = prepack_act_order_device_workspace_size(K, bits, group)
+    if ws_bytes == 0:
+        raise GPTQError(-2, "gptq_prepack_act_order_device")
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=qweight.device)
+    out = torch.empty_like(qweight)
+    perm = torch.empty(K, dtype=torch.int32, device=qweight.device)
+    rc = lib().gptq_prepack_act_order_device(_ptr(qweight, torch.int32, "qweight"), _ptr(g_idx, torch.int32, "g_idx"),
+                                             K, N, bits, group, _ptr(out, torch.int32, "qweight_out"),
+                                             _ptr(perm, torch.int32, "perm"), _ptr(workspace, name="workspace"),
+                                             workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "gptq_prepack_act_order_device")
     return out, perm
 
 

@@ -22,6 +22,8 @@ namespace gptq {
 namespace {
 
 constexpr int kSortThreads = 1024;   // one CTA: 32 warps, each owning a contiguous K/32 rows
+// status bit GPTQ_DEV_GIDX_GROUPS: the stand-alone device prepack found g_idx it cannot sort
+constexpr unsigned kStatusGidxGroups = 0x10u;
 
 // Where sorted row k' finds its code in a column: the packed word (row of qweight) and the bit
 // offset of the code of original row k inside it (LSB-first; a 3-bit code may run into the next
@@ -182,11 +184,12 @@ __global__ void __launch_bounds__(kSortThreads) k_sort_groups(const int32_t* __r
 // takes it out and a rotation places it).  Eight threads cover a 32-column row
 // segment, so each warp's 16-byte writes form 128-byte segments.  The copies are issued before
 // griddepcontrol.wait (they read the checkpoint, not the sort's output); the rest runs only when
-// the sort accepted g_idx (flag 1).
+// the sort accepted g_idx (flag 1).  status (nullable): with flag 0 the first CTA raises
+// kStatusGidxGroups there (the stand-alone prepack, which has no other path to take).
 template <int BITS>
 __global__ void __launch_bounds__(256) k_repack_rows(const uint32_t* __restrict__ qw,
                                                      const uint32_t* src, const int* flag, int K, int N,
-                                                     int sw, uint32_t* __restrict__ out) {
+                                                     int sw, uint32_t* __restrict__ out, unsigned* status) {
   using P = Pack<BITS>;
   constexpr int PER = P::kPerUnit;
   constexpr int ROWS = P::kRowsPerUnit;
@@ -208,7 +211,10 @@ __global__ void __launch_bounds__(256) k_repack_rows(const uint32_t* __restrict_
   // are plain (not restrict-qualified) pointers so that no load of them moves above the wait
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("cp.async.wait_all;" ::: "memory");   // own copies land before any exit
-  if (*static_cast<const volatile int*>(flag) != 1) return;
+  if (*static_cast<const volatile int*>(flag) != 1) {
+    if (status != nullptr && blockIdx.x == 0 && threadIdx.x == 0) atomicOr(status, kStatusGidxGroups);
+    return;
+  }
   __syncthreads();
   const int c4 = 4 * (threadIdx.x % vec);
   const int lanes = blockDim.x / vec;
@@ -336,7 +342,7 @@ cudaError_t launch_sort_bits(const int32_t* g_idx, int K, int G, int group, int3
 
 template <int BITS>
 cudaError_t launch_repack_bits(const int32_t* qweight, const uint32_t* src, const int* flag, int K, int N,
-                               int32_t* out, cudaStream_t stream) {
+                               int32_t* out, unsigned* status, cudaStream_t stream) {
   static std::atomic<unsigned long long> smem_set{0};
   const int sw = repack_strip_width(K, BITS);
   if (sw == 0) return cudaErrorInvalidValue;
@@ -354,7 +360,7 @@ cudaError_t launch_repack_bits(const int32_t* qweight, const uint32_t* src, cons
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, k_repack_rows<BITS>, reinterpret_cast<const uint32_t*>(qweight), src, flag, K,
-                            N, sw, reinterpret_cast<uint32_t*>(out));
+                            N, sw, reinterpret_cast<uint32_t*>(out), status);
 }
 
 }  // namespace
@@ -383,12 +389,12 @@ cudaError_t launch_sort_groups(const int32_t* g_idx, int K, int G, int group, in
 }
 
 cudaError_t launch_repack_rows(const int32_t* qweight, const uint32_t* src, const int* flag, int K, int N,
-                               int bits, int32_t* out, cudaStream_t stream) {
+                               int bits, int32_t* out, unsigned* status, cudaStream_t stream) {
   switch (bits) {
-    case 2: return launch_repack_bits<2>(qweight, src, flag, K, N, out, stream);
-    case 3: return launch_repack_bits<3>(qweight, src, flag, K, N, out, stream);
-    case 4: return launch_repack_bits<4>(qweight, src, flag, K, N, out, stream);
-    case 8: return launch_repack_bits<8>(qweight, src, flag, K, N, out, stream);
+    case 2: return launch_repack_bits<2>(qweight, src, flag, K, N, out, status, stream);
+    case 3: return launch_repack_bits<3>(qweight, src, flag, K, N, out, status, stream);
+    case 4: return launch_repack_bits<4>(qweight, src, flag, K, N, out, status, stream);
+    case 8: return launch_repack_bits<8>(qweight, src, flag, K, N, out, status, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -233,7 +233,7 @@ int gemm_act_order(const Problem& p, cudaStream_t s) {
   const size_t rest_bytes = l.total - l.rest;
   cudaError_t e = launch_sort_groups(p.g_idx, p.K, p.G, p.group, p.bits, perm, src, flag, s);
   if (e != cudaSuccess) return from_cuda(e);
-  e = launch_repack_rows(p.qweight, src, flag, p.K, p.N, p.bits, qw_sorted, s);
+  e = launch_repack_rows(p.qweight, src, flag, p.K, p.N, p.bits, qw_sorted, nullptr, s);
   if (e != cudaSuccess) return from_cuda(e);
 
   Problem q = p;
@@ -754,6 +754,45 @@ extern "C" int gptq_prepack_act_order(const int32_t* qweight, const int32_t* g_i
   for (size_t i = 0; i < out.size(); ++i) qweight_out[i] = static_cast<int32_t>(out[i]);
   for (int k = 0; k < K; ++k) perm[k] = order[k];
   return GPTQ_OK;
+}
+
+// The device prepack's workspace: the sort's flag (256 bytes), then each sorted row's code
+// position (K words, rounded up to 256 bytes).
+extern "C" size_t gptq_prepack_act_order_device_workspace_size(int K, int bits, int group) {
+  if (K <= 0 || K % 32 || group <= 0 || K % group || !gptq::bits_ok(bits)) return 0;
+  if (!gptq::sort_groups_fits(K, K / group, group) || gptq::repack_strip_width(K, bits) == 0) return 0;
+  return 256 + ((static_cast<size_t>(K) * 4 + 255) & ~static_cast<size_t>(255));
+}
+
+// gptq_prepack_act_order on the device: the same kernels gptq_gemm's act-order path runs per
+// call (the stable sort, then the repack, which writes only when every group holds `group` rows
+// and otherwise raises GPTQ_DEV_GIDX_GROUPS), then the ordering kernel, so that a GEMM issued
+// right after may read qweight_out before its own dependency wait.
+extern "C" int gptq_prepack_act_order_device(const int32_t* qweight, const int32_t* g_idx, int K, int N,
+                                             int bits, int group, int32_t* qweight_out, int32_t* perm,
+                                             void* workspace, size_t workspace_bytes, void* stream) {
+  if (!gptq::bits_ok(bits) || !qweight || !g_idx || !qweight_out || !perm || !workspace) return GPTQ_ERR_ARG;
+  if (K <= 0 || N <= 0 || K % 32 || N % 32 || group <= 0 || K % group) return GPTQ_ERR_SHAPE;
+  const size_t need = gptq_prepack_act_order_device_workspace_size(K, bits, group);
+  if (need == 0) return GPTQ_ERR_SHAPE;
+  if (workspace_bytes < need) return GPTQ_ERR_WORKSPACE;
+  if (!gptq::aligned(qweight, 16) || !gptq::aligned(qweight_out, 16) || !gptq::aligned(perm, 16) ||
+      !gptq::aligned(workspace, 16) || !gptq::aligned(g_idx, 4))
+    return GPTQ_ERR_ALIGN;
+  const uintptr_t in0 = reinterpret_cast<uintptr_t>(qweight), out0 = reinterpret_cast<uintptr_t>(qweight_out);
+  const uintptr_t bytes = static_cast<uintptr_t>(K) / 32 * bits * static_cast<uintptr_t>(N) * 4;
+  if (in0 < out0 + bytes && out0 < in0 + bytes) return GPTQ_ERR_ARG;   // the copy must not overlap
+  gptq::Problem p;
+  const int rc = gptq::device_ready(&p);
+  if (rc) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  int* flag = reinterpret_cast<int*>(ws);
+  uint32_t* src = reinterpret_cast<uint32_t*>(ws + 256);
+  cudaError_t e = gptq::launch_sort_groups(g_idx, K, K / group, group, bits, perm, src, flag, s);
+  if (e == cudaSuccess) e = gptq::launch_repack_rows(qweight, src, flag, K, N, bits, qweight_out, p.status, s);
+  if (e == cudaSuccess) e = gptq::launch_writer_fence(s);
+  return gptq::from_cuda(e);
 }
 
 extern "C" int gptq_quantize_rtn(const float* W, int K, int N, int bits, int group,

@@ -66,16 +66,17 @@ cudaError_t launch_gather_cols(const void* A, const int32_t* perm, int M, int K,
                                cudaStream_t stream);
 // Act-order on the device: the stable sort of the rows by g_idx (perm; src, the packed word and
 // bit offset of each sorted row's code; flag = 1 when every group holds exactly `group` rows,
-// else 0) and the packed weight rewritten in that order (only when the flag is 1).  Shared
-// memory per CTA is at most kMaxActOrderSmem; sort_groups_fits and repack_strip_width (0: no
-// strip fits) say whether a shape qualifies.
+// else 0) and the packed weight rewritten in that order (only when the flag is 1; with flag 0 and
+// a non-null status the repack raises kStatusGidxGroups there).  Shared memory per CTA is at most
+// kMaxActOrderSmem; sort_groups_fits and repack_strip_width (0: no strip fits) say whether a
+// shape qualifies.
 constexpr size_t kMaxActOrderSmem = 200 * 1024;
 bool sort_groups_fits(int K, int G, int group);
 int repack_strip_width(int K, int bits);
 cudaError_t launch_sort_groups(const int32_t* g_idx, int K, int G, int group, int bits, int32_t* perm,
                                uint32_t* src, int* flag, cudaStream_t stream);
 cudaError_t launch_repack_rows(const int32_t* qweight, const uint32_t* src, const int* flag, int K, int N,
-                               int bits, int32_t* out, cudaStream_t stream);
+                               int bits, int32_t* out, unsigned* status, cudaStream_t stream);
 cudaError_t launch_wait_selftest(unsigned* status, uint64_t limit_ns, int* flag, cudaStream_t stream);
 
 struct QuantProblem {
@@ -89,6 +90,9 @@ struct QuantProblem {
   unsigned* status;
 };
 cudaError_t launch_quantize(const QuantProblem& q, cudaStream_t stream);
+// An empty kernel launched without programmatic dependent launch: after it, a GEMM kernel that
+// reads the checkpoint before its dependency wait sees everything the kernels before it wrote.
+cudaError_t launch_writer_fence(cudaStream_t stream);
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link); false if
 // the driver refuses the map.  `dtype` is a CUtensorMapDataType, `swizzle` a CUtensorMapSwizzle.

@@ -185,8 +185,8 @@ __global__ void __launch_bounds__(kThreads) k_zeros_to_v1(int32_t* qzeros, long 
 // Launched after the writer kernels, without programmatic dependent launch, so it starts only
 // when they have completed and their stores are visible.  The GEMM kernels read the checkpoint
 // before their own dependency wait (they may start while the kernel before them runs); with
-// this kernel in between, a GEMM issued right after gptq_quantize_rtn overlaps only this empty
-// kernel, never the writers.
+// this kernel in between, a GEMM issued right after gptq_quantize_rtn (or after the device
+// prepack, which ends with it too) overlaps only this empty kernel, never the writers.
 __global__ void k_writer_fence() {}
 
 int grid_for(long long work) {
@@ -230,6 +230,11 @@ cudaError_t launch_quantize(const QuantProblem& q, cudaStream_t stream) {
     case 8: return launch_bits<8>(q, stream);
     default: return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t launch_writer_fence(cudaStream_t stream) {
+  k_writer_fence<<<1, 32, 0, stream>>>();
+  return cudaGetLastError();
 }
 
 }  // namespace gptq

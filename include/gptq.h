@@ -87,6 +87,9 @@ typedef enum {
 #define GPTQ_DEV_EXPERT_ROWS 0x8u /* gptq_gemm_grouped: an expert's row range was decreasing,
                                      outside [0, rows] or longer than max_m; its rows of C
                                      were not written                                        */
+#define GPTQ_DEV_GIDX_GROUPS 0x10u /* gptq_prepack_act_order_device: g_idx had an entry outside
+                                     [0, K/group) or a group not of exactly `group` rows;
+                                     qweight_out and perm were not written                   */
 
 /*
  * gptq_dequant -- write the dequantized weights W[k][n] = RN((q - zero) * scale).
@@ -195,6 +198,33 @@ int gptq_host_plan_destroy(gptq_host_plan* plan);
  */
 int gptq_prepack_act_order(const int32_t* qweight, const int32_t* g_idx, int K, int N, int bits,
                            int group, int32_t* qweight_out, int32_t* perm);
+
+/*
+ * gptq_prepack_act_order_device -- gptq_prepack_act_order for a checkpoint already in device
+ * memory, asynchronously on `stream` (page section "LLM 的权重量化": the groups are the row sets
+ * {k : g_idx[k] == g}).  It runs the stable sort and the repack that gptq_gemm's act-order path
+ * runs on every call, once: a model's load step, after which gptq_gemm_perm multiplies the
+ * sorted copy on every call.  perm and qweight_out are bit-identical to the host function's.
+ * Device pointers: qweight [K*bits/32, N], g_idx [K], qweight_out (same size as qweight, must not
+ * overlap it), perm [K], workspace (at least gptq_prepack_act_order_device_workspace_size(K, bits,
+ * group) bytes, caller-owned, overwritten).  Alignment: 16 bytes for qweight, qweight_out, perm
+ * and workspace; 4 for g_idx.
+ * Returns GPTQ_OK or a negative gptq_status (GPTQ_ERR_SHAPE where the workspace size is 0,
+ * GPTQ_ERR_WORKSPACE, GPTQ_ERR_ARG for overlapping weights); nothing is launched then.  A g_idx
+ * with an entry outside [0, K/group), or a group that does not hold exactly `group` rows, is found
+ * on the device: qweight_out and perm are left unwritten and GPTQ_DEV_GIDX_GROUPS is set in the
+ * device status word.  The call ends with an ordering step, so a GEMM may use qweight_out and
+ * perm as the very next call on the stream.
+ */
+int gptq_prepack_act_order_device(const int32_t* qweight, const int32_t* g_idx, int K, int N, int bits,
+                                  int group, int32_t* qweight_out, int32_t* perm, void* workspace,
+                                  size_t workspace_bytes, void* stream);
+
+/* Bytes of device workspace gptq_prepack_act_order_device needs: 256 + K * 4 rounded up to 256.
+ * 0 when the device sort does not take the shape (bits not 2/3/4/8, K not a multiple of 32 or of
+ * group, G * 128 + K * 2 above 200 KB, a group of more than 65535 rows, or a packed column of
+ * more than 200 KB in 4-column strips); the host function remains for those. */
+size_t gptq_prepack_act_order_device_workspace_size(int K, int bits, int group);
 
 /*
  * gptq_gemm_perm -- C[M, N] = A[:, perm] @ W[K, N] for a checkpoint prepacked by

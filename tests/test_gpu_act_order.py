@@ -11,7 +11,12 @@ sends g_idx whose groups are not all of `group` rows to the per-row-group kernel
     and bf16, v1 and v2;
   * g_idx with unequal groups (flag 0: the per-row-group kernels run, in the same stream order),
     and with an entry out of range (clamped and flagged, as without the workspace);
-  * repeated calls give identical bits."""
+  * repeated calls give identical bits;
+  * gptq_prepack_act_order_device (the same sort and repack, once, into caller buffers) equals the
+    host prepack bit for bit, a gptq_gemm_perm issued right after it on the stream meets the
+    oracle, and g_idx it cannot sort leaves its outputs unwritten and raises GPTQ_DEV_GIDX_GROUPS."""
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -87,6 +92,48 @@ def test_device_sort_matches_host_prepack(bits, group, K, N):
     assert np.array_equal(raw[q:q + qw_host.nbytes].view(np.int32).reshape(qw_host.shape), qw_host)
     Cref, B = _oracle(wl, ck, A)
     assert_gemm_close(C, Cref, B, "sorted rows b%d" % bits)
+
+
+@pytest.mark.parametrize("bits,group,K,N", [
+    (2, 64, 1024, 160), (3, 128, 640, 416), (4, 32, 512, 96), (8, 128, 384, 288), (4, 128, 16384, 64),
+    (3, 128, 5120, 1024)])
+def test_device_prepack_matches_host_prepack(bits, group, K, N):
+    wl = _wl(bits, group, "f16", 4, K, N, seed=bits * 7 + 1)
+    _, ck = checkpoint(wl, "v2")
+    qw, qz, sc, gi = to_device(ck)
+    qw_dev, perm_dev = g.prepack_act_order_device(qw, gi, K=K, N=N, bits=bits, group=group)
+    # the very next call on the stream uses them (the prepack ends with an ordering step)
+    A = gptq_inputs.draw_activations(wl, 4)
+    C = g.gemm_perm(A.to(DEV), perm_dev, qw_dev, qz, sc, bits=bits, group=group, fmt=ck["fmt"])
+    torch.cuda.synchronize()
+    qw_host, perm_host = g.prepack_act_order(ck["qweight"], ck["g_idx"], K=K, N=N, bits=bits, group=group)
+    assert np.array_equal(perm_dev.cpu().numpy(), perm_host)
+    assert np.array_equal(qw_dev.cpu().numpy(), qw_host)
+    Cref, B = _oracle(wl, ck, A)
+    assert_gemm_close(C, Cref, B, "device prepack b%d" % bits)
+
+
+@pytest.mark.parametrize("case", ["unequal_groups", "entry_out_of_range"])
+def test_device_prepack_leaves_outputs_for_unusable_g_idx(case):
+    bits, group, K, N = 4, 128, 1024, 160
+    wl = _wl(bits, group, "f16", 1, K, N)
+    _, ck = checkpoint(wl, "v2")
+    bad = ck["g_idx"].copy()
+    if case == "unequal_groups":
+        bad[np.flatnonzero(bad == 1)[0]] = 0                       # group 0: group + 1 rows
+    else:
+        bad[5] = K // group                                         # G: outside [0, G)
+    qw = torch.from_numpy(ck["qweight"]).to(DEV)
+    gi = torch.from_numpy(bad).to(DEV)
+    out = torch.full_like(qw, 0x5A5A5A5A)
+    perm = torch.full((K,), -7, dtype=torch.int32, device=DEV)
+    ws = torch.empty(g.prepack_act_order_device_workspace_size(K, bits, group), dtype=torch.uint8, device=DEV)
+    p = lambda t: ctypes.c_void_p(t.data_ptr())
+    rc = g.lib().gptq_prepack_act_order_device(p(qw), p(gi), K, N, bits, group, p(out), p(perm), p(ws),
+                                               ws.numel(), None)
+    assert rc == 0, g.strerror(rc)
+    assert g.device_status() == g.DEV_GIDX_GROUPS
+    assert bool((out == 0x5A5A5A5A).all()) and bool((perm == -7).all())
 
 
 CASES = [

@@ -28,6 +28,7 @@ def test_exports_every_declared_symbol(lib):
                                "gptq_repack_zeros_v1_to_v2", "gptq_quantize_rtn",
                                "gptq_get_device_status", "gptq_strerror",
                                "gptq_selftest_wait_timeout", "gptq_prepack_act_order",
+                               "gptq_prepack_act_order_device", "gptq_prepack_act_order_device_workspace_size",
                                "gptq_gemm_perm", "gptq_gemm_perm_workspace_size",
                                "gptq_gemm_perm_noalloc", "gptq_gemm_grouped",
                                "gptq_prepack_interleave", "gptq_gemm_interleaved",
@@ -204,6 +205,36 @@ def test_act_order_workspace_size(lib):
     assert g.act_order_workspace_size(4, 131072, 128, 4, 128) == 0  # a 4-column strip of 256 KB
     assert g.act_order_workspace_size(0, 512, 128, 4, 64) == 0
     assert g.act_order_workspace_size(4, 500, 128, 4, 64) == 0      # group does not divide K
+
+
+def test_prepack_act_order_device_workspace_size(lib):
+    # the sort's flag (256) + each sorted row's code position (K * 4, rounded up to 256)
+    assert g.prepack_act_order_device_workspace_size(5120, 3, 128) == 256 + 20480
+    assert g.prepack_act_order_device_workspace_size(96, 8, 32) == 256 + 512
+    assert g.prepack_act_order_device_workspace_size(512, 2, 16) == 256 + 2048   # any group size
+    assert g.prepack_act_order_device_workspace_size(4096, 4, 1) == 0     # 4096 groups: the sort's 520 KB
+    assert g.prepack_act_order_device_workspace_size(131072, 4, 128) == 0  # a 4-column strip of 256 KB
+    assert g.prepack_act_order_device_workspace_size(500, 4, 100) == 0     # K not a multiple of 32
+    assert g.prepack_act_order_device_workspace_size(512, 4, 100) == 0     # group does not divide K
+    assert g.prepack_act_order_device_workspace_size(512, 5, 64) == 0
+    assert g.prepack_act_order_device_workspace_size(512, 4, 0) == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(qweight=None), -1), (dict(g_idx=None), -1), (dict(out=None), -1), (dict(perm=None), -1),
+    (dict(ws=None), -1), (dict(bits=5), -1), (dict(K=48), -2), (dict(N=48), -2), (dict(group=100), -2),
+    (dict(group=0), -2), (dict(K=4096, group=1), -2), (dict(ws_bytes=256 + 1024 - 1), -4),
+    (dict(perm=P(0x30008)), -3), (dict(out=P(0x20008)), -3), (dict(g_idx=P(0x40002)), -3),
+    (dict(ws=P(0x50008)), -3),
+    (dict(out=P(0x10000 + 256 * 64 * 4 // 8 - 16)), -1),   # the last 16 bytes of qweight
+])
+def test_prepack_act_order_device_validation_without_gpu(lib, kw, code):
+    a = dict(qweight=FAKE, g_idx=P(0x40000), K=256, N=64, bits=4, group=32, out=P(0x20000),
+             perm=P(0x30000), ws=P(0x50000), ws_bytes=4096)
+    a.update(kw)
+    rc = lib.gptq_prepack_act_order_device(a["qweight"], a["g_idx"], a["K"], a["N"], a["bits"], a["group"],
+                                           a["out"], a["perm"], a["ws"], a["ws_bytes"], None)
+    assert rc == code
 
 
 def test_gemm_perm_workspace_size(lib):
