@@ -48,8 +48,8 @@ struct Args {
   // interleaved weights (gptq_prepack_interleave): k-tiles per 32-column block, else 0 (the
   // checkpoint's own row-major layout, read through the tensor map)
   int il_tiles;
-  // nullable: the kernel does nothing unless *run_flag == run_when (set by an earlier kernel in
-  // the stream; such launches are never programmatic-dependent, so the flag is final at entry)
+  // nullable: the kernel does nothing unless *run_flag == run_when (set by a kernel that completed
+  // before the kernel ahead of this launch started, so the flag is final at entry, PDL or not)
   const int* run_flag;
   int run_when;
 };
